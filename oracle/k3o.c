@@ -1,0 +1,260 @@
+/*
+ * k3o.c -- ORACLE of the MXFP4 routed-expert MoE layer.  TEST INFRASTRUCTURE ONLY.
+ *
+ * Plain scalar fp64 C99 (+ optional OpenMP over independent rows and tokens).  It is the
+ * plain definition of the layer written out; no blocking, fusion or reordering beyond the
+ * group-wise summation the README's MXFP4 mat-vec states.  It shares nothing with the CUDA
+ * library.  See k3o.h for the sources and the meaning of every argument.
+ */
+#include "k3o.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---- number formats (README Part II section 4) ------------------------------------ */
+
+/* E2M1: one sign bit, two exponent bits, one mantissa bit.  The sixteen values in code
+ * order, as the README's code table prints them (codes 8..15 are the negatives). */
+static const double E2M1_VALUES[16] = {
+    0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+    -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0,
+};
+
+double k3o_e2m1(int code) { return E2M1_VALUES[code & 15]; }
+
+/* E8M0: a bare biased exponent.  The MX spec reserves 0xFF for NaN; the README maps it to
+ * zero so that one corrupt byte silences its group instead of poisoning the row. */
+double k3o_e8m0(int byte)
+{
+    byte &= 255;
+    if (byte == 255) return 0.0;
+    return ldexp(1.0, byte - 127);
+}
+
+double k3o_bf16_value(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+uint16_t k3o_bf16_from_f32(float v)
+{
+    uint32_t u;
+    memcpy(&u, &v, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) /* NaN: keep it a NaN */
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb; /* round half to even on the 16 dropped bits */
+    return (uint16_t)(u >> 16);
+}
+
+/* ---- MXFP4 mat-vec (README Part II section 4) -------------------------------------- */
+
+/* Nibble of logical column col in one packed row: byte col/2, low nibble for the even
+ * column and high nibble for the odd one. */
+static int nibble_at(const uint8_t *row, int col)
+{
+    int byte = row[col / 2];
+    return (col % 2 == 0) ? (byte & 15) : (byte >> 4);
+}
+
+void k3o_matvec_mxfp4(double *y, const double *x, const uint8_t *packed,
+                      const uint8_t *scales, int in, int rows, int group)
+{
+    const int ngroup = (in + group - 1) / group;
+    const size_t rowbytes = (size_t)(in + 1) / 2;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (int r = 0; r < rows; r++) {
+        const uint8_t *prow = packed + (size_t)r * rowbytes;
+        const uint8_t *srow = scales + (size_t)r * ngroup;
+        double acc = 0.0;
+        for (int g = 0; g < ngroup; g++) {
+            const double s = k3o_e8m0(srow[g]);
+            if (s == 0.0) continue; /* a NaN scale silences the whole group */
+            const int c0 = g * group;
+            const int c1 = (c0 + group < in) ? c0 + group : in;
+            double part = 0.0;
+            for (int col = c0; col < c1; col++)
+                part += x[col] * k3o_e2m1(nibble_at(prow, col));
+            acc += part * s;
+        }
+        y[r] = acc;
+    }
+}
+
+/* ---- router (README Part II section 9) --------------------------------------------- */
+
+static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+void k3o_gates_for(const k3o_cfg *c, const double *sc, const int32_t *idx, double *gate)
+{
+    double sum = 0.0;
+    for (int j = 0; j < c->topk; j++) {
+        gate[j] = sc[idx[j]]; /* the unbiased score, never the selection score */
+        sum += gate[j];
+    }
+    if (c->renorm && sum > 0.0)
+        for (int j = 0; j < c->topk; j++) gate[j] /= sum;
+    for (int j = 0; j < c->topk; j++) gate[j] *= c->routed_scale;
+}
+
+int k3o_route(const k3o_cfg *c, const uint16_t *h, const uint16_t *wr, const float *bias,
+              int T, int32_t *idx, double *gate, double *gap, double *sc_out,
+              double *ch_out)
+{
+    if (!c || !h || !wr || !idx || !gate || T < 0) return K3O_ERR_ARG;
+    const int H = c->hidden, E = c->n_experts, K = c->topk;
+    if (H <= 0 || E <= 0 || K <= 0 || K > E) return K3O_ERR_ARG;
+    const size_t TE = (size_t)T * (size_t)E;
+    double *sc = (double *)malloc(sizeof(double) * (TE ? TE : 1));
+    double *ch = (double *)malloc(sizeof(double) * (TE ? TE : 1));
+    if (!sc || !ch) {
+        free(sc); free(ch);
+        return K3O_ERR_NOMEM;
+    }
+    /* scores: one independent dot product per (token, expert) */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (long long te = 0; te < (long long)TE; te++) {
+        const int t = (int)(te / E), e = (int)(te % E);
+        const uint16_t *ht = h + (size_t)t * H;
+        const uint16_t *we = wr + (size_t)e * H;
+        double logit = 0.0;
+        for (int i = 0; i < H; i++) logit += k3o_bf16_value(ht[i]) * k3o_bf16_value(we[i]);
+        sc[te] = sigmoid(logit);                          /* the unbiased score  */
+        ch[te] = sc[te] + (bias ? (double)bias[e] : 0.0); /* the selection score */
+    }
+    int err = 0;
+    /* selection: top-k by repeated arg-max, strict '>' so the lower index wins a tie */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (int t = 0; t < T; t++) {
+        const double *cht = ch + (size_t)t * E;
+        char *taken = (char *)calloc((size_t)E, 1);
+        if (!taken) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            err = 1;
+            continue;
+        }
+        int32_t *it = idx + (size_t)t * K;
+        for (int j = 0; j < K; j++) {
+            int best = -1;
+            for (int e = 0; e < E; e++)
+                if (!taken[e] && (best < 0 || cht[e] > cht[best])) best = e;
+            taken[best] = 1;
+            it[j] = best;
+        }
+        if (gap) {
+            int rest = -1;
+            for (int e = 0; e < E; e++)
+                if (!taken[e] && (rest < 0 || cht[e] > cht[rest])) rest = e;
+            gap[t] = (rest < 0) ? INFINITY : cht[it[K - 1]] - cht[rest];
+        }
+        k3o_gates_for(c, sc + (size_t)t * E, it, gate + (size_t)t * K);
+        free(taken);
+    }
+    if (sc_out) memcpy(sc_out, sc, sizeof(double) * TE);
+    if (ch_out) memcpy(ch_out, ch, sizeof(double) * TE);
+    free(sc); free(ch);
+    return err ? K3O_ERR_NOMEM : K3O_OK;
+}
+
+/* ---- expert FFN and the routed sum (README Part II section 9, step 3) -------------- */
+
+void k3o_activation(const k3o_cfg *c, const double *g, const double *u, double *act, int n)
+{
+    for (int i = 0; i < n; i++) {
+        if (c->act == 1) {
+            /* SiTU-GLU: the sigmoid takes the uncapped gate */
+            const double a = c->situ_b1 * tanh(g[i] / c->situ_b1) * sigmoid(g[i]);
+            const double b = c->situ_b2 * tanh(u[i] / c->situ_b2);
+            act[i] = a * b;
+        } else {
+            act[i] = g[i] * sigmoid(g[i]) * u[i]; /* SwiGLU: silu(g) * u */
+        }
+    }
+}
+
+int k3o_expert_ffn(const k3o_cfg *c, const k3o_expert *ex, const double *x, double *o)
+{
+    if (!c) return K3O_ERR_ARG;
+    const int L = c->latent, I = c->inter, G = c->group;
+    if (!ex || !ex->w1p || !ex->w1s || !ex->w3p || !ex->w3s || !ex->w2p || !ex->w2s)
+        return K3O_ERR_MISSING_EXPERT;
+    double *g = (double *)malloc(sizeof(double) * (size_t)I);
+    double *u = (double *)malloc(sizeof(double) * (size_t)I);
+    double *a = (double *)malloc(sizeof(double) * (size_t)I);
+    if (!g || !u || !a) {
+        free(g); free(u); free(a);
+        return K3O_ERR_NOMEM;
+    }
+    k3o_matvec_mxfp4(g, x, ex->w1p, ex->w1s, L, I, G);
+    k3o_matvec_mxfp4(u, x, ex->w3p, ex->w3s, L, I, G);
+    k3o_activation(c, g, u, a, I);
+    k3o_matvec_mxfp4(o, a, ex->w2p, ex->w2s, I, L, G);
+    free(g); free(u); free(a);
+    return K3O_OK;
+}
+
+int k3o_experts(const k3o_cfg *c, const k3o_expert *table, int n_table, const uint16_t *x,
+                const int32_t *idx, const double *gate, int T, double *y)
+{
+    if (!c || !table || !x || !idx || !gate || !y || T < 0) return K3O_ERR_ARG;
+    const int L = c->latent, K = c->topk;
+    if (L <= 0 || K <= 0) return K3O_ERR_ARG;
+    double *xd = (double *)malloc(sizeof(double) * (size_t)L);
+    double *o = (double *)malloc(sizeof(double) * (size_t)L);
+    if (!xd || !o) {
+        free(xd); free(o);
+        return K3O_ERR_NOMEM;
+    }
+    int rc = K3O_OK;
+    for (int t = 0; t < T && rc == K3O_OK; t++) {
+        double *yt = y + (size_t)t * L;
+        for (int i = 0; i < L; i++) {
+            xd[i] = k3o_bf16_value(x[(size_t)t * L + i]);
+            yt[i] = 0.0;
+        }
+        for (int j = 0; j < K; j++) {
+            const int e = idx[(size_t)t * K + j];
+            if (e < 0 || e >= n_table) { rc = K3O_ERR_MISSING_EXPERT; break; }
+            rc = k3o_expert_ffn(c, &table[e], xd, o);
+            if (rc != K3O_OK) break;
+            const double w = gate[(size_t)t * K + j];
+            for (int i = 0; i < L; i++) yt[i] += w * o[i];
+        }
+    }
+    free(xd); free(o);
+    return rc;
+}
+
+/* ---- RMSNorm (README Part II section 5) -------------------------------------------- */
+
+void k3o_rmsnorm(double *out, const double *x, int n, double eps)
+{
+    double ss = 0.0;
+    for (int i = 0; i < n; i++) ss += x[i] * x[i];
+    const double inv = 1.0 / sqrt(ss / (double)n + eps);
+    for (int i = 0; i < n; i++) out[i] = x[i] * inv;
+}
+
+int k3o_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,52 @@
+"""Plant plausible mistakes in copies of the oracle and check that the pins catch each one.
+
+Every mutant is a one-line change to a temporary copy of ``oracle/k3o.c``: a swapped
+nibble order, an off-by-one exponent bias, a flipped tie rule, gates taken from the biased
+score, a dropped renormalisation, a dropped group, gate and up swapped in SwiGLU, w1 and w3
+swapped, a transposed activation operand.  ``tests/test_oracle_pins.py`` runs against each
+mutant in a subprocess and must fail.  The oracle itself is never modified.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "k3o.c")
+
+MUTANTS = {
+    "nibble_swap": ("(col % 2 == 0) ? (byte & 15) : (byte >> 4)", "(col % 2 == 0) ? (byte >> 4) : (byte & 15)"),
+    "scale_bias_off_by_one": ("ldexp(1.0, byte - 127)", "ldexp(1.0, byte - 126)"),
+    "nan_scale_not_zero": ("if (byte == 255) return 0.0;", "if (byte == 256) return 0.0;"),
+    "tie_to_higher_index": ("(best < 0 || cht[e] > cht[best])", "(best < 0 || cht[e] >= cht[best])"),
+    "gates_from_selection_score": ("k3o_gates_for(c, sc + (size_t)t * E, it", "k3o_gates_for(c, ch + (size_t)t * E, it"),
+    "no_renorm": ("if (c->renorm && sum > 0.0)", "if (0)"),
+    "dropped_last_group": ("for (int g = 0; g < ngroup; g++) {", "for (int g = 0; g < ngroup - (ngroup > 1); g++) {"),
+    "swiglu_gate_up_swapped": ("act[i] = g[i] * sigmoid(g[i]) * u[i];", "act[i] = u[i] * sigmoid(u[i]) * g[i];"),
+    "w1_w3_swapped": ("k3o_matvec_mxfp4(g, x, ex->w1p, ex->w1s, L, I, G);", "k3o_matvec_mxfp4(g, x, ex->w3p, ex->w3s, L, I, G);"),
+    "gap_wrong_sign": ("cht[it[K - 1]] - cht[rest]", "cht[rest] - cht[it[K - 1]]"),
+    "bias_ignored": ("ch[te] = sc[te] + (bias ? (double)bias[e] : 0.0);", "ch[te] = sc[te];"),
+    "situ_capped_sigmoid": ("tanh(g[i] / c->situ_b1) * sigmoid(g[i])", "tanh(g[i] / c->situ_b1) * sigmoid(tanh(g[i]))"),
+    "rmsnorm_eps_outside": ("1.0 / sqrt(ss / (double)n + eps)", "1.0 / (sqrt(ss / (double)n) + eps)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    d = tmp_path / "mut"
+    d.mkdir()
+    shutil.copy(os.path.join(ROOT, "oracle", "k3o.h"), d / "k3o.h")
+    (d / "k3o.c").write_text(src.replace(old, new))
+    lib = str(d / "libk3o_mut.so")
+    subprocess.run(["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
+                    str(d / "k3o.c"), "-o", lib, "-lm"], check=True)
+    env = dict(os.environ, K3O_LIB=lib)
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                        "-x", "-q", "-p", "no:cacheprovider"], cwd=ROOT, env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
