@@ -1,0 +1,457 @@
+"""Benchmark of the MXFP4 routed-expert MoE layer on GB300 (one JSON line on stdout).
+
+Default workload: the batch-1 decode layer (1 token, 896 experts, top-16, bias N(0, 0.3)),
+the configuration the headline metric "MoE-layer tokens/s and achieved HBM TB/s (MXFP4
+experts, 896 choose 16)" is quoted on.  A step is one full layer: router GEMV, top-k,
+bucketing, GEMM1 (w1, w3, SwiGLU), GEMM2 (w2, gates), combine.  Inputs are seeded and
+synthetic (synth/), resident in HBM when the timed region starts.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 1]
+
+--gpus N > 1 runs under torchrun, one rank per GPU: every rank holds its own copy of the
+layer and decodes its own token stream (weak scaling, no collective on the data path); the
+timed region is bracketed by barriers and the slowest rank's time counts.
+
+--impl reference times the oracle (plain fp64 C on the host cores) on bounded samples of the
+same workload; it is the deliberately slow reference arm, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import dataclasses
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and achieved HBM TB/s (MXFP4 experts, 896 choose 16)"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ---- byte and MAC accounting (algorithmic, per step) ----------------------------------
+
+def layer_bytes(w: synth.Workload, distinct_experts: int, T: int) -> int:
+    """Bytes the layer must move: packed+scale bytes of the distinct experts touched, the
+    router weight and bias, h, x and y.  Intermediates and indices excluded."""
+    return (distinct_experts * w.expert_bytes + w.E * w.hidden * 2 + (w.E * 4 if w.bias != "none" else 0)
+            + T * w.hidden * 2 + T * w.latent * 2 + T * w.latent * 4)
+
+
+def gemm1_bytes(w: synth.Workload, distinct_experts: int, T: int) -> int:
+    """GEMM1's compulsory traffic: w1 and w3 (packed + scales) of the distinct experts, the
+    f16 copy of x it reads and the fp32 activations it writes."""
+    L, I = w.latent, w.inter
+    return distinct_experts * 2 * (I * L // 2 + I * L // 32) + T * L * 2 + T * w.k * I * 4
+
+
+def token_macs(w: synth.Workload) -> int:
+    return w.E * w.hidden + w.k * 3 * w.inter * w.latent
+
+
+# ---- clocks -------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r for r in csv.reader(io.StringIO(self.out or "")) if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---- distributed helpers (also exercised by the gloo tests) -------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_token_offset(rank: int, rotation: int) -> int:
+    """Each rank decodes its own slice of the seeded token stream."""
+    return rank * rotation
+
+
+# ---- CPU side: the oracle (cpu_baseline and the reference arm) ----------------------
+
+class OracleRunner:
+    """The oracle as it stands on the batch-1 decode workload: the token's router and its
+    16 expert FFNs, expert bytes from the host twin of the generator."""
+
+    def __init__(self, w: synth.Workload, token: int = 0):
+        import oracle
+        self.oracle = oracle
+        self.w = w
+        li = synth.layer_inputs(w, 0, T=token + 1)
+        self.h, self.x = li.h[token:token + 1], li.x[token:token + 1]
+        self.wr, self.bias = li.wr, li.bias
+        self.cfg = oracle.Cfg(hidden=w.hidden, n_experts=w.E, topk=w.k, latent=w.latent, inter=w.inter,
+                              routed_scale=w.routed_scale)
+        r = oracle.route(self.cfg, self.h, self.wr, self.bias)
+        self.idx, self.gate = r.idx, r.gate
+        self.table = {int(e): oracle.ExpertBytes(**synth.expert_host(w, 0, int(e))) for e in r.idx[0]}
+        self.xd = oracle.bf16_to_f64(self.x[0])
+
+    def token(self):
+        r = self.oracle.route(self.cfg, self.h, self.wr, self.bias)
+        return self.oracle.experts(self.cfg, self.table, self.x, r.idx, r.gate)
+
+    def piece(self, kind: str, j: int):
+        o, ex = self.oracle, self.table[int(self.idx[0, j % self.w.k])]
+        if kind == "route+ffn":
+            o.route(self.cfg, self.h, self.wr, self.bias)
+            o.expert_ffn(self.cfg, ex, self.xd)
+        elif kind == "ffn":
+            o.expert_ffn(self.cfg, ex, self.xd)
+        elif kind == "w1":
+            o.matvec_mxfp4(self.xd, ex.w1p, ex.w1s)
+        else:  # "w1/8": an eighth of w1's rows
+            n = self.w.inter // 8
+            o.matvec_mxfp4(self.xd, ex.w1p[:n], ex.w1s[:n])
+
+    def piece_macs(self, kind: str) -> int:
+        w = self.w
+        ffn = 3 * w.inter * w.latent
+        return {"route+ffn": w.E * w.hidden + ffn, "ffn": ffn, "w1": w.inter * w.latent,
+                "w1/8": (w.inter // 8) * w.latent}[kind]
+
+
+def cpu_baseline(w: synth.Workload, min_seconds: float = 10.0, max_tokens: int = 200):
+    import oracle
+    run = OracleRunner(w)
+    run.token()  # warm caches
+    n, t0 = 0, time.perf_counter()
+    while n < max_tokens:
+        run.token()
+        n += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"the batch-1 decode token's full layer (router over 896 experts + 16 expert FFNs, fp64), "
+                      f"repeated {n} times ({dt:.1f} s); expert bytes generated outside the timed region"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        if rank != 0:
+            dist.barrier()
+            dist.destroy_process_group()
+            return
+    import oracle
+    w = synth.WORKLOADS[args.workload]
+    if w.T != 1 or w.layers != 1:
+        raise SystemExit("--impl reference samples the batch-1 decode workload only")
+    run = OracleRunner(w)
+    budget = 150.0
+    kind = None
+    for k in ("route+ffn", "ffn", "w1", "w1/8"):
+        t0 = time.perf_counter()
+        run.piece(k, 0)
+        run.piece(k, 1)
+        est = (time.perf_counter() - t0) / 2
+        if (args.steps + args.warmup) * est <= budget:
+            kind = k
+            break
+    kind = kind or "w1/8"
+    for j in range(args.warmup):
+        run.piece(kind, j)
+    t0 = time.perf_counter()
+    for j in range(args.steps):
+        run.piece(kind, j)
+    dt = time.perf_counter() - t0
+    tok_per_step = run.piece_macs(kind) / token_macs(w)
+    value = args.steps * tok_per_step / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "tokens_per_step": tok_per_step, "experts": w.E, "topk": w.k},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+                         "sample": f"each step: the oracle's '{kind}' piece of the batch-1 decode token "
+                                   f"({run.piece_macs(kind)} of the token's {token_macs(w)} multiply-adds; "
+                                   f"tokens/s scaled by that fraction)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ---- GPU arm --------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import mxfp4_routed_expert_gemv_gb300 as k3
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = synth.WORKLOADS[args.workload]
+    if args.experts:
+        w = dataclasses.replace(w, E=args.experts, name=w.name + f" [profiling variant: {args.experts} experts]")
+    if w.layers != 1:
+        raise SystemExit("the stacked workload is a parity case, not a bench line")
+    free, total = torch.cuda.mem_get_info(dev)
+    need = w.E * w.expert_bytes + (4 << 30)
+    if need > free:
+        raise SystemExit(f"needs {need / 1e9:.1f} GB of HBM, {free / 1e9:.1f} GB free")
+
+    cfg = k3.Cfg(hidden=w.hidden, n_experts=w.E, topk=w.k, latent=w.latent, inter=w.inter,
+                 routed_scale=w.routed_scale)
+    experts = k3.Experts.from_dict(synth.experts_device(w, 0, dev))
+    rotation = args.rotation if w.T == 1 else 4
+    li = synth.layer_inputs(w, 0, T=w.T * rotation * world)
+    off = rank_token_offset(rank, rotation * w.T)
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    H = bf16(li.h[off:off + rotation * w.T]).view(rotation, w.T, w.hidden)
+    X = bf16(li.x[off:off + rotation * w.T]).view(rotation, w.T, w.latent)
+    wr = bf16(li.wr)
+    bias = None if li.bias is None else torch.from_numpy(li.bias).to(dev)
+    T = w.T
+    ws = k3.workspace(cfg, T, dev)
+    y = torch.empty((T, w.latent), dtype=torch.float32, device=dev)
+    idx = torch.empty((rotation, T, w.k), dtype=torch.int32, device=dev)
+    gate = torch.empty((T, w.k), dtype=torch.float32, device=dev)
+    status = torch.zeros(4, dtype=torch.int32, device=dev)
+
+    def step(i):  # one layer on the current stream
+        r = i % rotation
+        k3.k3moe_layer(cfg, H[r], wr, bias, experts, X[r], y, idx[r], gate, None, status, ws)
+
+    # eager warm-up (also configures the kernels' shared-memory limits before any capture)
+    n0 = k3.k3moe_launch_count()
+    step(0)
+    launches_per_step = k3.k3moe_launch_count() - n0
+    for i in range(1, args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    # The decode loop is replayed from CUDA graphs: one graph holds `rotation` consecutive
+    # layers (each on its own token input), a second one the K mod rotation remainder.
+    cap_stream = torch.cuda.Stream(dev)
+
+    def capture(n_steps, phase_events=None):
+        g = torch.cuda.CUDAGraph()
+        cap_stream.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.graph(g, stream=cap_stream):
+            for i in range(n_steps):
+                if phase_events is not None:
+                    k3.k3moe_set_phase_events(phase_events[i])
+                step(i)
+            if phase_events is not None:
+                k3.k3moe_set_phase_events(None)
+        torch.cuda.current_stream(dev).wait_stream(cap_stream)
+        return g
+
+    full = capture(rotation)
+    rem = args.steps % rotation
+    tail = capture(rem) if rem else None
+    for _ in range(2):
+        full.replay()
+    torch.cuda.synchronize(dev)
+    distinct = [len(set(idx[r].reshape(-1).tolist())) for r in range(rotation)]
+    stream = torch.cuda.current_stream(dev)
+
+    # timed region: exactly K layers
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps // rotation):
+            full.replay()
+        if tail is not None:
+            tail.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    launches = launches_per_step * args.steps
+    elapsed = e0.elapsed_time(e1) / 1e3
+    elapsed_max = max_over_ranks(elapsed, world, dev)
+    tokens = sum_over_ranks(T * args.steps, world, dev)
+    st = status.cpu().numpy()
+    if st[0] or st[1]:
+        raise SystemExit(f"device status reports dropped={st[0]} timeouts={st[1]}")
+
+    # phase pass: the same graph with event-record nodes between the phases; GEMM1 (the
+    # dominant kernel) duration = its events' difference on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(rotation)]
+    for row in evs:  # torch creates the CUDA event at its first record
+        for ev in row:
+            ev.record(stream)
+    torch.cuda.synchronize(dev)
+    timed = capture(rotation, evs)
+    samples = []
+    for _ in range(max(1, min(20, args.steps // rotation))):
+        timed.replay()
+        torch.cuda.synchronize(dev)
+        samples.append([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(rotation)])
+    ph = np.array(samples).reshape(-1, 5) / 1e3
+    gemm1_s = float(ph[:, 2].mean())
+    d_mean = float(np.mean(distinct))
+    g1_bytes = gemm1_bytes(w, d_mean, T)
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = json.load(open(peaks_path)) if os.path.exists(peaks_path) else {}
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or 6800.0
+    achieved = g1_bytes / gemm1_s / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        with open(prof) as f:
+            traffic = json.load(f).get(f"gemm1_workload{args.workload}")
+
+    # end to end through the host-buffer entry point (copies in and out, synchronised)
+    n_e2e = min(args.steps, 2000)
+    wsh = k3.workspace_host(cfg, T, dev)
+    hh = torch.empty((rotation, T, w.hidden), dtype=torch.bfloat16).pin_memory()
+    xh = torch.empty((rotation, T, w.latent), dtype=torch.bfloat16).pin_memory()
+    hh.copy_(H.cpu())
+    xh.copy_(X.cpu())
+    yh = torch.empty((T, w.latent), dtype=torch.float32).pin_memory()
+    for i in range(min(args.warmup, 50)):
+        k3.k3moe_layer_host(cfg, hh[i % rotation], wr, bias, experts, xh[i % rotation], yh, status, wsh)
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        k3.k3moe_layer_host(cfg, hh[i % rotation], wr, bias, experts, xh[i % rotation], yh, status, wsh)
+    e2e_dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+    e2e_value = sum_over_ranks(T * n_e2e, world, dev) / e2e_dt
+
+    lb = layer_bytes(w, d_mean, T)
+    value = tokens / elapsed_max
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * elapsed_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e2m1*f16->f32 (MXFP4 weights, fp32 accumulation)",
+        "data": "synthetic",
+        "config": {"workload": w.name, "tokens_per_step_per_gpu": T, "experts": w.E, "topk": w.k,
+                   "hidden": w.hidden, "latent": w.latent, "inter": w.inter,
+                   "distinct_experts_per_step": d_mean, "algorithmic_bytes_per_step": lb,
+                   "achieved_layer_TBps": lb * args.steps / elapsed / 1e12,
+                   "layer_frac_of_hbm_peak": lb * args.steps / elapsed / 1e9 / peak,
+                   "l2": f"inputs larger than L2: each step streams {lb / 1e6:.0f} MB (> {L2_BYTES / 1e6:.0f} MB L2) "
+                         f"and rotates among {rotation} seeded token inputs, so consecutive steps pick different experts",
+                   "phase_ms": {n: float(ph[:, j].mean() * 1e3) for j, n in
+                                enumerate(["route", "bucket+prep", "gemm1", "gemm2", "combine"])},
+                   "launch": "CUDA graph replay, programmatic dependent launch between kernels",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "k_gemm1 (w1+w3 MXFP4 GEMV, SwiGLU epilogue)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} hbm_gbs", "traffic": traffic,
+                     "algorithmic_bytes_per_launch": g1_bytes, "avg_launch_s": gemm1_s},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * (w.hidden + w.latent) * 2,
+                "d2h_bytes_per_step": T * w.latent * 4},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and w.T == 1:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50000)
+    ap.add_argument("--warmup", type=int, default=500)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=1, choices=[0, 1, 2, 3])
+    ap.add_argument("--rotation", type=int, default=64)
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the expert count (small-memory profiling variant, not a bench line)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

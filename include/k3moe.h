@@ -1,0 +1,186 @@
+/*
+ * k3moe.h -- C ABI of the MXFP4 routed-expert MoE layer on one GB300 (sm_103a).
+ *
+ * The layer (Kimi-K3 shape) is the one stated by the "kimi-k3-in-c" README, Part II
+ * section 9 "Picking 16 experts of 896" (router and per-token MoE), with experts stored as
+ * MXFP4 as in Part II section 4 "Reduction one: the experts already ship at half a byte"
+ * and the tensor shapes of "K3_ARTIFACT_AUDIT" (llm-atlas) section 4.3:
+ *
+ *   logit[t][e] = sum_i h[t][i] * Wr[e][i]                 router GEMV (bf16 in, fp32 sum)
+ *   sc = sigmoid(logit); ch = sc + bias[e]                 bias steers selection only
+ *   idx[t][0..k) = top-k of ch, descending; a tie goes to the lower expert index
+ *   gate[t][j] = routed_scale * sc[idx_j] / sum_j sc[idx_j]      (renorm on)
+ *   y[t] = sum_j gate[t][j] * W2[e_j] act(W1[e_j] x[t], W3[e_j] x[t])
+ *   MXFP4 weight w = E2M1[nibble] * 2^(scale - 127), one E8M0 scale per 32 consecutive
+ *   weights of a row, low nibble = even column, scale byte 255 -> the group is zero.
+ *   act = SwiGLU: silu(g) * u   (or SiTU-GLU, README section 9, when selected)
+ *
+ * Conventions for every entry point:
+ *   - Device pointers unless stated otherwise.  The caller owns every buffer.  No entry
+ *     point allocates device or host memory; scratch comes from the caller's workspace
+ *     `ws` of at least k3moe_workspace_size() bytes (device memory, 256-byte aligned).
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *     stream) and the call returns after enqueueing; results are ready when the stream
+ *     reaches that point.  k3moe_layer_host is the exception: it synchronises the stream.
+ *   - T == 0 is a no-op that returns K3MOE_OK once the configuration is valid (empty
+ *     tensors may carry NULL pointers).
+ *   - Host-side argument checks run first.  On any failure the call returns a non-zero
+ *     k3moe_status and enqueues nothing ("refuse, never guess": README Part II section 2).
+ *   - Device-side anomalies are counted into an optional device status block
+ *     (int32 status[4]): [0] assignments skipped because their expert index was out of
+ *     range, [1] bounded waits that ran out, [2..3] reserved.  The library only adds to
+ *     it (atomically); the caller zeroes it.  This follows the README's "counted, never
+ *     silent" expert-drop rule (Part II section 9).
+ *   - Pointers to bf16/fp32 tensors and to expert bytes must be 16-byte aligned.
+ *   - Row-major, contiguous tensors throughout.
+ *
+ * Thread safety: calls on different streams with disjoint workspaces may run
+ * concurrently.  Two calls that share a workspace must be ordered on the GPU.
+ */
+#ifndef K3MOE_H
+#define K3MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define K3MOE_ABI_VERSION 1
+
+typedef enum k3moe_status {
+    K3MOE_OK = 0,
+    K3MOE_ERR_INVALID = 1,     /* null pointer, negative size, k > E, bad enum value     */
+    K3MOE_ERR_UNSUPPORTED = 2, /* a shape the kernels do not handle (see k3moe_cfg)      */
+    K3MOE_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned                       */
+    K3MOE_ERR_WORKSPACE = 4,   /* ws is NULL/misaligned or smaller than required         */
+    K3MOE_ERR_CUDA = 5,        /* a CUDA launch or copy failed                           */
+    K3MOE_ERR_TIMEOUT = 6,     /* (device status only) a bounded wait ran out            */
+    K3MOE_ERR_DROPPED = 7      /* (device status only) expert index out of range         */
+} k3moe_status;
+
+typedef enum k3moe_act {
+    K3MOE_ACT_SWIGLU = 0, /* act = silu(g) * u                                            */
+    K3MOE_ACT_SITU = 1    /* act = b1*tanh(g/b1)*sigmoid(g) * b2*tanh(u/b2)  (README s.9) */
+} k3moe_act;
+
+/* Layer configuration; every field is required.  Supported: 1 <= topk <= min(E, 32),
+ * 1 <= n_experts <= 1024, group == 32, hidden % 8 == 0, latent and inter multiples of 32
+ * with latent <= 4096 and inter <= 4096.  Kimi K3: 7168, 896, 16, 3584, 3072, 32. */
+typedef struct k3moe_cfg {
+    int32_t hidden;       /* router input width H                                     */
+    int32_t n_experts;    /* E                                                        */
+    int32_t topk;         /* k                                                        */
+    int32_t latent;       /* L: expert input / output width                           */
+    int32_t inter;        /* I: expert intermediate width                             */
+    int32_t group;        /* MX group size (must be 32)                               */
+    int32_t renorm;       /* 1: gates renormalised over the chosen k; 0: not          */
+    float routed_scale;   /* gates are multiplied by this (2.5 in the K3 workloads)   */
+    int32_t act;          /* k3moe_act                                                */
+    float situ_b1;        /* SiTU caps (4.0, 25.0); ignored for SwiGLU                */
+    float situ_b2;
+} k3moe_cfg;
+
+/* The stacked expert tensors of one layer, checkpoint row layout (device memory):
+ *   w1_packed, w3_packed: uint8 [E][inter][latent/2]    nibble pairs, low = even column
+ *   w1_scale,  w3_scale:  uint8 [E][inter][latent/32]   E8M0
+ *   w2_packed:            uint8 [E][latent][inter/2]
+ *   w2_scale:             uint8 [E][latent][inter/32]
+ * For Kimi K3 that is 17,547,264 bytes per expert (audit section 4.3). */
+typedef struct k3moe_experts {
+    const uint8_t *w1_packed, *w1_scale;
+    const uint8_t *w3_packed, *w3_scale;
+    const uint8_t *w2_packed, *w2_scale;
+} k3moe_experts;
+
+/* Bytes of device workspace needed by k3moe_route / k3moe_experts_mxfp4 / k3moe_layer
+ * for T tokens (k3moe_layer_host needs k3moe_workspace_size_host).  Returns K3MOE_OK and
+ * writes *bytes, or an error for an unsupported configuration. */
+int k3moe_workspace_size(const k3moe_cfg *cfg, int32_t T, size_t *bytes);
+
+/* Router for T tokens (README Part II section 9, the k3_router statement).
+ *   h:    bf16 [T][hidden]          router input
+ *   wr:   bf16 [E][hidden]          router weight
+ *   bias: fp32 [E] or NULL          correction bias, added for selection only
+ *   idx:  int32 [T][k]  (out)       chosen experts, descending selection score; ties ->
+ *                                   lower index
+ *   gate: fp32 [T][k]   (out)       combine weights from the unbiased sigmoid scores
+ *   gap:  fp32 [T] or NULL (out)    k-th minus (k+1)-th selection score (+inf if k == E)
+ * Scores are fp32 sigmoids of fp32-accumulated bf16 dot products. */
+int k3moe_route(const k3moe_cfg *cfg, const void *h, const void *wr, const float *bias,
+                int32_t T, int32_t *idx, float *gate, float *gap, void *ws, size_t ws_bytes,
+                void *stream);
+
+/* The routed-expert sum for T tokens given a routing (README Part II section 9, step 3):
+ *   y[t] = sum_j gate[t][j] * W2[e] act(W1[e] x[t], W3[e] x[t]),  e = idx[t][j].
+ *   experts: the layer's expert tensors (struct in host memory, pointers to device memory)
+ *   x:    bf16 [T][latent]          expert input
+ *   idx:  int32 [T][k], gate: fp32 [T][k]
+ *   y:    fp32 [T][latent] (out)    fully overwritten (not accumulated into)
+ *   status: int32[4] device status block or NULL.  An index outside [0, E) skips that
+ *   assignment (its term is zero) and counts it in status[0].
+ * Expert weights stay packed in HBM; they are decoded in registers and never expanded. */
+int k3moe_experts_mxfp4(const k3moe_cfg *cfg, const k3moe_experts *experts, const void *x,
+                        const int32_t *idx, const float *gate, int32_t T, float *y,
+                        int32_t *status, void *ws, size_t ws_bytes, void *stream);
+
+/* Router + routed-expert sum in one call (the layer).  idx, gate and gap are optional
+ * outputs (NULL: kept in the workspace); other arguments as in the two calls above. */
+int k3moe_layer(const k3moe_cfg *cfg, const void *h, const void *wr, const float *bias,
+                const k3moe_experts *experts, const void *x, int32_t T, float *y,
+                int32_t *idx, float *gate, float *gap, int32_t *status, void *ws,
+                size_t ws_bytes, void *stream);
+
+/* Bytes of device workspace for k3moe_layer_host with T tokens: the device workspace of
+ * k3moe_layer plus staging room for h, x and y. */
+int k3moe_workspace_size_host(const k3moe_cfg *cfg, int32_t T, size_t *bytes);
+
+/* k3moe_layer with HOST input and output buffers: copies h (bf16 [T][hidden]) and x
+ * (bf16 [T][latent]) from host memory into the workspace, runs the layer, copies y (fp32
+ * [T][latent]) back to host memory, and synchronises the stream before returning.  Host
+ * buffers should be page-locked for asynchronous copies.  wr, bias, experts and status
+ * stay in device memory.  Returns K3MOE_ERR_CUDA if a copy or the synchronisation fails. */
+int k3moe_layer_host(const k3moe_cfg *cfg, const void *h_host, const void *wr,
+                     const float *bias, const k3moe_experts *experts, const void *x_host,
+                     int32_t T, float *y_host, int32_t *status, void *ws, size_t ws_bytes,
+                     void *stream);
+
+/* One MXFP4 mat-vec on the GPU (README Part II section 4, the k3_matmul_mxfp4 statement):
+ *   y[r] = sum_c W[r][c] x[c],  W = packed [rows][in/2] + scales [rows][in/32]
+ *   x: bf16 [in]; y: fp32 [rows] (out).  in must be a multiple of 32. */
+int k3moe_matvec_mxfp4(float *y, const void *x, const uint8_t *packed, const uint8_t *scales,
+                       int32_t in, int32_t rows, int32_t group, void *stream);
+
+/* Link between stacked layers: next-layer inputs from a layer output.
+ *   y: fp32 [T][L]; x_out: bf16 [T][L] (out); h_out: bf16 [T][2L] or NULL (out).
+ *   norm != 0: each token is RMS-normalised with unit weight, eps inside the square root
+ *   (README Part II section 5), before rounding to bf16 (nearest even).  h_out is x_out
+ *   tiled twice along the feature axis. */
+int k3moe_stack_link(const float *y, int32_t T, int32_t L, int32_t norm, float eps,
+                     void *x_out, void *h_out, void *stream);
+
+/* Per-phase timing hook for benchmarks.  events: n (== 6) cudaEvent_t handles (as void*)
+ * created by the caller, or NULL to switch the hook off.  While set, every k3moe_layer and
+ * k3moe_experts_mxfp4 call records, on its stream: [0] at entry, [1] after the router
+ * logits (decode-sized batches run the top-k inside the next phase), [2] after the top-k,
+ * bucketing and input preparation, [3] after GEMM1 (w1, w3, activation), [4] and [5] after
+ * GEMM2 (w2, gates and the combine, which is fused into it).  Process-wide, not thread-safe;
+ * recording breaks programmatic launch overlap between phases, so time throughput with
+ * the hook off.  Returns K3MOE_ERR_INVALID if n != 6 with non-NULL events. */
+int k3moe_set_phase_events(void *const *events, int32_t n);
+
+/* Number of kernels the library launched through the entry points above since load
+ * (host counter; for launch accounting in benchmarks). */
+int64_t k3moe_launch_count(void);
+
+/* Static string for a status code. */
+const char *k3moe_strerror(int status);
+
+/* K3MOE_ABI_VERSION of the loaded library. */
+int32_t k3moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* K3MOE_H */

@@ -1,0 +1,313 @@
+"""Python binding of libk3moe.so, the MXFP4 routed-expert MoE layer for one GB300.
+
+Argument marshalling only: every step of the layer runs in the library's CUDA kernels
+(sm_103a).  The functions carry the C ABI's names (include/k3moe.h) and take torch CUDA
+tensors; PyTorch supplies device memory and streams, nothing else.  There is no CPU path:
+importing works anywhere, but the first call loads libk3moe.so (building it with nvcc when
+it is missing or stale) and raises if that fails.
+
+The layer (README "kimi-k3-in-c", Part II section 9; expert format Part II section 4;
+shapes from "K3_ARTIFACT_AUDIT" section 4.3):
+  router logits h . Wr  ->  sigmoid scores (+ bias for selection)  ->  top-k, gates
+  -> per chosen expert: act(W1 x, W3 x) -> W2  ->  gate-weighted sum y.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+from typing import Optional
+
+from . import build as _build
+
+__all__ = [
+    "K3moeError", "Cfg", "Experts", "KIMI_K3", "lib", "workspace", "workspace_host",
+    "k3moe_workspace_size", "k3moe_workspace_size_host", "k3moe_route", "k3moe_experts_mxfp4",
+    "k3moe_layer", "k3moe_layer_host", "k3moe_matvec_mxfp4", "k3moe_stack_link",
+    "k3moe_launch_count", "k3moe_strerror", "k3moe_abi_version", "k3moe_set_phase_events",
+    "EXPORTED_SYMBOLS",
+]
+
+EXPORTED_SYMBOLS = (
+    "k3moe_workspace_size", "k3moe_workspace_size_host", "k3moe_route", "k3moe_experts_mxfp4",
+    "k3moe_layer", "k3moe_layer_host", "k3moe_matvec_mxfp4", "k3moe_stack_link",
+    "k3moe_launch_count", "k3moe_strerror", "k3moe_abi_version", "k3moe_set_phase_events",
+)
+
+ACT_SWIGLU, ACT_SITU = 0, 1
+
+
+class K3moeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status} ({k3moe_strerror(status)})")
+
+
+class _CCfg(ctypes.Structure):
+    _fields_ = [
+        ("hidden", ctypes.c_int32), ("n_experts", ctypes.c_int32), ("topk", ctypes.c_int32),
+        ("latent", ctypes.c_int32), ("inter", ctypes.c_int32), ("group", ctypes.c_int32),
+        ("renorm", ctypes.c_int32), ("routed_scale", ctypes.c_float), ("act", ctypes.c_int32),
+        ("situ_b1", ctypes.c_float), ("situ_b2", ctypes.c_float),
+    ]
+
+
+class _CExperts(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w1_packed", "w1_scale", "w3_packed", "w3_scale", "w2_packed", "w2_scale")]
+
+
+@dataclasses.dataclass(frozen=True)
+class Cfg:
+    """k3moe_cfg.  Defaults are the Kimi K3 layer with the workloads' routed scale 2.5."""
+
+    hidden: int = 7168
+    n_experts: int = 896
+    topk: int = 16
+    latent: int = 3584
+    inter: int = 3072
+    group: int = 32
+    renorm: int = 1
+    routed_scale: float = 2.5
+    act: int = ACT_SWIGLU
+    situ_b1: float = 4.0
+    situ_b2: float = 25.0
+
+    def c(self) -> _CCfg:
+        return _CCfg(self.hidden, self.n_experts, self.topk, self.latent, self.inter, self.group,
+                     self.renorm, self.routed_scale, self.act, self.situ_b1, self.situ_b2)
+
+
+KIMI_K3 = Cfg()
+
+
+@dataclasses.dataclass
+class Experts:
+    """Stacked expert tensors (torch uint8, device), checkpoint row layout:
+    w1p/w3p [E, I, L/2], w1s/w3s [E, I, L/32], w2p [E, L, I/2], w2s [E, L, I/32]."""
+
+    w1p: "object"
+    w1s: "object"
+    w3p: "object"
+    w3s: "object"
+    w2p: "object"
+    w2s: "object"
+
+    def c(self) -> _CExperts:
+        return _CExperts(*(t.data_ptr() for t in (self.w1p, self.w1s, self.w3p, self.w3s, self.w2p, self.w2s)))
+
+    @classmethod
+    def from_dict(cls, d) -> "Experts":
+        return cls(d["w1p"], d["w1s"], d["w3p"], d["w3s"], d["w2p"], d["w2s"])
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libk3moe.so (built from csrc/ with nvcc for sm_103a if needed)."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        pc, pe = ctypes.POINTER(_CCfg), ctypes.POINTER(_CExperts)
+        L.k3moe_workspace_size.argtypes = [pc, i32, ctypes.POINTER(sz)]
+        L.k3moe_workspace_size_host.argtypes = [pc, i32, ctypes.POINTER(sz)]
+        L.k3moe_route.argtypes = [pc, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
+        L.k3moe_experts_mxfp4.argtypes = [pc, pe, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+        L.k3moe_layer.argtypes = [pc, vp, vp, vp, pe, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.k3moe_layer_host.argtypes = [pc, vp, vp, vp, pe, vp, i32, vp, vp, vp, sz, vp]
+        L.k3moe_matvec_mxfp4.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
+        L.k3moe_stack_link.argtypes = [vp, i32, i32, i32, ctypes.c_float, vp, vp, vp]
+        L.k3moe_set_phase_events.restype = ctypes.c_int
+        L.k3moe_set_phase_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
+        L.k3moe_launch_count.restype = ctypes.c_int64
+        L.k3moe_launch_count.argtypes = []
+        L.k3moe_strerror.restype = ctypes.c_char_p
+        L.k3moe_strerror.argtypes = [ctypes.c_int]
+        L.k3moe_abi_version.restype = i32
+        L.k3moe_abi_version.argtypes = []
+        for n in ("k3moe_workspace_size", "k3moe_workspace_size_host", "k3moe_route",
+                  "k3moe_experts_mxfp4", "k3moe_layer", "k3moe_layer_host", "k3moe_matvec_mxfp4",
+                  "k3moe_stack_link"):
+            getattr(L, n).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _p(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise K3moeError(fn, rc)
+
+
+def _expect(t, name, dtype, shape, cuda=True):
+    import torch
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not cuda and t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    return t
+
+
+def k3moe_strerror(status: int) -> str:
+    return lib().k3moe_strerror(int(status)).decode()
+
+
+def k3moe_abi_version() -> int:
+    return int(lib().k3moe_abi_version())
+
+
+def k3moe_launch_count() -> int:
+    return int(lib().k3moe_launch_count())
+
+
+def k3moe_set_phase_events(events) -> None:
+    """events: six torch.cuda.Event (created with enable_timing) or None to switch off."""
+    if events is None:
+        _check("k3moe_set_phase_events", lib().k3moe_set_phase_events(None, 0))
+        return
+    handles = [e.cuda_event for e in events]
+    if not all(handles):
+        raise ValueError("record each event once before passing it (torch creates events lazily)")
+    arr = (ctypes.c_void_p * len(events))(*handles)
+    _check("k3moe_set_phase_events", lib().k3moe_set_phase_events(arr, len(events)))
+
+
+def k3moe_workspace_size(cfg: Cfg, T: int) -> int:
+    n = ctypes.c_size_t(0)
+    c = cfg.c()
+    _check("k3moe_workspace_size", lib().k3moe_workspace_size(ctypes.byref(c), int(T), ctypes.byref(n)))
+    return int(n.value)
+
+
+def k3moe_workspace_size_host(cfg: Cfg, T: int) -> int:
+    n = ctypes.c_size_t(0)
+    c = cfg.c()
+    _check("k3moe_workspace_size_host", lib().k3moe_workspace_size_host(ctypes.byref(c), int(T), ctypes.byref(n)))
+    return int(n.value)
+
+
+def workspace(cfg: Cfg, T: int, device="cuda"):
+    """A device workspace (uint8 tensor) for T tokens."""
+    import torch
+    return torch.empty(k3moe_workspace_size(cfg, T), dtype=torch.uint8, device=device)
+
+
+def workspace_host(cfg: Cfg, T: int, device="cuda"):
+    import torch
+    return torch.empty(k3moe_workspace_size_host(cfg, T), dtype=torch.uint8, device=device)
+
+
+def k3moe_route(cfg: Cfg, h, wr, bias, idx, gate, gap, ws, stream=None) -> None:
+    import torch
+    T = h.shape[0]
+    _expect(h, "h", torch.bfloat16, (T, cfg.hidden))
+    _expect(wr, "wr", torch.bfloat16, (cfg.n_experts, cfg.hidden))
+    if bias is not None:
+        _expect(bias, "bias", torch.float32, (cfg.n_experts,))
+    _expect(idx, "idx", torch.int32, (T, cfg.topk))
+    _expect(gate, "gate", torch.float32, (T, cfg.topk))
+    if gap is not None:
+        _expect(gap, "gap", torch.float32, (T,))
+    c = cfg.c()
+    _check("k3moe_route", lib().k3moe_route(ctypes.byref(c), _p(h), _p(wr), _p(bias), T, _p(idx), _p(gate),
+                                            _p(gap), _p(ws), ws.numel(), _stream(stream)))
+
+
+def k3moe_experts_mxfp4(cfg: Cfg, experts: Experts, x, idx, gate, y, status, ws, stream=None) -> None:
+    import torch
+    T = x.shape[0]
+    _expect(x, "x", torch.bfloat16, (T, cfg.latent))
+    _expect(idx, "idx", torch.int32, (T, cfg.topk))
+    _expect(gate, "gate", torch.float32, (T, cfg.topk))
+    _expect(y, "y", torch.float32, (T, cfg.latent))
+    if status is not None:
+        _expect(status, "status", torch.int32, (4,))
+    c, e = cfg.c(), experts.c()
+    _check("k3moe_experts_mxfp4", lib().k3moe_experts_mxfp4(
+        ctypes.byref(c), ctypes.byref(e), _p(x), _p(idx), _p(gate), T, _p(y), _p(status), _p(ws),
+        ws.numel(), _stream(stream)))
+
+
+def k3moe_layer(cfg: Cfg, h, wr, bias, experts: Experts, x, y, idx=None, gate=None, gap=None,
+                status=None, ws=None, stream=None) -> None:
+    import torch
+    T = h.shape[0]
+    _expect(h, "h", torch.bfloat16, (T, cfg.hidden))
+    _expect(wr, "wr", torch.bfloat16, (cfg.n_experts, cfg.hidden))
+    if bias is not None:
+        _expect(bias, "bias", torch.float32, (cfg.n_experts,))
+    _expect(x, "x", torch.bfloat16, (T, cfg.latent))
+    _expect(y, "y", torch.float32, (T, cfg.latent))
+    if idx is not None:
+        _expect(idx, "idx", torch.int32, (T, cfg.topk))
+    if gate is not None:
+        _expect(gate, "gate", torch.float32, (T, cfg.topk))
+    if gap is not None:
+        _expect(gap, "gap", torch.float32, (T,))
+    if status is not None:
+        _expect(status, "status", torch.int32, (4,))
+    if ws is None:
+        raise ValueError("ws (workspace) is required")
+    c, e = cfg.c(), experts.c()
+    _check("k3moe_layer", lib().k3moe_layer(
+        ctypes.byref(c), _p(h), _p(wr), _p(bias), ctypes.byref(e), _p(x), T, _p(y), _p(idx), _p(gate),
+        _p(gap), _p(status), _p(ws), ws.numel(), _stream(stream)))
+
+
+def k3moe_layer_host(cfg: Cfg, h_host, wr, bias, experts: Experts, x_host, y_host, status, ws,
+                     stream=None) -> None:
+    """The layer with host (ideally pinned) h, x and y; synchronises the stream."""
+    import torch
+    T = h_host.shape[0]
+    _expect(h_host, "h_host", torch.bfloat16, (T, cfg.hidden), cuda=False)
+    _expect(x_host, "x_host", torch.bfloat16, (T, cfg.latent), cuda=False)
+    _expect(y_host, "y_host", torch.float32, (T, cfg.latent), cuda=False)
+    _expect(wr, "wr", torch.bfloat16, (cfg.n_experts, cfg.hidden))
+    c, e = cfg.c(), experts.c()
+    _check("k3moe_layer_host", lib().k3moe_layer_host(
+        ctypes.byref(c), _p(h_host), _p(wr), _p(bias), ctypes.byref(e), _p(x_host), T, _p(y_host),
+        _p(status), _p(ws), ws.numel(), _stream(stream)))
+
+
+def k3moe_matvec_mxfp4(y, x, packed, scales, stream=None) -> None:
+    """y[rows] = W x for one MXFP4 matrix W (packed [rows, in/2], scales [rows, in/32])."""
+    import torch
+    n_in = x.shape[0]
+    rows = packed.shape[0]
+    _expect(x, "x", torch.bfloat16, (n_in,))
+    _expect(packed, "packed", torch.uint8, (rows, n_in // 2))
+    _expect(scales, "scales", torch.uint8, (rows, n_in // 32))
+    _expect(y, "y", torch.float32, (rows,))
+    _check("k3moe_matvec_mxfp4", lib().k3moe_matvec_mxfp4(_p(y), _p(x), _p(packed), _p(scales), n_in,
+                                                          rows, 32, _stream(stream)))
+
+
+def k3moe_stack_link(y, x_out, h_out=None, norm: bool = True, eps: float = 1e-5, stream=None) -> None:
+    import torch
+    T, L = y.shape
+    _expect(y, "y", torch.float32, (T, L))
+    _expect(x_out, "x_out", torch.bfloat16, (T, L))
+    if h_out is not None:
+        _expect(h_out, "h_out", torch.bfloat16, (T, 2 * L))
+    _check("k3moe_stack_link", lib().k3moe_stack_link(_p(y), T, L, 1 if norm else 0, float(eps), _p(x_out),
+                                                      _p(h_out), _stream(stream)))

@@ -1,0 +1,357 @@
+// abi.cu -- the extern "C" entry points of libk3moe.so (declared in include/k3moe.h):
+// argument validation, workspace carving and the launch sequence on the caller's stream.
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+
+#include "launch.h"
+
+namespace k3 {
+
+std::atomic<int64_t> g_launches{0};
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+namespace {
+
+constexpr int32_t kMaxTokens = 1 << 18;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_cfg(const k3moe_cfg* c) {
+  if (!c) return K3MOE_ERR_INVALID;
+  if (c->hidden <= 0 || c->n_experts <= 0 || c->topk <= 0 || c->latent <= 0 || c->inter <= 0)
+    return K3MOE_ERR_INVALID;
+  if (c->topk > c->n_experts) return K3MOE_ERR_INVALID;
+  if (c->renorm != 0 && c->renorm != 1) return K3MOE_ERR_INVALID;
+  if (c->act != K3MOE_ACT_SWIGLU && c->act != K3MOE_ACT_SITU) return K3MOE_ERR_INVALID;
+  if (c->act == K3MOE_ACT_SITU && !(c->situ_b1 > 0.f && c->situ_b2 > 0.f)) return K3MOE_ERR_INVALID;
+  if (c->group != kGroup) return K3MOE_ERR_UNSUPPORTED;
+  if (c->topk > kMaxTopk || c->n_experts > kMaxExperts) return K3MOE_ERR_UNSUPPORTED;
+  if (c->hidden % 8 != 0) return K3MOE_ERR_UNSUPPORTED;
+  if (c->latent % 32 != 0 || c->inter % 32 != 0) return K3MOE_ERR_UNSUPPORTED;
+  if (c->latent > 4096 || c->inter > 4096) return K3MOE_ERR_UNSUPPORTED;
+  return K3MOE_OK;
+}
+
+// Device workspace layout for T tokens (every region 256-byte aligned).
+struct Workspace {
+  float* logits;     // [T][E]
+  int32_t* idx;      // [T][k]
+  float* gate;       // [T][k]
+  float* gap;        // [T]
+  BucketOut b;
+  __half* x16;       // [T][L]
+  int32_t* xexp;     // [T]
+  float* act;        // [T*k][I]
+  float* ybuf;       // [T*k][L]
+  uint16_t* h_stage; // [T][H]  (host variant only)
+  uint16_t* x_stage; // [T][L]
+  float* y_stage;    // [T][L]
+};
+
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  template <typename T>
+  T* take(size_t count) {
+    off = (off + 255) & ~size_t(255);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+size_t carve(const k3moe_cfg* c, int32_t T, void* base, bool host_stage, Workspace* w) {
+  Carver cv{static_cast<uint8_t*>(base)};
+  const size_t E = c->n_experts, K = c->topk, L = c->latent, I = c->inter, H = c->hidden;
+  const size_t Tt = (size_t)std::max(T, 1);
+  const size_t P = Tt * K;
+  Workspace t{};
+  t.logits = cv.take<float>(Tt * E);
+  t.idx = cv.take<int32_t>(P);
+  t.gate = cv.take<float>(P);
+  t.gap = cv.take<float>(Tt);
+  t.b.counts = cv.take<int32_t>(E);
+  t.b.offsets = cv.take<int32_t>(E + 1);
+  t.b.perm = cv.take<int32_t>(P);
+  t.b.active = cv.take<int32_t>(E);
+  t.b.seg_off = cv.take<int32_t>(E);
+  t.b.seg_cnt = cv.take<int32_t>(E);
+  t.b.meta = cv.take<int32_t>(16);
+  t.b.chunk_base = cv.take<int32_t>(E * (size_t)bucket_chunks((int)Tt));
+  t.b.nvalid = cv.take<int32_t>(Tt);
+  t.b.cnt = cv.take<int32_t>(Tt * (L / 4));
+  t.x16 = cv.take<__half>(Tt * L);
+  t.xexp = cv.take<int32_t>(Tt);
+  t.act = cv.take<float>(P * I);
+  t.ybuf = cv.take<float>(P * L);
+  if (host_stage) {
+    t.h_stage = cv.take<uint16_t>(Tt * H);
+    t.x_stage = cv.take<uint16_t>(Tt * L);
+    t.y_stage = cv.take<float>(Tt * L);
+  }
+  if (w) *w = t;
+  return (cv.off + 255) & ~size_t(255);
+}
+
+int check_ws(const k3moe_cfg* c, int32_t T, void* ws, size_t ws_bytes, bool host_stage,
+             Workspace* w) {
+  if (!ws || !aligned(ws, 256)) return K3MOE_ERR_WORKSPACE;
+  if (ws_bytes < carve(c, T, nullptr, host_stage, nullptr)) return K3MOE_ERR_WORKSPACE;
+  carve(c, T, ws, host_stage, w);
+  return K3MOE_OK;
+}
+
+int check_experts(const k3moe_experts* e) {
+  if (!e) return K3MOE_ERR_INVALID;
+  const void* p[6] = {e->w1_packed, e->w1_scale, e->w3_packed, e->w3_scale, e->w2_packed,
+                      e->w2_scale};
+  for (const void* q : p) {
+    if (!q) return K3MOE_ERR_INVALID;
+    if (!aligned(q, 16)) return K3MOE_ERR_ALIGN;
+  }
+  return K3MOE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA; }
+
+// Optional phase events (k3moe_set_phase_events).
+cudaEvent_t g_phase[6] = {};
+bool g_phase_on = false;
+
+// Recorded as "external" so that, under stream capture, each record becomes an event-record
+// node of the graph (timed on every replay) rather than a capture-internal dependency.
+cudaError_t phase(int i, cudaStream_t s) {
+  return g_phase_on ? cudaEventRecordWithFlags(g_phase[i], s, cudaEventRecordExternal)
+                    : cudaSuccess;
+}
+
+#define K3_TRY(expr)                                  \
+  do {                                                \
+    cudaError_t _e = (expr);                          \
+    if (_e != cudaSuccess) return K3MOE_ERR_CUDA;     \
+  } while (0)
+
+// Router launches (logits + top-k) into idx/gate/gap.
+int run_route(const k3moe_cfg* c, const void* h, const void* wr, const float* bias, int32_t T,
+              int32_t* idx, float* gate, float* gap, const Workspace& w, cudaStream_t s) {
+  K3_TRY(launch_router_logits(static_cast<const uint16_t*>(h), static_cast<const uint16_t*>(wr),
+                              T, c->n_experts, c->hidden, w.logits, s, false));
+  K3_TRY(launch_topk(w.logits, bias, T, c->n_experts, c->topk, c->renorm, c->routed_scale, idx,
+                     gate, gap, s, true));
+  return K3MOE_OK;
+}
+
+// The layer (route = true) or the routed-expert sum alone (route = false):
+//   [router logits (+ top-k grid for large T)] -> preparation (top-k for decode-sized T,
+//   bucketing, x in f16, counters) -> GEMM1 (w1, w3, activation) -> GEMM2 (w2, gates, fused
+//   combine).  Decode-sized T takes 4 launches (3 without the router).
+int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
+                 const float* bias, const k3moe_experts* ex, const void* x, int32_t* idx,
+                 float* gate, float* gap, int32_t T, float* y, int32_t* status,
+                 const Workspace& w, cudaStream_t s) {
+  const int E = c->n_experts, K = c->topk, L = c->latent, I = c->inter;
+  ExpertPtrs ep{ex->w1_packed, ex->w1_scale, ex->w3_packed, ex->w3_scale, ex->w2_packed,
+                ex->w2_scale};
+  const bool fused_topk = route && prep_is_fused(T);
+  K3_TRY(phase(0, s));
+  if (route) {
+    K3_TRY(launch_router_logits(static_cast<const uint16_t*>(h), static_cast<const uint16_t*>(wr),
+                                T, E, c->hidden, w.logits, s, false));
+    if (!fused_topk)
+      K3_TRY(launch_topk(w.logits, bias, T, E, K, c->renorm, c->routed_scale, idx, gate, gap, s,
+                         true));
+  }
+  K3_TRY(phase(1, s));
+  PrepArgs p{fused_topk ? w.logits : nullptr, bias, E, K, c->renorm, c->routed_scale, idx, gate,
+             gap, T, L, static_cast<const uint16_t*>(x), w.x16, w.xexp, w.b, y, status};
+  K3_TRY(launch_prep(p, s, route));
+  K3_TRY(phase(2, s));
+  K3_TRY(launch_gemm1(ep, L, I, E, T, K, w.x16, w.xexp, w.b, w.act, c->act, c->situ_b1,
+                      c->situ_b2, status, s, true));
+  K3_TRY(phase(3, s));
+  K3_TRY(launch_gemm2(ep, L, I, E, T, K, w.act, gate, idx, w.b, w.ybuf, w.b.cnt, y, status, s,
+                      true));
+  K3_TRY(phase(4, s));
+  K3_TRY(phase(5, s));
+  return K3MOE_OK;
+}
+
+}  // namespace
+}  // namespace k3
+
+using namespace k3;
+
+extern "C" {
+
+int k3moe_workspace_size(const k3moe_cfg* cfg, int32_t T, size_t* bytes) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (!bytes || T < 0) return K3MOE_ERR_INVALID;
+  if (T > kMaxTokens) return K3MOE_ERR_UNSUPPORTED;
+  *bytes = carve(cfg, T, nullptr, false, nullptr);
+  return K3MOE_OK;
+}
+
+int k3moe_workspace_size_host(const k3moe_cfg* cfg, int32_t T, size_t* bytes) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (!bytes || T < 0) return K3MOE_ERR_INVALID;
+  if (T > kMaxTokens) return K3MOE_ERR_UNSUPPORTED;
+  *bytes = carve(cfg, T, nullptr, true, nullptr);
+  return K3MOE_OK;
+}
+
+int k3moe_route(const k3moe_cfg* cfg, const void* h, const void* wr, const float* bias, int32_t T,
+                int32_t* idx, float* gate, float* gap, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (T < 0) return K3MOE_ERR_INVALID;
+  if (T > kMaxTokens) return K3MOE_ERR_UNSUPPORTED;
+  if (T == 0) return K3MOE_OK;  // nothing to do; empty tensors may carry null pointers
+  if (!h || !wr || !idx || !gate) return K3MOE_ERR_INVALID;
+  if (!aligned(h, 16) || !aligned(wr, 16) || !aligned(idx, 4) || !aligned(gate, 4) ||
+      (bias && !aligned(bias, 4)) || (gap && !aligned(gap, 4)))
+    return K3MOE_ERR_ALIGN;
+  Workspace w;
+  if ((rc = check_ws(cfg, T, ws, ws_bytes, false, &w))) return rc;
+  return run_route(cfg, h, wr, bias, T, idx, gate, gap, w, static_cast<cudaStream_t>(stream));
+}
+
+int k3moe_experts_mxfp4(const k3moe_cfg* cfg, const k3moe_experts* experts, const void* x,
+                        const int32_t* idx, const float* gate, int32_t T, float* y,
+                        int32_t* status, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if ((rc = check_experts(experts))) return rc;
+  if (T < 0) return K3MOE_ERR_INVALID;
+  if (T > kMaxTokens) return K3MOE_ERR_UNSUPPORTED;
+  if (T == 0) return K3MOE_OK;
+  if (!x || !idx || !gate || !y) return K3MOE_ERR_INVALID;
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(idx, 4) || !aligned(gate, 4) ||
+      (status && !aligned(status, 4)))
+    return K3MOE_ERR_ALIGN;
+  Workspace w;
+  if ((rc = check_ws(cfg, T, ws, ws_bytes, false, &w))) return rc;
+  return run_pipeline(cfg, false, nullptr, nullptr, nullptr, experts, x, const_cast<int32_t*>(idx),
+                      const_cast<float*>(gate), nullptr, T, y, status, w,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int k3moe_layer(const k3moe_cfg* cfg, const void* h, const void* wr, const float* bias,
+                const k3moe_experts* experts, const void* x, int32_t T, float* y, int32_t* idx,
+                float* gate, float* gap, int32_t* status, void* ws, size_t ws_bytes,
+                void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if ((rc = check_experts(experts))) return rc;
+  if (T < 0) return K3MOE_ERR_INVALID;
+  if (T > kMaxTokens) return K3MOE_ERR_UNSUPPORTED;
+  if (T == 0) return K3MOE_OK;
+  if (!h || !wr || !x || !y) return K3MOE_ERR_INVALID;
+  if (!aligned(h, 16) || !aligned(wr, 16) || !aligned(x, 16) || !aligned(y, 16) ||
+      (bias && !aligned(bias, 4)) || (idx && !aligned(idx, 4)) || (gate && !aligned(gate, 4)) ||
+      (gap && !aligned(gap, 4)) || (status && !aligned(status, 4)))
+    return K3MOE_ERR_ALIGN;
+  Workspace w;
+  if ((rc = check_ws(cfg, T, ws, ws_bytes, false, &w))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* idx_use = idx ? idx : w.idx;
+  float* gate_use = gate ? gate : w.gate;
+  float* gap_use = gap ? gap : w.gap;
+  return run_pipeline(cfg, true, h, wr, bias, experts, x, idx_use, gate_use, gap_use, T, y, status,
+                      w, s);
+}
+
+int k3moe_layer_host(const k3moe_cfg* cfg, const void* h_host, const void* wr, const float* bias,
+                     const k3moe_experts* experts, const void* x_host, int32_t T, float* y_host,
+                     int32_t* status, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if ((rc = check_experts(experts))) return rc;
+  if (T < 0) return K3MOE_ERR_INVALID;
+  if (T > kMaxTokens) return K3MOE_ERR_UNSUPPORTED;
+  if (T == 0) return K3MOE_OK;
+  if (!h_host || !wr || !x_host || !y_host) return K3MOE_ERR_INVALID;
+  if (!aligned(wr, 16) || (bias && !aligned(bias, 4)) || (status && !aligned(status, 4)))
+    return K3MOE_ERR_ALIGN;
+  Workspace w;
+  if ((rc = check_ws(cfg, T, ws, ws_bytes, true, &w))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t hb = (size_t)T * cfg->hidden * 2, xb = (size_t)T * cfg->latent * 2,
+               yb = (size_t)T * cfg->latent * 4;
+  K3_TRY(cudaMemcpyAsync(w.h_stage, h_host, hb, cudaMemcpyHostToDevice, s));
+  K3_TRY(cudaMemcpyAsync(w.x_stage, x_host, xb, cudaMemcpyHostToDevice, s));
+  if ((rc = run_pipeline(cfg, true, w.h_stage, wr, bias, experts, w.x_stage, w.idx, w.gate, w.gap,
+                         T, w.y_stage, status, w, s)))
+    return rc;
+  K3_TRY(cudaMemcpyAsync(y_host, w.y_stage, yb, cudaMemcpyDeviceToHost, s));
+  K3_TRY(cudaStreamSynchronize(s));
+  return K3MOE_OK;
+}
+
+int k3moe_matvec_mxfp4(float* y, const void* x, const uint8_t* packed, const uint8_t* scales,
+                       int32_t in, int32_t rows, int32_t group, void* stream) {
+  if (!y || !x || !packed || !scales || in <= 0 || rows < 0) return K3MOE_ERR_INVALID;
+  if (group != kGroup || in % 32 != 0) return K3MOE_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(packed, 16) || !aligned(y, 4)) return K3MOE_ERR_ALIGN;
+  if (rows == 0) return K3MOE_OK;
+  return cuda_status(launch_matvec(y, static_cast<const uint16_t*>(x), packed, scales, in, rows,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+int k3moe_stack_link(const float* y, int32_t T, int32_t L, int32_t norm, float eps, void* x_out,
+                     void* h_out, void* stream) {
+  if (T < 0 || L <= 0 || !(eps >= 0.f)) return K3MOE_ERR_INVALID;
+  if (T == 0) return K3MOE_OK;
+  if (!y || !x_out) return K3MOE_ERR_INVALID;
+  if (!aligned(y, 4) || !aligned(x_out, 2) || (h_out && !aligned(h_out, 2))) return K3MOE_ERR_ALIGN;
+  return cuda_status(launch_stack_link(y, T, L, norm, eps, static_cast<uint16_t*>(x_out),
+                                       static_cast<uint16_t*>(h_out),
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+int k3moe_set_phase_events(void* const* events, int32_t n) {
+  if (!events) {
+    g_phase_on = false;
+    return K3MOE_OK;
+  }
+  if (n != 6) return K3MOE_ERR_INVALID;
+  for (int i = 0; i < 6; ++i) {
+    if (!events[i]) return K3MOE_ERR_INVALID;
+    g_phase[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  g_phase_on = true;
+  return K3MOE_OK;
+}
+
+int64_t k3moe_launch_count(void) { return g_launches.load(); }
+
+const char* k3moe_strerror(int status) {
+  switch (status) {
+    case K3MOE_OK: return "ok";
+    case K3MOE_ERR_INVALID: return "invalid argument";
+    case K3MOE_ERR_UNSUPPORTED: return "unsupported shape or configuration";
+    case K3MOE_ERR_ALIGN: return "pointer not aligned";
+    case K3MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case K3MOE_ERR_CUDA: return "CUDA launch or copy failed";
+    case K3MOE_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case K3MOE_ERR_DROPPED: return "expert index out of range (assignment skipped)";
+    default: return "unknown status";
+  }
+}
+
+int32_t k3moe_abi_version(void) { return K3MOE_ABI_VERSION; }
+
+}  // extern "C"

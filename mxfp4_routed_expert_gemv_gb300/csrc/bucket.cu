@@ -1,0 +1,272 @@
+// bucket.cu -- token -> expert bucketing (a counting sort of the T*k assignments) and the
+// per-call preparation of the expert GEMVs.
+//
+// Output: counts[E], offsets[E+1] (exclusive prefix of counts), perm[] = the valid
+// assignment ids a = t*k + j sorted by expert and, within an expert, by token (stable),
+// the list of active experts (count > 0) in ascending order with each one's perm offset
+// and token count, nvalid[t] (valid assignments of token t), zeroed combine counters, y
+// rows zeroed for tokens without a valid assignment, and x in the GEMVs' f16 form.  An
+// expert index outside [0, E) is skipped and counted in status[0] (the README's "counted,
+// never silent" expert-drop rule, Part II section 9).
+//
+// Decode-sized batches (T <= 32) take one CTA for everything, optionally including the
+// router's top-k, so the whole preparation is one launch.
+#include "launch.h"
+#include "topk.cuh"
+
+namespace k3 {
+namespace {
+
+constexpr int kChunkTokens = 16;  // tokens per block in the multi-block path
+constexpr int kSmallTokens = 32;
+
+// Exclusive scan of one int per thread over a block of exactly 1024 threads; *total gets
+// the block sum.
+__device__ int block_exclusive_scan_1024(int v, int* total) {
+  __shared__ int warp_tot[32];
+  __shared__ int tot;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = warp_tot[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    warp_tot[lane] = wi - w;  // exclusive prefix of the warp totals
+    if (lane == 31) tot = wi;
+  }
+  __syncthreads();
+  const int excl = warp_tot[warp] + incl - v;
+  *total = tot;
+  __syncthreads();  // warp_tot and tot are reused by the next call
+  return excl;
+}
+
+// Writes offsets/counts/active lists from per-expert counts c (thread e holds c).
+__device__ void publish_counts(int c, int E, const BucketOut& o, int* excl_out) {
+  int total;
+  const int excl = block_exclusive_scan_1024(c, &total);
+  const int e = threadIdx.x;
+  if (e < E) {
+    o.offsets[e] = excl;
+    o.counts[e] = c;
+  }
+  if (e == 0) o.offsets[E] = total;
+  const int flag = (e < E && c > 0) ? 1 : 0;
+  int nact;
+  const int pos = block_exclusive_scan_1024(flag, &nact);
+  if (flag) {
+    o.active[pos] = e;
+    o.seg_off[pos] = excl;
+    o.seg_cnt[pos] = c;
+  }
+  if (e == 0) {
+    o.meta[0] = nact;
+    o.meta[1] = total;
+  }
+  *excl_out = excl;
+}
+
+// One warp: x row (bf16) -> f16 scaled by 2^-e with the largest magnitude in [2^14, 2^15).
+// L % 32 == 0; 16-byte vector accesses when L % 256 == 0.
+__device__ void prep_x_warp(const uint16_t* xr, int L, __half* out, int32_t* xexp, int lane) {
+  float m = 0.f;
+  const bool vec = (L & 255) == 0;
+  if (vec) {
+    for (int c = lane * 8; c < L; c += 256) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + c));
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16lo(v.x)), fabsf(bf16hi(v.x))), fmaxf(fabsf(bf16lo(v.y)), fabsf(bf16hi(v.y)))));
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16lo(v.z)), fabsf(bf16hi(v.z))), fmaxf(fabsf(bf16lo(v.w)), fabsf(bf16hi(v.w)))));
+    }
+  } else {
+    for (int c = lane; c < L; c += 32) m = fmaxf(m, fabsf(__uint_as_float((uint32_t)xr[c] << 16)));
+  }
+  m = warp_max(m);
+  const int e = f16_exponent_for(m);
+  const Pow2Scale sc(e);
+  if (vec) {
+    for (int c = lane * 8; c < L; c += 256) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + c));
+      uint4 o;
+      o.x = pack_half2(sc(bf16lo(v.x)), sc(bf16hi(v.x)));
+      o.y = pack_half2(sc(bf16lo(v.y)), sc(bf16hi(v.y)));
+      o.z = pack_half2(sc(bf16lo(v.z)), sc(bf16hi(v.z)));
+      o.w = pack_half2(sc(bf16lo(v.w)), sc(bf16hi(v.w)));
+      *reinterpret_cast<uint4*>(out + c) = o;
+    }
+  } else {
+    for (int c = lane; c < L; c += 32) out[c] = __float2half_rn(sc(__uint_as_float((uint32_t)xr[c] << 16)));
+  }
+  if (lane == 0) *xexp = e;
+}
+
+// Per token: count valid assignments; zero y when there is none.
+__device__ void token_valid_warp(const int32_t* idx_t, int k, int E, int L, int32_t* nvalid_t,
+                                 float* y_t, int lane) {
+  int v = 0;
+  if (lane < k) {
+    const int e = idx_t[lane];
+    v = (e >= 0 && e < E) ? 1 : 0;
+  }
+  const int n = __popc(__ballot_sync(0xffffffffu, v));
+  if (lane == 0) *nvalid_t = n;
+  if (n == 0)
+    for (int c = lane; c < L; c += 32) y_t[c] = 0.f;
+}
+
+// Single block of 1024 threads, T <= kSmallTokens: [top-k], count, scan, stable scatter
+// token by token (one warp, lane j handles slot j), x prep, counters.
+__global__ void __launch_bounds__(1024) k_prep_small(PrepArgs p) {
+  pdl_wait();
+  pdl_launch();
+  __shared__ int cnt[kMaxExperts];
+  __shared__ int cur[kMaxExperts];
+  __shared__ uint64_t keys[1024];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = p.T, k = p.k, E = p.E;
+  if (p.logits) {
+    if (T == 1)
+      topk_block_sort(p.logits, p.bias, E, k, p.renorm, p.routed_scale, p.idx, p.gate, p.gap, keys);
+    else if (warp < T)
+      topk_warp(p.logits + (size_t)warp * E, p.bias, E, k, p.renorm, p.routed_scale,
+                p.idx + (size_t)warp * k, p.gate + (size_t)warp * k,
+                p.gap ? p.gap + warp : nullptr, lane);
+  }
+  cnt[tid] = 0;
+  __syncthreads();  // top-k results (global, this block) are visible from here on
+  const int P = T * k;
+  int dropped = 0;
+  for (int a = tid; a < P; a += blockDim.x) {
+    const int e = p.idx[a];
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    else ++dropped;
+  }
+  __syncthreads();
+  const int c = (tid < E) ? cnt[tid] : 0;
+  int excl;
+  publish_counts(c, E, p.b, &excl);
+  if (tid < E) cur[tid] = excl;
+  int dtot;
+  block_exclusive_scan_1024(dropped, &dtot);
+  if (tid == 0 && dtot > 0 && p.status) atomicAdd(p.status + kStatDropped, dtot);
+  __syncthreads();
+  if (warp == 0) {
+    for (int t = 0; t < T; ++t) {
+      if (lane < k) {
+        const int a = t * k + lane;
+        const int e = p.idx[a];
+        if (e >= 0 && e < E) p.b.perm[atomicAdd(&cur[e], 1)] = a;
+      }
+      __syncwarp();
+    }
+  } else {
+    for (int t = warp - 1; t < T; t += 31) {
+      prep_x_warp(p.x + (size_t)t * p.L, p.L, p.x16 + (size_t)t * p.L, p.xexp + t, lane);
+      token_valid_warp(p.idx + (size_t)t * k, k, E, p.L, p.b.nvalid + t, p.y + (size_t)t * p.L, lane);
+    }
+  }
+  const int ncnt = T * (p.L >> 2);
+  for (int i = tid; i < ncnt; i += blockDim.x) p.b.cnt[i] = 0;
+}
+
+// Multi-block path, pass 1: per-chunk histograms stored transposed [E][nchunks]; also the
+// chunk's tokens' nvalid, counters and empty-token y rows.
+__global__ void __launch_bounds__(256) k_bucket_count(PrepArgs p, int nchunks) {
+  pdl_wait();
+  pdl_launch();
+  __shared__ int hist[kMaxExperts];
+  const int T = p.T, k = p.k, E = p.E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int c = blockIdx.x;
+  const int t0 = c * kChunkTokens, t1 = min(T, t0 + kChunkTokens);
+  int dropped = 0;
+  for (int a = t0 * k + threadIdx.x; a < t1 * k; a += blockDim.x) {
+    const int e = p.idx[a];
+    if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    else ++dropped;
+  }
+  if (dropped && p.status) atomicAdd(p.status + kStatDropped, dropped);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t = t0 + warp; t < t1; t += blockDim.x >> 5)
+    token_valid_warp(p.idx + (size_t)t * k, k, E, p.L, p.b.nvalid + t, p.y + (size_t)t * p.L, lane);
+  const int nq = p.L >> 2;
+  for (int i = t0 * nq + threadIdx.x; i < t1 * nq; i += blockDim.x) p.b.cnt[i] = 0;
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) p.b.chunk_base[(size_t)e * nchunks + c] = hist[e];
+}
+
+// Pass 2 (one block): per-expert running sums over chunks, the global scan, and the
+// per-chunk base positions.
+__global__ void __launch_bounds__(1024) k_bucket_scan(int E, int nchunks, BucketOut o) {
+  pdl_wait();
+  pdl_launch();
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E) {
+    int32_t* cb = o.chunk_base + (size_t)e * nchunks;
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = cb[c];
+      cb[c] = run;
+      run += v;
+    }
+  }
+  int excl;
+  publish_counts(e < E ? run : 0, E, o, &excl);
+  if (e < E) {
+    int32_t* cb = o.chunk_base + (size_t)e * nchunks;
+    for (int c = 0; c < nchunks; ++c) cb[c] += excl;
+  }
+}
+
+// Pass 3: stable scatter of one chunk, token by token (one warp per block).
+__global__ void __launch_bounds__(32) k_bucket_scatter(const int32_t* __restrict__ idx, int T,
+                                                       int k, int E, int nchunks, BucketOut o) {
+  pdl_wait();
+  pdl_launch();
+  __shared__ int cur[kMaxExperts];
+  const int c = blockIdx.x, lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) cur[e] = o.chunk_base[(size_t)e * nchunks + c];
+  __syncwarp();
+  const int t1 = min(T, (c + 1) * kChunkTokens);
+  for (int t = c * kChunkTokens; t < t1; ++t) {
+    if (lane < k) {
+      const int a = t * k + lane;
+      const int e = idx[a];
+      if (e >= 0 && e < E) o.perm[atomicAdd(&cur[e], 1)] = a;
+    }
+    __syncwarp();
+  }
+}
+
+}  // namespace
+
+int bucket_chunks(int T) { return (T + kChunkTokens - 1) / kChunkTokens; }
+
+bool prep_is_fused(int T) { return T <= kSmallTokens; }
+
+cudaError_t launch_prep(const PrepArgs& p, cudaStream_t s, bool pdl) {
+  if (prep_is_fused(p.T)) return launch_kernel(k_prep_small, dim3(1), dim3(1024), 0, s, pdl, p);
+  // large batches: the top-k (if requested) runs as its own grid before this point
+  const int nch = bucket_chunks(p.T);
+  cudaError_t err = launch_kernel(k_bucket_count, dim3(nch), dim3(256), 0, s, pdl, p, nch);
+  if (err != cudaSuccess) return err;
+  err = launch_kernel(k_bucket_scan, dim3(1), dim3(1024), 0, s, true, p.E, nch, p.b);
+  if (err != cudaSuccess) return err;
+  err = launch_kernel(k_bucket_scatter, dim3(nch), dim3(32), 0, s, true,
+                      static_cast<const int32_t*>(p.idx), p.T, p.k, p.E, nch, p.b);
+  if (err != cudaSuccess) return err;
+  return launch_prep_x(p.x, p.T, p.L, p.x16, p.xexp, s, true);
+}
+
+}  // namespace k3

@@ -1,0 +1,102 @@
+// launch.h -- internal launch helpers and the launchers each kernel file exports.
+#pragma once
+
+#include <atomic>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace k3 {
+
+// Kernels launched through the library since load (host-side count).
+extern std::atomic<int64_t> g_launches;
+
+// Launch `kern` with an optional programmatic-dependent-launch attribute, so that the
+// kernel's CTAs may be scheduled while the previous kernel on the stream drains; every
+// kernel here calls griddepcontrol.wait before it reads what earlier kernels wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// Multiprocessor count of the current device (cached per device).
+int sm_count();
+
+// router.cu
+cudaError_t launch_router_logits(const uint16_t* h, const uint16_t* wr, int T, int E, int H,
+                                 float* logits, cudaStream_t s, bool pdl);
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,
+                        float routed_scale, int32_t* idx, float* gate, float* gap,
+                        cudaStream_t s, bool pdl);
+
+// bucket.cu
+struct BucketOut {
+  int32_t* counts;      // [E]
+  int32_t* offsets;     // [E+1]
+  int32_t* perm;        // [T*k]  assignment ids sorted by (expert, token)
+  int32_t* active;      // [E]    expert ids with at least one token, ascending
+  int32_t* seg_off;     // [E]    perm offset of each active expert's tokens
+  int32_t* seg_cnt;     // [E]    number of tokens of each active expert
+  int32_t* meta;        // [16]   [0] active experts, [1] valid assignments
+  int32_t* chunk_base;  // [E][nchunks] scratch of the multi-block path
+  int32_t* nvalid;      // [T]    valid assignments per token
+  int32_t* cnt;         // [T][L/4] combine counters (zeroed by the preparation)
+};
+
+// Everything the per-call preparation touches.  logits == nullptr: idx/gate come from the
+// caller (no top-k); otherwise the fused decode-size kernel also runs the router's top-k.
+struct PrepArgs {
+  const float* logits;
+  const float* bias;
+  int E, k, renorm;
+  float routed_scale;
+  int32_t* idx;
+  float* gate;
+  float* gap;
+  int T, L;
+  const uint16_t* x;
+  __half* x16;
+  int32_t* xexp;
+  BucketOut b;
+  float* y;
+  int32_t* status;
+};
+int bucket_chunks(int T);
+bool prep_is_fused(int T);
+cudaError_t launch_prep(const PrepArgs& p, cudaStream_t s, bool pdl);
+
+// gemv.cu
+struct ExpertPtrs {
+  const uint8_t *w1p, *w1s, *w3p, *w3s, *w2p, *w2s;
+};
+cudaError_t launch_prep_x(const uint16_t* x, int T, int L, __half* x16, int32_t* xexp,
+                          cudaStream_t s, bool pdl);
+cudaError_t launch_gemm1(const ExpertPtrs& w, int L, int I, int E, int T, int k,
+                         const __half* x16, const int32_t* xexp, const BucketOut& b,
+                         float* act, int act_kind, float b1, float b2, int32_t* status,
+                         cudaStream_t s, bool pdl);
+cudaError_t launch_gemm2(const ExpertPtrs& w, int L, int I, int E, int T, int k,
+                         const float* act, const float* gate, const int32_t* idx,
+                         const BucketOut& b, float* ybuf, int32_t* cnt, float* y,
+                         int32_t* status, cudaStream_t s, bool pdl);
+cudaError_t launch_matvec(float* y, const uint16_t* x, const uint8_t* packed,
+                          const uint8_t* scales, int in, int rows, cudaStream_t s);
+
+// stack.cu
+cudaError_t launch_stack_link(const float* y, int T, int L, int norm, float eps, uint16_t* x_out,
+                              uint16_t* h_out, cudaStream_t s);
+
+}  // namespace k3

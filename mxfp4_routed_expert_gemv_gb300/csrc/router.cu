@@ -1,0 +1,112 @@
+// router.cu -- router GEMV and the per-token top-k with gates.
+//
+// README "kimi-k3-in-c", Part II section 9 "Picking 16 experts of 896": the unbiased score
+// is sigmoid(h . Wr[e]); the selection score adds the correction bias; the top-k is taken
+// by repeated arg-max where a tie goes to the lower expert index; the combine weights come
+// from the unbiased scores, renormalised over the chosen k and multiplied by routed_scale.
+#include "launch.h"
+#include "topk.cuh"
+
+namespace k3 {
+namespace {
+
+constexpr int kRowsPerCta = 2;    // router rows per CTA
+constexpr int kQuarters = 4;      // warps per row, each a quarter of the hidden width
+constexpr int kVecPerLane = 8;    // 16-byte pieces a lane keeps in flight per batch
+
+// logits[t][e] = sum_i h[t][i] * wr[e][i].  A CTA holds 2 rows; each row is split into 4
+// quarters, one warp each, and every lane issues all its 16-byte loads of a batch before
+// using them, so a row's bytes are in flight at once.  Products of bf16 values are exact;
+// each fused add rounds once (fp32).  The 4 quarter sums are added in a fixed order.
+template <int TT>
+__global__ void __launch_bounds__(256) k_router_logits(const uint16_t* __restrict__ h,
+                                                       const uint16_t* __restrict__ wr, int T,
+                                                       int E, int H,
+                                                       float* __restrict__ logits) {
+  pdl_wait();
+  pdl_launch();
+  __shared__ float part[8][TT];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kRowsPerCta + (warp >> 2);
+  const int q = warp & 3;
+  const int t0 = blockIdx.y * TT;
+  const int nvec = H >> 3;
+  const int qn = (nvec + kQuarters - 1) / kQuarters;
+  const int qb = q * qn, qe = min(nvec, qb + qn);
+  float a0[TT], a1[TT];
+#pragma unroll
+  for (int tt = 0; tt < TT; ++tt) a0[tt] = a1[tt] = 0.f;
+  if (e < E) {
+    const uint4* wrow = reinterpret_cast<const uint4*>(wr + (size_t)e * H);
+    for (int base = qb; base < qe; base += 32 * kVecPerLane) {
+      uint4 wv[kVecPerLane];
+#pragma unroll
+      for (int i = 0; i < kVecPerLane; ++i) {
+        const int c = base + lane + 32 * i;
+        wv[i] = (c < qe) ? ldg_stream(wrow + c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int tt = 0; tt < TT; ++tt) {
+        if (t0 + tt >= T) break;
+        const uint4* hrow = reinterpret_cast<const uint4*>(h + (size_t)(t0 + tt) * H);
+#pragma unroll
+        for (int i = 0; i < kVecPerLane; ++i) {
+          const int c = base + lane + 32 * i;
+          if (c < qe) {
+            const uint4 v = __ldg(hrow + c);
+            fma_bf16x2(wv[i].x, v.x, a0[tt], a1[tt]);
+            fma_bf16x2(wv[i].y, v.y, a0[tt], a1[tt]);
+            fma_bf16x2(wv[i].z, v.z, a0[tt], a1[tt]);
+            fma_bf16x2(wv[i].w, v.w, a0[tt], a1[tt]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int tt = 0; tt < TT; ++tt) {
+    const float s = warp_sum(a0[tt] + a1[tt]);
+    if (lane == 0) part[warp][tt] = s;
+  }
+  __syncthreads();
+  if (q == 0 && e < E && lane < TT && t0 + lane < T) {
+    const int w0 = warp;  // warps w0..w0+3 hold this row's quarters
+    const float s = (part[w0][lane] + part[w0 + 1][lane]) + (part[w0 + 2][lane] + part[w0 + 3][lane]);
+    logits[(size_t)(t0 + lane) * E + e] = s;
+  }
+}
+
+__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits,
+                                              const float* __restrict__ bias, int T, int E,
+                                              int k, int renorm, float routed_scale,
+                                              int32_t* __restrict__ idx,
+                                              float* __restrict__ gate,
+                                              float* __restrict__ gap) {
+  pdl_wait();
+  pdl_launch();
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  topk_warp(logits + (size_t)t * E, bias, E, k, renorm, routed_scale, idx + (size_t)t * k,
+            gate + (size_t)t * k, gap ? gap + t : nullptr, threadIdx.x & 31);
+}
+
+}  // namespace
+
+cudaError_t launch_router_logits(const uint16_t* h, const uint16_t* wr, int T, int E, int H,
+                                 float* logits, cudaStream_t s, bool pdl) {
+  const unsigned gx = (E + kRowsPerCta - 1) / kRowsPerCta;
+  if (T <= 2)
+    return launch_kernel(k_router_logits<1>, dim3(gx, T), dim3(256), 0, s, pdl, h, wr, T, E, H,
+                         logits);
+  return launch_kernel(k_router_logits<4>, dim3(gx, (T + 3) / 4), dim3(256), 0, s, pdl, h, wr, T,
+                       E, H, logits);
+}
+
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,
+                        float routed_scale, int32_t* idx, float* gate, float* gap,
+                        cudaStream_t s, bool pdl) {
+  return launch_kernel(k_topk, dim3((T + 7) / 8), dim3(256), 0, s, pdl, logits, bias, T, E, k,
+                       renorm, routed_scale, idx, gate, gap);
+}
+
+}  // namespace k3

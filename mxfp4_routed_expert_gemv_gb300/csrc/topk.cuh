@@ -1,0 +1,143 @@
+// topk.cuh -- one warp's top-k with gates for one token (README "kimi-k3-in-c", Part II
+// section 9 "Picking 16 experts of 896").  Shared by the router's top-k kernel and the
+// fused decode-size preparation kernel.
+#pragma once
+
+#include "common.cuh"
+
+namespace k3 {
+
+__device__ __forceinline__ float sigmoid_f32(float z) { return 1.0f / (1.0f + expf(-z)); }
+
+// Lane l holds the selection scores (sigmoid(logit) + bias) of experts l, l+32, ... in
+// registers (E <= 1024).  Each round finds the lane-local best among untaken experts,
+// visited in increasing index order with a strict '>' (the lowest index of equal scores),
+// then a warp arg-max where a larger score wins and equal scores go to the lower index.
+// One extra round gives the best unchosen score for the gap.  NaN scores count as -inf.
+// Gates: the unbiased scores of the chosen experts, renormalised by their sum when renorm
+// is set and the sum is positive, times routed_scale.
+__device__ __forceinline__ void topk_warp(const float* lt, const float* bias, int E, int k,
+                                          int renorm, float routed_scale, int32_t* idx,
+                                          float* gate, float* gap, int lane) {
+  float ch[32];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int m = 0; m < 32; ++m) {
+    const int e = lane + 32 * m;
+    float v = -INFINITY;
+    if (e < E) {
+      v = sigmoid_f32(lt[e]) + (bias ? bias[e] : 0.0f);
+      if (isnan(v)) v = -INFINITY;
+    } else {
+      taken |= 1u << m;  // not an expert
+    }
+    ch[m] = v;
+  }
+  int my_e = -1;
+  float last_v = 0.f, next_v = -INFINITY;
+  const int rounds = (k < E) ? k + 1 : k;
+  for (int j = 0; j < rounds; ++j) {
+    float bv = -INFINITY;
+    int be = INT_MAX;
+#pragma unroll
+    for (int m = 0; m < 32; ++m) {
+      if (!((taken >> m) & 1u) && (be == INT_MAX || ch[m] > bv)) {
+        bv = ch[m];
+        be = lane + 32 * m;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if (j < k) {
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (lane == j) my_e = be;
+      last_v = bv;
+    } else {
+      next_v = bv;
+    }
+  }
+  const float s = (lane < k) ? sigmoid_f32(lt[my_e]) : 0.f;  // unbiased score of choice j
+  const float sum = warp_sum(s);
+  float g = s;
+  if (renorm && sum > 0.f) g = s / sum;
+  g *= routed_scale;
+  if (lane < k) {
+    idx[lane] = my_e;
+    gate[lane] = g;
+  }
+  if (gap && lane == 0) *gap = (k < E) ? (last_v - next_v) : INFINITY;
+}
+
+// Order-preserving map of a float onto uint32 (NaN and -0 normalised first).
+__device__ __forceinline__ uint32_t ordered_bits(float v) {
+  if (isnan(v)) v = -INFINITY;
+  v += 0.0f;  // -0 -> +0
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float from_ordered_bits(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
+// The same top-k for one token with a whole block of exactly 1024 threads (E <= 1024):
+// keys (descending selection score, then ascending expert index) are sorted by a bitonic
+// network in shared memory; the first k keys are the choice, key k gives the gap.  The
+// order and the tie rule are those of topk_warp.
+__device__ __forceinline__ void topk_block_sort(const float* lt, const float* bias, int E, int k,
+                                                int renorm, float routed_scale, int32_t* idx,
+                                                float* gate, float* gap, uint64_t* keys) {
+  const int tid = threadIdx.x;
+  uint64_t key = ~0ull;
+  if (tid < E) {
+    const float v = sigmoid_f32(lt[tid]) + (bias ? bias[tid] : 0.0f);
+    key = ((uint64_t)(~ordered_bits(v)) << 32) | (uint32_t)tid;
+  }
+  keys[tid] = key;
+  __syncthreads();
+  for (int size = 2; size <= 1024; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const int j = tid ^ stride;
+      if (j > tid) {
+        const uint64_t a = keys[tid], b = keys[j];
+        const bool asc = (tid & size) == 0;
+        if ((a > b) == asc) {
+          keys[tid] = b;
+          keys[j] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (tid < 32) {
+    const int lane = tid;
+    int e = -1;
+    float s = 0.f;
+    if (lane < k) {
+      e = (int)(uint32_t)(keys[lane] & 0xffffffffu);
+      s = sigmoid_f32(lt[e]);  // the unbiased score of choice j
+    }
+    const float sum = warp_sum(s);
+    float g = s;
+    if (renorm && sum > 0.f) g = s / sum;
+    g *= routed_scale;
+    if (lane < k) {
+      idx[lane] = e;
+      gate[lane] = g;
+    }
+    if (gap && lane == 0)
+      *gap = (k < E) ? from_ordered_bits(~(uint32_t)(keys[k - 1] >> 32)) -
+                           from_ordered_bits(~(uint32_t)(keys[k] >> 32))
+                     : INFINITY;
+  }
+  __syncthreads();
+}
+
+}  // namespace k3

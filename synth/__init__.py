@@ -193,14 +193,24 @@ def expert_shapes(w: Workload):
 _TID = {"w1p": W1P, "w1s": W1S, "w3p": W3P, "w3s": W3S, "w2p": W2P, "w2s": W2S}
 
 
-def expert_tensor(w: Workload, layer: int, expert: int, name: str) -> np.ndarray:
-    """One tensor of one expert, host twin of the device generator."""
+def expert_tensor_numpy(w: Workload, layer: int, expert: int, name: str) -> np.ndarray:
+    """One tensor of one expert from the numpy statement of the generator (slow)."""
     shape = expert_shapes(w)[name]
     n = shape[0] * shape[1]
     key = stream_key(w.layer_seed(layer), layer, _TID[name], expert)
     if name.endswith("s"):
         return scale_bytes(key, n).reshape(shape)
     return packed_bytes(key, n).reshape(shape)
+
+
+def expert_tensor(w: Workload, layer: int, expert: int, name: str) -> np.ndarray:
+    """One tensor of one expert on the host (compiled host loop; same stream definition
+    as the numpy statement above and the device kernels)."""
+    shape = expert_shapes(w)[name]
+    out = np.empty(shape, dtype=np.uint8)
+    _dev_lib().synth_host_fill_expert(out.ctypes.data, expert, out.size, w.layer_seed(layer), layer,
+                                      _TID[name], 1 if name.endswith("s") else 0, SCALE_LO, SCALE_SPAN)
+    return out
 
 
 def expert_host(w: Workload, layer: int, expert: int) -> Dict[str, np.ndarray]:
@@ -222,6 +232,9 @@ def _dev_lib():
         L.synth_fill_expert_tensor.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                                ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+        L.synth_host_fill_expert.restype = None
+        L.synth_host_fill_expert.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         _dev = L
     return _dev
 

@@ -85,3 +85,23 @@ extern "C" uint64_t synth_host_word(uint64_t seed, int layer, int tensor, int64_
   const uint64_t key = stream_key(seed, (uint64_t)layer, (uint64_t)tensor, (uint64_t)expert);
   return mix64(key + (uint64_t)(i + 1) * kGamma);
 }
+
+// Host fill of one expert's tensor (the same stream definition as the device kernels),
+// for the test side, which needs only the experts a routing touches.
+extern "C" void synth_host_fill_expert(uint8_t* dst, int64_t expert, int64_t bytes_per_expert,
+                                       uint64_t seed, int layer, int tensor, int is_scale, int lo,
+                                       int span) {
+  const uint64_t key = stream_key(seed, (uint64_t)layer, (uint64_t)tensor, (uint64_t)expert);
+  if (is_scale) {
+    for (int64_t b = 0; b < bytes_per_expert; ++b) {
+      const uint64_t v = mix64(key + (uint64_t)(b + 1) * kGamma);
+      dst[b] = (uint8_t)(lo + (uint32_t)(((v >> 32) * (uint64_t)span) >> 32));
+    }
+  } else {
+    for (int64_t w = 0; w * 8 < bytes_per_expert; ++w) {
+      const uint64_t v = mix64(key + (uint64_t)(w + 1) * kGamma);
+      const int64_t nb = (bytes_per_expert - w * 8) < 8 ? (bytes_per_expert - w * 8) : 8;
+      for (int b = 0; b < nb; ++b) dst[w * 8 + b] = (uint8_t)(v >> (8 * b));
+    }
+  }
+}

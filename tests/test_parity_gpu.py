@@ -1,0 +1,194 @@
+"""Layer parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small shapes (the oracle finishes in well under a second) cover several tiles and ragged
+tails, both bucketing paths, k == E, SiTU, NaN-scale groups, dropped and duplicate
+indices and T == 0.  The Kimi-K3 workloads run at full size in the launch configuration
+the benchmark times; the oracle checks every index it computes and y on sampled tokens.
+"""
+import gc
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from _parity import (DeviceLayer, compare_routing, compare_y, gpu_cfg, oracle_cfg, oracle_table,
+                     reference_routing_for_gpu, to_dev_bf16)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _k3():
+    import mxfp4_routed_expert_gemv_gb300 as k3
+    return k3
+
+
+def _check_layer(w, dl, rows=None, act=0, layer=0):
+    """Run the GPU layer on all tokens; check routing on `rows` (default: all) and y."""
+    y, idx, gate, gap, status = dl.run(act=act)
+    T = dl.h.shape[0]
+    rows = np.arange(T) if rows is None else np.asarray(rows)
+    ocfg = oracle_cfg(w, act)
+    r = oracle.route(ocfg, dl.li.h[rows], dl.li.wr, dl.li.bias)
+    local = np.arange(len(rows))
+    rep = compare_routing(ocfg, idx[rows], gate[rows], r, local)
+    ridx, rgate = reference_routing_for_gpu(ocfg, idx[rows], r, local)
+    table = oracle_table(w, layer, ridx.reshape(-1))
+    y_ref = oracle.experts(ocfg, table, dl.li.x[rows], ridx, rgate)
+    yr = compare_y(y[rows], y_ref)
+    assert status[0] == 0 and status[1] == 0
+    np.testing.assert_allclose(gap[rows], r.gap, rtol=1e-3, atol=1e-5)
+    return rep, yr
+
+
+SMALL = [
+    synth.small_workload(T=3, E=12, k=4, latent=256, inter=192, hidden=512),
+    synth.small_workload(T=7, E=33, k=5, latent=544, inter=160, hidden=264, seed=11),
+    synth.small_workload(T=1, E=5, k=5, latent=128, inter=96, hidden=128, seed=12),
+    synth.small_workload(T=37, E=100, k=8, latent=1024, inter=512, hidden=1024, seed=13),
+    synth.small_workload(T=300, E=64, k=16, latent=512, inter=256, hidden=256, seed=14),
+    synth.small_workload(T=2, E=1024, k=32, latent=64, inter=64, hidden=64, seed=15),
+    synth.small_workload(T=5, E=20, k=3, latent=4096, inter=4096, hidden=512, bias="none", seed=16),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_small_layer_parity(w):
+    dl = DeviceLayer(w)
+    _check_layer(w, dl)
+
+
+def test_small_layer_situ():
+    w = synth.small_workload(T=9, E=16, k=4, latent=320, inter=224, hidden=256, seed=21)
+    dl = DeviceLayer(w)
+    _check_layer(w, dl, act=1)
+
+
+def test_nan_scale_and_zero_nibble_groups():
+    """Scale byte 255 silences its group; nibbles 0 and 8 are +-0.  Planted in both the
+    device experts and the oracle's copies."""
+    w = synth.small_workload(T=4, E=6, k=3, latent=256, inter=128, hidden=128, seed=22)
+    k3 = _k3()
+    d = synth.experts_device(w, 0)
+    d["w1s"][:, :, 2] = 255
+    d["w2s"][1, 5:40, :] = 255
+    d["w3p"][2, :, 3:9] = 0x80
+    dl = DeviceLayer(w, experts=k3.Experts.from_dict(d))
+    y, idx, gate, gap, status = dl.run()
+    ocfg = oracle_cfg(w)
+    r = oracle.route(ocfg, dl.li.h, dl.li.wr, dl.li.bias)
+    compare_routing(ocfg, idx, gate, r, np.arange(w.T))
+    table = {e: oracle.ExpertBytes(*(d[n][e].cpu().numpy() for n in synth.TENSOR_SHAPES)) for e in range(w.E)}
+    compare_y(y, oracle.experts(ocfg, table, dl.li.x, r.idx, r.gate))
+
+
+def test_experts_entry_drops_and_duplicates():
+    """Out-of-range indices are skipped and counted; a duplicated expert counts twice."""
+    k3 = _k3()
+    w = synth.small_workload(T=4, E=10, k=4, latent=256, inter=128, hidden=128, seed=23)
+    d = synth.experts_device(w, 0)
+    ex = k3.Experts.from_dict(d)
+    li = synth.layer_inputs(w)
+    idx = np.array([[1, 2, 3, 4], [-1, 5, 5, 9], [10, 0, 7, 2], [3, 3, 3, 3]], dtype=np.int32)
+    gate = np.random.default_rng(0).uniform(0.1, 1.0, size=idx.shape).astype(np.float32)
+    cfg = gpu_cfg(w)
+    ws = k3.workspace(cfg, w.T)
+    y = torch.empty((w.T, w.latent), dtype=torch.float32, device="cuda")
+    st = torch.zeros(4, dtype=torch.int32, device="cuda")
+    k3.k3moe_experts_mxfp4(cfg, ex, to_dev_bf16(li.x), torch.from_numpy(idx).cuda(), torch.from_numpy(gate).cuda(),
+                           y, st, ws)
+    torch.cuda.synchronize()
+    assert st.cpu().numpy()[0] == 2
+    valid = (idx >= 0) & (idx < w.E)
+    ridx = np.where(valid, idx, 0).astype(np.int32)
+    rgate = np.where(valid, gate, 0.0).astype(np.float64)
+    table = oracle_table(w, 0, range(w.E))
+    compare_y(y.cpu().numpy(), oracle.experts(oracle_cfg(w), table, li.x, ridx, rgate))
+
+
+def test_zero_tokens_and_bad_arguments():
+    k3 = _k3()
+    w = synth.small_workload(T=2, E=8, k=2, latent=64, inter=64, hidden=64, seed=24)
+    dl = DeviceLayer(w)
+    cfg = gpu_cfg(w)
+    ws = k3.workspace(cfg, 0)
+    e = torch.empty((0, w.latent), dtype=torch.float32, device="cuda")
+    k3.k3moe_layer(cfg, dl.h[:0], dl.wr, dl.bias, dl.experts, dl.x[:0], e, ws=ws)
+    with pytest.raises(k3.K3moeError) as ei:
+        k3.k3moe_layer(cfg, dl.h, dl.wr, dl.bias, dl.experts, dl.x,
+                       torch.empty((2, w.latent), dtype=torch.float32, device="cuda"), ws=ws[:16])
+    assert ei.value.status == 4  # workspace too small
+    bad = k3.Cfg(hidden=w.hidden, n_experts=w.E, topk=w.k, latent=w.latent, inter=w.inter, group=16)
+    with pytest.raises(k3.K3moeError) as ei:
+        k3.k3moe_workspace_size(bad, 2)
+    assert ei.value.status == 2
+
+
+def test_repeat_calls_bit_identical():
+    w = synth.small_workload(T=6, E=24, k=6, latent=512, inter=256, hidden=256, seed=25)
+    dl = DeviceLayer(w)
+    a = dl.run()[0]
+    b = dl.run()[0]
+    assert np.array_equal(a, b)
+
+
+def test_batch_of_one_equals_row():
+    w = synth.small_workload(T=8, E=24, k=6, latent=512, inter=256, hidden=256, seed=26)
+    dl = DeviceLayer(w)
+    y = dl.run()[0]
+    for t in (0, 5):
+        y1 = dl.run(h=dl.h[t:t + 1].contiguous(), x=dl.x[t:t + 1].contiguous())[0]
+        assert np.array_equal(y1[0], y[t])
+
+
+# ---- Kimi-K3 workloads at full size ----------------------------------------------------
+
+def _free():
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def test_k3_tiny_4_tokens_64_experts():
+    w = synth.WORKLOADS[0]
+    dl = DeviceLayer(w)
+    rep, yr = _check_layer(w, dl)
+    print(f"\n[tiny] routing {rep}  y {yr}")
+
+
+def test_k3_decode_batch1():
+    w = synth.WORKLOADS[1]
+    dl = DeviceLayer(w)
+    rep, yr = _check_layer(w, dl)
+    print(f"\n[decode T=1] routing {rep}  y {yr}")
+    del dl
+    _free()
+
+
+def test_k3_batched_decode_64_skewed():
+    w = synth.WORKLOADS[2]
+    dl = DeviceLayer(w)
+    y, idx, gate, gap, status = dl.run()
+    ocfg = oracle_cfg(w)
+    r_all = oracle.route(ocfg, dl.li.h, dl.li.wr, dl.li.bias)
+    rep = compare_routing(ocfg, idx, gate, r_all, np.arange(w.T))
+    counts = np.bincount(idx.reshape(-1), minlength=w.E)
+    assert counts[dl.li.hot].min() >= 1
+    rows = np.arange(0, w.T, 4)
+    sub = oracle.Routing(r_all.idx[rows], r_all.gate[rows], r_all.gap[rows], r_all.sc[rows], r_all.ch[rows])
+    ridx, rgate = reference_routing_for_gpu(ocfg, idx[rows], sub, np.arange(len(rows)))
+    y_ref = oracle.experts(ocfg, oracle_table(w, 0, ridx.reshape(-1)), dl.li.x[rows], ridx, rgate)
+    yr = compare_y(y[rows], y_ref)
+    print(f"\n[batched decode T=64] routing {rep}  y {yr}  tokens/expert max {counts.max()}")
+    del dl
+    _free()
+
+
+def test_k3_prefill_4096_sampled():
+    w = synth.WORKLOADS[3]
+    dl = DeviceLayer(w)
+    rows = np.linspace(0, w.T - 1, 24).astype(np.int64)
+    rep, yr = _check_layer(w, dl, rows=rows)
+    print(f"\n[prefill T=4096, 24 sampled tokens] routing {rep}  y {yr}")
+    del dl
+    _free()

@@ -54,3 +54,12 @@ def test_inputs_shapes_and_moments():
     assert synth.layer_inputs(synth.WORKLOADS[0]).bias is None
     # deterministic: same seed, same bytes
     assert np.array_equal(synth.layer_inputs(w).h, li.h)
+
+
+def test_host_fill_matches_numpy_statement():
+    w = synth.small_workload()
+    for name in synth.TENSOR_SHAPES:
+        assert np.array_equal(synth.expert_tensor(w, 0, 3, name), synth.expert_tensor_numpy(w, 0, 3, name)), name
+    w1 = synth.WORKLOADS[4]
+    assert np.array_equal(synth.expert_tensor(w1, 5, 801, "w1s"), synth.expert_tensor_numpy(w1, 5, 801, "w1s"))
+    assert np.array_equal(synth.expert_tensor(w1, 5, 801, "w2p"), synth.expert_tensor_numpy(w1, 5, 801, "w2p"))
