@@ -57,7 +57,8 @@ typedef enum k3moe_status {
     K3MOE_ERR_WORKSPACE = 4,   /* ws is NULL/misaligned or smaller than required         */
     K3MOE_ERR_CUDA = 5,        /* a CUDA launch or copy failed                           */
     K3MOE_ERR_TIMEOUT = 6,     /* (device status only) a bounded wait ran out            */
-    K3MOE_ERR_DROPPED = 7      /* (device status only) expert index out of range         */
+    K3MOE_ERR_DROPPED = 7,     /* (device status only) expert index out of range         */
+    K3MOE_ERR_TOO_LARGE = 8    /* request exceeds the library's static scratch capacity  */
 } k3moe_status;
 
 typedef enum k3moe_act {
@@ -159,6 +160,34 @@ int k3moe_matvec_mxfp4(float *y, const void *x, const uint8_t *packed, const uin
  *   tiled twice along the feature axis. */
 int k3moe_stack_link(const float *y, int32_t T, int32_t L, int32_t norm, float eps,
                      void *x_out, void *h_out, void *stream);
+
+/* k3moe_layer for callers that cannot allocate device memory.  No counterpart on the
+ * pages: this is a deployment variant, not part of the method.
+ *
+ * Some callers cannot call cudaMalloc (or have no way to hand over a workspace): a host
+ * framework whose allocator owns all device memory and forbids raw allocations, a plugin
+ * that runs inside someone else's memory budget, or a latency-critical path where an
+ * allocation could block or fail.  This entry point takes the same inputs and outputs as
+ * k3moe_layer but no workspace: its scratch is one file-scope device array of
+ * K3MOE_STATIC_SCRATCH_BYTES (16 MiB), which every GPU that loads the library holds until
+ * the process exits.  It allocates nothing, on the device or the host.
+ *
+ *   - Capacity: a call whose k3moe_workspace_size(cfg, T) exceeds the array returns
+ *     K3MOE_ERR_TOO_LARGE and enqueues nothing (Kimi K3 shape: up to 38 tokens).
+ *   - Set-up: the first call on a device, with that device current, looks up the array's
+ *     device address (cudaGetSymbolAddress) and caches it; make that first call before any
+ *     stream capture begins.
+ *   - Sharing: all calls on a device share the one array and it keeps the previous call's
+ *     contents.  Every scratch value a call reads is written earlier in the same call (the
+ *     combine counters are zeroed by the call itself), so no clearing is needed between
+ *     calls; but calls that overlap on the GPU (different streams, no ordering between
+ *     them) race on the array and corrupt each other's results.  Order them on one stream.
+ * Arguments, layouts and errors are those of k3moe_layer. */
+#define K3MOE_STATIC_SCRATCH_BYTES (16u << 20)
+int k3moe_layer_static_scratch(const k3moe_cfg *cfg, const void *h, const void *wr,
+                               const float *bias, const k3moe_experts *experts, const void *x,
+                               int32_t T, float *y, int32_t *idx, float *gate, float *gap,
+                               int32_t *status, void *stream);
 
 /* Per-phase timing hook for benchmarks.  events: n (== 6) cudaEvent_t handles (as void*)
  * created by the caller, or NULL to switch the hook off.  While set, every k3moe_layer and

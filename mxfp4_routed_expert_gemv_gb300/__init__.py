@@ -24,14 +24,18 @@ __all__ = [
     "k3moe_workspace_size", "k3moe_workspace_size_host", "k3moe_route", "k3moe_experts_mxfp4",
     "k3moe_layer", "k3moe_layer_host", "k3moe_matvec_mxfp4", "k3moe_stack_link",
     "k3moe_launch_count", "k3moe_strerror", "k3moe_abi_version", "k3moe_set_phase_events",
-    "EXPORTED_SYMBOLS",
+    "k3moe_layer_static_scratch", "STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
     "k3moe_workspace_size", "k3moe_workspace_size_host", "k3moe_route", "k3moe_experts_mxfp4",
     "k3moe_layer", "k3moe_layer_host", "k3moe_matvec_mxfp4", "k3moe_stack_link",
     "k3moe_launch_count", "k3moe_strerror", "k3moe_abi_version", "k3moe_set_phase_events",
+    "k3moe_layer_static_scratch",
 )
+
+# Capacity of the library's file-scope scratch array (K3MOE_STATIC_SCRATCH_BYTES).
+STATIC_SCRATCH_BYTES = 16 << 20
 
 ACT_SWIGLU, ACT_SITU = 0, 1
 
@@ -117,6 +121,7 @@ def lib() -> ctypes.CDLL:
         L.k3moe_experts_mxfp4.argtypes = [pc, pe, vp, vp, vp, i32, vp, vp, vp, sz, vp]
         L.k3moe_layer.argtypes = [pc, vp, vp, vp, pe, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]
         L.k3moe_layer_host.argtypes = [pc, vp, vp, vp, pe, vp, i32, vp, vp, vp, sz, vp]
+        L.k3moe_layer_static_scratch.argtypes = [pc, vp, vp, vp, pe, vp, i32, vp, vp, vp, vp, vp, vp]
         L.k3moe_matvec_mxfp4.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
         L.k3moe_stack_link.argtypes = [vp, i32, i32, i32, ctypes.c_float, vp, vp, vp]
         L.k3moe_set_phase_events.restype = ctypes.c_int
@@ -129,7 +134,7 @@ def lib() -> ctypes.CDLL:
         L.k3moe_abi_version.argtypes = []
         for n in ("k3moe_workspace_size", "k3moe_workspace_size_host", "k3moe_route",
                   "k3moe_experts_mxfp4", "k3moe_layer", "k3moe_layer_host", "k3moe_matvec_mxfp4",
-                  "k3moe_stack_link"):
+                  "k3moe_stack_link", "k3moe_layer_static_scratch"):
             getattr(L, n).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -272,6 +277,35 @@ def k3moe_layer(cfg: Cfg, h, wr, bias, experts: Experts, x, y, idx=None, gate=No
     _check("k3moe_layer", lib().k3moe_layer(
         ctypes.byref(c), _p(h), _p(wr), _p(bias), ctypes.byref(e), _p(x), T, _p(y), _p(idx), _p(gate),
         _p(gap), _p(status), _p(ws), ws.numel(), _stream(stream)))
+
+
+def k3moe_layer_static_scratch(cfg: Cfg, h, wr, bias, experts: Experts, x, y, idx=None, gate=None,
+                               gap=None, status=None, stream=None) -> None:
+    """k3moe_layer without a workspace, for callers that cannot allocate device memory
+    (for example a host framework whose allocator owns all of it).  The library's own
+    16 MiB device array serves as scratch; it is shared by every call on the device, so
+    calls must be ordered on one stream.  Raises K3moeError (status 8) when the batch needs
+    more scratch than the array holds."""
+    import torch
+    T = h.shape[0]
+    _expect(h, "h", torch.bfloat16, (T, cfg.hidden))
+    _expect(wr, "wr", torch.bfloat16, (cfg.n_experts, cfg.hidden))
+    if bias is not None:
+        _expect(bias, "bias", torch.float32, (cfg.n_experts,))
+    _expect(x, "x", torch.bfloat16, (T, cfg.latent))
+    _expect(y, "y", torch.float32, (T, cfg.latent))
+    if idx is not None:
+        _expect(idx, "idx", torch.int32, (T, cfg.topk))
+    if gate is not None:
+        _expect(gate, "gate", torch.float32, (T, cfg.topk))
+    if gap is not None:
+        _expect(gap, "gap", torch.float32, (T,))
+    if status is not None:
+        _expect(status, "status", torch.int32, (4,))
+    c, e = cfg.c(), experts.c()
+    _check("k3moe_layer_static_scratch", lib().k3moe_layer_static_scratch(
+        ctypes.byref(c), _p(h), _p(wr), _p(bias), ctypes.byref(e), _p(x), T, _p(y), _p(idx), _p(gate),
+        _p(gap), _p(status), _stream(stream)))
 
 
 def k3moe_layer_host(cfg: Cfg, h_host, wr, bias, experts: Experts, x_host, y_host, status, ws,

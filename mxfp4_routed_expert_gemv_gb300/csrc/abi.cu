@@ -188,6 +188,24 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
   return K3MOE_OK;
 }
 
+// Scratch of k3moe_layer_static_scratch: one array per device that loads the library.  In
+// host code g_static_scratch names a host-side stand-in; its device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+static __device__ __align__(256) unsigned char g_static_scratch[K3MOE_STATIC_SCRATCH_BYTES];
+std::atomic<void*> g_static_scratch_addr[64];
+
+int static_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return K3MOE_ERR_CUDA;
+  void* p = g_static_scratch_addr[dev].load();
+  if (!p) {
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return K3MOE_ERR_CUDA;
+    g_static_scratch_addr[dev].store(p);
+  }
+  *out = p;
+  return K3MOE_OK;
+}
+
 }  // namespace
 }  // namespace k3
 
@@ -274,6 +292,32 @@ int k3moe_layer(const k3moe_cfg* cfg, const void* h, const void* wr, const float
                       w, s);
 }
 
+int k3moe_layer_static_scratch(const k3moe_cfg* cfg, const void* h, const void* wr,
+                               const float* bias, const k3moe_experts* experts, const void* x,
+                               int32_t T, float* y, int32_t* idx, float* gate, float* gap,
+                               int32_t* status, void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if ((rc = check_experts(experts))) return rc;
+  if (T < 0) return K3MOE_ERR_INVALID;
+  if (T > kMaxTokens) return K3MOE_ERR_UNSUPPORTED;
+  if (T == 0) return K3MOE_OK;
+  if (!h || !wr || !x || !y) return K3MOE_ERR_INVALID;
+  if (!aligned(h, 16) || !aligned(wr, 16) || !aligned(x, 16) || !aligned(y, 16) ||
+      (bias && !aligned(bias, 4)) || (idx && !aligned(idx, 4)) || (gate && !aligned(gate, 4)) ||
+      (gap && !aligned(gap, 4)) || (status && !aligned(status, 4)))
+    return K3MOE_ERR_ALIGN;
+  const size_t need = carve(cfg, T, nullptr, false, nullptr);
+  if (need > K3MOE_STATIC_SCRATCH_BYTES) return K3MOE_ERR_TOO_LARGE;
+  void* base = nullptr;
+  if ((rc = static_scratch_address(&base))) return rc;
+  Workspace w;
+  carve(cfg, T, base, false, &w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return run_pipeline(cfg, true, h, wr, bias, experts, x, idx ? idx : w.idx, gate ? gate : w.gate,
+                      gap ? gap : w.gap, T, y, status, w, s);
+}
+
 int k3moe_layer_host(const k3moe_cfg* cfg, const void* h_host, const void* wr, const float* bias,
                      const k3moe_experts* experts, const void* x_host, int32_t T, float* y_host,
                      int32_t* status, void* ws, size_t ws_bytes, void* stream) {
@@ -348,6 +392,7 @@ const char* k3moe_strerror(int status) {
     case K3MOE_ERR_CUDA: return "CUDA launch or copy failed";
     case K3MOE_ERR_TIMEOUT: return "a bounded device wait ran out";
     case K3MOE_ERR_DROPPED: return "expert index out of range (assignment skipped)";
+    case K3MOE_ERR_TOO_LARGE: return "request exceeds the static scratch capacity (16 MiB)";
     default: return "unknown status";
   }
 }
