@@ -178,9 +178,8 @@ int k3moe_stack_link(const float *y, int32_t T, int32_t L, int32_t norm, float e
  *     device address (cudaGetSymbolAddress) and caches it; make that first call before any
  *     stream capture begins.
  *   - Sharing: all calls on a device share the one array and it keeps the previous call's
- *     contents.  Every scratch value a call reads is written earlier in the same call (the
- *     combine counters are zeroed by the call itself), so no clearing is needed between
- *     calls; but calls that overlap on the GPU (different streams, no ordering between
+ *     contents.  Every scratch value a call reads is written earlier in the same call, so
+ *     no clearing is needed between calls; but calls that overlap on the GPU (different streams, no ordering between
  *     them) race on the array and corrupt each other's results.  Order them on one stream.
  * Arguments, layouts and errors are those of k3moe_layer. */
 #define K3MOE_STATIC_SCRATCH_BYTES (16u << 20)
@@ -193,8 +192,8 @@ int k3moe_layer_static_scratch(const k3moe_cfg *cfg, const void *h, const void *
  * created by the caller, or NULL to switch the hook off.  While set, every k3moe_layer and
  * k3moe_experts_mxfp4 call records, on its stream: [0] at entry, [1] after the router
  * logits (decode-sized batches run the top-k inside the next phase), [2] after the top-k,
- * bucketing and input preparation, [3] after GEMM1 (w1, w3, activation), [4] and [5] after
- * GEMM2 (w2, gates and the combine, which is fused into it).  Process-wide, not thread-safe;
+ * bucketing and input preparation, [3] after GEMM1 (w1, w3, activation), [4] after GEMM2
+ * (w2, gates), [5] after the combine.  Process-wide, not thread-safe;
  * recording breaks programmatic launch overlap between phases, so time throughput with
  * the hook off.  Returns K3MOE_ERR_INVALID if n != 6 with non-NULL events. */
 int k3moe_set_phase_events(void *const *events, int32_t n);

@@ -91,7 +91,6 @@ size_t carve(const k3moe_cfg* c, int32_t T, void* base, bool host_stage, Workspa
   t.b.meta = cv.take<int32_t>(16);
   t.b.chunk_base = cv.take<int32_t>(E * (size_t)bucket_chunks((int)Tt));
   t.b.nvalid = cv.take<int32_t>(Tt);
-  t.b.cnt = cv.take<int32_t>(Tt * (L / 4));
   t.x16 = cv.take<__half>(Tt * L);
   t.xexp = cv.take<int32_t>(Tt);
   t.act = cv.take<float>(P * I);
@@ -155,8 +154,8 @@ int run_route(const k3moe_cfg* c, const void* h, const void* wr, const float* bi
 
 // The layer (route = true) or the routed-expert sum alone (route = false):
 //   [router logits (+ top-k grid for large T)] -> preparation (top-k for decode-sized T,
-//   bucketing, x in f16, counters) -> GEMM1 (w1, w3, activation) -> GEMM2 (w2, gates, fused
-//   combine).  Decode-sized T takes 4 launches (3 without the router).
+//   bucketing, x in f16) -> GEMM1 (w1, w3, activation) -> GEMM2 (w2, gates) -> combine.
+//   Decode-sized T takes 5 launches (4 without the router).
 int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
                  const float* bias, const k3moe_experts* ex, const void* x, int32_t* idx,
                  float* gate, float* gap, int32_t T, float* y, int32_t* status,
@@ -181,9 +180,9 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
   K3_TRY(launch_gemm1(ep, L, I, E, T, K, w.x16, w.xexp, w.b, w.act, c->act, c->situ_b1,
                       c->situ_b2, status, s, true));
   K3_TRY(phase(3, s));
-  K3_TRY(launch_gemm2(ep, L, I, E, T, K, w.act, gate, idx, w.b, w.ybuf, w.b.cnt, y, status, s,
-                      true));
+  K3_TRY(launch_gemm2(ep, L, I, E, T, K, w.act, gate, w.b, w.ybuf, status, s, true));
   K3_TRY(phase(4, s));
+  K3_TRY(launch_combine(w.ybuf, idx, T, K, E, L, y, s, true));
   K3_TRY(phase(5, s));
   return K3MOE_OK;
 }

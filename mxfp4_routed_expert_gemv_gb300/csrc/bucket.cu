@@ -4,8 +4,7 @@
 // Output: counts[E], offsets[E+1] (exclusive prefix of counts), perm[] = the valid
 // assignment ids a = t*k + j sorted by expert and, within an expert, by token (stable),
 // the list of active experts (count > 0) in ascending order with each one's perm offset
-// and token count, nvalid[t] (valid assignments of token t), zeroed combine counters, y
-// rows zeroed for tokens without a valid assignment, and x in the GEMVs' f16 form.  An
+// and token count, nvalid[t] (valid assignments of token t), and x in the GEMVs' f16 form.  An
 // expert index outside [0, E) is skipped and counted in status[0] (the README's "counted,
 // never silent" expert-drop rule, Part II section 9).
 //
@@ -110,7 +109,8 @@ __device__ void prep_x_warp(const uint16_t* xr, int L, __half* out, int32_t* xex
   if (lane == 0) *xexp = e;
 }
 
-// Per token: count valid assignments; zero y when there is none.
+// Per token: count valid assignments (y of a token without one is zeroed here; the
+// combine writes every token's y as well).
 __device__ void token_valid_warp(const int32_t* idx_t, int k, int E, int L, int32_t* nvalid_t,
                                  float* y_t, int lane) {
   int v = 0;
@@ -125,7 +125,7 @@ __device__ void token_valid_warp(const int32_t* idx_t, int k, int E, int L, int3
 }
 
 // Single block of 1024 threads, T <= kSmallTokens: [top-k], count, scan, stable scatter
-// token by token (one warp, lane j handles slot j), x prep, counters.
+// token by token (one warp, lane j handles slot j), x prep.
 __global__ void __launch_bounds__(1024) k_prep_small(PrepArgs p) {
   pdl_wait();
   pdl_launch();
@@ -175,12 +175,10 @@ __global__ void __launch_bounds__(1024) k_prep_small(PrepArgs p) {
       token_valid_warp(p.idx + (size_t)t * k, k, E, p.L, p.b.nvalid + t, p.y + (size_t)t * p.L, lane);
     }
   }
-  const int ncnt = T * (p.L >> 2);
-  for (int i = tid; i < ncnt; i += blockDim.x) p.b.cnt[i] = 0;
 }
 
 // Multi-block path, pass 1: per-chunk histograms stored transposed [E][nchunks]; also the
-// chunk's tokens' nvalid, counters and empty-token y rows.
+// chunk's tokens' nvalid.
 __global__ void __launch_bounds__(256) k_bucket_count(PrepArgs p, int nchunks) {
   pdl_wait();
   pdl_launch();
@@ -200,8 +198,6 @@ __global__ void __launch_bounds__(256) k_bucket_count(PrepArgs p, int nchunks) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int t = t0 + warp; t < t1; t += blockDim.x >> 5)
     token_valid_warp(p.idx + (size_t)t * k, k, E, p.L, p.b.nvalid + t, p.y + (size_t)t * p.L, lane);
-  const int nq = p.L >> 2;
-  for (int i = t0 * nq + threadIdx.x; i < t1 * nq; i += blockDim.x) p.b.cnt[i] = 0;
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) p.b.chunk_base[(size_t)e * nchunks + c] = hist[e];
 }

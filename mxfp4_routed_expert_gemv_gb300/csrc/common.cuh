@@ -75,6 +75,57 @@ __device__ __forceinline__ void dot8_e2m1_f16(uint32_t w, uint32_t x01, uint32_t
       : "r"(w), "r"(x01), "r"(x23), "r"(x45), "r"(x67));
 }
 
+// Four nibble pairs (one 32-bit word) -> four exact f16x2 (low nibble -> low half).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t"
+      ".reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t"
+      "}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+// acc += a * b with f16 operands and fp32 accumulation (exact product, one rounding).
+__device__ __forceinline__ float fma_f16_f32(unsigned short a, unsigned short b, float acc) {
+  asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc) : "h"(a), "h"(b));
+  return acc;
+}
+
+// The 32 activations of one MX group as separate f16 halves, unpacked once and shared by
+// every row that meets the group.
+struct XHalves {
+  unsigned short v[32];
+  __device__ __forceinline__ explicit XHalves(const uint32_t (&x)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      v[2 * i] = (unsigned short)(x[i] & 0xffffu);
+      v[2 * i + 1] = (unsigned short)(x[i] >> 16);
+    }
+  }
+};
+
+// One MX group of one row (16 bytes = 32 E2M1 weights) against pre-unpacked activations,
+// unscaled; two accumulation chains.
+__device__ __forceinline__ float dot32_halves(const uint4 w, const XHalves& x) {
+  float p0 = 0.f, p1 = 0.f;
+  const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t h[4];
+    e2m1x8_to_f16x2(words[q], h);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      p0 = fma_f16_f32((unsigned short)(h[b] & 0xffffu), x.v[8 * q + 2 * b], p0);
+      p1 = fma_f16_f32((unsigned short)(h[b] >> 16), x.v[8 * q + 2 * b + 1], p1);
+    }
+  }
+  return p0 + p1;
+}
+
 // One MX group: 32 E2M1 weights (16 bytes) dotted with 32 f16 activations (16 x f16x2),
 // unscaled.
 __device__ __forceinline__ float dot32_e2m1_f16(const uint4 w, const uint32_t (&x)[16]) {

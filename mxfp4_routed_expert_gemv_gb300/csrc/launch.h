@@ -53,7 +53,6 @@ struct BucketOut {
   int32_t* meta;        // [16]   [0] active experts, [1] valid assignments
   int32_t* chunk_base;  // [E][nchunks] scratch of the multi-block path
   int32_t* nvalid;      // [T]    valid assignments per token
-  int32_t* cnt;         // [T][L/4] combine counters (zeroed by the preparation)
 };
 
 // Everything the per-call preparation touches.  logits == nullptr: idx/gate come from the
@@ -84,16 +83,19 @@ struct ExpertPtrs {
 };
 cudaError_t launch_prep_x(const uint16_t* x, int T, int L, __half* x16, int32_t* xexp,
                           cudaStream_t s, bool pdl);
+cudaError_t launch_matvec(float* y, const uint16_t* x, const uint8_t* packed,
+                          const uint8_t* scales, int in, int rows, cudaStream_t s);
+
+// experts.cu
 cudaError_t launch_gemm1(const ExpertPtrs& w, int L, int I, int E, int T, int k,
                          const __half* x16, const int32_t* xexp, const BucketOut& b,
                          float* act, int act_kind, float b1, float b2, int32_t* status,
                          cudaStream_t s, bool pdl);
 cudaError_t launch_gemm2(const ExpertPtrs& w, int L, int I, int E, int T, int k,
-                         const float* act, const float* gate, const int32_t* idx,
-                         const BucketOut& b, float* ybuf, int32_t* cnt, float* y,
+                         const float* act, const float* gate, const BucketOut& b, float* ybuf,
                          int32_t* status, cudaStream_t s, bool pdl);
-cudaError_t launch_matvec(float* y, const uint16_t* x, const uint8_t* packed,
-                          const uint8_t* scales, int in, int rows, cudaStream_t s);
+cudaError_t launch_combine(const float* ybuf, const int32_t* idx, int T, int k, int E, int L,
+                           float* y, cudaStream_t s, bool pdl);
 
 // stack.cu
 cudaError_t launch_stack_link(const float* y, int T, int L, int norm, float eps, uint16_t* x_out,
