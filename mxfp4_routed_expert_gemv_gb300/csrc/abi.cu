@@ -5,6 +5,7 @@
 #include <cstring>
 
 #include "launch.h"
+#include "mxq.cuh"
 
 namespace k3 {
 
@@ -51,9 +52,15 @@ struct Workspace {
   float* gate;       // [T][k]
   float* gap;        // [T]
   BucketOut b;
-  __half* x16;       // [T][L]
-  int32_t* xexp;     // [T]
-  float* act;        // [T*k][I]
+  bool tc;           // tensor-core expert path (shapes it tiles) or the CUDA-core GEMV
+  __half* x16;       // [T][L]                  (GEMV path)
+  int32_t* xexp;     // [T]                     (GEMV path)
+  float* act;        // [T*k][I]                (GEMV path)
+  uint8_t* xq;       // [T*k*kTerms][L/2]       (tensor-core path: x as MXFP4 terms)
+  uint8_t* xsf;      // [T*k*kTerms][L/32]
+  uint8_t* aq;       // [T*k*kTerms][I/2]       (tensor-core path: act as MXFP4 terms)
+  uint8_t* asf;      // [T*k*kTerms][I/32]
+  float* part;       // split-tile partial sums (tensor-core path)
   float* ybuf;       // [T*k][L]
   uint16_t* h_stage; // [T][H]  (host variant only)
   uint16_t* x_stage; // [T][L]
@@ -91,9 +98,21 @@ size_t carve(const k3moe_cfg* c, int32_t T, void* base, bool host_stage, Workspa
   t.b.meta = cv.take<int32_t>(16);
   t.b.chunk_base = cv.take<int32_t>(E * (size_t)bucket_chunks((int)Tt));
   t.b.nvalid = cv.take<int32_t>(Tt);
-  t.x16 = cv.take<__half>(Tt * L);
-  t.xexp = cv.take<int32_t>(Tt);
-  t.act = cv.take<float>(P * I);
+  t.b.inv = cv.take<int32_t>(P);
+  t.b.ntile_base = cv.take<int32_t>(E + 1);
+  t.b.flags = cv.take<int32_t>(2 * (size_t)kTcMaxGrid);
+  t.tc = tc_path_supported((int)L, (int)I);
+  if (t.tc) {
+    t.xq = cv.take<uint8_t>(P * kTerms * (L / 2));
+    t.xsf = cv.take<uint8_t>(P * kTerms * (L / 32));
+    t.aq = cv.take<uint8_t>(P * kTerms * (I / 2));
+    t.asf = cv.take<uint8_t>(P * kTerms * (I / 32));
+    t.part = cv.take<float>(tc_part_floats((int)Tt));
+  } else {
+    t.x16 = cv.take<__half>(Tt * L);
+    t.xexp = cv.take<int32_t>(Tt);
+    t.act = cv.take<float>(P * I);
+  }
   t.ybuf = cv.take<float>(P * L);
   if (host_stage) {
     t.h_stage = cv.take<uint16_t>(Tt * H);
@@ -174,14 +193,27 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
   }
   K3_TRY(phase(1, s));
   PrepArgs p{fused_topk ? w.logits : nullptr, bias, E, K, c->renorm, c->routed_scale, idx, gate,
-             gap, T, L, static_cast<const uint16_t*>(x), w.x16, w.xexp, w.b, y, status};
+             gap, T, L, static_cast<const uint16_t*>(x), w.tc ? nullptr : w.x16, w.xexp, w.b, y,
+             status};
   K3_TRY(launch_prep(p, s, route));
-  K3_TRY(phase(2, s));
-  K3_TRY(launch_gemm1(ep, L, I, E, T, K, w.x16, w.xexp, w.b, w.act, c->act, c->situ_b1,
-                      c->situ_b2, status, s, true));
-  K3_TRY(phase(3, s));
-  K3_TRY(launch_gemm2(ep, L, I, E, T, K, w.act, gate, w.b, w.ybuf, status, s, true));
-  K3_TRY(phase(4, s));
+  if (w.tc) {
+    K3_TRY(launch_split_x(static_cast<const uint16_t*>(x), T, L, K, E, idx, w.b.inv, w.xq, w.xsf,
+                          s, true));
+    K3_TRY(phase(2, s));
+    K3_TRY(launch_tc_gemm1(ep, L, I, E, T, K, w.xq, w.xsf, w.b, w.aq, w.asf, c->act, c->situ_b1,
+                           c->situ_b2, w.part, w.b.flags, status, s, true));
+    K3_TRY(phase(3, s));
+    K3_TRY(launch_tc_gemm2(ep, L, I, E, T, K, w.aq, w.asf, gate, w.b, w.ybuf, w.part,
+                           w.b.flags + kTcMaxGrid, status, s, true));
+    K3_TRY(phase(4, s));
+  } else {
+    K3_TRY(phase(2, s));
+    K3_TRY(launch_gemm1(ep, L, I, E, T, K, w.x16, w.xexp, w.b, w.act, c->act, c->situ_b1,
+                        c->situ_b2, status, s, true));
+    K3_TRY(phase(3, s));
+    K3_TRY(launch_gemm2(ep, L, I, E, T, K, w.act, gate, w.b, w.ybuf, status, s, true));
+    K3_TRY(phase(4, s));
+  }
   K3_TRY(launch_combine(w.ybuf, idx, T, K, E, L, y, s, true));
   K3_TRY(phase(5, s));
   return K3MOE_OK;

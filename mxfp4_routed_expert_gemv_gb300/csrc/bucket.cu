@@ -73,6 +73,12 @@ __device__ void publish_counts(int c, int E, const BucketOut& o, int* excl_out) 
     o.meta[0] = nact;
     o.meta[1] = total;
   }
+  // tensor-core tiles: ceil(count / kTcTokTile) per active expert, prefix over active experts
+  int nt_tot;
+  const int nt_excl = block_exclusive_scan_1024(flag ? (c + kTcTokTile - 1) / kTcTokTile : 0, &nt_tot);
+  if (flag) o.ntile_base[pos] = nt_excl;
+  if (e == 0) o.ntile_base[nact] = nt_tot;
+  if (e < 2 * kTcMaxGrid) o.flags[e] = 0;
   *excl_out = excl;
 }
 
@@ -165,13 +171,17 @@ __global__ void __launch_bounds__(1024) k_prep_small(PrepArgs p) {
       if (lane < k) {
         const int a = t * k + lane;
         const int e = p.idx[a];
-        if (e >= 0 && e < E) p.b.perm[atomicAdd(&cur[e], 1)] = a;
+        if (e >= 0 && e < E) {
+          const int pos = atomicAdd(&cur[e], 1);
+          p.b.perm[pos] = a;
+          p.b.inv[a] = pos;
+        }
       }
       __syncwarp();
     }
   } else {
     for (int t = warp - 1; t < T; t += 31) {
-      prep_x_warp(p.x + (size_t)t * p.L, p.L, p.x16 + (size_t)t * p.L, p.xexp + t, lane);
+      if (p.x16) prep_x_warp(p.x + (size_t)t * p.L, p.L, p.x16 + (size_t)t * p.L, p.xexp + t, lane);
       token_valid_warp(p.idx + (size_t)t * k, k, E, p.L, p.b.nvalid + t, p.y + (size_t)t * p.L, lane);
     }
   }
@@ -239,7 +249,11 @@ __global__ void __launch_bounds__(32) k_bucket_scatter(const int32_t* __restrict
     if (lane < k) {
       const int a = t * k + lane;
       const int e = idx[a];
-      if (e >= 0 && e < E) o.perm[atomicAdd(&cur[e], 1)] = a;
+      if (e >= 0 && e < E) {
+        const int pos = atomicAdd(&cur[e], 1);
+        o.perm[pos] = a;
+        o.inv[a] = pos;
+      }
     }
     __syncwarp();
   }
@@ -262,6 +276,7 @@ cudaError_t launch_prep(const PrepArgs& p, cudaStream_t s, bool pdl) {
   err = launch_kernel(k_bucket_scatter, dim3(nch), dim3(32), 0, s, true,
                       static_cast<const int32_t*>(p.idx), p.T, p.k, p.E, nch, p.b);
   if (err != cudaSuccess) return err;
+  if (!p.x16) return cudaSuccess;
   return launch_prep_x(p.x, p.T, p.L, p.x16, p.xexp, s, true);
 }
 

@@ -42,6 +42,10 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
                         float routed_scale, int32_t* idx, float* gate, float* gap,
                         cudaStream_t s, bool pdl);
 
+// Tensor-core expert path (moe_tc.cu): tokens per tile, and the largest grid it launches.
+constexpr int kTcTokTile = 16;
+constexpr int kTcMaxGrid = 192;
+
 // bucket.cu
 struct BucketOut {
   int32_t* counts;      // [E]
@@ -53,6 +57,9 @@ struct BucketOut {
   int32_t* meta;        // [16]   [0] active experts, [1] valid assignments
   int32_t* chunk_base;  // [E][nchunks] scratch of the multi-block path
   int32_t* nvalid;      // [T]    valid assignments per token
+  int32_t* inv;         // [T*k]  perm position of each valid assignment id
+  int32_t* ntile_base;  // [E+1]  tensor-core tiles (kTcTokTile tokens) before each active expert
+  int32_t* flags;       // [2 * kTcMaxGrid] split-tile flags of the two tensor-core GEMMs (zeroed)
 };
 
 // Everything the per-call preparation touches.  logits == nullptr: idx/gate come from the
@@ -96,6 +103,24 @@ cudaError_t launch_gemm2(const ExpertPtrs& w, int L, int I, int E, int T, int k,
                          int32_t* status, cudaStream_t s, bool pdl);
 cudaError_t launch_combine(const float* ybuf, const int32_t* idx, int T, int k, int E, int L,
                            float* y, cudaStream_t s, bool pdl);
+
+// moe_tc.cu
+bool tc_path_supported(int L, int I);
+int tc_grid();
+int tc_npart(int T);
+size_t tc_part_floats(int T);
+cudaError_t launch_split_x(const uint16_t* x, int T, int L, int k, int E, const int32_t* idx,
+                           const int32_t* inv, uint8_t* xq, uint8_t* xsf, cudaStream_t s,
+                           bool pdl);
+cudaError_t launch_tc_gemm1(const ExpertPtrs& w, int L, int I, int E, int T, int k,
+                            const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,
+                            uint8_t* act_q, uint8_t* act_sf, int act_kind, float b1, float b2,
+                            float* part, int32_t* flags, int32_t* status, cudaStream_t s,
+                            bool pdl);
+cudaError_t launch_tc_gemm2(const ExpertPtrs& w, int L, int I, int E, int T, int k,
+                            const uint8_t* act_q, const uint8_t* act_sf, const float* gate,
+                            const BucketOut& b, float* ybuf, float* part, int32_t* flags,
+                            int32_t* status, cudaStream_t s, bool pdl);
 
 // stack.cu
 cudaError_t launch_stack_link(const float* y, int T, int L, int norm, float eps, uint16_t* x_out,

@@ -1,0 +1,76 @@
+// mxq.cuh -- activations in MXFP4 "terms" for the block-scaled tensor-core path.
+//
+// A vector v (bf16 x, or fp32 act) is written as a sum of kTerms MXFP4 vectors: for each
+// group of 32 elements, term 0 is v rounded to E2M1 under the group's own E8M0 scale (the
+// smallest power of two that puts the group's largest magnitude at or below 6), term 1 the
+// same rounding of what term 0 left over, and so on.  Each term gains about two bits, so
+// four terms carry v to roughly 2^-8 of the group maximum: the same order as the bf16 input
+// itself.  The weights' E2M1 codes and scales are the checkpoint's own bytes (README
+// "kimi-k3-in-c", Part II section 4); only the activations are split.
+#pragma once
+#include <cstdint>
+
+namespace k3 {
+
+constexpr int kTerms = 4;
+
+// E8M0 exponent e (unbiased) of a group with largest magnitude amax: the smallest e with
+// amax <= 6 * 2^e, clamped to the E8M0 range; amax == 0 gives e = 0.
+__device__ __forceinline__ int mx_scale_exp(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  if (amax == 0.f || (b >> 23) == 0) return amax == 0.f ? 0 : -127;
+  const int x = (int)((b >> 23) & 255u) - 127;  // amax = m * 2^x, m in [1, 2)
+  int e = x - 2 + ((b & 0x7FFFFFu) > 0x400000u ? 1 : 0);  // m > 1.5 needs one more
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// Round a (|a| <= 6) to the nearest E2M1 value, ties to the even code; returns the 4-bit
+// code (bit 3 = sign) and the value it stands for.
+__device__ __forceinline__ uint32_t e2m1_rne(float a, float* val) {
+  const float m = fabsf(a);
+  uint32_t c;
+  float v;
+  if (m <= 0.25f) { c = 0; v = 0.f; }
+  else if (m < 0.75f) { c = 1; v = 0.5f; }
+  else if (m <= 1.25f) { c = 2; v = 1.f; }
+  else if (m < 1.75f) { c = 3; v = 1.5f; }
+  else if (m <= 2.5f) { c = 4; v = 2.f; }
+  else if (m < 3.5f) { c = 5; v = 3.f; }
+  else if (m <= 5.f) { c = 6; v = 4.f; }
+  else { c = 7; v = 6.f; }
+  const bool neg = __float_as_uint(a) >> 31;
+  *val = neg ? -v : v;
+  return c | (neg ? 8u : 0u);
+}
+
+// 2^e as a float for e in [-127, 127] (exact: 2^-127 is a subnormal).
+__device__ __forceinline__ float pow2f(int e) {
+  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00200000u);
+}
+
+// One warp, one group of 32 elements (lane i holds element i): the kTerms terms.  On return
+// lanes 0, 8, 16, 24 hold word (lane/8) of each term's 16 packed bytes (low nibble = even
+// element) in words[t], and every lane holds each term's E8M0 byte in sf[t].
+__device__ __forceinline__ void mx_split_group(float v, uint32_t (&words)[kTerms],
+                                               uint32_t (&sf)[kTerms]) {
+  const int lane = threadIdx.x & 31;
+  float r = v;
+#pragma unroll
+  for (int t = 0; t < kTerms; ++t) {
+    float amax = fabsf(r);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const int e = mx_scale_exp(amax);
+    float q;
+    const uint32_t code = e2m1_rne(r * pow2f(-e), &q);
+    r -= q * pow2f(e);
+    uint32_t w = code << (4 * (lane & 7));
+    w |= __shfl_xor_sync(0xffffffffu, w, 1);
+    w |= __shfl_xor_sync(0xffffffffu, w, 2);
+    w |= __shfl_xor_sync(0xffffffffu, w, 4);
+    words[t] = w;
+    sf[t] = (uint32_t)(e + 127);
+  }
+}
+
+}  // namespace k3

@@ -1,0 +1,137 @@
+// tc.cuh -- thin inline-PTX wrappers for the sm_100-family tensor-core path: tensor memory
+// (TMEM) allocation, loads and stores, the block-scaled MMA (kind::mxf4: E2M1 x E2M1 with one
+// E8M0 scale per 32 elements of K), its completion signal, and TMA tensor copies.
+//
+// Shared-memory matrix descriptor (64 bits), K-major operand:
+//   bits  0-13  start address >> 4
+//   bits 16-29  leading byte offset >> 4 (distance between core matrices along K)
+//   bits 32-45  stride byte offset >> 4  (distance between 8-row groups along M or N)
+//   bits 46-47  descriptor version (1)
+//   bits 49-51  base offset (0: every swizzle atom starts 1024-byte aligned)
+//   bits 61-63  layout: 0 no swizzle (8-row x 16-byte core matrices), 2 128-byte swizzle
+// Instruction descriptor (32 bits) of the block-scaled kinds:
+//   bits 4-5 B scale byte id, 7-9 A format, 10-12 B format (E2M1 = 1 for kind::mxf4),
+//   15/16 A/B major (0 = K-major), 17-22 N >> 3, 23 scale format (1 = UE8M0),
+//   24-28 M >> 4, 29-30 A scale byte id, 31 K size (0 = 64 for kind::mxf4).
+// Scale factors in TMEM (M = 128, scale_vec::2X, scale byte id 0), as measured on sm_103a:
+//   A: row m reads lane m of column (sfa + m/32); byte 0 scales K elements 0..31 of the MMA,
+//      byte 1 elements 32..63.
+//   B: column n reads column (sfb + n/32) in the lane quarter of the row being computed, so
+//      its scales sit in lane 32q + n%32 of every quarter q.
+//   sfa and sfb are kept on 4-column boundaries (a scale address off that grid was refused
+//   with a misaligned-address error).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+
+namespace k3 {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+constexpr uint32_t kLayoutNone = 0, kLayout128B = 2;
+
+__host__ __device__ constexpr uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                                 uint32_t layout) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) |
+         ((uint64_t)(layout & 7u) << 61);
+}
+
+// kind::mxf4, E2M1 x E2M1, UE8M0 scales, both operands K-major, dense, K = 64.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, int a_sf_id, int b_sf_id) {
+  return ((uint32_t)(b_sf_id & 3) << 4) | (1u << 7) | (1u << 10) |
+         ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) |
+         ((uint32_t)(a_sf_id & 3) << 29);
+}
+
+// ---- TMEM allocation (one full warp executes each)
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               :: "r"(smem_addr(dst)), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+               :: "r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// generic-proxy writes to shared memory -> visible to the tensor core / TMA (async proxy)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- TMEM stores / loads: warp w reaches lanes [32*(w%4), 32*(w%4)+32); thread i of the warp
+// handles lane 32*(w%4)+i; consecutive registers are consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_st_x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" :: "r"(taddr), "r"(v)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t v0, uint32_t v1,
+                                           uint32_t v2, uint32_t v3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
+               :: "r"(taddr), "r"(v0), "r"(v1), "r"(v2), "r"(v3) : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---- the block-scaled MMA: D[M x N] (+)= (A * sfA) (B * sfB)^T over K = 64, issued by one
+// thread; D, sfA and sfB are TMEM addresses, A and B shared-memory descriptors.
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+         "r"(accumulate)
+      : "memory");
+}
+// arrive once on an mbarrier when every MMA this thread issued before has completed
+__device__ __forceinline__ void mma_commit(uint64_t* mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               :: "r"(smem_addr(mbar)) : "memory");
+}
+
+// ---- TMA tensor copies (global -> shared), completion counted in bytes on an mbarrier.
+// x is the innermost coordinate in bytes (a multiple of 16), y the row.
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int32_t x,
+                                            int32_t y, uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3}], [%4];"
+      :: "r"(smem_addr(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+         "r"(smem_addr(mbar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+}  // namespace tc
+}  // namespace k3
