@@ -101,6 +101,7 @@ size_t carve(const k3moe_cfg* c, int32_t T, void* base, bool host_stage, Workspa
   t.b.inv = cv.take<int32_t>(P);
   t.b.ntile_base = cv.take<int32_t>(E + 1);
   t.b.flags = cv.take<int32_t>(2 * (size_t)kTcMaxGrid);
+  t.b.ready = cv.take<int32_t>((P + kTcTokTile - 1) / kTcTokTile + E + 1);
   t.tc = tc_path_supported((int)L, (int)I);
   if (t.tc) {
     t.xq = cv.take<uint8_t>(P * kTerms * (L / 2));
@@ -155,6 +156,8 @@ cudaError_t phase(int i, cudaStream_t s) {
                     : cudaSuccess;
 }
 
+void phase3(cudaStream_t s) { phase(3, s); }
+
 #define K3_TRY(expr)                                  \
   do {                                                \
     cudaError_t _e = (expr);                          \
@@ -200,11 +203,9 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
     K3_TRY(launch_split_x(static_cast<const uint16_t*>(x), T, L, K, E, idx, w.b.inv, w.xq, w.xsf,
                           s, true));
     K3_TRY(phase(2, s));
-    K3_TRY(launch_tc_gemm1(ep, L, I, E, T, K, w.xq, w.xsf, w.b, w.aq, w.asf, c->act, c->situ_b1,
-                           c->situ_b2, w.part, w.b.flags, status, s, true));
-    K3_TRY(phase(3, s));
-    K3_TRY(launch_tc_gemm2(ep, L, I, E, T, K, w.aq, w.asf, gate, w.b, w.ybuf, w.part,
-                           w.b.flags + kTcMaxGrid, status, s, true));
+    K3_TRY(launch_tc_experts(ep, L, I, E, T, K, w.xq, w.xsf, w.b, w.aq, w.asf, c->act,
+                             c->situ_b1, c->situ_b2, gate, w.ybuf, w.part, status, s, true,
+                             phase3));
     K3_TRY(phase(4, s));
   } else {
     K3_TRY(phase(2, s));

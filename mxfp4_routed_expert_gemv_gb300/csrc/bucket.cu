@@ -79,6 +79,7 @@ __device__ void publish_counts(int c, int E, const BucketOut& o, int* excl_out) 
   if (flag) o.ntile_base[pos] = nt_excl;
   if (e == 0) o.ntile_base[nact] = nt_tot;
   if (e < 2 * kTcMaxGrid) o.flags[e] = 0;
+  for (int i = e; i < nt_tot; i += blockDim.x) o.ready[i] = 0;
   *excl_out = excl;
 }
 

@@ -44,7 +44,7 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
 
 // Tensor-core expert path (moe_tc.cu): tokens per tile, and the largest grid it launches.
 constexpr int kTcTokTile = 16;
-constexpr int kTcMaxGrid = 192;
+constexpr int kTcMaxGrid = 160;
 
 // bucket.cu
 struct BucketOut {
@@ -59,7 +59,8 @@ struct BucketOut {
   int32_t* nvalid;      // [T]    valid assignments per token
   int32_t* inv;         // [T*k]  perm position of each valid assignment id
   int32_t* ntile_base;  // [E+1]  tensor-core tiles (kTcTokTile tokens) before each active expert
-  int32_t* flags;       // [2 * kTcMaxGrid] split-tile flags of the two tensor-core GEMMs (zeroed)
+  int32_t* flags;       // [2 * kTcMaxGrid] arrivals at tiles shared between CTAs (zeroed)
+  int32_t* ready;       // [P/16 + E + 1] finished first-GEMM row tiles per tile group (zeroed)
 };
 
 // Everything the per-call preparation touches.  logits == nullptr: idx/gate come from the
@@ -112,15 +113,11 @@ size_t tc_part_floats(int T);
 cudaError_t launch_split_x(const uint16_t* x, int T, int L, int k, int E, const int32_t* idx,
                            const int32_t* inv, uint8_t* xq, uint8_t* xsf, cudaStream_t s,
                            bool pdl);
-cudaError_t launch_tc_gemm1(const ExpertPtrs& w, int L, int I, int E, int T, int k,
-                            const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,
-                            uint8_t* act_q, uint8_t* act_sf, int act_kind, float b1, float b2,
-                            float* part, int32_t* flags, int32_t* status, cudaStream_t s,
-                            bool pdl);
-cudaError_t launch_tc_gemm2(const ExpertPtrs& w, int L, int I, int E, int T, int k,
-                            const uint8_t* act_q, const uint8_t* act_sf, const float* gate,
-                            const BucketOut& b, float* ybuf, float* part, int32_t* flags,
-                            int32_t* status, cudaStream_t s, bool pdl);
+cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k,
+                              const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,
+                              uint8_t* act_q, uint8_t* act_sf, int act_kind, float b1, float b2,
+                              const float* gate, float* ybuf, float* part, int32_t* status,
+                              cudaStream_t s, bool pdl, void (*between)(cudaStream_t));
 
 // stack.cu
 cudaError_t launch_stack_link(const float* y, int T, int L, int norm, float eps, uint16_t* x_out,

@@ -10,17 +10,21 @@
 // activation written as kTerms MXFP4 terms per token (mxq.cuh), one MMA column per term; the
 // hardware applies each term's scales, so a token's product is the sum of its columns.
 //
-// Work: tiles of 128 weight rows x (up to 16 of an expert's tokens) x the full reduction,
-// cut into units of 512 reduction elements.  The grid is one CTA per SM; CTA c takes units
-// [U c / G, U (c+1) / G) of the whole list (balanced to within one unit whatever the
-// routing).  A tile cut between CTAs is finished by the CTA holding its first unit: the
-// others leave their partial sums and a flag, and it adds them in CTA order (deterministic).
+// Two launches of one persistent kernel: phase 0 (w1, w3 -> act terms) and phase 1 (w2 ->
+// gate * o per assignment).  A phase is a list of tiles of 128 weight rows x (up to 16 of an
+// expert's tokens) x the full reduction, cut into units of 512 reduction elements; CTA c (one
+// per SM) takes units [U c / G, U (c+1) / G), balanced to one unit whatever the routing.  A
+// tile cut by a range boundary is finished by the CTA holding its first unit (its "head"),
+// which processes it last; the others process their part first and leave it in global
+// memory with a flag.  While the head's last MMAs run, a helper thread waits for those flags
+// and bulk-copies the parts into shared memory, so the end of the kernel does no global round
+// trip.  Parts are added in CTA order (deterministic).
 //
-// Roles (320 threads): warps 0-3 epilogue (TMEM lane quarters 0-3), warps 4-7 move each
+// Roles (352 threads): warps 0-3 epilogue (TMEM lane quarters 0-3), warps 4-7 move each
 // stage's scales into TMEM (a 0xFF scale byte, "no value", becomes 0 there), warp 8 issues
-// the TMA copies into a 4-stage ring, warp 9 allocates TMEM and issues the MMAs.  Every
-// wait is bounded; one that runs out sets the status block's timeout count and the CTA
-// stops issuing new work.
+// the weight TMA copies into a 4-stage ring, warp 10 the activation copies (and then fetches
+// the parts of a shared last tile), warp 9 allocates TMEM and issues the MMAs.  Every wait is
+// bounded; one that runs out sets the status block's timeout count and the CTA stops.
 #include "launch.h"
 #include "mxq.cuh"
 #include "tc.cuh"
@@ -29,86 +33,75 @@
 namespace k3 {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kKStage = 512;                                 // reduction elements per stage
 constexpr int kMmas = kKStage / 64;                          // MMAs per stage (K = 64 each)
 constexpr int kTokTile = kTcTokTile;                         // tokens per tile
-constexpr int kNMax = kTokTile * kTerms;                     // B rows (MMA N) per tile
+constexpr int kNMax = kTokTile * kTerms;                     // MMA N of a full tile
 constexpr int kRowsTile = 128;                               // MMA M
-constexpr uint32_t kABytes = kRowsTile * (kKStage / 2);      // 32768
-constexpr uint32_t kBBytes = kNMax * (kKStage / 2);          // 16384
+constexpr int kStages = 4;
+constexpr uint32_t kABytes = kRowsTile * (kKStage / 2);      // 32768: two 16 KB swizzle columns
+constexpr uint32_t kBKatom = kNMax * 128;                    // one 128-byte swizzle column of B
+constexpr uint32_t kBBytes = 2 * kBKatom;
 constexpr uint32_t kSABytes = kRowsTile * (kKStage / 32);    // 2048
 constexpr uint32_t kSBBytes = kNMax * (kKStage / 32);        // 1024
-constexpr uint32_t kOffB = kABytes, kOffSA = kABytes + kBBytes, kOffSB = kOffSA + kSABytes;
+constexpr uint32_t kOffB = kABytes, kOffSA = kOffB + kBBytes, kOffSB = kOffSA + kSABytes;
 constexpr uint32_t kStageBytes = kOffSB + kSBBytes;          // 52224 = 51 x 1024
-constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024;
-constexpr int kThreads = 320;
-constexpr int kSfWarp0 = 4, kProdWarp = 8, kMmaWarp = 9;
+constexpr uint32_t kFixBytes = 16384;                        // parts of a shared last tile
+constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kFixBytes + 1024;
+constexpr int kThreads = 352;
+constexpr int kSfWarp0 = 4, kProdWarp = 8, kMmaWarp = 9, kBWarp = 10;
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: accumulators in [0, 256), buffer b at 128 b, matrix m at + 64 m; the scale
-// ring in [256, 512), stage s at 256 + 64 s: A scales of MMA j at + 4 j (+ lane quarter),
-// B scales at + 32 + 4 j (+ 1 for B rows 32..63).
-constexpr uint32_t kAccCols = 128, kSfBase = 256, kSfStageCols = 64;
+// TMEM columns: accumulator buffer b at 128 b, matrix m at + 64 m; the scale ring at
+// 256 + 64 s for stage s: A scales of MMA j at + 4 j (+ lane quarter), B scales at
+// + 32 + 4 j (+ 1 for B rows 32..63).
+constexpr uint32_t kAccCols = 128, kMatCols = 64, kSfBase = 256, kSfStageCols = 64;
 constexpr int kEpiBar = 1;  // named barrier of the four epilogue warps
 
 static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+static_assert(kSfBase + kStages * kSfStageCols <= kTmemCols, "TMEM budget");
+static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
 
-struct TcArgs {
-  int K, R, KC, RT, k;
-  const int32_t *active, *seg_off, *seg_cnt, *meta, *perm, *ntile_base;
-  // GEMM1: activation terms out ([P * kTerms][I/2] codes, [P * kTerms][I/32] scales)
-  uint8_t *act_q, *act_sf;
-  int I, act_kind;
+struct FArgs {
+  int ph;                  // 0: w1, w3 -> act terms; 1: w2 -> gate * o
+  int k, L, I, act_kind;
   float b1, b2;
-  // GEMM2: gate-weighted per-assignment outputs [T*k][L]
+  int KC, RT, R;           // reduction chunks, row tiles, rows per expert
+  const int32_t *active, *seg_off, *seg_cnt, *meta, *perm, *ntile_base;
+  uint8_t *act_q, *act_sf;  // phase-0 output = phase-1 activation operand
   const float* gate;
-  float* ybuf;
-  // split tiles: partial sums [grid][2 * npart][128] and flags [grid]
-  float* part;
-  int npart;
-  int32_t* flags;
+  float* ybuf;              // [T*k][L]
+  float* part;              // [kTcMaxGrid] parts of shared tiles (one per CTA)
+  int npart;                // tokens per part
+  int32_t* flags;           // [kTcMaxGrid] part written (zeroed before the launch)
   int32_t* status;
 };
 
-struct Cursor {
-  int a, n, rt, kc, tile;
-};
+__device__ __forceinline__ long long range_lo(long long U, int c, int G) { return U * c / G; }
 
-__device__ __forceinline__ void cursor_at(Cursor& c, long long u, const TcArgs& a) {
-  const long long t = u / a.KC;
-  c.kc = (int)(u - t * a.KC);
-  c.tile = (int)t;
-  const int ntg = (int)(t / a.RT);
-  c.rt = (int)(t - (long long)ntg * a.RT);
-  int lo = 0, hi = a.meta[0] - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (a.ntile_base[mid] <= ntg) lo = mid;
-    else hi = mid - 1;
-  }
-  c.a = lo;
-  c.n = ntg - a.ntile_base[lo];
-}
-
-__device__ __forceinline__ void cursor_next(Cursor& c, const TcArgs& a) {
-  if (++c.kc < a.KC) return;
-  c.kc = 0;
-  ++c.tile;
-  if (++c.rt < a.RT) return;
-  c.rt = 0;
-  if (++c.n < (a.seg_cnt[c.a] + kTokTile - 1) / kTokTile) return;
-  c.n = 0;
-  ++c.a;
+// floats of one CTA's part: NM matrices x npart tokens x 128 rows, element (m, j, r) at
+// (m * npart + j) * 128 + r
+__device__ __forceinline__ size_t part_floats(int NM, int npart) {
+  return (size_t)NM * npart * 128;
 }
 
 struct TileInfo {
-  int expert, pos0, ntok, N;
+  int rt, expert, pos0, ntok, N;
 };
-__device__ __forceinline__ TileInfo tile_info(const Cursor& c, const TcArgs& a) {
+// tile -> (active expert slot, token group, row tile) and what the kernel needs of it
+__device__ __forceinline__ TileInfo tile_info(int tile, const FArgs& f) {
   TileInfo t;
-  t.expert = a.active[c.a];
-  t.pos0 = a.seg_off[c.a] + c.n * kTokTile;
-  t.ntok = min(kTokTile, a.seg_cnt[c.a] - c.n * kTokTile);
+  const int ntg = tile / f.RT;
+  t.rt = tile - ntg * f.RT;
+  int lo = 0, hi = f.meta[0] - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (f.ntile_base[mid] <= ntg) lo = mid;
+    else hi = mid - 1;
+  }
+  const int n = ntg - f.ntile_base[lo];
+  t.expert = f.active[lo];
+  t.pos0 = f.seg_off[lo] + n * kTokTile;
+  t.ntok = min(kTokTile, f.seg_cnt[lo] - n * kTokTile);
   t.N = ((t.ntok * kTerms + 15) / 16) * 16;
   return t;
 }
@@ -142,42 +135,54 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
   return v;
 }
 
-// 16 TMEM columns of this warp's lane quarter into registers (load and wait in one asm, so
-// no register is read before the data is there)
-__device__ __forceinline__ void tmem_load16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "{\n\ttcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
-      "%10, %11, %12, %13, %14, %15}, [%16];\n\ttcgen05.wait::ld.sync.aligned;\n\t}"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+// generic-proxy global writes seen through an acquire -> later bulk/TMA (async proxy) reads
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
-    k_moe_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mS0,
-             const __grid_constant__ CUtensorMap mA1, const __grid_constant__ CUtensorMap mS1,
-             const __grid_constant__ CUtensorMap mB, const __grid_constant__ CUtensorMap mSB,
-             const TcArgs a) {
-  constexpr int NM = MODE == 0 ? 2 : 1;  // weight matrices per unit (w1 and w3, or w2)
+// Maps: phase 0: [0] w1 [1] w1 scales [2] w3 [3] w3 scales [4] x terms [5] their scales;
+// phase 1: [0] w2 [1] w2 scales [2] w2 [3] w2 scales [4] act terms [5] their scales.
+struct Maps {
+  CUtensorMap m[6];
+};
+
+// The CTA's range in tiles: the first tile (maybe shared, part at the front), whole tiles,
+// the last tile (maybe shared, this CTA its head: parts of later CTAs are added to it).
+struct Range {
+  long long u0, u1;
+  int t_first, t_last;
+  bool tail_first;   // the first tile started in an earlier CTA: leave a part
+  bool head_last;    // the last tile continues in later CTAs: add their parts
+};
+__device__ __forceinline__ Range make_range(long long U, int KC, int c, int G) {
+  Range r;
+  r.u0 = range_lo(U, c, G);
+  r.u1 = range_lo(U, c + 1, G);
+  r.t_first = (int)(r.u0 / KC);
+  r.t_last = r.u1 > r.u0 ? (int)((r.u1 - 1) / KC) : r.t_first - 1;
+  r.tail_first = r.u1 > r.u0 && r.u0 % KC != 0;
+  r.head_last = r.u1 > r.u0 && r.u1 % KC != 0 && (r.t_last != r.t_first || !r.tail_first);
+  return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ Maps mp,
+                                                        const FArgs f) {
   extern __shared__ uint8_t dsm[];
-  __shared__ __align__(8) uint64_t full[kStages], sfready[kStages], empty[kStages];
-  __shared__ __align__(8) uint64_t accfull[2], accempty[2], drained;
+  __shared__ __align__(8) uint64_t fullA[kStages], fullB[kStages], sfready[kStages], empty[kStages];
+  __shared__ __align__(8) uint64_t accfull[2], accempty[2], drained, fixfull;
   __shared__ uint32_t tbase;
   __shared__ int abort_flag;
-  __shared__ int flag_ok;
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) &
                                            ~uintptr_t(1023));
+  float* fix = reinterpret_cast<float*>(sm + (size_t)kStages * kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int NM = f.ph == 0 ? 2 : 1;  // weight matrices per unit: w1 and w3, or w2
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&fullA[s], 1);
+      mbar_init(&fullB[s], 1);
       mbar_init(&sfready[s], 4);
       mbar_init(&empty[s], 1);
     }
@@ -186,65 +191,113 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&accempty[b], 4);
     }
     mbar_init(&drained, 1);
+    mbar_init(&fixfull, 1);
     fence_mbar_init();
     abort_flag = 0;
   }
-  pdl_wait();
-  const long long U = (long long)a.ntile_base[a.meta[0]] * a.RT * a.KC;
-  const long long u0 = U * blockIdx.x / gridDim.x, u1 = U * (blockIdx.x + 1) / gridDim.x;
-  const bool busy = u1 > u0;
-  if (warp == kMmaWarp && busy) {
+  if (warp == kMmaWarp) {
     tc::tmem_alloc(&tbase, kTmemCols);
     tc::tmem_relinquish();
   }
+  if (warp == kProdWarp && lane == 0)
+    for (int i = 0; i < 6; ++i) tc::tma_prefetch_map(&mp.m[i]);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  pdl_wait();
   pdl_launch();
-  if (!busy) return;
   const uint32_t t0 = tbase;
   volatile int* abort_v = &abort_flag;
 
-  if (warp == kProdWarp) {
-    // ---------------------------------------------------------------- TMA producer
+  const long long U = (long long)f.ntile_base[f.meta[0]] * f.RT * f.KC;
+  const Range rg = make_range(U, f.KC, cta, G);
+  const int ntiles = rg.t_last - rg.t_first + 1;  // tiles this CTA touches (0 if idle)
+  // the later CTAs whose parts the head tile needs, and where their parts land in `fix`
+  int fix_c0 = cta + 1, fix_c1 = cta;  // [fix_c0, fix_c1]
+  if (rg.head_last) {
+    const long long tend = (long long)(rg.t_last + 1) * f.KC;
+    while (fix_c1 + 1 < G && range_lo(U, fix_c1 + 1, G) < tend) ++fix_c1;
+  }
+  const size_t pf = part_floats(NM, f.npart);
+  // an idle CTA (empty range, when there are fewer units than CTAs) leaves no part
+  auto idle = [&](int c) { return range_lo(U, c + 1, G) == range_lo(U, c, G); };
+  int nfix = 0;
+  for (int c = fix_c0; c <= fix_c1; ++c) nfix += idle(c) ? 0 : 1;
+  const bool fix_smem = (size_t)nfix * pf * 4 <= kFixBytes;
+
+  if (warp == kProdWarp || warp == kBWarp) {
+    // ------------------------------------- TMA: weights (warp 8), activations (warp 10)
     if (lane == 0) {
-      tc::tma_prefetch_map(&mA0);
-      tc::tma_prefetch_map(&mS0);
-      tc::tma_prefetch_map(&mB);
-      tc::tma_prefetch_map(&mSB);
-      Cursor c;
-      cursor_at(c, u0, a);
+      const bool wts = warp == kProdWarp;
       int it = 0;
-      for (long long u = u0; u < u1 && !*abort_v; ++u, cursor_next(c, a)) {
-        const TileInfo ti = tile_info(c, a);
+      bool stop = false;
+      for (int ti_ = 0; ti_ < ntiles && !stop; ++ti_) {
+        const int tile = rg.t_first + ti_;
+        const TileInfo ti = tile_info(tile, f);
+        const int kb = ti_ == 0 ? (int)(rg.u0 - (long long)tile * f.KC) : 0;
+        const int ke = ti_ == ntiles - 1 ? (int)(rg.u1 - (long long)tile * f.KC) : f.KC;
         const int nbox = ti.N / 16;
-        const int arow = ti.expert * a.R + c.rt * kRowsTile;
-        for (int m = 0; m < NM; ++m, ++it) {
-          const int s = it % kStages;
-          if (it >= kStages && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1, a.status)) {
-            *abort_v = 1;
+        const int arow = ti.expert * f.R + ti.rt * kRowsTile;
+        for (int kc = kb; kc < ke && !stop; ++kc) {
+          for (int m = 0; m < NM; ++m, ++it) {
+            const int s = it % kStages;
+            if (*abort_v ||
+                (it >= kStages && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1, f.status))) {
+              *abort_v = 1;
+              stop = true;
+              break;
+            }
+            uint8_t* st = sm + (size_t)s * kStageBytes;
+            if (wts) {
+              mbar_arrive_expect_tx(&fullA[s], kABytes + kSABytes);
+              tc::tma_load_2d(st, &mp.m[2 * m], kc * 256, arow, &fullA[s]);
+              tc::tma_load_2d(st + 16384, &mp.m[2 * m], kc * 256 + 128, arow, &fullA[s]);
+              tc::tma_load_2d(st + kOffSA, &mp.m[2 * m + 1], kc * 16, arow, &fullA[s]);
+            } else {
+              const int brow0 = ti.pos0 * kTerms;
+              mbar_arrive_expect_tx(&fullB[s], (uint32_t)nbox * (2 * 2048 + 256));
+              for (int b = 0; b < nbox; ++b) {
+                tc::tma_load_2d(st + kOffB + b * 2048, &mp.m[4], kc * 256, brow0 + 16 * b, &fullB[s]);
+                tc::tma_load_2d(st + kOffB + kBKatom + b * 2048, &mp.m[4], kc * 256 + 128,
+                                brow0 + 16 * b, &fullB[s]);
+                tc::tma_load_2d(st + kOffSB + b * 256, &mp.m[5], kc * 16, brow0 + 16 * b, &fullB[s]);
+              }
+            }
+          }
+        }
+      }
+      if (!wts && !stop && rg.head_last && fix_smem) {
+        // parts of the shared last tile: wait for each later CTA's flag, then bulk-copy its
+        // part into `fix` (it lands while this CTA's last MMAs run)
+        mbar_arrive_expect_tx(&fixfull, (uint32_t)(nfix * pf * 4));
+        bool ok = true;
+        int slot = 0;
+        for (int c = fix_c0; c <= fix_c1 && ok; ++c) {
+          if (idle(c)) continue;
+          int got = 0;
+          for (uint32_t q = 0; q < kWaitPolls && !got && !*abort_v; ++q) {
+            got = ld_acquire(f.flags + c) == 1;
+            if (!got) __nanosleep(256);
+          }
+          if (!got) {
+            ok = false;
             break;
           }
-          uint8_t* st = sm + (size_t)s * kStageBytes;
-          const CUtensorMap* mA = m == 0 ? &mA0 : &mA1;
-          const CUtensorMap* mS = m == 0 ? &mS0 : &mS1;
-          mbar_arrive_expect_tx(&full[s], kABytes + kSABytes + (uint32_t)nbox * (2 * 2048 + 256));
-          tc::tma_load_2d(st, mA, c.kc * 256, arow, &full[s]);
-          tc::tma_load_2d(st + 16384, mA, c.kc * 256 + 128, arow, &full[s]);
-          tc::tma_load_2d(st + kOffSA, mS, c.kc * 16, arow, &full[s]);
-          for (int b = 0; b < nbox; ++b) {
-            const int brow = ti.pos0 * kTerms + 16 * b;
-            tc::tma_load_2d(st + kOffB + b * 2048, &mB, c.kc * 256, brow, &full[s]);
-            tc::tma_load_2d(st + kOffB + 8192 + b * 2048, &mB, c.kc * 256 + 128, brow, &full[s]);
-            tc::tma_load_2d(st + kOffSB + b * 256, &mSB, c.kc * 16, brow, &full[s]);
-          }
+          fence_proxy_async_global();
+          bulk_g2s(fix + (size_t)slot * pf, f.part + (size_t)c * pf, (uint32_t)(pf * 4), &fixfull);
+          ++slot;
+        }
+        if (!ok) {
+          if (!*abort_v && f.status) atomicAdd(f.status + kStatTimeout, 1);
+          *abort_v = 1;
+          stop = true;
         }
       }
       if (*abort_v) {
         // copies still in flight land before the CTA leaves: wait for each stage's last fill
         for (int d = 1; d <= kStages && d <= it; ++d) {
           const int i = it - d;
-          mbar_wait(&full[i % kStages], (i / kStages) & 1, nullptr);
+          mbar_wait(wts ? &fullA[i % kStages] : &fullB[i % kStages], (i / kStages) & 1, nullptr);
         }
       }
     }
@@ -253,227 +306,213 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- scales -> TMEM
     const int q = warp & 3;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-    Cursor c;
-    cursor_at(c, u0, a);
     int it = 0;
     bool stop = false;
-    for (long long u = u0; u < u1 && !stop; ++u, cursor_next(c, a)) {
-      const int N = tile_info(c, a).N;
-      for (int m = 0; m < NM; ++m, ++it) {
-        const int s = it % kStages;
-        const bool ok = !*abort_v && mbar_wait(&full[s], (it / kStages) & 1, lane == 0 ? a.status : nullptr);
-        if (!__all_sync(0xffffffffu, ok)) {
-          *abort_v = 1;
-          stop = true;
-          break;
-        }
-        const uint8_t* st = sm + (size_t)s * kStageBytes;
-        const uint32_t ring = t0 + lane_off + kSfBase + (uint32_t)s * kSfStageCols;
-        const uint4 sa = *reinterpret_cast<const uint4*>(st + kOffSA + 16 * (32 * q + lane));
-        const uint32_t wa[4] = {clear_ff_bytes(sa.x), clear_ff_bytes(sa.y), clear_ff_bytes(sa.z),
-                                clear_ff_bytes(sa.w)};
-#pragma unroll
-        for (int j = 0; j < kMmas; ++j)
-          tc::tmem_st_x1(ring + 4 * j + q, (wa[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-        const uint4 sb0 = *reinterpret_cast<const uint4*>(st + kOffSB + 16 * lane);
-        const uint32_t wb0[4] = {sb0.x, sb0.y, sb0.z, sb0.w};
-#pragma unroll
-        for (int j = 0; j < kMmas; ++j)
-          tc::tmem_st_x1(ring + 32 + 4 * j, (wb0[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-        if (N > 32) {
-          const uint4 sb1 = *reinterpret_cast<const uint4*>(st + kOffSB + 16 * (32 + lane));
-          const uint32_t wb1[4] = {sb1.x, sb1.y, sb1.z, sb1.w};
+    for (int ti_ = 0; ti_ < ntiles && !stop; ++ti_) {
+      const int tile = rg.t_first + ti_;
+      const int N = tile_info(tile, f).N;
+      const int kb = ti_ == 0 ? (int)(rg.u0 - (long long)tile * f.KC) : 0;
+      const int ke = ti_ == ntiles - 1 ? (int)(rg.u1 - (long long)tile * f.KC) : f.KC;
+      for (int kc = kb; kc < ke && !stop; ++kc) {
+        for (int m = 0; m < NM; ++m, ++it) {
+          const int s = it % kStages;
+          const uint32_t par = (it / kStages) & 1;
+          const bool ok = !*abort_v &&
+                          mbar_wait(&fullA[s], par, lane == 0 ? f.status : nullptr) &&
+                          mbar_wait(&fullB[s], par, lane == 0 ? f.status : nullptr);
+          if (!__all_sync(0xffffffffu, ok)) {
+            *abort_v = 1;
+            stop = true;
+            break;
+          }
+          const uint8_t* st = sm + (size_t)s * kStageBytes;
+          const uint32_t ring = t0 + lane_off + kSfBase + (uint32_t)s * kSfStageCols;
+          const uint4 sa = *reinterpret_cast<const uint4*>(st + kOffSA + 16 * (32 * q + lane));
+          const uint32_t wa[4] = {clear_ff_bytes(sa.x), clear_ff_bytes(sa.y), clear_ff_bytes(sa.z),
+                                  clear_ff_bytes(sa.w)};
 #pragma unroll
           for (int j = 0; j < kMmas; ++j)
-            tc::tmem_st_x1(ring + 33 + 4 * j, (wb1[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+            tc::tmem_st_x1(ring + 4 * j + q, (wa[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+          const uint4 sb0 = *reinterpret_cast<const uint4*>(st + kOffSB + 16 * lane);
+          const uint32_t wb0[4] = {sb0.x, sb0.y, sb0.z, sb0.w};
+#pragma unroll
+          for (int j = 0; j < kMmas; ++j)
+            tc::tmem_st_x1(ring + 32 + 4 * j, (wb0[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+          if (N > 32) {
+            const uint4 sb1 = *reinterpret_cast<const uint4*>(st + kOffSB + 16 * (32 + lane));
+            const uint32_t wb1[4] = {sb1.x, sb1.y, sb1.z, sb1.w};
+#pragma unroll
+            for (int j = 0; j < kMmas; ++j)
+              tc::tmem_st_x1(ring + 33 + 4 * j, (wb1[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+          }
+          tc::tmem_st_wait();
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sfready[s]);
         }
-        tc::tmem_st_wait();
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sfready[s]);
       }
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issue
     if (lane == 0) {
-      Cursor c;
-      cursor_at(c, u0, a);
-      int it = 0, tcount = 0;
-      for (long long u = u0; u < u1 && !*abort_v; ++u, cursor_next(c, a)) {
-        const bool first = (u == u0) || c.kc == 0;
-        const bool last = (u == u1 - 1) || c.kc == a.KC - 1;
-        const int b = tcount & 1;
-        if (first && tcount >= 2 && !mbar_wait(&accempty[b], ((tcount >> 1) - 1) & 1, a.status)) {
+      int it = 0;
+      bool stop = false;
+      for (int ti_ = 0; ti_ < ntiles && !stop; ++ti_) {
+        const int tile = rg.t_first + ti_;
+        const int kb = ti_ == 0 ? (int)(rg.u0 - (long long)tile * f.KC) : 0;
+        const int ke = ti_ == ntiles - 1 ? (int)(rg.u1 - (long long)tile * f.KC) : f.KC;
+        const int b = ti_ & 1;
+        if (ti_ >= 2 && !mbar_wait(&accempty[b], ((ti_ >> 1) - 1) & 1, f.status)) {
           *abort_v = 1;
+          stop = true;
           break;
         }
-        const uint32_t idesc = tc::idesc_mxf4(kRowsTile, tile_info(c, a).N, 0, 0);
-        bool ok = true;
-        for (int m = 0; m < NM; ++m, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1;
-          if (!mbar_wait(&full[s], ph, a.status) || !mbar_wait(&sfready[s], ph, a.status)) {
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-          const uint32_t st = tc::smem_addr(sm + (size_t)s * kStageBytes);
-          const uint32_t d = t0 + (uint32_t)b * kAccCols + 64u * m;
-          const uint32_t sfr = t0 + kSfBase + (uint32_t)s * kSfStageCols;
+        const uint32_t idesc = tc::idesc_mxf4(kRowsTile, tile_info(tile, f).N, 0, 0);
+        for (int kc = kb; kc < ke && !stop; ++kc) {
+          for (int m = 0; m < NM; ++m, ++it) {
+            const int s = it % kStages;
+            const uint32_t par = (it / kStages) & 1;
+            if (*abort_v || !mbar_wait(&fullA[s], par, f.status) ||
+                !mbar_wait(&fullB[s], par, f.status) || !mbar_wait(&sfready[s], par, f.status)) {
+              *abort_v = 1;
+              stop = true;
+              break;
+            }
+            tc::fence_after_sync();
+            const uint32_t st = tc::smem_addr(sm + (size_t)s * kStageBytes);
+            const uint32_t d = t0 + (uint32_t)b * kAccCols + kMatCols * m;
+            const uint32_t sfr = t0 + kSfBase + (uint32_t)s * kSfStageCols;
 #pragma unroll
-          for (int j = 0; j < kMmas; ++j) {
-            const uint32_t koff = (uint32_t)(j >> 2) * 16384u + (uint32_t)(j & 3) * 32u;
-            const uint32_t kboff = (uint32_t)(j >> 2) * 8192u + (uint32_t)(j & 3) * 32u;
-            const uint64_t ad = tc::smem_desc(st + koff, 16, 1024, tc::kLayout128B);
-            const uint64_t bd = tc::smem_desc(st + kOffB + kboff, 16, 1024, tc::kLayout128B);
-            tc::mma_mxf4(d, ad, bd, idesc, sfr + 4 * j, sfr + 32 + 4 * j,
-                         (first && j == 0) ? 0u : 1u);
+            for (int j = 0; j < kMmas; ++j) {
+              const uint32_t koff = (uint32_t)(j >> 2) * 16384u + (uint32_t)(j & 3) * 32u;
+              const uint32_t kboff = (uint32_t)(j >> 2) * kBKatom + (uint32_t)(j & 3) * 32u;
+              const uint64_t ad = tc::smem_desc(st + koff, 16, 1024, tc::kLayout128B);
+              const uint64_t bd = tc::smem_desc(st + kOffB + kboff, 16, 1024, tc::kLayout128B);
+              tc::mma_mxf4(d, ad, bd, idesc, sfr + 4 * j, sfr + 32 + 4 * j,
+                           (kc == kb && j == 0) ? 0u : 1u);
+            }
+            tc::mma_commit(&empty[s]);
           }
-          tc::mma_commit(&empty[s]);
         }
-        if (!ok) {
-          *abort_v = 1;
-          break;
-        }
-        if (last) {
-          tc::mma_commit(&accfull[b]);
-          ++tcount;
-        }
+        if (!stop) tc::mma_commit(&accfull[b]);
       }
       tc::mma_commit(&drained);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 4) {
     // ---------------------------------------------------------------- epilogue (warps 0-3)
+    // Token by token (a short loop, not unrolled: this code runs once per tile, at the end
+    // of the kernel for the last one, and stays small): each token's kTerms columns come
+    // straight from TMEM and are summed in column order.
     const int q = warp;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     const int row = 32 * q + lane;  // row within the tile
-    int tcount = 0;
-    long long u = u0;
-    while (u < u1) {
-      Cursor c;
-      cursor_at(c, u, a);
-      const TileInfo ti = tile_info(c, a);
-      const long long tu0 = (long long)c.tile * a.KC, tu1 = tu0 + a.KC;
-      const bool head = tu0 >= u0;
-      const int b = tcount & 1;
-      const int bad = (*abort_v || !mbar_wait(&accfull[b], (tcount >> 1) & 1, a.status)) ? 1 : 0;
+    for (int ti_ = 0; ti_ < ntiles; ++ti_) {
+      const int tile = rg.t_first + ti_;
+      const TileInfo ti = tile_info(tile, f);
+      const int b = ti_ & 1;
+      const bool write_part = ti_ == 0 && rg.tail_first;          // leave a part for the head
+      const bool add_parts = ti_ == ntiles - 1 && rg.head_last;    // add the later CTAs' parts
+      int bad = (*abort_v || !mbar_wait(&accfull[b], (ti_ >> 1) & 1, f.status)) ? 1 : 0;
+      if (add_parts && !bad) {
+        if (fix_smem) {
+          // the helper's copies complete this phase; if it gave up it set abort_v, and the
+          // bounded wait ends here as well
+          bad = (*abort_v || !mbar_wait(&fixfull, 0, f.status)) ? 1 : 0;
+        } else if (threadIdx.x == 0) {
+          // parts too large for `fix`: wait for their flags here, read them from global below
+          for (int c = fix_c0; c <= fix_c1 && !bad; ++c) {
+            if (idle(c)) continue;
+            int got = 0;
+            for (uint32_t qq = 0; qq < kWaitPolls && !got && !*abort_v; ++qq) {
+              got = ld_acquire(f.flags + c) == 1;
+              if (!got) __nanosleep(256);
+            }
+            if (!got) {
+              if (!*abort_v && f.status) atomicAdd(f.status + kStatTimeout, 1);
+              bad = 1;
+            }
+          }
+        }
+      }
       if (bar_or(kEpiBar, 128, bad)) {
         *abort_v = 1;
         break;
       }
       tc::fence_after_sync();
-      float acc[NM][kNMax];
+      const uint32_t tacc = t0 + lane_off + (uint32_t)b * kAccCols;
+      const int grp = (ti.rt * kRowsTile + 32 * q) >> 5;            // phase 0: act group
+      const bool in_range = ti.rt * kRowsTile + 32 * q < f.R;
+      float* mine = f.part + (size_t)cta * pf;
+#pragma unroll 1
+      for (int j = 0; j < ti.ntok; ++j) {
+        float v[2] = {0.f, 0.f};
 #pragma unroll
-      for (int m = 0; m < NM; ++m)
-#pragma unroll
-        for (int c0 = 0; c0 < kNMax; c0 += 16) {
-          float v[16];
-          if (c0 < ti.N) {
-            tmem_load16(t0 + lane_off + (uint32_t)b * kAccCols + 64u * m + c0, v);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = 0.f;
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) acc[m][c0 + i] = v[i];
+        for (int m = 0; m < 2; ++m) {
+          if (m >= NM) break;
+          uint32_t r[4];
+          asm volatile(
+              "{\n\ttcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];\n\t"
+              "tcgen05.wait::ld.sync.aligned;\n\t}"
+              : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+              : "r"(tacc + kMatCols * m + (uint32_t)(j * kTerms))
+              : "memory");
+          v[m] = ((__uint_as_float(r[0]) + __uint_as_float(r[1])) + __uint_as_float(r[2])) +
+                 __uint_as_float(r[3]);
         }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&accempty[b]);
-      ++tcount;
-
-      float* my_part = a.part + (size_t)blockIdx.x * 2 * a.npart * kRowsTile;
-      if (!head) {
-        // leave the partial sums for the tile's first CTA
-#pragma unroll
-        for (int m = 0; m < NM; ++m)
-#pragma unroll
-          for (int cc = 0; cc < kNMax; ++cc)
-            if (cc < ti.N) my_part[((size_t)m * a.npart + cc) * kRowsTile + row] = acc[m][cc];
-        __threadfence();
-        named_bar(kEpiBar, 128);
-        if (threadIdx.x == 0) st_release(a.flags + blockIdx.x, 1);
-      } else {
-        bool failed = false;
-        if (tu1 > u1) {
-          for (int oc = blockIdx.x + 1; oc < (int)gridDim.x; ++oc) {
-            const long long ou0 = U * oc / gridDim.x;
-            if (ou0 >= tu1) break;
-            if (U * (oc + 1) / gridDim.x == ou0) continue;  // an idle CTA leaves nothing
-            if (threadIdx.x == 0) {
-              int ok = 0;
-              for (uint32_t i = 0; i < kWaitPolls && !ok; ++i) ok = ld_acquire(a.flags + oc) == 1;
-              if (!ok && a.status) atomicAdd(a.status + kStatTimeout, 1);
-              flag_ok = ok;
+        if (write_part) {
+          for (int m = 0; m < NM; ++m) mine[((size_t)m * f.npart + j) * kRowsTile + row] = v[m];
+          continue;
+        }
+        if (add_parts) {
+          for (int m = 0; m < NM; ++m) {
+            const size_t off = ((size_t)m * f.npart + j) * kRowsTile + row;
+            int slot = 0;
+            for (int c = fix_c0; c <= fix_c1; ++c) {
+              if (idle(c)) continue;
+              v[m] += fix_smem ? fix[(size_t)slot * pf + off] : __ldcg(f.part + (size_t)c * pf + off);
+              ++slot;
             }
-            named_bar(kEpiBar, 128);
-            const bool got = flag_ok != 0;
-            named_bar(kEpiBar, 128);  // flag_ok is rewritten by the next wait
-            if (!got) {
-              *abort_v = 1;
-              failed = true;
-              break;
-            }
-            const float* op = a.part + (size_t)oc * 2 * a.npart * kRowsTile;
-#pragma unroll
-            for (int m = 0; m < NM; ++m)
-#pragma unroll
-              for (int cc = 0; cc < kNMax; ++cc)
-                if (cc < ti.N) acc[m][cc] += __ldcg(op + ((size_t)m * a.npart + cc) * kRowsTile + row);
           }
         }
-        if (failed) break;
-        const int r_exp = c.rt * kRowsTile + row;  // row within the expert
-        if (MODE == 0) {
-          // SwiGLU (or SiTU-GLU) per token, then its kTerms MXFP4 terms for the second GEMM;
-          // this warp's 32 rows are one group of 32 along the second GEMM's reduction
-          const bool in_range = c.rt * kRowsTile + 32 * q < a.R;
-#pragma unroll
-          for (int j = 0; j < kTokTile; ++j) {
-            if (j >= ti.ntok) break;
-            float g = 0.f, uu = 0.f;
+        if (f.ph == 0) {
+          // SwiGLU (or SiTU-GLU), then the token's kTerms MXFP4 terms for phase 1; this warp's
+          // 32 rows are one group of 32 along phase 1's reduction
+          const float act = activation(v[0], v[1], f.act_kind, f.b1, f.b2);
+          uint32_t words[kTerms], sfb[kTerms];
+          mx_split_group(act, words, sfb);
+          if (in_range) {
+            const size_t p = (size_t)(ti.pos0 + j);
 #pragma unroll
             for (int t = 0; t < kTerms; ++t) {
-              g += acc[0][j * kTerms + t];
-              uu += acc[NM - 1][j * kTerms + t];
-            }
-            const float act = activation(g, uu, a.act_kind, a.b1, a.b2);
-            uint32_t words[kTerms], sf[kTerms];
-            mx_split_group(act, words, sf);
-            if (in_range) {
-              const size_t p = (size_t)(ti.pos0 + j);
-              const int grp = (c.rt * kRowsTile + 32 * q) >> 5;
-#pragma unroll
-              for (int t = 0; t < kTerms; ++t) {
-                const size_t r2 = p * kTerms + t;
-                if ((lane & 7) == 0)
-                  *reinterpret_cast<uint32_t*>(a.act_q + r2 * (size_t)(a.I >> 1) + grp * 16 +
-                                               4 * (lane >> 3)) = words[t];
-                if (lane == 0) a.act_sf[r2 * (size_t)(a.I >> 5) + grp] = (uint8_t)sf[t];
-              }
+              const size_t r2 = p * kTerms + t;
+              if ((lane & 7) == 0)
+                *reinterpret_cast<uint32_t*>(f.act_q + r2 * (size_t)(f.I >> 1) + grp * 16 +
+                                             4 * (lane >> 3)) = words[t];
+              if (lane == 0) f.act_sf[r2 * (size_t)(f.I >> 5) + grp] = (uint8_t)sfb[t];
             }
           }
         } else {
-#pragma unroll
-          for (int j = 0; j < kTokTile; ++j) {
-            if (j >= ti.ntok) break;
-            float o = 0.f;
-#pragma unroll
-            for (int t = 0; t < kTerms; ++t) o += acc[0][j * kTerms + t];
-            const int asg = a.perm[ti.pos0 + j];
-            if (r_exp < a.R) a.ybuf[(size_t)asg * a.R + r_exp] = a.gate[asg] * o;
-          }
+          const int asg = f.perm[ti.pos0 + j];
+          const int r_exp = ti.rt * kRowsTile + row;  // row within the expert
+          if (r_exp < f.R) f.ybuf[(size_t)asg * f.L + r_exp] = f.gate[asg] * v[0];
         }
       }
-      u = min(u1, tu1);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&accempty[b]);
+      if (write_part) {
+        __threadfence();
+        named_bar(kEpiBar, 128);
+        if (threadIdx.x == 0) st_release(f.flags + cta, 1);
+      }
     }
   }
 
   // ------------------------------------------------------------------ teardown
   __syncthreads();
   if (warp == kMmaWarp) {
-    if (lane == 0) mbar_wait(&drained, 0, a.status);
+    if (lane == 0) mbar_wait(&drained, 0, f.status);
     __syncwarp();
     tc::fence_after_sync();
     tc::tmem_dealloc(t0, kTmemCols);
@@ -495,11 +534,15 @@ __global__ void __launch_bounds__(512) k_split_x(const uint16_t* __restrict__ x,
   const float v = __uint_as_float((uint32_t)x[(size_t)t * L + 32 * grp + lane] << 16);
   uint32_t words[kTerms], sf[kTerms];
   mx_split_group(v, words, sf);
+  int my_pos = -1;  // lane j < k: perm position of assignment j of this token (-1: dropped)
+  if (lane < k) {
+    const int e = idx[t * k + lane];
+    if (e >= 0 && e < E) my_pos = inv[t * k + lane];
+  }
   for (int j = 0; j < k; ++j) {
-    const int asg = t * k + j;
-    const int e = idx[asg];
-    if (e < 0 || e >= E) continue;
-    const size_t p = (size_t)inv[asg];
+    const int pj = __shfl_sync(0xffffffffu, my_pos, j);
+    if (pj < 0) continue;
+    const size_t p = (size_t)pj;
 #pragma unroll
     for (int tt = 0; tt < kTerms; ++tt) {
       const size_t r = p * kTerms + tt;
@@ -510,36 +553,15 @@ __global__ void __launch_bounds__(512) k_split_x(const uint16_t* __restrict__ x,
   }
 }
 
-template <int MODE>
-cudaError_t launch_tc(const CUtensorMap (&maps)[6], const TcArgs& a, int grid, cudaStream_t s,
-                      bool pdl) {
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_moe_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev] = 1;
-  }
-  return launch_kernel(k_moe_tc<MODE>, dim3(grid), dim3(kThreads), kSmemBytes, s, pdl, maps[0],
-                       maps[1], maps[2], maps[3], maps[4], maps[5], a);
-}
-
 }  // namespace
 
 bool tc_path_supported(int L, int I) { return L % kKStage == 0 && I % kKStage == 0; }
 
 int tc_grid() { return sm_count() < kTcMaxGrid ? sm_count() : kTcMaxGrid; }
 
-size_t tc_part_floats(int T) {
-  return (size_t)kTcMaxGrid * 2 * tc_npart(T) * kRowsTile;
-}
+int tc_npart(int T) { return T < kTokTile ? T : kTokTile; }  // tokens per tile, at most
 
-int tc_npart(int T) {
-  const int tok = T < kTokTile ? T : kTokTile;
-  return ((tok * kTerms + 15) / 16) * 16;
-}
+size_t tc_part_floats(int T) { return (size_t)kTcMaxGrid * 2 * tc_npart(T) * kRowsTile; }
 
 cudaError_t launch_split_x(const uint16_t* x, int T, int L, int k, int E, const int32_t* idx,
                            const int32_t* inv, uint8_t* xq, uint8_t* xsf, cudaStream_t s,
@@ -548,49 +570,55 @@ cudaError_t launch_split_x(const uint16_t* x, int T, int L, int k, int E, const 
                        inv, xq, xsf);
 }
 
-cudaError_t launch_tc_gemm1(const ExpertPtrs& w, int L, int I, int E, int T, int k,
-                            const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,
-                            uint8_t* act_q, uint8_t* act_sf, int act_kind, float b1, float b2,
-                            float* part, int32_t* flags, int32_t* status, cudaStream_t s,
-                            bool pdl) {
+cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k,
+                              const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,
+                              uint8_t* act_q, uint8_t* act_sf, int act_kind, float b1, float b2,
+                              const float* gate, float* ybuf, float* part, int32_t* status,
+                              cudaStream_t s, bool pdl, void (*between)(cudaStream_t)) {
   const uint64_t P4 = (uint64_t)T * k * kTerms;
-  CUtensorMap maps[6];
-  if (!make_map_2d(&maps[0], w.w1p, L / 2, (uint64_t)E * I, 128, 128, true) ||
-      !make_map_2d(&maps[1], w.w1s, L / 32, (uint64_t)E * I, 16, 128, false) ||
-      !make_map_2d(&maps[2], w.w3p, L / 2, (uint64_t)E * I, 128, 128, true) ||
-      !make_map_2d(&maps[3], w.w3s, L / 32, (uint64_t)E * I, 16, 128, false) ||
-      !make_map_2d(&maps[4], xq, L / 2, P4, 128, 16, true) ||
-      !make_map_2d(&maps[5], xsf, L / 32, P4, 16, 16, false))
+  Maps m0, m1;
+  if (!make_map_2d(&m0.m[0], w.w1p, L / 2, (uint64_t)E * I, 128, 128, true) ||
+      !make_map_2d(&m0.m[1], w.w1s, L / 32, (uint64_t)E * I, 16, 128, false) ||
+      !make_map_2d(&m0.m[2], w.w3p, L / 2, (uint64_t)E * I, 128, 128, true) ||
+      !make_map_2d(&m0.m[3], w.w3s, L / 32, (uint64_t)E * I, 16, 128, false) ||
+      !make_map_2d(&m0.m[4], xq, L / 2, P4, 128, 16, true) ||
+      !make_map_2d(&m0.m[5], xsf, L / 32, P4, 16, 16, false) ||
+      !make_map_2d(&m1.m[0], w.w2p, I / 2, (uint64_t)E * L, 128, 128, true) ||
+      !make_map_2d(&m1.m[1], w.w2s, I / 32, (uint64_t)E * L, 16, 128, false) ||
+      !make_map_2d(&m1.m[4], act_q, I / 2, P4, 128, 16, true) ||
+      !make_map_2d(&m1.m[5], act_sf, I / 32, P4, 16, 16, false))
     return cudaErrorInvalidValue;
-  TcArgs a{};
-  a.K = L; a.R = I; a.KC = L / kKStage; a.RT = (I + kRowsTile - 1) / kRowsTile; a.k = k;
-  a.active = b.active; a.seg_off = b.seg_off; a.seg_cnt = b.seg_cnt; a.meta = b.meta;
-  a.perm = b.perm; a.ntile_base = b.ntile_base;
-  a.act_q = act_q; a.act_sf = act_sf; a.I = I; a.act_kind = act_kind; a.b1 = b1; a.b2 = b2;
-  a.part = part; a.npart = tc_npart(T); a.flags = flags; a.status = status;
-  return launch_tc<0>(maps, a, tc_grid(), s, pdl);
-}
-
-cudaError_t launch_tc_gemm2(const ExpertPtrs& w, int L, int I, int E, int T, int k,
-                            const uint8_t* act_q, const uint8_t* act_sf, const float* gate,
-                            const BucketOut& b, float* ybuf, float* part, int32_t* flags,
-                            int32_t* status, cudaStream_t s, bool pdl) {
-  const uint64_t P4 = (uint64_t)T * k * kTerms;
-  CUtensorMap maps[6];
-  if (!make_map_2d(&maps[0], w.w2p, I / 2, (uint64_t)E * L, 128, 128, true) ||
-      !make_map_2d(&maps[1], w.w2s, I / 32, (uint64_t)E * L, 16, 128, false) ||
-      !make_map_2d(&maps[4], act_q, I / 2, P4, 128, 16, true) ||
-      !make_map_2d(&maps[5], act_sf, I / 32, P4, 16, 16, false))
-    return cudaErrorInvalidValue;
-  maps[2] = maps[0];
-  maps[3] = maps[1];
-  TcArgs a{};
-  a.K = I; a.R = L; a.KC = I / kKStage; a.RT = (L + kRowsTile - 1) / kRowsTile; a.k = k;
-  a.active = b.active; a.seg_off = b.seg_off; a.seg_cnt = b.seg_cnt; a.meta = b.meta;
-  a.perm = b.perm; a.ntile_base = b.ntile_base;
-  a.gate = gate; a.ybuf = ybuf;
-  a.part = part; a.npart = tc_npart(T); a.flags = flags; a.status = status;
-  return launch_tc<1>(maps, a, tc_grid(), s, pdl);
+  m1.m[2] = m1.m[0];
+  m1.m[3] = m1.m[1];
+  FArgs f{};
+  f.k = k; f.L = L; f.I = I; f.act_kind = act_kind; f.b1 = b1; f.b2 = b2;
+  f.active = b.active; f.seg_off = b.seg_off; f.seg_cnt = b.seg_cnt; f.meta = b.meta;
+  f.perm = b.perm; f.ntile_base = b.ntile_base;
+  f.act_q = act_q; f.act_sf = act_sf; f.gate = gate; f.ybuf = ybuf;
+  f.part = part; f.npart = tc_npart(T);
+  f.status = status;
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_moe_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = 1;
+  }
+  // phase 0 (w1, w3), then phase 1 (w2): the second launch reads what the first wrote, across
+  // the kernel boundary (its CTAs wait in griddepcontrol.wait until the first has completed)
+  f.ph = 0;
+  f.KC = L / kKStage; f.RT = (I + kRowsTile - 1) / kRowsTile; f.R = I;
+  f.flags = b.flags;
+  cudaError_t e = launch_kernel(k_moe_tc, dim3(tc_grid()), dim3(kThreads), kSmemBytes, s, pdl,
+                                m0, f);
+  if (e != cudaSuccess) return e;
+  if (between) between(s);
+  f.ph = 1;
+  f.KC = I / kKStage; f.RT = (L + kRowsTile - 1) / kRowsTile; f.R = L;
+  f.flags = b.flags + kTcMaxGrid;
+  return launch_kernel(k_moe_tc, dim3(tc_grid()), dim3(kThreads), kSmemBytes, s, true, m1, f);
 }
 
 }  // namespace k3
