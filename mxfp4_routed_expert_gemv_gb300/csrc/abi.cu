@@ -187,9 +187,12 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
                 ex->w2_scale};
   const bool fused_topk = route && prep_is_fused(T);
   K3_TRY(phase(0, s));
+  const bool one = w.tc && fused_topk && T == 1;  // router + one preparation launch
   if (route) {
     K3_TRY(launch_router_logits(static_cast<const uint16_t*>(h), static_cast<const uint16_t*>(wr),
-                                T, E, c->hidden, w.logits, s, false));
+                                T, E, c->hidden, w.logits, s, false,
+                                static_cast<const uint16_t*>(x), L, one ? w.xq : nullptr,
+                                one ? w.xsf : nullptr));
     if (!fused_topk)
       K3_TRY(launch_topk(w.logits, bias, T, E, K, c->renorm, c->routed_scale, idx, gate, gap, s,
                          true));
@@ -198,10 +201,14 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
   PrepArgs p{fused_topk ? w.logits : nullptr, bias, E, K, c->renorm, c->routed_scale, idx, gate,
              gap, T, L, static_cast<const uint16_t*>(x), w.tc ? nullptr : w.x16, w.xexp, w.b, y,
              status};
-  K3_TRY(launch_prep(p, s, route));
+  if (one) {
+    K3_TRY(launch_prep_one(p, s, route));
+  } else {
+    K3_TRY(launch_prep(p, s, route));
+    if (w.tc)
+      K3_TRY(launch_split_x(static_cast<const uint16_t*>(x), T, L, K, w.b, w.xq, w.xsf, s, true));
+  }
   if (w.tc) {
-    K3_TRY(launch_split_x(static_cast<const uint16_t*>(x), T, L, K, E, idx, w.b.inv, w.xq, w.xsf,
-                          s, true));
     K3_TRY(phase(2, s));
     K3_TRY(launch_tc_experts(ep, L, I, E, T, K, w.xq, w.xsf, w.b, w.aq, w.asf, c->act,
                              c->situ_b1, c->situ_b2, gate, w.ybuf, w.part, status, s, true,

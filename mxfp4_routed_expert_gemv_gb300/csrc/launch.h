@@ -36,8 +36,12 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 int sm_count();
 
 // router.cu
+// With xq set (T == 1 only) the launch also writes x's kTerms MXFP4 terms into rows
+// 0 .. kTerms-1 of xq / xsf.
 cudaError_t launch_router_logits(const uint16_t* h, const uint16_t* wr, int T, int E, int H,
-                                 float* logits, cudaStream_t s, bool pdl);
+                                 float* logits, cudaStream_t s, bool pdl,
+                                 const uint16_t* x = nullptr, int L = 0, uint8_t* xq = nullptr,
+                                 uint8_t* xsf = nullptr);
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,
                         float routed_scale, int32_t* idx, float* gate, float* gap,
                         cudaStream_t s, bool pdl);
@@ -84,6 +88,9 @@ struct PrepArgs {
 int bucket_chunks(int T);
 bool prep_is_fused(int T);
 cudaError_t launch_prep(const PrepArgs& p, cudaStream_t s, bool pdl);
+// One token with the router's top-k, tensor-core path: top-k and buckets in one launch
+// (E <= 1024, k <= 32); x's terms come from the router launch.
+cudaError_t launch_prep_one(const PrepArgs& p, cudaStream_t s, bool pdl);
 
 // gemv.cu
 struct ExpertPtrs {
@@ -110,9 +117,8 @@ bool tc_path_supported(int L, int I);
 int tc_grid();
 int tc_npart(int T);
 size_t tc_part_floats(int T);
-cudaError_t launch_split_x(const uint16_t* x, int T, int L, int k, int E, const int32_t* idx,
-                           const int32_t* inv, uint8_t* xq, uint8_t* xsf, cudaStream_t s,
-                           bool pdl);
+cudaError_t launch_split_x(const uint16_t* x, int T, int L, int k, const BucketOut& b,
+                           uint8_t* xq, uint8_t* xsf, cudaStream_t s, bool pdl);
 cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k,
                               const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,
                               uint8_t* act_q, uint8_t* act_sf, int act_kind, float b1, float b2,

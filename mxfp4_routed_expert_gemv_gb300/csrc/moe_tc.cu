@@ -63,6 +63,7 @@ static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
 
 struct FArgs {
   int ph;                  // 0: w1, w3 -> act terms; 1: w2 -> gate * o
+  int one_token;           // T == 1: phase-0 activation rows are 0 .. kTerms-1
   int k, L, I, act_kind;
   float b1, b2;
   int KC, RT, R;           // reduction chunks, row tiles, rows per expert
@@ -254,7 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
               tc::tma_load_2d(st + 16384, &mp.m[2 * m], kc * 256 + 128, arow, &fullA[s]);
               tc::tma_load_2d(st + kOffSA, &mp.m[2 * m + 1], kc * 16, arow, &fullA[s]);
             } else {
-              const int brow0 = ti.pos0 * kTerms;
+              // one token: its terms are rows 0 .. kTerms-1 whatever the position (the router
+              // launch writes only those; the per-position layout repeats them)
+              const int brow0 = f.one_token ? 0 : ti.pos0 * kTerms;
               mbar_arrive_expect_tx(&fullB[s], (uint32_t)nbox * (2 * 2048 + 256));
               for (int b = 0; b < nbox; ++b) {
                 tc::tma_load_2d(st + kOffB + b * 2048, &mp.m[4], kc * 256, brow0 + 16 * b, &fullB[s]);
@@ -521,35 +524,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
 
 // x (bf16, one row per token) -> kTerms MXFP4 terms per (token, expert) position, in the
 // bucket order: rows p * kTerms + t of xq [P*kTerms][L/2] and xsf [P*kTerms][L/32].  Grid
-// (T, L/512), 16 warps: warp w handles group 16 * blockIdx.y + w of token blockIdx.x.
+// (T*k positions, L/512): one CTA per position and 512-wide slice, warp w quantises group
+// 16 * blockIdx.y + w of the position's token; positions past the valid count leave.
 __global__ void __launch_bounds__(512) k_split_x(const uint16_t* __restrict__ x, int L, int k,
-                                                 int E, const int32_t* __restrict__ idx,
-                                                 const int32_t* __restrict__ inv,
+                                                 const int32_t* __restrict__ perm,
+                                                 const int32_t* __restrict__ meta,
                                                  uint8_t* __restrict__ xq,
                                                  uint8_t* __restrict__ xsf) {
   pdl_wait();
   pdl_launch();
-  const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pos = blockIdx.x;
+  if (pos >= meta[1]) return;
+  const int t = perm[pos] / k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = blockIdx.y * 16 + warp;
   const float v = __uint_as_float((uint32_t)x[(size_t)t * L + 32 * grp + lane] << 16);
   uint32_t words[kTerms], sf[kTerms];
   mx_split_group(v, words, sf);
-  int my_pos = -1;  // lane j < k: perm position of assignment j of this token (-1: dropped)
-  if (lane < k) {
-    const int e = idx[t * k + lane];
-    if (e >= 0 && e < E) my_pos = inv[t * k + lane];
-  }
-  for (int j = 0; j < k; ++j) {
-    const int pj = __shfl_sync(0xffffffffu, my_pos, j);
-    if (pj < 0) continue;
-    const size_t p = (size_t)pj;
 #pragma unroll
-    for (int tt = 0; tt < kTerms; ++tt) {
-      const size_t r = p * kTerms + tt;
-      if ((lane & 7) == 0)
-        *reinterpret_cast<uint32_t*>(xq + r * (size_t)(L >> 1) + grp * 16 + 4 * (lane >> 3)) = words[tt];
-      if (lane == 0) xsf[r * (size_t)(L >> 5) + grp] = (uint8_t)sf[tt];
-    }
+  for (int tt = 0; tt < kTerms; ++tt) {
+    const size_t r = (size_t)pos * kTerms + tt;
+    if ((lane & 7) == 0)
+      *reinterpret_cast<uint32_t*>(xq + r * (size_t)(L >> 1) + grp * 16 + 4 * (lane >> 3)) = words[tt];
+    if (lane == 0) xsf[r * (size_t)(L >> 5) + grp] = (uint8_t)sf[tt];
   }
 }
 
@@ -563,11 +560,11 @@ int tc_npart(int T) { return T < kTokTile ? T : kTokTile; }  // tokens per tile,
 
 size_t tc_part_floats(int T) { return (size_t)kTcMaxGrid * 2 * tc_npart(T) * kRowsTile; }
 
-cudaError_t launch_split_x(const uint16_t* x, int T, int L, int k, int E, const int32_t* idx,
-                           const int32_t* inv, uint8_t* xq, uint8_t* xsf, cudaStream_t s,
-                           bool pdl) {
-  return launch_kernel(k_split_x, dim3(T, L / kKStage), dim3(512), 0, s, pdl, x, L, k, E, idx,
-                       inv, xq, xsf);
+cudaError_t launch_split_x(const uint16_t* x, int T, int L, int k, const BucketOut& b,
+                           uint8_t* xq, uint8_t* xsf, cudaStream_t s, bool pdl) {
+  return launch_kernel(k_split_x, dim3(T * k, L / kKStage), dim3(512), 0, s, pdl, x, L, k,
+                       static_cast<const int32_t*>(b.perm), static_cast<const int32_t*>(b.meta),
+                       xq, xsf);
 }
 
 cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k,
@@ -609,6 +606,7 @@ cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, i
   // phase 0 (w1, w3), then phase 1 (w2): the second launch reads what the first wrote, across
   // the kernel boundary (its CTAs wait in griddepcontrol.wait until the first has completed)
   f.ph = 0;
+  f.one_token = T == 1;
   f.KC = L / kKStage; f.RT = (I + kRowsTile - 1) / kRowsTile; f.R = I;
   f.flags = b.flags;
   cudaError_t e = launch_kernel(k_moe_tc, dim3(tc_grid()), dim3(kThreads), kSmemBytes, s, pdl,
@@ -616,6 +614,7 @@ cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, i
   if (e != cudaSuccess) return e;
   if (between) between(s);
   f.ph = 1;
+  f.one_token = 0;
   f.KC = I / kKStage; f.RT = (L + kRowsTile - 1) / kRowsTile; f.R = L;
   f.flags = b.flags + kTcMaxGrid;
   return launch_kernel(k_moe_tc, dim3(tc_grid()), dim3(kThreads), kSmemBytes, s, true, m1, f);

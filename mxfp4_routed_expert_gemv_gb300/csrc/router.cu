@@ -5,6 +5,7 @@
 // by repeated arg-max where a tie goes to the lower expert index; the combine weights come
 // from the unbiased scores, renormalised over the chosen k and multiplied by routed_scale.
 #include "launch.h"
+#include "mxq.cuh"
 #include "topk.cuh"
 
 namespace k3 {
@@ -18,11 +19,17 @@ constexpr int kVecPerLane = 8;    // 16-byte pieces a lane keeps in flight per b
 // quarters, one warp each, and every lane issues all its 16-byte loads of a batch before
 // using them, so a row's bytes are in flight at once.  Products of bf16 values are exact;
 // each fused add rounds once (fp32).  The 4 quarter sums are added in a fixed order.
+// With xq set (one token), warps 0 .. L/32-1 of the grid also write the token's x as kTerms
+// MXFP4 terms (rows 0 .. kTerms-1 of xq / xsf): work that does not depend on the routing,
+// done here so that no separate launch is spent on it.
 template <int TT>
 __global__ void __launch_bounds__(256) k_router_logits(const uint16_t* __restrict__ h,
                                                        const uint16_t* __restrict__ wr, int T,
                                                        int E, int H,
-                                                       float* __restrict__ logits) {
+                                                       float* __restrict__ logits,
+                                                       const uint16_t* __restrict__ x, int L,
+                                                       uint8_t* __restrict__ xq,
+                                                       uint8_t* __restrict__ xsf) {
   pdl_wait();
   pdl_launch();
   __shared__ float part[8][TT];
@@ -74,6 +81,20 @@ __global__ void __launch_bounds__(256) k_router_logits(const uint16_t* __restric
     const float s = (part[w0][lane] + part[w0 + 1][lane]) + (part[w0 + 2][lane] + part[w0 + 3][lane]);
     logits[(size_t)(t0 + lane) * E + e] = s;
   }
+  if (xq) {
+    const int grp = blockIdx.x * 8 + warp;
+    if (grp < (L >> 5)) {
+      const float v = __uint_as_float((uint32_t)x[32 * grp + lane] << 16);
+      uint32_t words[kTerms], sf[kTerms];
+      mx_split_group(v, words, sf);
+#pragma unroll
+      for (int t = 0; t < kTerms; ++t) {
+        if ((lane & 7) == 0)
+          *reinterpret_cast<uint32_t*>(xq + (size_t)t * (L >> 1) + grp * 16 + 4 * (lane >> 3)) = words[t];
+        if (lane == 0) xsf[(size_t)t * (L >> 5) + grp] = (uint8_t)sf[t];
+      }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits,
@@ -93,13 +114,15 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits,
 }  // namespace
 
 cudaError_t launch_router_logits(const uint16_t* h, const uint16_t* wr, int T, int E, int H,
-                                 float* logits, cudaStream_t s, bool pdl) {
+                                 float* logits, cudaStream_t s, bool pdl, const uint16_t* x,
+                                 int L, uint8_t* xq, uint8_t* xsf) {
   const unsigned gx = (E + kRowsPerCta - 1) / kRowsPerCta;
+  if (xq && (T != 1 || (int)gx * 8 < (L >> 5))) return cudaErrorInvalidValue;
   if (T <= 2)
     return launch_kernel(k_router_logits<1>, dim3(gx, T), dim3(256), 0, s, pdl, h, wr, T, E, H,
-                         logits);
+                         logits, x, L, xq, xsf);
   return launch_kernel(k_router_logits<4>, dim3(gx, (T + 3) / 4), dim3(256), 0, s, pdl, h, wr, T,
-                       E, H, logits);
+                       E, H, logits, x, L, xq, xsf);
 }
 
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,
