@@ -173,7 +173,7 @@ int k3moe_stack_link(const float *y, int32_t T, int32_t L, int32_t norm, float e
  * the process exits.  It allocates nothing, on the device or the host.
  *
  *   - Capacity: a call whose k3moe_workspace_size(cfg, T) exceeds the array returns
- *     K3MOE_ERR_TOO_LARGE and enqueues nothing (Kimi K3 shape: up to 30 tokens).
+ *     K3MOE_ERR_TOO_LARGE and enqueues nothing (Kimi K3 shape: up to 27 tokens).
  *   - Set-up: the first call on a device, with that device current, looks up the array's
  *     device address (cudaGetSymbolAddress) and caches it; make that first call before any
  *     stream capture begins.

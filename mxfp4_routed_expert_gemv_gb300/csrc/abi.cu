@@ -102,6 +102,7 @@ size_t carve(const k3moe_cfg* c, int32_t T, void* base, bool host_stage, Workspa
   t.b.ntile_base = cv.take<int32_t>(E + 1);
   t.b.flags = cv.take<int32_t>(2 * (size_t)kTcMaxGrid);
   t.b.ready = cv.take<int32_t>((P + kTcTokTile - 1) / kTcTokTile + E + 1);
+  t.b.tiles = cv.take<int4>((P + kTcTokTile - 1) / kTcTokTile + E + 1);
   t.tc = tc_path_supported((int)L, (int)I);
   if (t.tc) {
     t.xq = cv.take<uint8_t>(P * kTerms * (L / 2));

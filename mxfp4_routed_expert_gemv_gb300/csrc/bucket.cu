@@ -77,8 +77,15 @@ __device__ void publish_counts(int c, int E, const BucketOut& o, int* excl_out) 
   // tensor-core tiles: ceil(count / kTcTokTile) per active expert, prefix over active experts
   int nt_tot;
   const int nt_excl = block_exclusive_scan_1024(flag ? (c + kTcTokTile - 1) / kTcTokTile : 0, &nt_tot);
-  if (flag) o.ntile_base[pos] = nt_excl;
-  if (e == 0) o.ntile_base[nact] = nt_tot;
+  if (flag) {
+    o.ntile_base[pos] = nt_excl;
+    for (int n = 0; n * kTcTokTile < c; ++n)
+      o.tiles[nt_excl + n] = make_int4(e, excl + n * kTcTokTile, min(kTcTokTile, c - n * kTcTokTile), 0);
+  }
+  if (e == 0) {
+    o.ntile_base[nact] = nt_tot;
+    o.meta[2] = nt_tot;
+  }
   if (e < 2 * kTcMaxGrid) o.flags[e] = 0;
   for (int i = e; i < nt_tot; i += blockDim.x) o.ready[i] = 0;
   *excl_out = excl;
@@ -278,11 +285,13 @@ __global__ void __launch_bounds__(1024) k_prep_one(PrepArgs p) {
       p.b.inv[j] = lane;
       p.b.ntile_base[lane] = lane;
       p.b.ready[lane] = 0;
+      p.b.tiles[lane] = make_int4(ej, lane, 1, 0);
     }
     if (lane == 0) {
       p.b.ntile_base[k] = k;
       p.b.meta[0] = k;
       p.b.meta[1] = k;
+      p.b.meta[2] = k;
       p.b.nvalid[0] = k;
     }
   }

@@ -58,13 +58,14 @@ struct BucketOut {
   int32_t* active;      // [E]    expert ids with at least one token, ascending
   int32_t* seg_off;     // [E]    perm offset of each active expert's tokens
   int32_t* seg_cnt;     // [E]    number of tokens of each active expert
-  int32_t* meta;        // [16]   [0] active experts, [1] valid assignments
+  int32_t* meta;        // [16]   [0] active experts, [1] valid assignments, [2] token groups
   int32_t* chunk_base;  // [E][nchunks] scratch of the multi-block path
   int32_t* nvalid;      // [T]    valid assignments per token
   int32_t* inv;         // [T*k]  perm position of each valid assignment id
   int32_t* ntile_base;  // [E+1]  tensor-core tiles (kTcTokTile tokens) before each active expert
   int32_t* flags;       // [2 * kTcMaxGrid] arrivals at tiles shared between CTAs (zeroed)
   int32_t* ready;       // [P/16 + E + 1] finished first-GEMM row tiles per tile group (zeroed)
+  int4* tiles;          // [P/16 + E + 1] per token group: expert, first position, tokens, 0
 };
 
 // Everything the per-call preparation touches.  logits == nullptr: idx/gate come from the

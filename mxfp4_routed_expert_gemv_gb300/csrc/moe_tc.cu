@@ -36,30 +36,41 @@ namespace {
 constexpr int kKStage = 512;                                 // reduction elements per stage
 constexpr int kMmas = kKStage / 64;                          // MMAs per stage (K = 64 each)
 constexpr int kTokTile = kTcTokTile;                         // tokens per tile
-constexpr int kNMax = kTokTile * kTerms;                     // MMA N of a full tile
 constexpr int kRowsTile = 128;                               // MMA M
-constexpr int kStages = 4;
 constexpr uint32_t kABytes = kRowsTile * (kKStage / 2);      // 32768: two 16 KB swizzle columns
-constexpr uint32_t kBKatom = kNMax * 128;                    // one 128-byte swizzle column of B
-constexpr uint32_t kBBytes = 2 * kBKatom;
 constexpr uint32_t kSABytes = kRowsTile * (kKStage / 32);    // 2048
-constexpr uint32_t kSBBytes = kNMax * (kKStage / 32);        // 1024
-constexpr uint32_t kOffB = kABytes, kOffSA = kOffB + kBBytes, kOffSB = kOffSA + kSABytes;
-constexpr uint32_t kStageBytes = kOffSB + kSBBytes;          // 52224 = 51 x 1024
 constexpr uint32_t kFixBytes = 16384;                        // parts of a shared last tile
-constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kFixBytes + 1024;
 constexpr int kThreads = 352;
 constexpr int kSfWarp0 = 4, kProdWarp = 8, kMmaWarp = 9, kBWarp = 10;
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: accumulator buffer b at 128 b, matrix m at + 64 m; the scale ring at
-// 256 + 64 s for stage s: A scales of MMA j at + 4 j (+ lane quarter), B scales at
-// + 32 + 4 j (+ 1 for B rows 32..63).
-constexpr uint32_t kAccCols = 128, kMatCols = 64, kSfBase = 256, kSfStageCols = 64;
+constexpr uint32_t kSfStageCols = 64;
 constexpr int kEpiBar = 1;  // named barrier of the four epilogue warps
 
-static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
-static_assert(kSfBase + kStages * kSfStageCols <= kTmemCols, "TMEM budget");
-static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
+// Shared-memory and TMEM layout for tiles of at most NMAX activation rows (MMA N): 16 for
+// batches of up to 4 tokens (the smaller activation slot leaves room for a fifth ring
+// stage), 64 otherwise.
+//   stage: A [0, 32 KB) | B two 128-byte columns of NMAX rows | A scales 128 x 16 B |
+//          B scales NMAX x 16 B, padded to a multiple of 1024 bytes;
+//   TMEM:  accumulator buffer b at b * kAccCols, matrix m at + m * kMatCols; the scale ring
+//          from kSfBase, stage s at + 64 s: A scales of MMA j at + 4 j (+ lane quarter),
+//          B scales at + 32 + 4 j (+ 1 for B rows 32..63).
+template <int NMAX>
+struct Lay {
+  static constexpr int kNMax = NMAX;
+  static constexpr uint32_t kBKatom = NMAX * 128;
+  static constexpr uint32_t kBBytes = 2 * kBKatom;
+  static constexpr uint32_t kSBBytes = NMAX * (kKStage / 32);
+  static constexpr uint32_t kOffB = kABytes, kOffSA = kOffB + kBBytes, kOffSB = kOffSA + kSABytes;
+  static constexpr uint32_t kStageBytes = ((kOffSB + kSBBytes + 1023) / 1024) * 1024;
+  static constexpr int kStages = NMAX <= 16 ? 5 : 4;
+  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kFixBytes + 1024;
+  static constexpr uint32_t kMatCols = NMAX <= 16 ? 32 : 64;
+  static constexpr uint32_t kAccCols = 2 * kMatCols;
+  static constexpr uint32_t kSfBase = 2 * kAccCols;
+  static_assert(kSfBase + kStages * kSfStageCols <= kTmemCols, "TMEM budget");
+  static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
+  static_assert(NMAX % 16 == 0 && NMAX <= 64, "tile height");
+};
 
 struct FArgs {
   int ph;                  // 0: w1, w3 -> act terms; 1: w2 -> gate * o
@@ -67,7 +78,8 @@ struct FArgs {
   int k, L, I, act_kind;
   float b1, b2;
   int KC, RT, R;           // reduction chunks, row tiles, rows per expert
-  const int32_t *active, *seg_off, *seg_cnt, *meta, *perm, *ntile_base;
+  const int32_t *meta, *perm;
+  const int4* tiles;        // per token group: expert, first position, token count
   uint8_t *act_q, *act_sf;  // phase-0 output = phase-1 activation operand
   const float* gate;
   float* ybuf;              // [T*k][L]
@@ -79,6 +91,8 @@ struct FArgs {
 
 __device__ __forceinline__ long long range_lo(long long U, int c, int G) { return U * c / G; }
 
+int tc_grid_size() { return sm_count() < kTcMaxGrid ? sm_count() : kTcMaxGrid; }
+
 // floats of one CTA's part: NM matrices x npart tokens x 128 rows, element (m, j, r) at
 // (m * npart + j) * 128 + r
 __device__ __forceinline__ size_t part_floats(int NM, int npart) {
@@ -88,21 +102,16 @@ __device__ __forceinline__ size_t part_floats(int NM, int npart) {
 struct TileInfo {
   int rt, expert, pos0, ntok, N;
 };
-// tile -> (active expert slot, token group, row tile) and what the kernel needs of it
+// tile -> (row tile, and from the preparation's table of token groups: expert, first
+// position, token count)
 __device__ __forceinline__ TileInfo tile_info(int tile, const FArgs& f) {
   TileInfo t;
   const int ntg = tile / f.RT;
   t.rt = tile - ntg * f.RT;
-  int lo = 0, hi = f.meta[0] - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (f.ntile_base[mid] <= ntg) lo = mid;
-    else hi = mid - 1;
-  }
-  const int n = ntg - f.ntile_base[lo];
-  t.expert = f.active[lo];
-  t.pos0 = f.seg_off[lo] + n * kTokTile;
-  t.ntok = min(kTokTile, f.seg_cnt[lo] - n * kTokTile);
+  const int4 g = __ldg(f.tiles + ntg);
+  t.expert = g.x;
+  t.pos0 = g.y;
+  t.ntok = g.z;
   t.N = ((t.ntok * kTerms + 15) / 16) * 16;
   return t;
 }
@@ -166,8 +175,14 @@ __device__ __forceinline__ Range make_range(long long U, int KC, int c, int G) {
   return r;
 }
 
+template <int NMAX>
 __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ Maps mp,
                                                         const FArgs f) {
+  using Y = Lay<NMAX>;
+  constexpr int kStages = Y::kStages;
+  constexpr uint32_t kStageBytes = Y::kStageBytes, kBKatom = Y::kBKatom;
+  constexpr uint32_t kOffB = Y::kOffB, kOffSA = Y::kOffSA, kOffSB = Y::kOffSB;
+  constexpr uint32_t kAccCols = Y::kAccCols, kMatCols = Y::kMatCols, kSfBase = Y::kSfBase;
   extern __shared__ uint8_t dsm[];
   __shared__ __align__(8) uint64_t fullA[kStages], fullB[kStages], sfready[kStages], empty[kStages];
   __shared__ __align__(8) uint64_t accfull[2], accempty[2], drained, fixfull;
@@ -205,12 +220,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  pdl_wait();
+  // Phase 0 reads what the preparation wrote: everyone waits for the previous launch.  Phase
+  // 1 starts streaming its weights at once: the routing it reads was complete before phase
+  // 0 passed this point (phase 0 lets this launch start only after its own wait), and only
+  // the activation terms come from phase 0, so only the thread that loads them waits.
+  if (f.ph == 0) pdl_wait();
   pdl_launch();
   const uint32_t t0 = tbase;
   volatile int* abort_v = &abort_flag;
 
-  const long long U = (long long)f.ntile_base[f.meta[0]] * f.RT * f.KC;
+  const long long U = (long long)f.meta[2] * f.RT * f.KC;
   const Range rg = make_range(U, f.KC, cta, G);
   const int ntiles = rg.t_last - rg.t_first + 1;  // tiles this CTA touches (0 if idle)
   // the later CTAs whose parts the head tile needs, and where their parts land in `fix`
@@ -220,6 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
     while (fix_c1 + 1 < G && range_lo(U, fix_c1 + 1, G) < tend) ++fix_c1;
   }
   const size_t pf = part_floats(NM, f.npart);
+  // this phase's parts (the phases have separate regions: phase 1 may start before phase 0
+  // has finished with its parts)
+  float* const parts = f.part + (f.ph == 0 ? 0 : (size_t)kTcMaxGrid * part_floats(2, f.npart));
   // an idle CTA (empty range, when there are fewer units than CTAs) leaves no part
   auto idle = [&](int c) { return range_lo(U, c + 1, G) == range_lo(U, c, G); };
   int nfix = 0;
@@ -230,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
     // ------------------------------------- TMA: weights (warp 8), activations (warp 10)
     if (lane == 0) {
       const bool wts = warp == kProdWarp;
+      if (!wts && f.ph == 1) pdl_wait();  // the activation terms are phase 0's output
       int it = 0;
       bool stop = false;
       for (int ti_ = 0; ti_ < ntiles && !stop; ++ti_) {
@@ -287,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
             break;
           }
           fence_proxy_async_global();
-          bulk_g2s(fix + (size_t)slot * pf, f.part + (size_t)c * pf, (uint32_t)(pf * 4), &fixfull);
+          bulk_g2s(fix + (size_t)slot * pf, parts + (size_t)c * pf, (uint32_t)(pf * 4), &fixfull);
           ++slot;
         }
         if (!ok) {
@@ -341,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
 #pragma unroll
           for (int j = 0; j < kMmas; ++j)
             tc::tmem_st_x1(ring + 32 + 4 * j, (wb0[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-          if (N > 32) {
+          if (NMAX > 32 && N > 32) {
             const uint4 sb1 = *reinterpret_cast<const uint4*>(st + kOffSB + 16 * (32 + lane));
             const uint32_t wb1[4] = {sb1.x, sb1.y, sb1.z, sb1.w};
 #pragma unroll
@@ -446,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
       const uint32_t tacc = t0 + lane_off + (uint32_t)b * kAccCols;
       const int grp = (ti.rt * kRowsTile + 32 * q) >> 5;            // phase 0: act group
       const bool in_range = ti.rt * kRowsTile + 32 * q < f.R;
-      float* mine = f.part + (size_t)cta * pf;
+      float* mine = parts + (size_t)cta * pf;
 #pragma unroll 1
       for (int j = 0; j < ti.ntok; ++j) {
         float v[2] = {0.f, 0.f};
@@ -473,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
             int slot = 0;
             for (int c = fix_c0; c <= fix_c1; ++c) {
               if (idle(c)) continue;
-              v[m] += fix_smem ? fix[(size_t)slot * pf + off] : __ldcg(f.part + (size_t)c * pf + off);
+              v[m] += fix_smem ? fix[(size_t)slot * pf + off] : __ldcg(parts + (size_t)c * pf + off);
               ++slot;
             }
           }
@@ -550,15 +573,36 @@ __global__ void __launch_bounds__(512) k_split_x(const uint16_t* __restrict__ x,
   }
 }
 
+template <int NMAX>
+cudaError_t launch_tc_n(const Maps& mp, const FArgs& f, cudaStream_t s, bool pdl) {
+  static int configured[64] = {0};
+  constexpr size_t smem = Lay<NMAX>::kSmemBytes;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_moe_tc<NMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = 1;
+  }
+  return launch_kernel(k_moe_tc<NMAX>, dim3(tc_grid_size()), dim3(kThreads), smem, s, pdl, mp, f);
+}
+
+// Batches of up to 4 tokens have at most 4 tokens per expert: 16-row activation tiles.
+cudaError_t launch_tc(const Maps& mp, const FArgs& f, int T, cudaStream_t s, bool pdl) {
+  if (T * kTerms <= 16) return launch_tc_n<16>(mp, f, s, pdl);
+  return launch_tc_n<64>(mp, f, s, pdl);
+}
+
 }  // namespace
 
 bool tc_path_supported(int L, int I) { return L % kKStage == 0 && I % kKStage == 0; }
 
-int tc_grid() { return sm_count() < kTcMaxGrid ? sm_count() : kTcMaxGrid; }
+int tc_grid() { return tc_grid_size(); }
 
 int tc_npart(int T) { return T < kTokTile ? T : kTokTile; }  // tokens per tile, at most
 
-size_t tc_part_floats(int T) { return (size_t)kTcMaxGrid * 2 * tc_npart(T) * kRowsTile; }
+size_t tc_part_floats(int T) { return (size_t)kTcMaxGrid * 3 * tc_npart(T) * kRowsTile; }
 
 cudaError_t launch_split_x(const uint16_t* x, int T, int L, int k, const BucketOut& b,
                            uint8_t* xq, uint8_t* xsf, cudaStream_t s, bool pdl) {
@@ -589,35 +633,24 @@ cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, i
   m1.m[3] = m1.m[1];
   FArgs f{};
   f.k = k; f.L = L; f.I = I; f.act_kind = act_kind; f.b1 = b1; f.b2 = b2;
-  f.active = b.active; f.seg_off = b.seg_off; f.seg_cnt = b.seg_cnt; f.meta = b.meta;
-  f.perm = b.perm; f.ntile_base = b.ntile_base;
+  f.meta = b.meta; f.perm = b.perm; f.tiles = b.tiles;
   f.act_q = act_q; f.act_sf = act_sf; f.gate = gate; f.ybuf = ybuf;
   f.part = part; f.npart = tc_npart(T);
   f.status = status;
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_moe_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev] = 1;
-  }
   // phase 0 (w1, w3), then phase 1 (w2): the second launch reads what the first wrote, across
   // the kernel boundary (its CTAs wait in griddepcontrol.wait until the first has completed)
   f.ph = 0;
   f.one_token = T == 1;
   f.KC = L / kKStage; f.RT = (I + kRowsTile - 1) / kRowsTile; f.R = I;
   f.flags = b.flags;
-  cudaError_t e = launch_kernel(k_moe_tc, dim3(tc_grid()), dim3(kThreads), kSmemBytes, s, pdl,
-                                m0, f);
+  cudaError_t e = launch_tc(m0, f, T, s, pdl);
   if (e != cudaSuccess) return e;
   if (between) between(s);
   f.ph = 1;
   f.one_token = 0;
   f.KC = I / kKStage; f.RT = (L + kRowsTile - 1) / kRowsTile; f.R = L;
   f.flags = b.flags + kTcMaxGrid;
-  return launch_kernel(k_moe_tc, dim3(tc_grid()), dim3(kThreads), kSmemBytes, s, true, m1, f);
+  return launch_tc(m1, f, T, s, true);
 }
 
 }  // namespace k3
