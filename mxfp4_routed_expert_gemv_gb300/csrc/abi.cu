@@ -100,8 +100,7 @@ size_t carve(const k3moe_cfg* c, int32_t T, void* base, bool host_stage, Workspa
   t.b.nvalid = cv.take<int32_t>(Tt);
   t.b.inv = cv.take<int32_t>(P);
   t.b.ntile_base = cv.take<int32_t>(E + 1);
-  t.b.flags = cv.take<int32_t>(2 * (size_t)kTcMaxGrid);
-  t.b.ready = cv.take<int32_t>((P + kTcTokTile - 1) / kTcTokTile + E + 1);
+  t.b.flags = cv.take<int32_t>(kTcFlags);
   t.b.tiles = cv.take<int4>((P + kTcTokTile - 1) / kTcTokTile + E + 1);
   t.tc = tc_path_supported((int)L, (int)I);
   if (t.tc) {
@@ -188,12 +187,16 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
                 ex->w2_scale};
   const bool fused_topk = route && prep_is_fused(T);
   K3_TRY(phase(0, s));
-  const bool one = w.tc && fused_topk && T == 1;  // router + one preparation launch
+  // one token with the router's top-k on the tensor-core path: the router launch also
+  // writes x's terms and zeroes the GEMMs' flags, and the GEMM CTAs route the token
+  // themselves (no preparation launch)
+  const bool one = w.tc && fused_topk && T == 1 && (K <= 31 || K == E);
   if (route) {
     K3_TRY(launch_router_logits(static_cast<const uint16_t*>(h), static_cast<const uint16_t*>(wr),
-                                T, E, c->hidden, w.logits, s, false,
+                                T, E, c->hidden, w.logits, s, true,
                                 static_cast<const uint16_t*>(x), L, one ? w.xq : nullptr,
-                                one ? w.xsf : nullptr));
+                                one ? w.xsf : nullptr, one ? w.b.flags : nullptr,
+                                one ? kTcFlags : 0));
     if (!fused_topk)
       K3_TRY(launch_topk(w.logits, bias, T, E, K, c->renorm, c->routed_scale, idx, gate, gap, s,
                          true));
@@ -202,9 +205,8 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
   PrepArgs p{fused_topk ? w.logits : nullptr, bias, E, K, c->renorm, c->routed_scale, idx, gate,
              gap, T, L, static_cast<const uint16_t*>(x), w.tc ? nullptr : w.x16, w.xexp, w.b, y,
              status};
-  if (one) {
-    K3_TRY(launch_prep_one(p, s, route));
-  } else {
+  const RouteOne ro{w.logits, bias, c->renorm, c->routed_scale, idx, gate, gap};
+  if (!one) {
     K3_TRY(launch_prep(p, s, route));
     if (w.tc)
       K3_TRY(launch_split_x(static_cast<const uint16_t*>(x), T, L, K, w.b, w.xq, w.xsf, s, true));
@@ -213,7 +215,7 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
     K3_TRY(phase(2, s));
     K3_TRY(launch_tc_experts(ep, L, I, E, T, K, w.xq, w.xsf, w.b, w.aq, w.asf, c->act,
                              c->situ_b1, c->situ_b2, gate, w.ybuf, w.part, status, s, true,
-                             phase3));
+                             phase3, one ? &ro : nullptr));
     K3_TRY(phase(4, s));
   } else {
     K3_TRY(phase(2, s));

@@ -86,8 +86,7 @@ __device__ void publish_counts(int c, int E, const BucketOut& o, int* excl_out) 
     o.ntile_base[nact] = nt_tot;
     o.meta[2] = nt_tot;
   }
-  if (e < 2 * kTcMaxGrid) o.flags[e] = 0;
-  for (int i = e; i < nt_tot; i += blockDim.x) o.ready[i] = 0;
+  for (int i = e; i < kTcFlags; i += blockDim.x) o.flags[i] = 0;
   *excl_out = excl;
 }
 
@@ -196,107 +195,6 @@ __global__ void __launch_bounds__(1024) k_prep_small(PrepArgs p) {
   }
 }
 
-// Batch-1 decode with the router's top-k, on the tensor-core path: one block of 1024 threads
-// does the whole preparation with warp-level steps and two block barriers.
-//  1. top-k: key = (order-preserving bits of the selection score, then ~expert) so a larger
-//     key is a better choice and equal scores go to the lower index (the README's rule,
-//     Part II section 9); each warp sorts its 32 keys (bitonic, shuffles), warp 0 merges
-//     the 32 sorted lists, taking k + 1 keys (the last one gives the gap).
-//  2. buckets: the k chosen experts are distinct, so each has one assignment: sorting them
-//     by expert gives the active list, and position i holds assignment perm[i].
-// x's MXFP4 terms are written by the router launch (they do not depend on the routing).
-__global__ void __launch_bounds__(1024) k_prep_one(PrepArgs p) {
-  pdl_wait();
-  pdl_launch();
-  __shared__ unsigned long long cand[32][33];
-  __shared__ unsigned long long best[33];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int E = p.E, k = p.k;
-  unsigned long long key = 0ull;  // 0: no expert (below every real key)
-  if (tid < E) {
-    const float v = sigmoid_f32(p.logits[tid]) + (p.bias ? p.bias[tid] : 0.0f);
-    key = ((unsigned long long)ordered_bits(v) << 32) | (uint32_t)(~(uint32_t)tid);
-  }
-#pragma unroll
-  for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, stride);
-      const bool desc = (lane & size) == 0, lo = (lane & stride) == 0;
-      const unsigned long long mx = key > other ? key : other, mn = key > other ? other : key;
-      key = (lo == desc) ? mx : mn;
-    }
-  }
-  cand[warp][lane] = key;
-  if (lane == 0) cand[warp][32] = 0ull;
-  if (tid < 2 * kTcMaxGrid) p.b.flags[tid] = 0;
-  __syncthreads();
-  if (warp == 0) {
-    int pos = 0;
-    unsigned long long head = cand[lane][0];
-    for (int r = 0; r <= k && r < 33; ++r) {
-      unsigned long long m = head;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long x = __shfl_xor_sync(0xffffffffu, m, o);
-        m = x > m ? x : m;
-      }
-      if (lane == 0) best[r] = m;
-      if (m != 0ull && head == m) head = pos < 32 ? cand[lane][++pos] : 0ull;
-    }
-    __syncwarp();
-    // choice j on lane j: expert, unbiased score, gate
-    int e = -1;
-    float s = 0.f;
-    if (lane < k) {
-      e = (int)(~(uint32_t)(best[lane] & 0xffffffffull));
-      s = sigmoid_f32(p.logits[e]);
-    }
-    const float sum = warp_sum(s);
-    float g = s;
-    if (p.renorm && sum > 0.f) g = s / sum;
-    g *= p.routed_scale;
-    if (lane < k) {
-      p.idx[lane] = e;
-      p.gate[lane] = g;
-    }
-    if (p.gap && lane == 0)
-      *p.gap = (k < E) ? from_ordered_bits((uint32_t)(best[k - 1] >> 32)) -
-                             from_ordered_bits((uint32_t)(best[k] >> 32))
-                       : INFINITY;
-    // buckets: sort (expert, choice) ascending by expert
-    uint32_t bk = lane < k ? ((uint32_t)e << 5) | (uint32_t)lane : 0xffffffffu;
-#pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        const uint32_t other = __shfl_xor_sync(0xffffffffu, bk, stride);
-        const bool asc = (lane & size) == 0, lo = (lane & stride) == 0;
-        const uint32_t mn = bk < other ? bk : other, mx = bk < other ? other : bk;
-        bk = (lo == asc) ? mn : mx;
-      }
-    }
-    if (lane < k) {
-      const int ej = (int)(bk >> 5), j = (int)(bk & 31u);
-      p.b.active[lane] = ej;
-      p.b.seg_off[lane] = lane;
-      p.b.seg_cnt[lane] = 1;
-      p.b.perm[lane] = j;
-      p.b.inv[j] = lane;
-      p.b.ntile_base[lane] = lane;
-      p.b.ready[lane] = 0;
-      p.b.tiles[lane] = make_int4(ej, lane, 1, 0);
-    }
-    if (lane == 0) {
-      p.b.ntile_base[k] = k;
-      p.b.meta[0] = k;
-      p.b.meta[1] = k;
-      p.b.meta[2] = k;
-      p.b.nvalid[0] = k;
-    }
-  }
-}
-
 // Multi-block path, pass 1: per-chunk histograms stored transposed [E][nchunks]; also the
 // chunk's tokens' nvalid.
 __global__ void __launch_bounds__(256) k_bucket_count(PrepArgs p, int nchunks) {
@@ -374,10 +272,6 @@ __global__ void __launch_bounds__(32) k_bucket_scatter(const int32_t* __restrict
 int bucket_chunks(int T) { return (T + kChunkTokens - 1) / kChunkTokens; }
 
 bool prep_is_fused(int T) { return T <= kSmallTokens; }
-
-cudaError_t launch_prep_one(const PrepArgs& p, cudaStream_t s, bool pdl) {
-  return launch_kernel(k_prep_one, dim3(1), dim3(1024), 0, s, pdl, p);
-}
 
 cudaError_t launch_prep(const PrepArgs& p, cudaStream_t s, bool pdl) {
   if (prep_is_fused(p.T)) return launch_kernel(k_prep_small, dim3(1), dim3(1024), 0, s, pdl, p);

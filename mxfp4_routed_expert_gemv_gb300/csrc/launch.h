@@ -41,7 +41,8 @@ int sm_count();
 cudaError_t launch_router_logits(const uint16_t* h, const uint16_t* wr, int T, int E, int H,
                                  float* logits, cudaStream_t s, bool pdl,
                                  const uint16_t* x = nullptr, int L = 0, uint8_t* xq = nullptr,
-                                 uint8_t* xsf = nullptr);
+                                 uint8_t* xsf = nullptr, int32_t* zero = nullptr,
+                                 int nzero = 0);
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,
                         float routed_scale, int32_t* idx, float* gate, float* gap,
                         cudaStream_t s, bool pdl);
@@ -49,6 +50,11 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
 // Tensor-core expert path (moe_tc.cu): tokens per tile, and the largest grid it launches.
 constexpr int kTcTokTile = 16;
 constexpr int kTcMaxGrid = 160;
+// Flags of the tensor-core path, zeroed before each call: [0, kTcMaxGrid) parts of the first
+// GEMM's shared tiles written, [kTcMaxGrid, 2 kTcMaxGrid) the same for the second GEMM,
+// [kTcRouteFlag] the single-token routing published by the first GEMM.
+constexpr int kTcRouteFlag = 2 * kTcMaxGrid;
+constexpr int kTcFlags = 2 * kTcMaxGrid + 1;
 
 // bucket.cu
 struct BucketOut {
@@ -63,8 +69,7 @@ struct BucketOut {
   int32_t* nvalid;      // [T]    valid assignments per token
   int32_t* inv;         // [T*k]  perm position of each valid assignment id
   int32_t* ntile_base;  // [E+1]  tensor-core tiles (kTcTokTile tokens) before each active expert
-  int32_t* flags;       // [2 * kTcMaxGrid] arrivals at tiles shared between CTAs (zeroed)
-  int32_t* ready;       // [P/16 + E + 1] finished first-GEMM row tiles per tile group (zeroed)
+  int32_t* flags;       // [kTcFlags] tensor-core path flags (zeroed before each call)
   int4* tiles;          // [P/16 + E + 1] per token group: expert, first position, tokens, 0
 };
 
@@ -89,9 +94,6 @@ struct PrepArgs {
 int bucket_chunks(int T);
 bool prep_is_fused(int T);
 cudaError_t launch_prep(const PrepArgs& p, cudaStream_t s, bool pdl);
-// One token with the router's top-k, tensor-core path: top-k and buckets in one launch
-// (E <= 1024, k <= 32); x's terms come from the router launch.
-cudaError_t launch_prep_one(const PrepArgs& p, cudaStream_t s, bool pdl);
 
 // gemv.cu
 struct ExpertPtrs {
@@ -120,11 +122,22 @@ int tc_npart(int T);
 size_t tc_part_floats(int T);
 cudaError_t launch_split_x(const uint16_t* x, int T, int L, int k, const BucketOut& b,
                            uint8_t* xq, uint8_t* xsf, cudaStream_t s, bool pdl);
+// One token routed inside the expert GEMMs (no preparation launch): the router's logits and
+// the top-k parameters; CTA 0 of the first GEMM publishes idx / gate / gap (and the tile
+// table, in BucketOut's tiles / perm, for the second GEMM).  Needs E <= 1056, k <= 31 or k == E.
+struct RouteOne {
+  const float *logits, *bias;
+  int renorm;
+  float routed_scale;
+  int32_t* idx;
+  float *gate, *gap;
+};
 cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k,
                               const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,
                               uint8_t* act_q, uint8_t* act_sf, int act_kind, float b1, float b2,
                               const float* gate, float* ybuf, float* part, int32_t* status,
-                              cudaStream_t s, bool pdl, void (*between)(cudaStream_t));
+                              cudaStream_t s, bool pdl, void (*between)(cudaStream_t),
+                              const RouteOne* ro = nullptr);
 
 // stack.cu
 cudaError_t launch_stack_link(const float* y, int T, int L, int norm, float eps, uint16_t* x_out,

@@ -29,6 +29,7 @@
 #include "mxq.cuh"
 #include "tc.cuh"
 #include "tmap.h"
+#include "topk.cuh"
 
 namespace k3 {
 namespace {
@@ -75,6 +76,17 @@ struct Lay {
 struct FArgs {
   int ph;                  // 0: w1, w3 -> act terms; 1: w2 -> gate * o
   int one_token;           // T == 1: phase-0 activation rows are 0 .. kTerms-1
+  // route_one: one token, no preparation launch.  Phase-0 CTAs each route the token from the
+  // router's logits; CTA 0 publishes idx, gate, gap, the tile table (tiles_out, perm_out)
+  // and then route_flag; phase-1 CTAs read the published table.
+  int route_one;
+  const float *logits, *bias;
+  int E, renorm;
+  float routed_scale;
+  int32_t* idx_out;
+  float *gate_out, *gap_out;
+  int4* tiles_out;
+  int32_t *perm_out, *route_flag;
   int k, L, I, act_kind;
   float b1, b2;
   int KC, RT, R;           // reduction chunks, row tiles, rows per expert
@@ -89,7 +101,13 @@ struct FArgs {
   int32_t* status;
 };
 
-__device__ __forceinline__ long long range_lo(long long U, int c, int G) { return U * c / G; }
+// Units [lo(c), lo(c+1)) of U go to CTA c of G: lo(c) = floor(U c / G), from U = q G + r as
+// q c + floor(r c / G), in 32-bit arithmetic (U < 2^31, r c < G^2).
+struct Split {
+  int U, q, r, G;
+  __device__ __forceinline__ Split(int U_, int G_) : U(U_), q(U_ / G_), r(U_ % G_), G(G_) {}
+  __device__ __forceinline__ int lo(int c) const { return q * c + (r * c) / G; }
+};
 
 int tc_grid_size() { return sm_count() < kTcMaxGrid ? sm_count() : kTcMaxGrid; }
 
@@ -102,13 +120,13 @@ __device__ __forceinline__ size_t part_floats(int NM, int npart) {
 struct TileInfo {
   int rt, expert, pos0, ntok, N;
 };
-// tile -> (row tile, and from the preparation's table of token groups: expert, first
-// position, token count)
-__device__ __forceinline__ TileInfo tile_info(int tile, const FArgs& f) {
+// tile -> (row tile, and from the table of token groups: expert, first position, token
+// count); the table is the preparation's, or this CTA's own for a single routed token
+__device__ __forceinline__ TileInfo tile_info(int tile, const FArgs& f, const int4* own) {
   TileInfo t;
   const int ntg = tile / f.RT;
   t.rt = tile - ntg * f.RT;
-  const int4 g = __ldg(f.tiles + ntg);
+  const int4 g = f.route_one ? own[ntg] : __ldg(f.tiles + ntg);
   t.expert = g.x;
   t.pos0 = g.y;
   t.ntok = g.z;
@@ -116,8 +134,72 @@ __device__ __forceinline__ TileInfo tile_info(int tile, const FArgs& f) {
   return t;
 }
 
+__device__ __forceinline__ void st_release(int32_t* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// One token's routing for an expert-GEMM CTA (every thread calls it).  Phase 0: the CTA
+// routes the token itself from the router's logits (the ring, free until the producers
+// start, is the scratch); CTA 0 also publishes the result and then the route flag.  Phase 1:
+// the table CTA 0 of phase 0 published, after its flag.  Out (shared): tiles[i] =
+// (expert, i, 1) for the chosen experts in ascending order, perm[i] = the choice index of
+// tile i, gate[j] = gate of choice j.  Returns the number of token groups (0 after a timeout).
+__device__ __forceinline__ int route_one_token(const FArgs& f, uint8_t* scratch, int4* tiles,
+                                               int* perm, float* gate, bool publish) {
+  __shared__ int ngroups;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, k = f.k;
+  if (f.ph == 0) {
+    const OneTokenChoice c = topk_one_token<3>(
+        f.logits, f.bias, f.E, k, f.renorm, f.routed_scale, publish ? f.gap_out : nullptr,
+        reinterpret_cast<unsigned long long*>(scratch), reinterpret_cast<float*>(scratch + 4096));
+    if (warp == 0) {
+      if (lane < k) {
+        gate[lane] = c.g;
+        tiles[c.rank] = make_int4(c.e, c.rank, 1, 0);
+        perm[c.rank] = lane;
+        if (publish) {
+          f.idx_out[lane] = c.e;
+          f.gate_out[lane] = c.g;
+          f.tiles_out[c.rank] = make_int4(c.e, c.rank, 1, 0);
+          f.perm_out[c.rank] = lane;
+        }
+      }
+      if (publish) {
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          st_release(f.route_flag, 1);
+        }
+      }
+      if (lane == 0) ngroups = k;
+    }
+  } else if (warp == 0) {
+    int got = 0;
+    for (uint32_t q = 0; q < kWaitPolls && !got; ++q) {
+      got = ld_acquire(f.route_flag) == 1;
+      if (!got) __nanosleep(64);
+    }
+    if (got && lane < k) {
+      tiles[lane] = __ldcg(f.tiles_out + lane);
+      perm[lane] = __ldcg(f.perm_out + lane);
+      gate[lane] = __ldcg(f.gate_out + lane);
+    }
+    if (lane == 0) {
+      ngroups = got ? k : 0;
+      if (!got && f.status) atomicAdd(f.status + kStatTimeout, 1);
+    }
+  }
+  __syncthreads();
+  return ngroups;
+}
+
 // bytes 0xFF -> 0x00 (an E8M0 "no value" becomes the smallest scale: the group adds nothing
-// measurable, as the pages' decoder's zero group)
+// measurable, as the zero group of the README "kimi-k3-in-c" decoder, Part II section 4)
 __device__ __forceinline__ uint32_t clear_ff_bytes(uint32_t w) {
   const uint32_t t = ~w;
   const uint32_t y = ((t & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | t;  // bit 7 clear iff the byte of t is 0
@@ -136,15 +218,6 @@ __device__ __forceinline__ int bar_or(uint32_t id, uint32_t n, int v) {
   return (int)r;
 }
 
-__device__ __forceinline__ void st_release(int32_t* p, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ int ld_acquire(const int32_t* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // generic-proxy global writes seen through an acquire -> later bulk/TMA (async proxy) reads
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -152,6 +225,8 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 
 // Maps: phase 0: [0] w1 [1] w1 scales [2] w3 [3] w3 scales [4] x terms [5] their scales;
 // phase 1: [0] w2 [1] w2 scales [2] w2 [3] w2 scales [4] act terms [5] their scales.
+// Per phase: [0..1] first weight matrix and its scales, [2..3] the second (phase 0: w3;
+// phase 1: w2 again), [4..5] activation terms and scales.
 struct Maps {
   CUtensorMap m[6];
 };
@@ -159,15 +234,15 @@ struct Maps {
 // The CTA's range in tiles: the first tile (maybe shared, part at the front), whole tiles,
 // the last tile (maybe shared, this CTA its head: parts of later CTAs are added to it).
 struct Range {
-  long long u0, u1;
+  int u0, u1;
   int t_first, t_last;
   bool tail_first;   // the first tile started in an earlier CTA: leave a part
   bool head_last;    // the last tile continues in later CTAs: add their parts
 };
-__device__ __forceinline__ Range make_range(long long U, int KC, int c, int G) {
+__device__ __forceinline__ Range make_range(const Split& sp, int KC, int c) {
   Range r;
-  r.u0 = range_lo(U, c, G);
-  r.u1 = range_lo(U, c + 1, G);
+  r.u0 = sp.lo(c);
+  r.u1 = sp.lo(c + 1);
   r.t_first = (int)(r.u0 / KC);
   r.t_last = r.u1 > r.u0 ? (int)((r.u1 - 1) / KC) : r.t_first - 1;
   r.tail_first = r.u1 > r.u0 && r.u0 % KC != 0;
@@ -188,6 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
   __shared__ __align__(8) uint64_t accfull[2], accempty[2], drained, fixfull;
   __shared__ uint32_t tbase;
   __shared__ int abort_flag;
+  __shared__ int4 own_tiles[32];  // route_one: this CTA's table of token groups
+  __shared__ int own_perm[32];
+  __shared__ float own_gate[32];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) &
                                            ~uintptr_t(1023));
   float* fix = reinterpret_cast<float*>(sm + (size_t)kStages * kStageBytes);
@@ -220,30 +298,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  // Phase 0 reads what the preparation wrote: everyone waits for the previous launch.  Phase
-  // 1 starts streaming its weights at once: the routing it reads was complete before phase
-  // 0 passed this point (phase 0 lets this launch start only after its own wait), and only
-  // the activation terms come from phase 0, so only the thread that loads them waits.
+  // Phase 0 reads what the preparation (or the router) wrote: everyone waits for the previous
+  // launch.  Phase 1 starts streaming its weights at once: the routing it reads (or the
+  // logits it routes from) was complete before phase 0 passed this point (phase 0 lets this
+  // launch start only after its own wait), and only the activation terms come from phase 0,
+  // so only the thread that loads them waits.
   if (f.ph == 0) pdl_wait();
   pdl_launch();
   const uint32_t t0 = tbase;
   volatile int* abort_v = &abort_flag;
+  const int ngroups = f.route_one ? route_one_token(f, sm, own_tiles, own_perm, own_gate,
+                                                    f.ph == 0 && cta == 0)
+                                  : f.meta[2];
 
-  const long long U = (long long)f.meta[2] * f.RT * f.KC;
-  const Range rg = make_range(U, f.KC, cta, G);
+  const Split sp(ngroups * f.RT * f.KC, G);
+  const Range rg = make_range(sp, f.KC, cta);
   const int ntiles = rg.t_last - rg.t_first + 1;  // tiles this CTA touches (0 if idle)
   // the later CTAs whose parts the head tile needs, and where their parts land in `fix`
   int fix_c0 = cta + 1, fix_c1 = cta;  // [fix_c0, fix_c1]
   if (rg.head_last) {
-    const long long tend = (long long)(rg.t_last + 1) * f.KC;
-    while (fix_c1 + 1 < G && range_lo(U, fix_c1 + 1, G) < tend) ++fix_c1;
+    const int tend = (rg.t_last + 1) * f.KC;
+    while (fix_c1 + 1 < G && sp.lo(fix_c1 + 1) < tend) ++fix_c1;
   }
   const size_t pf = part_floats(NM, f.npart);
   // this phase's parts (the phases have separate regions: phase 1 may start before phase 0
   // has finished with its parts)
   float* const parts = f.part + (f.ph == 0 ? 0 : (size_t)kTcMaxGrid * part_floats(2, f.npart));
   // an idle CTA (empty range, when there are fewer units than CTAs) leaves no part
-  auto idle = [&](int c) { return range_lo(U, c + 1, G) == range_lo(U, c, G); };
+  auto idle = [&](int c) { return sp.lo(c + 1) == sp.lo(c); };
   int nfix = 0;
   for (int c = fix_c0; c <= fix_c1; ++c) nfix += idle(c) ? 0 : 1;
   const bool fix_smem = (size_t)nfix * pf * 4 <= kFixBytes;
@@ -253,13 +335,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
     if (lane == 0) {
       const bool wts = warp == kProdWarp;
       if (!wts && f.ph == 1) pdl_wait();  // the activation terms are phase 0's output
+      const uint64_t once = tc::make_policy_evict_first();  // weights: read once per call
       int it = 0;
       bool stop = false;
       for (int ti_ = 0; ti_ < ntiles && !stop; ++ti_) {
         const int tile = rg.t_first + ti_;
-        const TileInfo ti = tile_info(tile, f);
-        const int kb = ti_ == 0 ? (int)(rg.u0 - (long long)tile * f.KC) : 0;
-        const int ke = ti_ == ntiles - 1 ? (int)(rg.u1 - (long long)tile * f.KC) : f.KC;
+        const TileInfo ti = tile_info(tile, f, own_tiles);
+        const int kb = ti_ == 0 ? rg.u0 - tile * f.KC : 0;
+        const int ke = ti_ == ntiles - 1 ? rg.u1 - tile * f.KC : f.KC;
         const int nbox = ti.N / 16;
         const int arow = ti.expert * f.R + ti.rt * kRowsTile;
         for (int kc = kb; kc < ke && !stop; ++kc) {
@@ -274,9 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
             uint8_t* st = sm + (size_t)s * kStageBytes;
             if (wts) {
               mbar_arrive_expect_tx(&fullA[s], kABytes + kSABytes);
-              tc::tma_load_2d(st, &mp.m[2 * m], kc * 256, arow, &fullA[s]);
-              tc::tma_load_2d(st + 16384, &mp.m[2 * m], kc * 256 + 128, arow, &fullA[s]);
-              tc::tma_load_2d(st + kOffSA, &mp.m[2 * m + 1], kc * 16, arow, &fullA[s]);
+              tc::tma_load_2d_hint(st, &mp.m[2 * m], kc * 256, arow, &fullA[s], once);
+              tc::tma_load_2d_hint(st + 16384, &mp.m[2 * m], kc * 256 + 128, arow, &fullA[s],
+                                   once);
+              tc::tma_load_2d_hint(st + kOffSA, &mp.m[2 * m + 1], kc * 16, arow, &fullA[s], once);
             } else {
               // one token: its terms are rows 0 .. kTerms-1 whatever the position (the router
               // launch writes only those; the per-position layout repeats them)
@@ -336,9 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
     bool stop = false;
     for (int ti_ = 0; ti_ < ntiles && !stop; ++ti_) {
       const int tile = rg.t_first + ti_;
-      const int N = tile_info(tile, f).N;
-      const int kb = ti_ == 0 ? (int)(rg.u0 - (long long)tile * f.KC) : 0;
-      const int ke = ti_ == ntiles - 1 ? (int)(rg.u1 - (long long)tile * f.KC) : f.KC;
+      const int N = tile_info(tile, f, own_tiles).N;
+      const int kb = ti_ == 0 ? rg.u0 - tile * f.KC : 0;
+      const int ke = ti_ == ntiles - 1 ? rg.u1 - tile * f.KC : f.KC;
       for (int kc = kb; kc < ke && !stop; ++kc) {
         for (int m = 0; m < NM; ++m, ++it) {
           const int s = it % kStages;
@@ -385,15 +469,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
       bool stop = false;
       for (int ti_ = 0; ti_ < ntiles && !stop; ++ti_) {
         const int tile = rg.t_first + ti_;
-        const int kb = ti_ == 0 ? (int)(rg.u0 - (long long)tile * f.KC) : 0;
-        const int ke = ti_ == ntiles - 1 ? (int)(rg.u1 - (long long)tile * f.KC) : f.KC;
+        const int kb = ti_ == 0 ? rg.u0 - tile * f.KC : 0;
+        const int ke = ti_ == ntiles - 1 ? rg.u1 - tile * f.KC : f.KC;
         const int b = ti_ & 1;
         if (ti_ >= 2 && !mbar_wait(&accempty[b], ((ti_ >> 1) - 1) & 1, f.status)) {
           *abort_v = 1;
           stop = true;
           break;
         }
-        const uint32_t idesc = tc::idesc_mxf4(kRowsTile, tile_info(tile, f).N, 0, 0);
+        const uint32_t idesc = tc::idesc_mxf4(kRowsTile, tile_info(tile, f, own_tiles).N, 0, 0);
         for (int kc = kb; kc < ke && !stop; ++kc) {
           for (int m = 0; m < NM; ++m, ++it) {
             const int s = it % kStages;
@@ -435,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
     const int row = 32 * q + lane;  // row within the tile
     for (int ti_ = 0; ti_ < ntiles; ++ti_) {
       const int tile = rg.t_first + ti_;
-      const TileInfo ti = tile_info(tile, f);
+      const TileInfo ti = tile_info(tile, f, own_tiles);
       const int b = ti_ & 1;
       const bool write_part = ti_ == 0 && rg.tail_first;          // leave a part for the head
       const bool add_parts = ti_ == ntiles - 1 && rg.head_last;    // add the later CTAs' parts
@@ -519,9 +603,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
             }
           }
         } else {
-          const int asg = f.perm[ti.pos0 + j];
+          const int asg = f.route_one ? own_perm[ti.pos0 + j] : f.perm[ti.pos0 + j];
+          const float gj = f.route_one ? own_gate[asg] : f.gate[asg];
           const int r_exp = ti.rt * kRowsTile + row;  // row within the expert
-          if (r_exp < f.R) f.ybuf[(size_t)asg * f.L + r_exp] = f.gate[asg] * v[0];
+          if (r_exp < f.R) f.ybuf[(size_t)asg * f.L + r_exp] = gj * v[0];
         }
       }
       tc::fence_before_sync();
@@ -615,7 +700,8 @@ cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, i
                               const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,
                               uint8_t* act_q, uint8_t* act_sf, int act_kind, float b1, float b2,
                               const float* gate, float* ybuf, float* part, int32_t* status,
-                              cudaStream_t s, bool pdl, void (*between)(cudaStream_t)) {
+                              cudaStream_t s, bool pdl, void (*between)(cudaStream_t),
+                              const RouteOne* ro) {
   const uint64_t P4 = (uint64_t)T * k * kTerms;
   Maps m0, m1;
   if (!make_map_2d(&m0.m[0], w.w1p, L / 2, (uint64_t)E * I, 128, 128, true) ||
@@ -631,12 +717,25 @@ cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, i
     return cudaErrorInvalidValue;
   m1.m[2] = m1.m[0];
   m1.m[3] = m1.m[1];
+  // unit counts stay below 2^31 (32-bit range arithmetic in the kernel)
+  const uint64_t groups = (uint64_t)T * k / kTokTile + E + 1;
+  if (groups * ((L + kRowsTile - 1) / kRowsTile) * (L / kKStage) >= (1ull << 31) ||
+      groups * ((I + kRowsTile - 1) / kRowsTile) * (L / kKStage) >= (1ull << 31) ||
+      groups * ((L + kRowsTile - 1) / kRowsTile) * (I / kKStage) >= (1ull << 31))
+    return cudaErrorInvalidValue;
   FArgs f{};
   f.k = k; f.L = L; f.I = I; f.act_kind = act_kind; f.b1 = b1; f.b2 = b2;
   f.meta = b.meta; f.perm = b.perm; f.tiles = b.tiles;
   f.act_q = act_q; f.act_sf = act_sf; f.gate = gate; f.ybuf = ybuf;
   f.part = part; f.npart = tc_npart(T);
   f.status = status;
+  if (ro) {
+    f.route_one = 1;
+    f.logits = ro->logits; f.bias = ro->bias; f.E = E;
+    f.renorm = ro->renorm; f.routed_scale = ro->routed_scale;
+    f.idx_out = ro->idx; f.gate_out = ro->gate; f.gap_out = ro->gap;
+    f.tiles_out = b.tiles; f.perm_out = b.perm; f.route_flag = b.flags + kTcRouteFlag;
+  }
   // phase 0 (w1, w3), then phase 1 (w2): the second launch reads what the first wrote, across
   // the kernel boundary (its CTAs wait in griddepcontrol.wait until the first has completed)
   f.ph = 0;

@@ -20,8 +20,8 @@ constexpr int kVecPerLane = 8;    // 16-byte pieces a lane keeps in flight per b
 // using them, so a row's bytes are in flight at once.  Products of bf16 values are exact;
 // each fused add rounds once (fp32).  The 4 quarter sums are added in a fixed order.
 // With xq set (one token), warps 0 .. L/32-1 of the grid also write the token's x as kTerms
-// MXFP4 terms (rows 0 .. kTerms-1 of xq / xsf): work that does not depend on the routing,
-// done here so that no separate launch is spent on it.
+// MXFP4 terms (rows 0 .. kTerms-1 of xq / xsf), and CTA 0 zeroes `zero` [nzero]: work that
+// does not depend on the routing, done here so that no separate launch is spent on it.
 template <int TT>
 __global__ void __launch_bounds__(256) k_router_logits(const uint16_t* __restrict__ h,
                                                        const uint16_t* __restrict__ wr, int T,
@@ -29,9 +29,12 @@ __global__ void __launch_bounds__(256) k_router_logits(const uint16_t* __restric
                                                        float* __restrict__ logits,
                                                        const uint16_t* __restrict__ x, int L,
                                                        uint8_t* __restrict__ xq,
-                                                       uint8_t* __restrict__ xsf) {
+                                                       uint8_t* __restrict__ xsf,
+                                                       int32_t* __restrict__ zero, int nzero) {
   pdl_wait();
   pdl_launch();
+  if (zero && blockIdx.x == 0 && blockIdx.y == 0)  // counters the next launches start from
+    for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
   __shared__ float part[8][TT];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * kRowsPerCta + (warp >> 2);
@@ -115,14 +118,14 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits,
 
 cudaError_t launch_router_logits(const uint16_t* h, const uint16_t* wr, int T, int E, int H,
                                  float* logits, cudaStream_t s, bool pdl, const uint16_t* x,
-                                 int L, uint8_t* xq, uint8_t* xsf) {
+                                 int L, uint8_t* xq, uint8_t* xsf, int32_t* zero, int nzero) {
   const unsigned gx = (E + kRowsPerCta - 1) / kRowsPerCta;
   if (xq && (T != 1 || (int)gx * 8 < (L >> 5))) return cudaErrorInvalidValue;
   if (T <= 2)
     return launch_kernel(k_router_logits<1>, dim3(gx, T), dim3(256), 0, s, pdl, h, wr, T, E, H,
-                         logits, x, L, xq, xsf);
+                         logits, x, L, xq, xsf, zero, nzero);
   return launch_kernel(k_router_logits<4>, dim3(gx, (T + 3) / 4), dim3(256), 0, s, pdl, h, wr, T,
-                       E, H, logits, x, L, xq, xsf);
+                       E, H, logits, x, L, xq, xsf, zero, nzero);
 }
 
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,

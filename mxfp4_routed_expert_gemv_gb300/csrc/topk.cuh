@@ -1,6 +1,6 @@
-// topk.cuh -- one warp's top-k with gates for one token (README "kimi-k3-in-c", Part II
-// section 9 "Picking 16 experts of 896").  Shared by the router's top-k kernel and the
-// fused decode-size preparation kernel.
+// topk.cuh -- the top-k with gates for one token (README "kimi-k3-in-c", Part II section 9
+// "Picking 16 experts of 896"): one warp's version for the router's top-k kernel, and a
+// block's version for the batch-1 preparation and the expert GEMMs that route in-kernel.
 #pragma once
 
 #include "common.cuh"
@@ -138,6 +138,117 @@ __device__ __forceinline__ void topk_block_sort(const float* lt, const float* bi
                      : INFINITY;
   }
   __syncthreads();
+}
+
+// One token's top-k with a whole block, for decode: the same choice, order and tie rule as
+// topk_warp, by sorting instead of repeated arg-max.  Key = (order bits of the selection
+// score, then ~expert), so a larger key is a better choice and equal scores go to the lower
+// index; key 0 stands for "no expert" and sorts last.
+//  1. warp w holds the keys of experts 32(LPW w + j) + lane, j < LPW, and sorts each 32-key
+//     list descending (bitonic, shuffles; the LPW lists are independent, so they overlap);
+//  2. two sorted lists merge into the top 32 of their union by one max against the other
+//     list reversed (a bitonic sequence) and five clean-up steps; the warp merges its own
+//     lists, then the warps' lists merge pairwise in a tree through shared memory;
+//  3. warp 0 ends with the top 32 keys, best first: choice j < k on lane j, key k for the gap.
+// Needs k <= 31 (or k == E), E <= 32 * LPW * (warps); every thread calls it.  lists: shared
+// [warps * 32]; sig: shared [E] (each expert's unbiased score, for the gates).  On warp 0,
+// lane j < k returns choice j's expert e, gate g, and rank (its place among the chosen
+// experts in ascending index order); lane 0 writes the gap when gap is set.
+struct OneTokenChoice {
+  int e;
+  float g;
+  int rank;
+};
+
+__device__ __forceinline__ unsigned long long top32_clean(unsigned long long v, int lane) {
+#pragma unroll
+  for (int stride = 16; stride > 0; stride >>= 1) {
+    const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, stride);
+    const bool lo = (lane & stride) == 0;
+    v = lo ? (v > o ? v : o) : (v > o ? o : v);
+  }
+  return v;
+}
+
+template <int LPW>
+__device__ __forceinline__ OneTokenChoice topk_one_token(const float* lt, const float* bias,
+                                                         int E, int k, int renorm,
+                                                         float routed_scale, float* gap,
+                                                         unsigned long long* lists, float* sig) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  unsigned long long key[LPW];
+  float lg[LPW], bs[LPW];
+#pragma unroll
+  for (int j = 0; j < LPW; ++j) {  // lt read at L2 (written by an earlier launch)
+    const int e = (warp * LPW + j) * 32 + lane;
+    lg[j] = e < E ? __ldcg(lt + e) : 0.f;
+    bs[j] = (e < E && bias) ? bias[e] : 0.f;
+  }
+#pragma unroll
+  for (int j = 0; j < LPW; ++j) {
+    const int e = (warp * LPW + j) * 32 + lane;
+    key[j] = 0ull;
+    if (e < E) {
+      const float sg = sigmoid_f32(lg[j]);
+      sig[e] = sg;
+      key[j] = ((unsigned long long)ordered_bits(sg + bs[j]) << 32) | (uint32_t)(~(uint32_t)e);
+    }
+  }
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const bool desc = (lane & size) == 0, lo = (lane & stride) == 0;
+#pragma unroll
+      for (int j = 0; j < LPW; ++j) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, key[j], stride);
+        const unsigned long long mx = key[j] > o ? key[j] : o, mn = key[j] > o ? o : key[j];
+        key[j] = (lo == desc) ? mx : mn;
+      }
+    }
+  }
+  unsigned long long acc = key[0];
+#pragma unroll
+  for (int j = 1; j < LPW; ++j) {
+    const unsigned long long o = __shfl_sync(0xffffffffu, key[j], 31 - lane);
+    acc = top32_clean(acc > o ? acc : o, lane);
+  }
+  lists[warp * 32 + lane] = acc;
+  __syncthreads();
+  for (int n = nwarps; n > 1;) {
+    const int h = (n + 1) >> 1;
+    if (warp < n - h) {
+      const unsigned long long o = lists[(warp + h) * 32 + 31 - lane];
+      acc = top32_clean(acc > o ? acc : o, lane);
+      lists[warp * 32 + lane] = acc;
+    }
+    n = h;
+    __syncthreads();
+  }
+  OneTokenChoice c = {-1, 0.f, 0};
+  if (warp == 0) {
+    const unsigned long long kth = __shfl_sync(0xffffffffu, acc, k > 0 ? k - 1 : 0);
+    const unsigned long long next = __shfl_sync(0xffffffffu, acc, k < 32 ? k : 31);
+    float s = 0.f;
+    if (lane < k) {
+      c.e = (int)(~(uint32_t)(acc & 0xffffffffull));
+      s = sig[c.e];  // the unbiased score of choice j
+    }
+    const float sum = warp_sum(s);
+    c.g = s;
+    if (renorm && sum > 0.f) c.g = s / sum;
+    c.g *= routed_scale;
+    if (gap && lane == 0)
+      *gap = (k < E) ? from_ordered_bits((uint32_t)(kth >> 32)) -
+                           from_ordered_bits((uint32_t)(next >> 32))
+                     : INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int ei = __shfl_sync(0xffffffffu, c.e, i);
+      if (i < k && ei < c.e) ++c.rank;
+    }
+  }
+  return c;
 }
 
 }  // namespace k3
