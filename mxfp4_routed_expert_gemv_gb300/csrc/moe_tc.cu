@@ -149,11 +149,12 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
 // the table CTA 0 of phase 0 published, after its flag.  Out (shared): tiles[i] =
 // (expert, i, 1) for the chosen experts in ascending order, perm[i] = the choice index of
 // tile i, gate[j] = gate of choice j.  Returns the number of token groups (0 after a timeout).
+template <int PH>
 __device__ __forceinline__ int route_one_token(const FArgs& f, uint8_t* scratch, int4* tiles,
                                                int* perm, float* gate, bool publish) {
   __shared__ int ngroups;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, k = f.k;
-  if (f.ph == 0) {
+  if (PH == 0) {
     const OneTokenChoice c = topk_one_token<3>(
         f.logits, f.bias, f.E, k, f.renorm, f.routed_scale, publish ? f.gap_out : nullptr,
         reinterpret_cast<unsigned long long*>(scratch), reinterpret_cast<float*>(scratch + 4096));
@@ -250,7 +251,7 @@ __device__ __forceinline__ Range make_range(const Split& sp, int KC, int c) {
   return r;
 }
 
-template <int NMAX>
+template <int NMAX, int PH>
 __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ Maps mp,
                                                         const FArgs f) {
   using Y = Lay<NMAX>;
@@ -271,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
   float* fix = reinterpret_cast<float*>(sm + (size_t)kStages * kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;
-  const int NM = f.ph == 0 ? 2 : 1;  // weight matrices per unit: w1 and w3, or w2
+  constexpr int NM = PH == 0 ? 2 : 1;  // weight matrices per unit: w1 and w3, or w2
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -303,12 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
   // logits it routes from) was complete before phase 0 passed this point (phase 0 lets this
   // launch start only after its own wait), and only the activation terms come from phase 0,
   // so only the thread that loads them waits.
-  if (f.ph == 0) pdl_wait();
+  if (PH == 0) pdl_wait();
   pdl_launch();
   const uint32_t t0 = tbase;
   volatile int* abort_v = &abort_flag;
-  const int ngroups = f.route_one ? route_one_token(f, sm, own_tiles, own_perm, own_gate,
-                                                    f.ph == 0 && cta == 0)
+  const int ngroups = f.route_one ? route_one_token<PH>(f, sm, own_tiles, own_perm, own_gate,
+                                                        PH == 0 && cta == 0)
                                   : f.meta[2];
 
   const Split sp(ngroups * f.RT * f.KC, G);
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
   const size_t pf = part_floats(NM, f.npart);
   // this phase's parts (the phases have separate regions: phase 1 may start before phase 0
   // has finished with its parts)
-  float* const parts = f.part + (f.ph == 0 ? 0 : (size_t)kTcMaxGrid * part_floats(2, f.npart));
+  float* const parts = f.part + (PH == 0 ? 0 : (size_t)kTcMaxGrid * part_floats(2, f.npart));
   // an idle CTA (empty range, when there are fewer units than CTAs) leaves no part
   auto idle = [&](int c) { return sp.lo(c + 1) == sp.lo(c); };
   int nfix = 0;
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
     // ------------------------------------- TMA: weights (warp 8), activations (warp 10)
     if (lane == 0) {
       const bool wts = warp == kProdWarp;
-      if (!wts && f.ph == 1) pdl_wait();  // the activation terms are phase 0's output
+      if (!wts && PH == 1) pdl_wait();  // the activation terms are phase 0's output
       const uint64_t once = tc::make_policy_evict_first();  // weights: read once per call
       int it = 0;
       bool stop = false;
@@ -585,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
             }
           }
         }
-        if (f.ph == 0) {
+        if (PH == 0) {
           // SwiGLU (or SiTU-GLU), then the token's kTerms MXFP4 terms for phase 1; this warp's
           // 32 rows are one group of 32 along phase 1's reduction
           const float act = activation(v[0], v[1], f.act_kind, f.b1, f.b2);
@@ -658,25 +659,28 @@ __global__ void __launch_bounds__(512) k_split_x(const uint16_t* __restrict__ x,
   }
 }
 
-template <int NMAX>
+template <int NMAX, int PH>
 cudaError_t launch_tc_n(const Maps& mp, const FArgs& f, cudaStream_t s, bool pdl) {
   static int configured[64] = {0};
   constexpr size_t smem = Lay<NMAX>::kSmemBytes;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_moe_tc<NMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_moe_tc<NMAX, PH>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
-  return launch_kernel(k_moe_tc<NMAX>, dim3(tc_grid_size()), dim3(kThreads), smem, s, pdl, mp, f);
+  return launch_kernel(k_moe_tc<NMAX, PH>, dim3(tc_grid_size()), dim3(kThreads), smem, s, pdl,
+                       mp, f);
 }
 
 // Batches of up to 4 tokens have at most 4 tokens per expert: 16-row activation tiles.
+// Each phase is its own kernel (a launch holds only its phase's code).
 cudaError_t launch_tc(const Maps& mp, const FArgs& f, int T, cudaStream_t s, bool pdl) {
-  if (T * kTerms <= 16) return launch_tc_n<16>(mp, f, s, pdl);
-  return launch_tc_n<64>(mp, f, s, pdl);
+  if (T * kTerms <= 16)
+    return f.ph == 0 ? launch_tc_n<16, 0>(mp, f, s, pdl) : launch_tc_n<16, 1>(mp, f, s, pdl);
+  return f.ph == 0 ? launch_tc_n<64, 0>(mp, f, s, pdl) : launch_tc_n<64, 1>(mp, f, s, pdl);
 }
 
 }  // namespace
