@@ -40,34 +40,37 @@ constexpr int kTokTile = kTcTokTile;                         // tokens per tile
 constexpr int kRowsTile = 128;                               // MMA M
 constexpr uint32_t kABytes = kRowsTile * (kKStage / 2);      // 32768: two 16 KB swizzle columns
 constexpr uint32_t kSABytes = kRowsTile * (kKStage / 32);    // 2048
-constexpr uint32_t kFixBytes = 16384;                        // parts of a shared last tile
 constexpr int kThreads = 352;
 constexpr int kSfWarp0 = 4, kProdWarp = 8, kMmaWarp = 9, kBWarp = 10;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfStageCols = 64;
 constexpr int kEpiBar = 1;  // named barrier of the four epilogue warps
 
-// Shared-memory and TMEM layout for tiles of at most NMAX activation rows (MMA N): 16 for
-// batches of up to 4 tokens (the smaller activation slot leaves room for a fifth ring
-// stage), 64 otherwise.
-//   stage: A [0, 32 KB) | B two 128-byte columns of NMAX rows | A scales 128 x 16 B |
-//          B scales NMAX x 16 B, padded to a multiple of 1024 bytes;
+// Shared-memory and TMEM layout for tiles of at most NMAX activation rows (MMA N: 16 for
+// batches of up to 4 tokens, 64 otherwise) and NM weight matrices per unit (2 in the first
+// GEMM, w1 and w3; 1 in the second).  A ring stage holds one whole unit: the NM matrices'
+// 128 x 512 chunks share the stage's activation chunk, so a stage is 64 KB of weights in the
+// first GEMM (fewer, larger TMA batches stream HBM faster than more, smaller ones).
+//   stage: A of matrix m at m * 32 KB | B two 128-byte columns of NMAX rows | A scales of
+//          matrix m, 128 x 16 B each | B scales NMAX x 16 B, padded to a multiple of 1 KB;
 //   TMEM:  accumulator buffer b at b * kAccCols, matrix m at + m * kMatCols; the scale ring
-//          from kSfBase, stage s at + 64 s: A scales of MMA j at + 4 j (+ lane quarter),
-//          B scales at + 32 + 4 j (+ 1 for B rows 32..63).
-template <int NMAX>
+//          from kSfBase, stage s at + kSfStageCols s: A scales of matrix m, MMA j at
+//          + 32 m + 4 j (+ lane quarter), B scales at + 32 NM + 4 j (+ 1 for B rows 32..63);
+//   fix:   the parts a head tile adds, after the ring (kFixBytes).
+template <int NMAX, int NM>
 struct Lay {
-  static constexpr int kNMax = NMAX;
   static constexpr uint32_t kBKatom = NMAX * 128;
   static constexpr uint32_t kBBytes = 2 * kBKatom;
   static constexpr uint32_t kSBBytes = NMAX * (kKStage / 32);
-  static constexpr uint32_t kOffB = kABytes, kOffSA = kOffB + kBBytes, kOffSB = kOffSA + kSABytes;
+  static constexpr uint32_t kOffB = NM * kABytes, kOffSA = kOffB + kBBytes;
+  static constexpr uint32_t kOffSB = kOffSA + NM * kSABytes;
   static constexpr uint32_t kStageBytes = ((kOffSB + kSBBytes + 1023) / 1024) * 1024;
-  static constexpr int kStages = NMAX <= 16 ? 5 : 4;
+  static constexpr int kStages = NM == 2 ? (NMAX <= 16 ? 3 : 2) : (NMAX <= 16 ? 5 : 4);
+  static constexpr uint32_t kFixBytes = NMAX <= 16 && NM == 2 ? 4096 : 16384;
   static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kFixBytes + 1024;
   static constexpr uint32_t kMatCols = NMAX <= 16 ? 32 : 64;
   static constexpr uint32_t kAccCols = 2 * kMatCols;
   static constexpr uint32_t kSfBase = 2 * kAccCols;
+  static constexpr uint32_t kSfStageCols = 32 * (NM + 1);
   static_assert(kSfBase + kStages * kSfStageCols <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
   static_assert(NMAX % 16 == 0 && NMAX <= 64, "tile height");
@@ -254,11 +257,13 @@ __device__ __forceinline__ Range make_range(const Split& sp, int KC, int c) {
 template <int NMAX, int PH>
 __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ Maps mp,
                                                         const FArgs f) {
-  using Y = Lay<NMAX>;
+  constexpr int NM = PH == 0 ? 2 : 1;  // weight matrices per unit: w1 and w3, or w2
+  using Y = Lay<NMAX, NM>;
   constexpr int kStages = Y::kStages;
   constexpr uint32_t kStageBytes = Y::kStageBytes, kBKatom = Y::kBKatom;
   constexpr uint32_t kOffB = Y::kOffB, kOffSA = Y::kOffSA, kOffSB = Y::kOffSB;
   constexpr uint32_t kAccCols = Y::kAccCols, kMatCols = Y::kMatCols, kSfBase = Y::kSfBase;
+  constexpr uint32_t kSfStageCols = Y::kSfStageCols, kFixBytes = Y::kFixBytes;
   extern __shared__ uint8_t dsm[];
   __shared__ __align__(8) uint64_t fullA[kStages], fullB[kStages], sfready[kStages], empty[kStages];
   __shared__ __align__(8) uint64_t accfull[2], accempty[2], drained, fixfull;
@@ -272,7 +277,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
   float* fix = reinterpret_cast<float*>(sm + (size_t)kStages * kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;
-  constexpr int NM = PH == 0 ? 2 : 1;  // weight matrices per unit: w1 and w3, or w2
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -346,33 +350,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
         const int ke = ti_ == ntiles - 1 ? rg.u1 - tile * f.KC : f.KC;
         const int nbox = ti.N / 16;
         const int arow = ti.expert * f.R + ti.rt * kRowsTile;
-        for (int kc = kb; kc < ke && !stop; ++kc) {
-          for (int m = 0; m < NM; ++m, ++it) {
-            const int s = it % kStages;
-            if (*abort_v ||
-                (it >= kStages && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1, f.status))) {
-              *abort_v = 1;
-              stop = true;
-              break;
-            }
-            uint8_t* st = sm + (size_t)s * kStageBytes;
-            if (wts) {
-              mbar_arrive_expect_tx(&fullA[s], kABytes + kSABytes);
-              tc::tma_load_2d_hint(st, &mp.m[2 * m], kc * 256, arow, &fullA[s], once);
-              tc::tma_load_2d_hint(st + 16384, &mp.m[2 * m], kc * 256 + 128, arow, &fullA[s],
+        for (int kc = kb; kc < ke && !stop; ++kc, ++it) {
+          const int s = it % kStages;
+          if (*abort_v ||
+              (it >= kStages && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1, f.status))) {
+            *abort_v = 1;
+            stop = true;
+            break;
+          }
+          uint8_t* st = sm + (size_t)s * kStageBytes;
+          if (wts) {
+            mbar_arrive_expect_tx(&fullA[s], NM * (kABytes + kSABytes));
+#pragma unroll
+            for (int m = 0; m < NM; ++m) {
+              uint8_t* sa = st + m * kABytes;
+              tc::tma_load_2d_hint(sa, &mp.m[2 * m], kc * 256, arow, &fullA[s], once);
+              tc::tma_load_2d_hint(sa + 16384, &mp.m[2 * m], kc * 256 + 128, arow, &fullA[s],
                                    once);
-              tc::tma_load_2d_hint(st + kOffSA, &mp.m[2 * m + 1], kc * 16, arow, &fullA[s], once);
-            } else {
-              // one token: its terms are rows 0 .. kTerms-1 whatever the position (the router
-              // launch writes only those; the per-position layout repeats them)
-              const int brow0 = f.one_token ? 0 : ti.pos0 * kTerms;
-              mbar_arrive_expect_tx(&fullB[s], (uint32_t)nbox * (2 * 2048 + 256));
-              for (int b = 0; b < nbox; ++b) {
-                tc::tma_load_2d(st + kOffB + b * 2048, &mp.m[4], kc * 256, brow0 + 16 * b, &fullB[s]);
-                tc::tma_load_2d(st + kOffB + kBKatom + b * 2048, &mp.m[4], kc * 256 + 128,
-                                brow0 + 16 * b, &fullB[s]);
-                tc::tma_load_2d(st + kOffSB + b * 256, &mp.m[5], kc * 16, brow0 + 16 * b, &fullB[s]);
-              }
+              tc::tma_load_2d_hint(st + kOffSA + m * kSABytes, &mp.m[2 * m + 1], kc * 16, arow,
+                                   &fullA[s], once);
+            }
+          } else {
+            // one token: its terms are rows 0 .. kTerms-1 whatever the position (the router
+            // launch writes only those; the per-position layout repeats them)
+            const int brow0 = f.one_token ? 0 : ti.pos0 * kTerms;
+            mbar_arrive_expect_tx(&fullB[s], (uint32_t)nbox * (2 * 2048 + 256));
+            for (int b = 0; b < nbox; ++b) {
+              tc::tma_load_2d(st + kOffB + b * 2048, &mp.m[4], kc * 256, brow0 + 16 * b, &fullB[s]);
+              tc::tma_load_2d(st + kOffB + kBKatom + b * 2048, &mp.m[4], kc * 256 + 128,
+                              brow0 + 16 * b, &fullB[s]);
+              tc::tma_load_2d(st + kOffSB + b * 256, &mp.m[5], kc * 16, brow0 + 16 * b, &fullB[s]);
             }
           }
         }
@@ -424,43 +431,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
       const int N = tile_info(tile, f, own_tiles).N;
       const int kb = ti_ == 0 ? rg.u0 - tile * f.KC : 0;
       const int ke = ti_ == ntiles - 1 ? rg.u1 - tile * f.KC : f.KC;
-      for (int kc = kb; kc < ke && !stop; ++kc) {
-        for (int m = 0; m < NM; ++m, ++it) {
-          const int s = it % kStages;
-          const uint32_t par = (it / kStages) & 1;
-          const bool ok = !*abort_v &&
-                          mbar_wait(&fullA[s], par, lane == 0 ? f.status : nullptr) &&
-                          mbar_wait(&fullB[s], par, lane == 0 ? f.status : nullptr);
-          if (!__all_sync(0xffffffffu, ok)) {
-            *abort_v = 1;
-            stop = true;
-            break;
-          }
-          const uint8_t* st = sm + (size_t)s * kStageBytes;
-          const uint32_t ring = t0 + lane_off + kSfBase + (uint32_t)s * kSfStageCols;
-          const uint4 sa = *reinterpret_cast<const uint4*>(st + kOffSA + 16 * (32 * q + lane));
-          const uint32_t wa[4] = {clear_ff_bytes(sa.x), clear_ff_bytes(sa.y), clear_ff_bytes(sa.z),
-                                  clear_ff_bytes(sa.w)};
-#pragma unroll
-          for (int j = 0; j < kMmas; ++j)
-            tc::tmem_st_x1(ring + 4 * j + q, (wa[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-          const uint4 sb0 = *reinterpret_cast<const uint4*>(st + kOffSB + 16 * lane);
-          const uint32_t wb0[4] = {sb0.x, sb0.y, sb0.z, sb0.w};
-#pragma unroll
-          for (int j = 0; j < kMmas; ++j)
-            tc::tmem_st_x1(ring + 32 + 4 * j, (wb0[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-          if (NMAX > 32 && N > 32) {
-            const uint4 sb1 = *reinterpret_cast<const uint4*>(st + kOffSB + 16 * (32 + lane));
-            const uint32_t wb1[4] = {sb1.x, sb1.y, sb1.z, sb1.w};
-#pragma unroll
-            for (int j = 0; j < kMmas; ++j)
-              tc::tmem_st_x1(ring + 33 + 4 * j, (wb1[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-          }
-          tc::tmem_st_wait();
-          tc::fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sfready[s]);
+      for (int kc = kb; kc < ke && !stop; ++kc, ++it) {
+        const int s = it % kStages;
+        const uint32_t par = (it / kStages) & 1;
+        const bool ok = !*abort_v &&
+                        mbar_wait(&fullA[s], par, lane == 0 ? f.status : nullptr) &&
+                        mbar_wait(&fullB[s], par, lane == 0 ? f.status : nullptr);
+        if (!__all_sync(0xffffffffu, ok)) {
+          *abort_v = 1;
+          stop = true;
+          break;
         }
+        const uint8_t* st = sm + (size_t)s * kStageBytes;
+        const uint32_t ring = t0 + lane_off + kSfBase + (uint32_t)s * kSfStageCols;
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+          const uint4 sa =
+              *reinterpret_cast<const uint4*>(st + kOffSA + m * kSABytes + 16 * (32 * q + lane));
+          const uint32_t wa[4] = {clear_ff_bytes(sa.x), clear_ff_bytes(sa.y),
+                                  clear_ff_bytes(sa.z), clear_ff_bytes(sa.w)};
+#pragma unroll
+          for (int j = 0; j < kMmas; ++j)
+            tc::tmem_st_x1(ring + 32 * m + 4 * j + q, (wa[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+        }
+        const uint32_t rb = ring + 32 * NM;
+        const uint4 sb0 = *reinterpret_cast<const uint4*>(st + kOffSB + 16 * lane);
+        const uint32_t wb0[4] = {sb0.x, sb0.y, sb0.z, sb0.w};
+#pragma unroll
+        for (int j = 0; j < kMmas; ++j)
+          tc::tmem_st_x1(rb + 4 * j, (wb0[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+        if (NMAX > 32 && N > 32) {
+          const uint4 sb1 = *reinterpret_cast<const uint4*>(st + kOffSB + 16 * (32 + lane));
+          const uint32_t wb1[4] = {sb1.x, sb1.y, sb1.z, sb1.w};
+#pragma unroll
+          for (int j = 0; j < kMmas; ++j)
+            tc::tmem_st_x1(rb + 1 + 4 * j, (wb1[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+        }
+        tc::tmem_st_wait();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfready[s]);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -479,31 +489,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
           break;
         }
         const uint32_t idesc = tc::idesc_mxf4(kRowsTile, tile_info(tile, f, own_tiles).N, 0, 0);
-        for (int kc = kb; kc < ke && !stop; ++kc) {
-          for (int m = 0; m < NM; ++m, ++it) {
-            const int s = it % kStages;
-            const uint32_t par = (it / kStages) & 1;
-            if (*abort_v || !mbar_wait(&fullA[s], par, f.status) ||
-                !mbar_wait(&fullB[s], par, f.status) || !mbar_wait(&sfready[s], par, f.status)) {
-              *abort_v = 1;
-              stop = true;
-              break;
-            }
-            tc::fence_after_sync();
-            const uint32_t st = tc::smem_addr(sm + (size_t)s * kStageBytes);
+        for (int kc = kb; kc < ke && !stop; ++kc, ++it) {
+          const int s = it % kStages;
+          const uint32_t par = (it / kStages) & 1;
+          if (*abort_v || !mbar_wait(&fullA[s], par, f.status) ||
+              !mbar_wait(&fullB[s], par, f.status) || !mbar_wait(&sfready[s], par, f.status)) {
+            *abort_v = 1;
+            stop = true;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t st = tc::smem_addr(sm + (size_t)s * kStageBytes);
+          const uint32_t sfr = t0 + kSfBase + (uint32_t)s * kSfStageCols;
+#pragma unroll
+          for (int m = 0; m < NM; ++m) {
             const uint32_t d = t0 + (uint32_t)b * kAccCols + kMatCols * m;
-            const uint32_t sfr = t0 + kSfBase + (uint32_t)s * kSfStageCols;
 #pragma unroll
             for (int j = 0; j < kMmas; ++j) {
-              const uint32_t koff = (uint32_t)(j >> 2) * 16384u + (uint32_t)(j & 3) * 32u;
+              const uint32_t koff = m * kABytes + (uint32_t)(j >> 2) * 16384u + (uint32_t)(j & 3) * 32u;
               const uint32_t kboff = (uint32_t)(j >> 2) * kBKatom + (uint32_t)(j & 3) * 32u;
               const uint64_t ad = tc::smem_desc(st + koff, 16, 1024, tc::kLayout128B);
               const uint64_t bd = tc::smem_desc(st + kOffB + kboff, 16, 1024, tc::kLayout128B);
-              tc::mma_mxf4(d, ad, bd, idesc, sfr + 4 * j, sfr + 32 + 4 * j,
+              tc::mma_mxf4(d, ad, bd, idesc, sfr + 32 * m + 4 * j, sfr + 32 * NM + 4 * j,
                            (kc == kb && j == 0) ? 0u : 1u);
             }
-            tc::mma_commit(&empty[s]);
           }
+          tc::mma_commit(&empty[s]);
         }
         if (!stop) tc::mma_commit(&accfull[b]);
       }
@@ -662,7 +673,7 @@ __global__ void __launch_bounds__(512) k_split_x(const uint16_t* __restrict__ x,
 template <int NMAX, int PH>
 cudaError_t launch_tc_n(const Maps& mp, const FArgs& f, cudaStream_t s, bool pdl) {
   static int configured[64] = {0};
-  constexpr size_t smem = Lay<NMAX>::kSmemBytes;
+  constexpr size_t smem = Lay<NMAX, PH == 0 ? 2 : 1>::kSmemBytes;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !configured[dev]) {
