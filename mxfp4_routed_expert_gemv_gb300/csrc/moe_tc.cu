@@ -12,7 +12,7 @@
 //
 // Two launches of one persistent kernel: phase 0 (w1, w3 -> act terms) and phase 1 (w2 ->
 // gate * o per assignment).  A phase is a list of tiles of 128 weight rows x (up to 16 of an
-// expert's tokens) x the full reduction, cut into units of 512 reduction elements; CTA c (one
+// expert's tokens) x the full reduction, cut into units of 512 (or 1024) reduction elements; CTA c (one
 // per SM) takes units [U c / G, U (c+1) / G), balanced to one unit whatever the routing.  A
 // tile cut by a range boundary is finished by the CTA holding its first unit (its "head"),
 // which processes it last; the others process their part first and leave it in global
@@ -22,9 +22,10 @@
 //
 // Roles (352 threads): warps 0-3 epilogue (TMEM lane quarters 0-3), warps 4-7 move each
 // stage's scales into TMEM (a 0xFF scale byte, "no value", becomes 0 there), warp 8 issues
-// the weight TMA copies into a 4-stage ring, warp 10 the activation copies (and then fetches
-// the parts of a shared last tile), warp 9 allocates TMEM and issues the MMAs.  Every wait is
-// bounded; one that runs out sets the status block's timeout count and the CTA stops.
+// the weight TMA copies into the ring (one 64 KB unit per stage, see Lay), warp 10 the
+// activation copies (and then fetches the parts of a shared last tile), warp 9 allocates
+// TMEM and issues the MMAs.  Every wait is bounded; one that runs out sets the status
+// block's timeout count and the CTA stops.  Each phase (and unit shape) is its own kernel.
 #include "launch.h"
 #include "mxq.cuh"
 #include "tc.cuh"
@@ -46,31 +47,35 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kEpiBar = 1;  // named barrier of the four epilogue warps
 
 // Shared-memory and TMEM layout for tiles of at most NMAX activation rows (MMA N: 16 for
-// batches of up to 4 tokens, 64 otherwise) and NM weight matrices per unit (2 in the first
-// GEMM, w1 and w3; 1 in the second).  A ring stage holds one whole unit: the NM matrices'
-// 128 x 512 chunks share the stage's activation chunk, so a stage is 64 KB of weights in the
-// first GEMM (fewer, larger TMA batches stream HBM faster than more, smaller ones).
-//   stage: A of matrix m at m * 32 KB | B two 128-byte columns of NMAX rows | A scales of
-//          matrix m, 128 x 16 B each | B scales NMAX x 16 B, padded to a multiple of 1 KB;
+// batches of up to 4 tokens, 64 otherwise), NM weight matrices per unit (2 in the first
+// GEMM, w1 and w3; 1 in the second) and KS 512-chunks of the reduction per unit (1, or 2 in
+// the second GEMM when its reduction allows).  A ring stage holds one whole unit: NM x KS
+// weight blocks of 128 x 512, so a stage is 64 KB of weights either way (fewer, larger TMA
+// batches stream HBM faster than more, smaller ones).  Block (m, ks) is sub-block
+// sb = m KS + ks.
+//   stage: A of sub-block sb at sb * 32 KB | B of chunk ks (two 128-byte columns of NMAX
+//          rows) | A scales of sb, 128 x 16 B each | B scales of ks, NMAX x 16 B each,
+//          padded to a multiple of 1 KB;
 //   TMEM:  accumulator buffer b at b * kAccCols, matrix m at + m * kMatCols; the scale ring
-//          from kSfBase, stage s at + kSfStageCols s: A scales of matrix m, MMA j at
-//          + 32 m + 4 j (+ lane quarter), B scales at + 32 NM + 4 j (+ 1 for B rows 32..63);
+//          from kSfBase, stage s at + kSfStageCols s: A scales of sb, MMA j at + 32 sb + 4 j
+//          (+ lane quarter), B scales of ks at + 32 (NM KS + ks) + 4 j (+ 1 for B rows 32..63);
 //   fix:   the parts a head tile adds, after the ring (kFixBytes).
-template <int NMAX, int NM>
+template <int NMAX, int NM, int KS>
 struct Lay {
   static constexpr uint32_t kBKatom = NMAX * 128;
   static constexpr uint32_t kBBytes = 2 * kBKatom;
   static constexpr uint32_t kSBBytes = NMAX * (kKStage / 32);
-  static constexpr uint32_t kOffB = NM * kABytes, kOffSA = kOffB + kBBytes;
-  static constexpr uint32_t kOffSB = kOffSA + NM * kSABytes;
-  static constexpr uint32_t kStageBytes = ((kOffSB + kSBBytes + 1023) / 1024) * 1024;
-  static constexpr int kStages = NM == 2 ? (NMAX <= 16 ? 3 : 2) : (NMAX <= 16 ? 5 : 4);
+  static constexpr uint32_t kOffB = NM * KS * kABytes, kOffSA = kOffB + KS * kBBytes;
+  static constexpr uint32_t kOffSB = kOffSA + NM * KS * kSABytes;
+  static constexpr uint32_t kStageBytes = ((kOffSB + KS * kSBBytes + 1023) / 1024) * 1024;
+  static constexpr int kStages =
+      NM * KS == 2 ? (NMAX <= 16 && NM == 2 ? 3 : 2) : (NMAX <= 16 ? 5 : 4);
   static constexpr uint32_t kFixBytes = NMAX <= 16 && NM == 2 ? 4096 : 16384;
   static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kFixBytes + 1024;
   static constexpr uint32_t kMatCols = NMAX <= 16 ? 32 : 64;
   static constexpr uint32_t kAccCols = 2 * kMatCols;
   static constexpr uint32_t kSfBase = 2 * kAccCols;
-  static constexpr uint32_t kSfStageCols = 32 * (NM + 1);
+  static constexpr uint32_t kSfStageCols = 32 * (NM * KS + KS);
   static_assert(kSfBase + kStages * kSfStageCols <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
   static_assert(NMAX % 16 == 0 && NMAX <= 64, "tile height");
@@ -254,14 +259,15 @@ __device__ __forceinline__ Range make_range(const Split& sp, int KC, int c) {
   return r;
 }
 
-template <int NMAX, int PH>
+template <int NMAX, int PH, int KS>
 __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ Maps mp,
                                                         const FArgs f) {
   constexpr int NM = PH == 0 ? 2 : 1;  // weight matrices per unit: w1 and w3, or w2
-  using Y = Lay<NMAX, NM>;
+  using Y = Lay<NMAX, NM, KS>;
   constexpr int kStages = Y::kStages;
   constexpr uint32_t kStageBytes = Y::kStageBytes, kBKatom = Y::kBKatom;
   constexpr uint32_t kOffB = Y::kOffB, kOffSA = Y::kOffSA, kOffSB = Y::kOffSB;
+  constexpr uint32_t kBBytes = Y::kBBytes, kSBBytes = Y::kSBBytes;
   constexpr uint32_t kAccCols = Y::kAccCols, kMatCols = Y::kMatCols, kSfBase = Y::kSfBase;
   constexpr uint32_t kSfStageCols = Y::kSfStageCols, kFixBytes = Y::kFixBytes;
   extern __shared__ uint8_t dsm[];
@@ -360,26 +366,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
           }
           uint8_t* st = sm + (size_t)s * kStageBytes;
           if (wts) {
-            mbar_arrive_expect_tx(&fullA[s], NM * (kABytes + kSABytes));
+            mbar_arrive_expect_tx(&fullA[s], NM * KS * (kABytes + kSABytes));
 #pragma unroll
             for (int m = 0; m < NM; ++m) {
-              uint8_t* sa = st + m * kABytes;
-              tc::tma_load_2d_hint(sa, &mp.m[2 * m], kc * 256, arow, &fullA[s], once);
-              tc::tma_load_2d_hint(sa + 16384, &mp.m[2 * m], kc * 256 + 128, arow, &fullA[s],
-                                   once);
-              tc::tma_load_2d_hint(st + kOffSA + m * kSABytes, &mp.m[2 * m + 1], kc * 16, arow,
-                                   &fullA[s], once);
+#pragma unroll
+              for (int ks = 0; ks < KS; ++ks) {
+                const int sb = m * KS + ks, x = (kc * KS + ks) * 256;
+                uint8_t* sa = st + sb * kABytes;
+                tc::tma_load_2d_hint(sa, &mp.m[2 * m], x, arow, &fullA[s], once);
+                tc::tma_load_2d_hint(sa + 16384, &mp.m[2 * m], x + 128, arow, &fullA[s], once);
+                tc::tma_load_2d_hint(st + kOffSA + sb * kSABytes, &mp.m[2 * m + 1],
+                                     (kc * KS + ks) * 16, arow, &fullA[s], once);
+              }
             }
           } else {
             // one token: its terms are rows 0 .. kTerms-1 whatever the position (the router
             // launch writes only those; the per-position layout repeats them)
             const int brow0 = f.one_token ? 0 : ti.pos0 * kTerms;
-            mbar_arrive_expect_tx(&fullB[s], (uint32_t)nbox * (2 * 2048 + 256));
-            for (int b = 0; b < nbox; ++b) {
-              tc::tma_load_2d(st + kOffB + b * 2048, &mp.m[4], kc * 256, brow0 + 16 * b, &fullB[s]);
-              tc::tma_load_2d(st + kOffB + kBKatom + b * 2048, &mp.m[4], kc * 256 + 128,
-                              brow0 + 16 * b, &fullB[s]);
-              tc::tma_load_2d(st + kOffSB + b * 256, &mp.m[5], kc * 16, brow0 + 16 * b, &fullB[s]);
+            mbar_arrive_expect_tx(&fullB[s], (uint32_t)(KS * nbox) * (2 * 2048 + 256));
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+              uint8_t* sbk = st + kOffB + ks * kBBytes;
+              const int x = (kc * KS + ks) * 256;
+              for (int b = 0; b < nbox; ++b) {
+                tc::tma_load_2d(sbk + b * 2048, &mp.m[4], x, brow0 + 16 * b, &fullB[s]);
+                tc::tma_load_2d(sbk + kBKatom + b * 2048, &mp.m[4], x + 128, brow0 + 16 * b,
+                                &fullB[s]);
+                tc::tma_load_2d(st + kOffSB + ks * kSBBytes + b * 256, &mp.m[5],
+                                (kc * KS + ks) * 16, brow0 + 16 * b, &fullB[s]);
+              }
             }
           }
         }
@@ -445,27 +460,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
         const uint8_t* st = sm + (size_t)s * kStageBytes;
         const uint32_t ring = t0 + lane_off + kSfBase + (uint32_t)s * kSfStageCols;
 #pragma unroll
-        for (int m = 0; m < NM; ++m) {
+        for (int sb = 0; sb < NM * KS; ++sb) {
           const uint4 sa =
-              *reinterpret_cast<const uint4*>(st + kOffSA + m * kSABytes + 16 * (32 * q + lane));
+              *reinterpret_cast<const uint4*>(st + kOffSA + sb * kSABytes + 16 * (32 * q + lane));
           const uint32_t wa[4] = {clear_ff_bytes(sa.x), clear_ff_bytes(sa.y),
                                   clear_ff_bytes(sa.z), clear_ff_bytes(sa.w)};
 #pragma unroll
           for (int j = 0; j < kMmas; ++j)
-            tc::tmem_st_x1(ring + 32 * m + 4 * j + q, (wa[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+            tc::tmem_st_x1(ring + 32 * sb + 4 * j + q, (wa[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
         }
-        const uint32_t rb = ring + 32 * NM;
-        const uint4 sb0 = *reinterpret_cast<const uint4*>(st + kOffSB + 16 * lane);
-        const uint32_t wb0[4] = {sb0.x, sb0.y, sb0.z, sb0.w};
 #pragma unroll
-        for (int j = 0; j < kMmas; ++j)
-          tc::tmem_st_x1(rb + 4 * j, (wb0[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-        if (NMAX > 32 && N > 32) {
-          const uint4 sb1 = *reinterpret_cast<const uint4*>(st + kOffSB + 16 * (32 + lane));
-          const uint32_t wb1[4] = {sb1.x, sb1.y, sb1.z, sb1.w};
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint32_t rb = ring + 32 * (NM * KS + ks);
+          const uint8_t* sbs = st + kOffSB + ks * kSBBytes;
+          const uint4 sb0 = *reinterpret_cast<const uint4*>(sbs + 16 * lane);
+          const uint32_t wb0[4] = {sb0.x, sb0.y, sb0.z, sb0.w};
 #pragma unroll
           for (int j = 0; j < kMmas; ++j)
-            tc::tmem_st_x1(rb + 1 + 4 * j, (wb1[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+            tc::tmem_st_x1(rb + 4 * j, (wb0[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+          if (NMAX > 32 && N > 32) {
+            const uint4 sb1 = *reinterpret_cast<const uint4*>(sbs + 16 * (32 + lane));
+            const uint32_t wb1[4] = {sb1.x, sb1.y, sb1.z, sb1.w};
+#pragma unroll
+            for (int j = 0; j < kMmas; ++j)
+              tc::tmem_st_x1(rb + 1 + 4 * j, (wb1[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+          }
         }
         tc::tmem_st_wait();
         tc::fence_before_sync();
@@ -505,13 +524,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
           for (int m = 0; m < NM; ++m) {
             const uint32_t d = t0 + (uint32_t)b * kAccCols + kMatCols * m;
 #pragma unroll
-            for (int j = 0; j < kMmas; ++j) {
-              const uint32_t koff = m * kABytes + (uint32_t)(j >> 2) * 16384u + (uint32_t)(j & 3) * 32u;
-              const uint32_t kboff = (uint32_t)(j >> 2) * kBKatom + (uint32_t)(j & 3) * 32u;
-              const uint64_t ad = tc::smem_desc(st + koff, 16, 1024, tc::kLayout128B);
-              const uint64_t bd = tc::smem_desc(st + kOffB + kboff, 16, 1024, tc::kLayout128B);
-              tc::mma_mxf4(d, ad, bd, idesc, sfr + 32 * m + 4 * j, sfr + 32 * NM + 4 * j,
-                           (kc == kb && j == 0) ? 0u : 1u);
+            for (int ks = 0; ks < KS; ++ks) {
+              const int sb = m * KS + ks;
+#pragma unroll
+              for (int j = 0; j < kMmas; ++j) {
+                const uint32_t koff =
+                    sb * kABytes + (uint32_t)(j >> 2) * 16384u + (uint32_t)(j & 3) * 32u;
+                const uint32_t kboff =
+                    ks * kBBytes + (uint32_t)(j >> 2) * kBKatom + (uint32_t)(j & 3) * 32u;
+                const uint64_t ad = tc::smem_desc(st + koff, 16, 1024, tc::kLayout128B);
+                const uint64_t bd = tc::smem_desc(st + kOffB + kboff, 16, 1024, tc::kLayout128B);
+                tc::mma_mxf4(d, ad, bd, idesc, sfr + 32 * sb + 4 * j,
+                             sfr + 32 * (NM * KS + ks) + 4 * j,
+                             (kc == kb && ks == 0 && j == 0) ? 0u : 1u);
+              }
             }
           }
           tc::mma_commit(&empty[s]);
@@ -670,28 +696,35 @@ __global__ void __launch_bounds__(512) k_split_x(const uint16_t* __restrict__ x,
   }
 }
 
-template <int NMAX, int PH>
-cudaError_t launch_tc_n(const Maps& mp, const FArgs& f, cudaStream_t s, bool pdl) {
+template <int NMAX, int PH, int KS>
+cudaError_t launch_tc_n(const Maps& mp, FArgs f, cudaStream_t s, bool pdl) {
   static int configured[64] = {0};
-  constexpr size_t smem = Lay<NMAX, PH == 0 ? 2 : 1>::kSmemBytes;
+  constexpr size_t smem = Lay<NMAX, PH == 0 ? 2 : 1, KS>::kSmemBytes;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_moe_tc<NMAX, PH>,
+    cudaError_t e = cudaFuncSetAttribute(k_moe_tc<NMAX, PH, KS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
-  return launch_kernel(k_moe_tc<NMAX, PH>, dim3(tc_grid_size()), dim3(kThreads), smem, s, pdl,
-                       mp, f);
+  f.KC /= KS;  // units of KS chunks per tile
+  return launch_kernel(k_moe_tc<NMAX, PH, KS>, dim3(tc_grid_size()), dim3(kThreads), smem, s,
+                       pdl, mp, f);
 }
 
+// Each phase is its own kernel (a launch holds only its phase's code); the second GEMM
+// takes two 512-chunks per unit when its reduction (f.KC chunks) divides evenly.
+template <int NMAX>
+cudaError_t launch_tc_phase(const Maps& mp, const FArgs& f, cudaStream_t s, bool pdl) {
+  if (f.ph == 0) return launch_tc_n<NMAX, 0, 1>(mp, f, s, pdl);
+  if (f.KC % 2 == 0) return launch_tc_n<NMAX, 1, 2>(mp, f, s, pdl);
+  return launch_tc_n<NMAX, 1, 1>(mp, f, s, pdl);
+}
 // Batches of up to 4 tokens have at most 4 tokens per expert: 16-row activation tiles.
-// Each phase is its own kernel (a launch holds only its phase's code).
 cudaError_t launch_tc(const Maps& mp, const FArgs& f, int T, cudaStream_t s, bool pdl) {
-  if (T * kTerms <= 16)
-    return f.ph == 0 ? launch_tc_n<16, 0>(mp, f, s, pdl) : launch_tc_n<16, 1>(mp, f, s, pdl);
-  return f.ph == 0 ? launch_tc_n<64, 0>(mp, f, s, pdl) : launch_tc_n<64, 1>(mp, f, s, pdl);
+  if (T * kTerms <= 16) return launch_tc_phase<16>(mp, f, s, pdl);
+  return launch_tc_phase<64>(mp, f, s, pdl);
 }
 
 }  // namespace
