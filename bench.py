@@ -48,11 +48,23 @@ def layer_bytes(w: synth.Workload, distinct_experts: int, T: int) -> int:
             + T * w.hidden * 2 + T * w.latent * 2 + T * w.latent * 4)
 
 
+TERMS = 4  # MXFP4 terms per activation vector on the tensor-core path
+
+
 def gemm1_bytes(w: synth.Workload, distinct_experts: int, T: int) -> int:
-    """GEMM1's compulsory traffic: w1 and w3 (packed + scales) of the distinct experts, the
-    f16 copy of x it reads and the fp32 activations it writes."""
+    """The first expert GEMM's compulsory traffic: w1 and w3 (packed + scales) of the distinct
+    experts, the MXFP4 terms of x it reads (one copy for a single token, else one per
+    (token, expert) position) and the terms of act it writes (one per position)."""
     L, I = w.latent, w.inter
-    return distinct_experts * 2 * (I * L // 2 + I * L // 32) + T * L * 2 + T * w.k * I * 4
+    x_rows = TERMS if T == 1 else T * w.k * TERMS
+    return (distinct_experts * 2 * (I * L // 2 + I * L // 32) + x_rows * (L // 2 + L // 32)
+            + T * w.k * TERMS * (I // 2 + I // 32))
+
+
+def gemm1_flops(w: synth.Workload, T: int) -> int:
+    """Useful multiply-adds of the first expert GEMM, as FLOP: 2 matrices x I x L per
+    (token, expert) pair."""
+    return 2 * 2 * w.inter * w.latent * T * w.k
 
 
 def token_macs(w: synth.Workload) -> int:
@@ -373,6 +385,8 @@ def run_ours(args):
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
     achieved = g1_bytes / gemm1_s / 1e9
+    g1_flops = gemm1_flops(w, T)
+    fp4_peak = peaks.get("bf16_tflops", 0.0) * 6.0 or None
     traffic = None
     prof = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(prof):
@@ -402,7 +416,8 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * elapsed_max / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e2m1*f16->f32 (MXFP4 weights, fp32 accumulation)",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e2m1 x e2m1 (MXFP4 weights x 4-term MXFP4 activations, tcgen05 kind::mxf4, fp32 accumulation)",
         "data": "synthetic",
         "config": {"workload": w.name, "tokens_per_step_per_gpu": T, "experts": w.E, "topk": w.k,
                    "hidden": w.hidden, "latent": w.latent, "inter": w.inter,
@@ -415,10 +430,17 @@ def run_ours(args):
                                 enumerate(["route", "bucket+prep", "gemm1", "gemm2", "combine"])},
                    "launch": "CUDA graph replay, programmatic dependent launch between kernels",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": "k_gemm1 (w1+w3 MXFP4 GEMV, SwiGLU epilogue)",
+        "roofline": {"bound": "hbm",
+                     "kernel": f"k_moe_tc<{16 if T * TERMS <= 16 else 64},0> (w1+w3 block-scaled "
+                               "tcgen05 GEMM fed by TMA, SwiGLU + MXFP4-term epilogue)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_src} hbm_gbs", "traffic": traffic,
-                     "algorithmic_bytes_per_launch": g1_bytes, "avg_launch_s": gemm1_s},
+                     "algorithmic_bytes_per_launch": g1_bytes, "avg_launch_s": gemm1_s,
+                     "tensor": {"useful_tflops": g1_flops / gemm1_s / 1e12,
+                                "fp4_peak_tflops": fp4_peak,
+                                "fp4_peak_source": "measured bf16_tflops x 6 (nominal fp4:bf16 ratio)",
+                                "frac_useful": g1_flops / gemm1_s / 1e12 / fp4_peak if fp4_peak else None,
+                                "issued_per_useful": TERMS}},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * (w.hidden + w.latent) * 2,
                 "d2h_bytes_per_step": T * w.latent * 4},
         "gpu_launches": int(launches),
