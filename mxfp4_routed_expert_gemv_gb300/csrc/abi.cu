@@ -209,7 +209,8 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
   if (!one) {
     K3_TRY(launch_prep(p, s, route));
     if (w.tc)
-      K3_TRY(launch_split_x(static_cast<const uint16_t*>(x), T, L, K, w.b, w.xq, w.xsf, s, true));
+      K3_TRY(launch_split_x(static_cast<const uint16_t*>(x), T, L, K, E, idx, w.b, w.xq, w.xsf,
+                            s, true));
   }
   if (w.tc) {
     K3_TRY(phase(2, s));

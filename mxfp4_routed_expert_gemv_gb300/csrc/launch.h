@@ -120,8 +120,9 @@ bool tc_path_supported(int L, int I);
 int tc_grid();
 int tc_npart(int T);
 size_t tc_part_floats(int T);
-cudaError_t launch_split_x(const uint16_t* x, int T, int L, int k, const BucketOut& b,
-                           uint8_t* xq, uint8_t* xsf, cudaStream_t s, bool pdl);
+cudaError_t launch_split_x(const uint16_t* x, int T, int L, int k, int E, const int32_t* idx,
+                           const BucketOut& b, uint8_t* xq, uint8_t* xsf, cudaStream_t s,
+                           bool pdl);
 // One token routed inside the expert GEMMs (no preparation launch): the router's logits and
 // the top-k parameters; CTA 0 of the first GEMM publishes idx / gate / gap (and the tile
 // table, in BucketOut's tiles / perm, for the second GEMM).  Needs E <= 1056, k <= 31 or k == E.

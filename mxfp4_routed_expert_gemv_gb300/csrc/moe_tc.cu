@@ -99,6 +99,7 @@ struct FArgs {
   float b1, b2;
   int KC, RT, R;           // reduction chunks, row tiles, rows per expert
   const int32_t *meta, *perm;
+  const int32_t* nbase;     // [active experts + 1] first token group of each active expert
   const int4* tiles;        // per token group: expert, first position, token count
   uint8_t *act_q, *act_sf;  // phase-0 output = phase-1 activation operand
   const float* gate;
@@ -127,20 +128,53 @@ __device__ __forceinline__ size_t part_floats(int NM, int npart) {
 
 struct TileInfo {
   int rt, expert, pos0, ntok, N;
+  bool shared_rows;  // other tiles of this launch read the same weight rows
 };
-// tile -> (row tile, and from the table of token groups: expert, first position, token
-// count); the table is the preparation's, or this CTA's own for a single routed token
-__device__ __forceinline__ TileInfo tile_info(int tile, const FArgs& f, const int4* own) {
-  TileInfo t;
-  const int ntg = tile / f.RT;
-  t.rt = tile - ntg * f.RT;
-  const int4 g = f.route_one ? own[ntg] : __ldg(f.tiles + ntg);
-  t.expert = g.x;
-  t.pos0 = g.y;
-  t.ntok = g.z;
-  t.N = ((t.ntok * kTerms + 15) / 16) * 16;
-  return t;
-}
+// Tiles in order: expert by expert (active experts ascending), and within an expert with n
+// token groups, row tile by row tile, each row tile once per group (tile = base + rt n + g),
+// so that the n tiles reading the same 128 weight rows follow each other and the rows come
+// from L2 after the first.  A cursor walks a CTA's tiles in increasing order: it finds the
+// expert block of its first tile by bisection over the groups' prefix (nbase, from the
+// preparation), then steps block by block.  One routed token: one group per expert, from
+// the CTA's own table.
+struct TileCursor {
+  int a = -1, gb = 0, n = 1, t_lo = 0, t_hi = 0;
+  __device__ __forceinline__ TileInfo get(int tile, const FArgs& f, const int4* own) {
+    TileInfo t;
+    int ntg;
+    if (f.route_one) {
+      ntg = tile / f.RT;
+      t.rt = tile - ntg * f.RT;
+      n = 1;
+    } else {
+      if (a < 0) {  // bisection: the last active expert whose first tile is <= tile
+        int lo = 0, hi = f.meta[0] - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (__ldg(f.nbase + mid) * f.RT <= tile) lo = mid; else hi = mid - 1;
+        }
+        a = lo - 1;
+      }
+      while (a < 0 || tile >= t_hi) {
+        ++a;
+        gb = __ldg(f.nbase + a);
+        n = __ldg(f.nbase + a + 1) - gb;
+        t_lo = gb * f.RT;
+        t_hi = t_lo + n * f.RT;
+      }
+      const int local = tile - t_lo;
+      t.rt = local / n;
+      ntg = gb + (local - t.rt * n);
+    }
+    const int4 g = f.route_one ? own[ntg] : __ldg(f.tiles + ntg);
+    t.expert = g.x;
+    t.pos0 = g.y;
+    t.ntok = g.z;
+    t.N = ((t.ntok * kTerms + 15) / 16) * 16;
+    t.shared_rows = n > 1;
+    return t;
+  }
+};
 
 __device__ __forceinline__ void st_release(int32_t* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -236,6 +270,24 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 // phase 1: [0] w2 [1] w2 scales [2] w2 [3] w2 scales [4] act terms [5] their scales.
 // Per phase: [0..1] first weight matrix and its scales, [2..3] the second (phase 0: w3;
 // phase 1: w2 again), [4..5] activation terms and scales.
+// N consecutive 32-bit TMEM columns of this warp's lane quarter into registers (N = 4 or 16),
+// waiting for the load.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(N == 4 || N == 16, "column count");
+  if constexpr (N == 4) {
+    asm volatile(
+        "{\n\ttcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t}"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+        : "r"(taddr)
+        : "memory");
+  } else {
+    tc::tmem_ld_x16(taddr, r);
+    tc::tmem_ld_wait();
+  }
+}
+
 struct Maps {
   CUtensorMap m[6];
 };
@@ -263,6 +315,7 @@ template <int NMAX, int PH, int KS>
 __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ Maps mp,
                                                         const FArgs f) {
   constexpr int NM = PH == 0 ? 2 : 1;  // weight matrices per unit: w1 and w3, or w2
+  constexpr int TB = NMAX / 16;        // tokens per epilogue step
   using Y = Lay<NMAX, NM, KS>;
   constexpr int kStages = Y::kStages;
   constexpr uint32_t kStageBytes = Y::kStageBytes, kBKatom = Y::kBKatom;
@@ -346,12 +399,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
     if (lane == 0) {
       const bool wts = warp == kProdWarp;
       if (!wts && PH == 1) pdl_wait();  // the activation terms are phase 0's output
-      const uint64_t once = tc::make_policy_evict_first();  // weights: read once per call
+      // weights read once per call go evict-first; rows that several token groups read
+      // (consecutive tiles) stay at normal priority for the reuse
+      const uint64_t once = tc::make_policy_evict_first(), reused = tc::make_policy_evict_normal();
       int it = 0;
       bool stop = false;
+      TileCursor cur;
       for (int ti_ = 0; ti_ < ntiles && !stop; ++ti_) {
         const int tile = rg.t_first + ti_;
-        const TileInfo ti = tile_info(tile, f, own_tiles);
+        const TileInfo ti = cur.get(tile, f, own_tiles);
         const int kb = ti_ == 0 ? rg.u0 - tile * f.KC : 0;
         const int ke = ti_ == ntiles - 1 ? rg.u1 - tile * f.KC : f.KC;
         const int nbox = ti.N / 16;
@@ -366,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
           }
           uint8_t* st = sm + (size_t)s * kStageBytes;
           if (wts) {
+            const uint64_t pol = ti.shared_rows ? reused : once;
             mbar_arrive_expect_tx(&fullA[s], NM * KS * (kABytes + kSABytes));
 #pragma unroll
             for (int m = 0; m < NM; ++m) {
@@ -373,10 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
               for (int ks = 0; ks < KS; ++ks) {
                 const int sb = m * KS + ks, x = (kc * KS + ks) * 256;
                 uint8_t* sa = st + sb * kABytes;
-                tc::tma_load_2d_hint(sa, &mp.m[2 * m], x, arow, &fullA[s], once);
-                tc::tma_load_2d_hint(sa + 16384, &mp.m[2 * m], x + 128, arow, &fullA[s], once);
+                tc::tma_load_2d_hint(sa, &mp.m[2 * m], x, arow, &fullA[s], pol);
+                tc::tma_load_2d_hint(sa + 16384, &mp.m[2 * m], x + 128, arow, &fullA[s], pol);
                 tc::tma_load_2d_hint(st + kOffSA + sb * kSABytes, &mp.m[2 * m + 1],
-                                     (kc * KS + ks) * 16, arow, &fullA[s], once);
+                                     (kc * KS + ks) * 16, arow, &fullA[s], pol);
               }
             }
           } else {
@@ -441,9 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     int it = 0;
     bool stop = false;
+    TileCursor cur;
     for (int ti_ = 0; ti_ < ntiles && !stop; ++ti_) {
       const int tile = rg.t_first + ti_;
-      const int N = tile_info(tile, f, own_tiles).N;
+      const int N = cur.get(tile, f, own_tiles).N;
       const int kb = ti_ == 0 ? rg.u0 - tile * f.KC : 0;
       const int ke = ti_ == ntiles - 1 ? rg.u1 - tile * f.KC : f.KC;
       for (int kc = kb; kc < ke && !stop; ++kc, ++it) {
@@ -497,6 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
     if (lane == 0) {
       int it = 0;
       bool stop = false;
+      TileCursor cur;
       for (int ti_ = 0; ti_ < ntiles && !stop; ++ti_) {
         const int tile = rg.t_first + ti_;
         const int kb = ti_ == 0 ? rg.u0 - tile * f.KC : 0;
@@ -507,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
           stop = true;
           break;
         }
-        const uint32_t idesc = tc::idesc_mxf4(kRowsTile, tile_info(tile, f, own_tiles).N, 0, 0);
+        const uint32_t idesc = tc::idesc_mxf4(kRowsTile, cur.get(tile, f, own_tiles).N, 0, 0);
         for (int kc = kb; kc < ke && !stop; ++kc, ++it) {
           const int s = it % kStages;
           const uint32_t par = (it / kStages) & 1;
@@ -555,9 +614,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
     const int q = warp;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     const int row = 32 * q + lane;  // row within the tile
+    TileCursor cur;
     for (int ti_ = 0; ti_ < ntiles; ++ti_) {
       const int tile = rg.t_first + ti_;
-      const TileInfo ti = tile_info(tile, f, own_tiles);
+      const TileInfo ti = cur.get(tile, f, own_tiles);
       const int b = ti_ & 1;
       const bool write_part = ti_ == 0 && rg.tail_first;          // leave a part for the head
       const bool add_parts = ti_ == ntiles - 1 && rg.head_last;    // add the later CTAs' parts
@@ -592,59 +652,79 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
       const int grp = (ti.rt * kRowsTile + 32 * q) >> 5;            // phase 0: act group
       const bool in_range = ti.rt * kRowsTile + 32 * q < f.R;
       float* mine = parts + (size_t)cta * pf;
+      // TB tokens at a time (4 with 64-row activation tiles, 1 otherwise): one TMEM load of
+      // their 4 TB columns per matrix, then their epilogues side by side
 #pragma unroll 1
-      for (int j = 0; j < ti.ntok; ++j) {
-        float v[2] = {0.f, 0.f};
+      for (int j0 = 0; j0 < ti.ntok; j0 += TB) {
+        float v[TB][2];
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          if (m >= NM) break;
-          uint32_t r[4];
-          asm volatile(
-              "{\n\ttcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];\n\t"
-              "tcgen05.wait::ld.sync.aligned;\n\t}"
-              : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-              : "r"(tacc + kMatCols * m + (uint32_t)(j * kTerms))
-              : "memory");
-          v[m] = ((__uint_as_float(r[0]) + __uint_as_float(r[1])) + __uint_as_float(r[2])) +
-                 __uint_as_float(r[3]);
+        for (int m = 0; m < NM; ++m) {
+          uint32_t r[4 * TB];
+          tmem_ld_cols<4 * TB>(tacc + kMatCols * m + (uint32_t)(j0 * kTerms), r);
+#pragma unroll
+          for (int jj = 0; jj < TB; ++jj)
+            v[jj][m] = ((__uint_as_float(r[4 * jj]) + __uint_as_float(r[4 * jj + 1])) +
+                        __uint_as_float(r[4 * jj + 2])) +
+                       __uint_as_float(r[4 * jj + 3]);
         }
+        const int nj = min(TB, ti.ntok - j0);
         if (write_part) {
-          for (int m = 0; m < NM; ++m) mine[((size_t)m * f.npart + j) * kRowsTile + row] = v[m];
+#pragma unroll
+          for (int jj = 0; jj < TB; ++jj)
+            if (jj < nj)
+              for (int m = 0; m < NM; ++m)
+                mine[((size_t)m * f.npart + j0 + jj) * kRowsTile + row] = v[jj][m];
           continue;
         }
         if (add_parts) {
-          for (int m = 0; m < NM; ++m) {
-            const size_t off = ((size_t)m * f.npart + j) * kRowsTile + row;
-            int slot = 0;
-            for (int c = fix_c0; c <= fix_c1; ++c) {
-              if (idle(c)) continue;
-              v[m] += fix_smem ? fix[(size_t)slot * pf + off] : __ldcg(parts + (size_t)c * pf + off);
-              ++slot;
+#pragma unroll
+          for (int jj = 0; jj < TB; ++jj) {
+            if (jj >= nj) break;
+            for (int m = 0; m < NM; ++m) {
+              const size_t off = ((size_t)m * f.npart + j0 + jj) * kRowsTile + row;
+              int slot = 0;
+              for (int c = fix_c0; c <= fix_c1; ++c) {
+                if (idle(c)) continue;
+                v[jj][m] += fix_smem ? fix[(size_t)slot * pf + off]
+                                     : __ldcg(parts + (size_t)c * pf + off);
+                ++slot;
+              }
             }
           }
         }
         if (PH == 0) {
-          // SwiGLU (or SiTU-GLU), then the token's kTerms MXFP4 terms for phase 1; this warp's
-          // 32 rows are one group of 32 along phase 1's reduction
-          const float act = activation(v[0], v[1], f.act_kind, f.b1, f.b2);
-          uint32_t words[kTerms], sfb[kTerms];
-          mx_split_group(act, words, sfb);
-          if (in_range) {
-            const size_t p = (size_t)(ti.pos0 + j);
+          // SwiGLU (or SiTU-GLU), then each token's kTerms MXFP4 terms for phase 1; this
+          // warp's 32 rows are one group of 32 along phase 1's reduction
+          float act[TB];
 #pragma unroll
-            for (int t = 0; t < kTerms; ++t) {
-              const size_t r2 = p * kTerms + t;
-              if ((lane & 7) == 0)
-                *reinterpret_cast<uint32_t*>(f.act_q + r2 * (size_t)(f.I >> 1) + grp * 16 +
-                                             4 * (lane >> 3)) = words[t];
-              if (lane == 0) f.act_sf[r2 * (size_t)(f.I >> 5) + grp] = (uint8_t)sfb[t];
+          for (int jj = 0; jj < TB; ++jj)
+            act[jj] = activation(v[jj][0], v[jj][NM - 1], f.act_kind, f.b1, f.b2);
+          uint32_t words[TB][kTerms], sfb[TB][kTerms];
+          mx_split_groups<TB>(act, words, sfb);
+          if (in_range) {
+#pragma unroll
+            for (int jj = 0; jj < TB; ++jj) {
+              if (jj >= nj) break;
+              const size_t p = (size_t)(ti.pos0 + j0 + jj);
+#pragma unroll
+              for (int t = 0; t < kTerms; ++t) {
+                const size_t r2 = p * kTerms + t;
+                if ((lane & 7) == 0)
+                  *reinterpret_cast<uint32_t*>(f.act_q + r2 * (size_t)(f.I >> 1) + grp * 16 +
+                                               4 * (lane >> 3)) = words[jj][t];
+                if (lane == 0) f.act_sf[r2 * (size_t)(f.I >> 5) + grp] = (uint8_t)sfb[jj][t];
+              }
             }
           }
         } else {
-          const int asg = f.route_one ? own_perm[ti.pos0 + j] : f.perm[ti.pos0 + j];
-          const float gj = f.route_one ? own_gate[asg] : f.gate[asg];
           const int r_exp = ti.rt * kRowsTile + row;  // row within the expert
-          if (r_exp < f.R) f.ybuf[(size_t)asg * f.L + r_exp] = gj * v[0];
+#pragma unroll
+          for (int jj = 0; jj < TB; ++jj) {
+            if (jj >= nj) break;
+            const int asg = f.route_one ? own_perm[ti.pos0 + j0 + jj] : f.perm[ti.pos0 + j0 + jj];
+            const float gj = f.route_one ? own_gate[asg] : f.gate[asg];
+            if (r_exp < f.R) f.ybuf[(size_t)asg * f.L + r_exp] = gj * v[jj][0];
+          }
         }
       }
       tc::fence_before_sync();
@@ -670,29 +750,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
 
 // x (bf16, one row per token) -> kTerms MXFP4 terms per (token, expert) position, in the
 // bucket order: rows p * kTerms + t of xq [P*kTerms][L/2] and xsf [P*kTerms][L/32].  Grid
-// (T*k positions, L/512): one CTA per position and 512-wide slice, warp w quantises group
-// 16 * blockIdx.y + w of the position's token; positions past the valid count leave.
+// (T, L/512): one CTA per token and 512-wide slice; warp w splits group 16 * blockIdx.y + w
+// of the token once and writes the terms to each of the token's valid positions (inv of
+// its slots; slots whose expert index is out of range have none).
 __global__ void __launch_bounds__(512) k_split_x(const uint16_t* __restrict__ x, int L, int k,
-                                                 const int32_t* __restrict__ perm,
-                                                 const int32_t* __restrict__ meta,
+                                                 int E, const int32_t* __restrict__ idx,
+                                                 const int32_t* __restrict__ inv,
                                                  uint8_t* __restrict__ xq,
                                                  uint8_t* __restrict__ xsf) {
   pdl_wait();
   pdl_launch();
-  const int pos = blockIdx.x;
-  if (pos >= meta[1]) return;
-  const int t = perm[pos] / k;
+  const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = blockIdx.y * 16 + warp;
   const float v = __uint_as_float((uint32_t)x[(size_t)t * L + 32 * grp + lane] << 16);
   uint32_t words[kTerms], sf[kTerms];
   mx_split_group(v, words, sf);
+  for (int j = 0; j < k; ++j) {
+    const int a = t * k + j;
+    const int e = idx[a];
+    if (e < 0 || e >= E) continue;
+    const int pos = inv[a];
 #pragma unroll
-  for (int tt = 0; tt < kTerms; ++tt) {
-    const size_t r = (size_t)pos * kTerms + tt;
-    if ((lane & 7) == 0)
-      *reinterpret_cast<uint32_t*>(xq + r * (size_t)(L >> 1) + grp * 16 + 4 * (lane >> 3)) = words[tt];
-    if (lane == 0) xsf[r * (size_t)(L >> 5) + grp] = (uint8_t)sf[tt];
+    for (int tt = 0; tt < kTerms; ++tt) {
+      const size_t r = (size_t)pos * kTerms + tt;
+      if ((lane & 7) == 0)
+        *reinterpret_cast<uint32_t*>(xq + r * (size_t)(L >> 1) + grp * 16 + 4 * (lane >> 3)) = words[tt];
+      if (lane == 0) xsf[r * (size_t)(L >> 5) + grp] = (uint8_t)sf[tt];
+    }
   }
 }
 
@@ -737,11 +822,11 @@ int tc_npart(int T) { return T < kTokTile ? T : kTokTile; }  // tokens per tile,
 
 size_t tc_part_floats(int T) { return (size_t)kTcMaxGrid * 3 * tc_npart(T) * kRowsTile; }
 
-cudaError_t launch_split_x(const uint16_t* x, int T, int L, int k, const BucketOut& b,
-                           uint8_t* xq, uint8_t* xsf, cudaStream_t s, bool pdl) {
-  return launch_kernel(k_split_x, dim3(T * k, L / kKStage), dim3(512), 0, s, pdl, x, L, k,
-                       static_cast<const int32_t*>(b.perm), static_cast<const int32_t*>(b.meta),
-                       xq, xsf);
+cudaError_t launch_split_x(const uint16_t* x, int T, int L, int k, int E, const int32_t* idx,
+                           const BucketOut& b, uint8_t* xq, uint8_t* xsf, cudaStream_t s,
+                           bool pdl) {
+  return launch_kernel(k_split_x, dim3(T, L / kKStage), dim3(512), 0, s, pdl, x, L, k, E, idx,
+                       static_cast<const int32_t*>(b.inv), xq, xsf);
 }
 
 cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k,
@@ -773,7 +858,7 @@ cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, i
     return cudaErrorInvalidValue;
   FArgs f{};
   f.k = k; f.L = L; f.I = I; f.act_kind = act_kind; f.b1 = b1; f.b2 = b2;
-  f.meta = b.meta; f.perm = b.perm; f.tiles = b.tiles;
+  f.meta = b.meta; f.perm = b.perm; f.tiles = b.tiles; f.nbase = b.ntile_base;
   f.act_q = act_q; f.act_sf = act_sf; f.gate = gate; f.ybuf = ybuf;
   f.part = part; f.npart = tc_npart(T);
   f.status = status;

@@ -73,4 +73,41 @@ __device__ __forceinline__ void mx_split_group(float v, uint32_t (&words)[kTerms
   }
 }
 
+// The same for TB independent groups at once (one value each per lane): the terms of all
+// groups advance together, so their shuffle chains interleave.
+template <int TB>
+__device__ __forceinline__ void mx_split_groups(const float (&v)[TB], uint32_t (&words)[TB][kTerms],
+                                                uint32_t (&sf)[TB][kTerms]) {
+  const int lane = threadIdx.x & 31;
+  float r[TB];
+#pragma unroll
+  for (int b = 0; b < TB; ++b) r[b] = v[b];
+#pragma unroll
+  for (int t = 0; t < kTerms; ++t) {
+    float amax[TB];
+#pragma unroll
+    for (int b = 0; b < TB; ++b) amax[b] = fabsf(r[b]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int b = 0; b < TB; ++b) amax[b] = fmaxf(amax[b], __shfl_xor_sync(0xffffffffu, amax[b], o));
+    uint32_t w[TB];
+#pragma unroll
+    for (int b = 0; b < TB; ++b) {
+      const int e = mx_scale_exp(amax[b]);
+      float q;
+      const uint32_t code = e2m1_rne(r[b] * pow2f(-e), &q);
+      r[b] -= q * pow2f(e);
+      w[b] = code << (4 * (lane & 7));
+      sf[b][t] = (uint32_t)(e + 127);
+    }
+#pragma unroll
+    for (int o = 1; o <= 4; o <<= 1)
+#pragma unroll
+      for (int b = 0; b < TB; ++b) w[b] |= __shfl_xor_sync(0xffffffffu, w[b], o);
+#pragma unroll
+    for (int b = 0; b < TB; ++b) words[b][t] = w[b];
+  }
+}
+
 }  // namespace k3
