@@ -168,7 +168,8 @@ void phase3(cudaStream_t s) { phase(3, s); }
 int run_route(const k3moe_cfg* c, const void* h, const void* wr, const float* bias, int32_t T,
               int32_t* idx, float* gate, float* gap, const Workspace& w, cudaStream_t s) {
   K3_TRY(launch_router_logits(static_cast<const uint16_t*>(h), static_cast<const uint16_t*>(wr),
-                              T, c->n_experts, c->hidden, w.logits, s, false));
+                              T, c->n_experts, c->hidden, w.logits, s, false, nullptr, 0,
+                              nullptr, nullptr, nullptr, 0, nullptr));
   K3_TRY(launch_topk(w.logits, bias, T, c->n_experts, c->topk, c->renorm, c->routed_scale, idx,
                      gate, gap, s, true));
   return K3MOE_OK;
@@ -196,7 +197,7 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
                                 T, E, c->hidden, w.logits, s, true,
                                 static_cast<const uint16_t*>(x), L, one ? w.xq : nullptr,
                                 one ? w.xsf : nullptr, one ? w.b.flags : nullptr,
-                                one ? kTcFlags : 0));
+                                one ? kTcFlags : 0, status));
     if (!fused_topk)
       K3_TRY(launch_topk(w.logits, bias, T, E, K, c->renorm, c->routed_scale, idx, gate, gap, s,
                          true));

@@ -42,7 +42,11 @@ cudaError_t launch_router_logits(const uint16_t* h, const uint16_t* wr, int T, i
                                  float* logits, cudaStream_t s, bool pdl,
                                  const uint16_t* x = nullptr, int L = 0, uint8_t* xq = nullptr,
                                  uint8_t* xsf = nullptr, int32_t* zero = nullptr,
-                                 int nzero = 0);
+                                 int nzero = 0, int32_t* status = nullptr);
+// From this many tokens the router logits run as a tensor-core GEMM (router.cu), when the
+// hidden width allows (router_tc_supported).
+constexpr int kRouterTcMinTokens = 64;
+inline bool router_tc_supported(int H) { return H >= 64 && H % 8 == 0; }
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,
                         float routed_scale, int32_t* idx, float* gate, float* gap,
                         cudaStream_t s, bool pdl);

@@ -139,10 +139,11 @@ struct TileInfo {
 // the CTA's own table.
 struct TileCursor {
   int a = -1, gb = 0, n = 1, t_lo = 0, t_hi = 0;
+  template <bool ONE>
   __device__ __forceinline__ TileInfo get(int tile, const FArgs& f, const int4* own) {
     TileInfo t;
     int ntg;
-    if (f.route_one) {
+    if constexpr (ONE) {
       ntg = tile / f.RT;
       t.rt = tile - ntg * f.RT;
       n = 1;
@@ -166,7 +167,7 @@ struct TileCursor {
       t.rt = local / n;
       ntg = gb + (local - t.rt * n);
     }
-    const int4 g = f.route_one ? own[ntg] : __ldg(f.tiles + ntg);
+    const int4 g = ONE ? own[ntg] : __ldg(f.tiles + ntg);
     t.expert = g.x;
     t.pos0 = g.y;
     t.ntok = g.z;
@@ -311,7 +312,7 @@ __device__ __forceinline__ Range make_range(const Split& sp, int KC, int c) {
   return r;
 }
 
-template <int NMAX, int PH, int KS>
+template <int NMAX, int PH, int KS, bool ONE>
 __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ Maps mp,
                                                         const FArgs f) {
   constexpr int NM = PH == 0 ? 2 : 1;  // weight matrices per unit: w1 and w3, or w2
@@ -371,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
   pdl_launch();
   const uint32_t t0 = tbase;
   volatile int* abort_v = &abort_flag;
-  const int ngroups = f.route_one ? route_one_token<PH>(f, sm, own_tiles, own_perm, own_gate,
+  const int ngroups = ONE ? route_one_token<PH>(f, sm, own_tiles, own_perm, own_gate,
                                                         PH == 0 && cta == 0)
                                   : f.meta[2];
 
@@ -407,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
       TileCursor cur;
       for (int ti_ = 0; ti_ < ntiles && !stop; ++ti_) {
         const int tile = rg.t_first + ti_;
-        const TileInfo ti = cur.get(tile, f, own_tiles);
+        const TileInfo ti = cur.get<ONE>(tile, f, own_tiles);
         const int kb = ti_ == 0 ? rg.u0 - tile * f.KC : 0;
         const int ke = ti_ == ntiles - 1 ? rg.u1 - tile * f.KC : f.KC;
         const int nbox = ti.N / 16;
@@ -501,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
     TileCursor cur;
     for (int ti_ = 0; ti_ < ntiles && !stop; ++ti_) {
       const int tile = rg.t_first + ti_;
-      const int N = cur.get(tile, f, own_tiles).N;
+      const int N = cur.get<ONE>(tile, f, own_tiles).N;
       const int kb = ti_ == 0 ? rg.u0 - tile * f.KC : 0;
       const int ke = ti_ == ntiles - 1 ? rg.u1 - tile * f.KC : f.KC;
       for (int kc = kb; kc < ke && !stop; ++kc, ++it) {
@@ -566,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
           stop = true;
           break;
         }
-        const uint32_t idesc = tc::idesc_mxf4(kRowsTile, cur.get(tile, f, own_tiles).N, 0, 0);
+        const uint32_t idesc = tc::idesc_mxf4(kRowsTile, cur.get<ONE>(tile, f, own_tiles).N, 0, 0);
         for (int kc = kb; kc < ke && !stop; ++kc, ++it) {
           const int s = it % kStages;
           const uint32_t par = (it / kStages) & 1;
@@ -617,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
     TileCursor cur;
     for (int ti_ = 0; ti_ < ntiles; ++ti_) {
       const int tile = rg.t_first + ti_;
-      const TileInfo ti = cur.get(tile, f, own_tiles);
+      const TileInfo ti = cur.get<ONE>(tile, f, own_tiles);
       const int b = ti_ & 1;
       const bool write_part = ti_ == 0 && rg.tail_first;          // leave a part for the head
       const bool add_parts = ti_ == ntiles - 1 && rg.head_last;    // add the later CTAs' parts
@@ -721,8 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
 #pragma unroll
           for (int jj = 0; jj < TB; ++jj) {
             if (jj >= nj) break;
-            const int asg = f.route_one ? own_perm[ti.pos0 + j0 + jj] : f.perm[ti.pos0 + j0 + jj];
-            const float gj = f.route_one ? own_gate[asg] : f.gate[asg];
+            const int asg = ONE ? own_perm[ti.pos0 + j0 + jj] : f.perm[ti.pos0 + j0 + jj];
+            const float gj = ONE ? own_gate[asg] : f.gate[asg];
             if (r_exp < f.R) f.ybuf[(size_t)asg * f.L + r_exp] = gj * v[jj][0];
           }
         }
@@ -781,35 +782,37 @@ __global__ void __launch_bounds__(512) k_split_x(const uint16_t* __restrict__ x,
   }
 }
 
-template <int NMAX, int PH, int KS>
+template <int NMAX, int PH, int KS, bool ONE>
 cudaError_t launch_tc_n(const Maps& mp, FArgs f, cudaStream_t s, bool pdl) {
   static int configured[64] = {0};
   constexpr size_t smem = Lay<NMAX, PH == 0 ? 2 : 1, KS>::kSmemBytes;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_moe_tc<NMAX, PH, KS>,
+    cudaError_t e = cudaFuncSetAttribute(k_moe_tc<NMAX, PH, KS, ONE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
   f.KC /= KS;  // units of KS chunks per tile
-  return launch_kernel(k_moe_tc<NMAX, PH, KS>, dim3(tc_grid_size()), dim3(kThreads), smem, s,
-                       pdl, mp, f);
+  return launch_kernel(k_moe_tc<NMAX, PH, KS, ONE>, dim3(tc_grid_size()), dim3(kThreads), smem,
+                       s, pdl, mp, f);
 }
 
-// Each phase is its own kernel (a launch holds only its phase's code); the second GEMM
-// takes two 512-chunks per unit when its reduction (f.KC chunks) divides evenly.
-template <int NMAX>
+// Each phase is its own kernel (a launch holds only its phase's code, and a single routed
+// token's kernels hold only its in-kernel routing); the second GEMM takes two 512-chunks per
+// unit when its reduction (f.KC chunks) divides evenly.
+template <int NMAX, bool ONE>
 cudaError_t launch_tc_phase(const Maps& mp, const FArgs& f, cudaStream_t s, bool pdl) {
-  if (f.ph == 0) return launch_tc_n<NMAX, 0, 1>(mp, f, s, pdl);
-  if (f.KC % 2 == 0) return launch_tc_n<NMAX, 1, 2>(mp, f, s, pdl);
-  return launch_tc_n<NMAX, 1, 1>(mp, f, s, pdl);
+  if (f.ph == 0) return launch_tc_n<NMAX, 0, 1, ONE>(mp, f, s, pdl);
+  if (f.KC % 2 == 0) return launch_tc_n<NMAX, 1, 2, ONE>(mp, f, s, pdl);
+  return launch_tc_n<NMAX, 1, 1, ONE>(mp, f, s, pdl);
 }
 // Batches of up to 4 tokens have at most 4 tokens per expert: 16-row activation tiles.
 cudaError_t launch_tc(const Maps& mp, const FArgs& f, int T, cudaStream_t s, bool pdl) {
-  if (T * kTerms <= 16) return launch_tc_phase<16>(mp, f, s, pdl);
-  return launch_tc_phase<64>(mp, f, s, pdl);
+  if (f.route_one) return launch_tc_phase<16, true>(mp, f, s, pdl);  // one token
+  if (T * kTerms <= 16) return launch_tc_phase<16, false>(mp, f, s, pdl);
+  return launch_tc_phase<64, false>(mp, f, s, pdl);
 }
 
 }  // namespace

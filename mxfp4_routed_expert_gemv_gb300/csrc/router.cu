@@ -6,6 +6,8 @@
 // from the unbiased scores, renormalised over the chosen k and multiplied by routed_scale.
 #include "launch.h"
 #include "mxq.cuh"
+#include "tc.cuh"
+#include "tmap.h"
 #include "topk.cuh"
 
 namespace k3 {
@@ -100,6 +102,114 @@ __global__ void __launch_bounds__(256) k_router_logits(const uint16_t* __restric
   }
 }
 
+// Batches (T >= 64): the router as a tensor-core GEMM, logits[t][e] = sum_i h[t][i] Wr[e][i].
+// One CTA per 128 experts x 128 tokens: TMA brings 64-wide K slices of Wr and h (bf16, 128-byte
+// swizzle) into a 4-stage ring, one thread issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32 in
+// TMEM, K = 16 each), and all four warps read the accumulator back (lane = expert row,
+// column = token).  Products of bf16 values are exact; the sums are fp32.  A K tail past H
+// reads zeros.  Every wait is bounded: one that runs out counts a timeout and the CTA skips
+// its output.
+constexpr int kRtStages = 4;
+constexpr uint32_t kRtTile = 128 * 128;  // one 128-row x 128-byte operand slice
+
+__global__ void __launch_bounds__(128, 1) k_router_tc(const __grid_constant__ CUtensorMap mw,
+                                                      const __grid_constant__ CUtensorMap mh,
+                                                      int T, int E, int H,
+                                                      float* __restrict__ logits,
+                                                      int32_t* __restrict__ status) {
+  extern __shared__ uint8_t dsm[];
+  __shared__ __align__(8) uint64_t full[kRtStages], empty[kRtStages], done;
+  __shared__ uint32_t tbase;
+  __shared__ int bad;
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) &
+                                           ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e0 = blockIdx.x * 128, t0 = blockIdx.y * 128;
+  const int nk = (H + 63) / 64;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRtStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&done, 1);
+    fence_mbar_init();
+    bad = 0;
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&tbase, 128);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  pdl_wait();
+  pdl_launch();
+  const uint32_t tacc = tbase;
+  if (warp == 0 && lane == 0) {
+    int i = 0;
+    for (; i < nk; ++i) {
+      const int s = i % kRtStages;
+      if (i >= kRtStages && !mbar_wait(&empty[s], ((i / kRtStages) - 1) & 1, status)) {
+        bad = 1;
+        break;
+      }
+      uint8_t* st = sm + (size_t)s * 2 * kRtTile;
+      mbar_arrive_expect_tx(&full[s], 2 * kRtTile);
+      tc::tma_load_2d(st, &mw, i * 128, e0, &full[s]);
+      tc::tma_load_2d(st + kRtTile, &mh, i * 128, t0, &full[s]);
+    }
+    if (bad)  // copies in flight land before the CTA leaves
+      for (int d = 1; d <= kRtStages && d <= i; ++d)
+        mbar_wait(&full[(i - d) % kRtStages], ((i - d) / kRtStages) & 1, nullptr);
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t idesc = tc::idesc_bf16(128, 128);
+    int i = 0;
+    for (; i < nk; ++i) {
+      const int s = i % kRtStages;
+      if (!mbar_wait(&full[s], (i / kRtStages) & 1, status)) {
+        bad = 1;
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t st = tc::smem_addr(sm + (size_t)s * 2 * kRtTile);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint64_t ad = tc::smem_desc(st + 32 * j, 16, 1024, tc::kLayout128B);
+        const uint64_t bd = tc::smem_desc(st + kRtTile + 32 * j, 16, 1024, tc::kLayout128B);
+        tc::mma_bf16(tacc, ad, bd, idesc, (i == 0 && j == 0) ? 0u : 1u);
+      }
+      tc::mma_commit(&empty[s]);
+    }
+    tc::mma_commit(&done);
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(&done, 0, threadIdx.x == 0 ? status : nullptr);
+  tc::fence_after_sync();
+  if (__syncthreads_or(!ok || bad) == 0) {
+    const int e = e0 + 32 * warp + lane;
+    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+#pragma unroll 1
+    for (int c0 = 0; c0 < 128; c0 += 16) {
+      uint32_t r[16];
+      tc::tmem_ld_x16(tacc + lane_off + c0, r);
+      tc::tmem_ld_wait();
+      if (e < E) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int t = t0 + c0 + c;
+          if (t < T) logits[(size_t)t * E + e] = __uint_as_float(r[c]);
+        }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tacc, 128);
+  }
+}
+
 __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits,
                                               const float* __restrict__ bias, int T, int E,
                                               int k, int renorm, float routed_scale,
@@ -118,7 +228,26 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits,
 
 cudaError_t launch_router_logits(const uint16_t* h, const uint16_t* wr, int T, int E, int H,
                                  float* logits, cudaStream_t s, bool pdl, const uint16_t* x,
-                                 int L, uint8_t* xq, uint8_t* xsf, int32_t* zero, int nzero) {
+                                 int L, uint8_t* xq, uint8_t* xsf, int32_t* zero, int nzero,
+                                 int32_t* status) {
+  if (T >= kRouterTcMinTokens && !xq && !zero && router_tc_supported(H)) {
+    CUtensorMap mw, mh;
+    if (!make_map_2d(&mw, wr, (uint64_t)H * 2, E, 128, 128, true) ||
+        !make_map_2d(&mh, h, (uint64_t)H * 2, T, 128, 128, true))
+      return cudaErrorInvalidValue;
+    static int configured[64] = {0};
+    constexpr size_t smem = (size_t)kRtStages * 2 * kRtTile + 1024;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+      const cudaError_t e = cudaFuncSetAttribute(
+          k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) configured[dev] = 1;
+    }
+    return launch_kernel(k_router_tc, dim3((E + 127) / 128, (T + 127) / 128), dim3(128), smem, s,
+                         pdl, mw, mh, T, E, H, logits, status);
+  }
   const unsigned gx = (E + kRowsPerCta - 1) / kRowsPerCta;
   if (xq && (T != 1 || (int)gx * 8 < (L >> 5))) return cudaErrorInvalidValue;
   if (T <= 2)

@@ -47,6 +47,13 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, int a_sf_id, int
          ((uint32_t)(a_sf_id & 3) << 29);
 }
 
+// kind::f16 with bf16 A and B, fp32 D, both operands K-major, dense, K = 16: bits 4-5 D
+// format (1 = F32), 7-9 / 10-12 A / B format (1 = BF16), 17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
 // ---- TMEM allocation (one full warp executes each)
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -110,6 +117,15 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64
       "[%5], p;\n\t}"
       :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
          "r"(accumulate)
+      : "memory");
+}
+// D[M x N] (+)= A B^T over K = 16, bf16 operands from shared memory, fp32 D in TMEM.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // arrive once on an mbarrier when every MMA this thread issued before has completed

@@ -9,7 +9,9 @@ Rules (the workloads' statement, with the readings listed in the design notes):
     checked against the oracle's expert sum for the GPU's choice, with gates the oracle
     computes for that choice from its own scores.
   * gates: |gate_gpu - gate_ref| <= GATE_RTOL * |gate_ref| (fp32 sigmoid of an fp32 sum
-    against fp64).
+    against fp64; from 64 tokens the router's sums run on the tensor cores, whose fp32
+    accumulation of the bf16 products rounds differently from a sequential fp32 sum, hence
+    1e-4 rather than the 1e-5 a CUDA-core dot reaches).
   * y: ||dy||_2 / ||y_ref||_2 <= REL_L2 and max|dy| / max|y_ref| <= MAX_REL.
 """
 from __future__ import annotations
@@ -23,7 +25,7 @@ import oracle
 import synth
 
 GAP_TIE = 1e-4
-GATE_RTOL = 1e-5
+GATE_RTOL = 1e-4
 REL_L2 = 2e-3
 MAX_REL = 1e-2
 
