@@ -59,7 +59,7 @@ constexpr int kEpiBar = 1;  // named barrier of the four epilogue warps
 //   TMEM:  accumulator buffer b at b * kAccCols, matrix m at + m * kMatCols; the scale ring
 //          from kSfBase, stage s at + kSfStageCols s: A scales of sb, MMA j at + 32 sb + 4 j
 //          (+ lane quarter), B scales of ks at + 32 (NM KS + ks) + 4 j (+ 1 for B rows 32..63);
-//   fix:   the parts a head tile adds, after the ring (kFixBytes).
+//   fix:   the parts a head tile adds, after the ring (kFixBytes), then the act buffer.
 template <int NMAX, int NM, int KS>
 struct Lay {
   static constexpr uint32_t kBKatom = NMAX * 128;
@@ -71,7 +71,11 @@ struct Lay {
   static constexpr int kStages =
       NM * KS == 2 ? (NMAX <= 16 && NM == 2 ? 3 : 2) : (NMAX <= 16 ? 5 : 4);
   static constexpr uint32_t kFixBytes = NMAX <= 16 && NM == 2 ? 4096 : 16384;
-  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kFixBytes + 1024;
+  // first GEMM with 64-row activation tiles: act of a tile's tokens, [warp][token][33]
+  // floats, so that one lane can split one token's group of 32 rows (see the epilogue)
+  static constexpr uint32_t kActBufBytes = NMAX == 64 && NM == 2 ? 4 * kTokTile * 33 * 4 : 0;
+  static constexpr size_t kSmemBytes =
+      (size_t)kStages * kStageBytes + kFixBytes + kActBufBytes + 1024;
   static constexpr uint32_t kMatCols = NMAX <= 16 ? 32 : 64;
   static constexpr uint32_t kAccCols = 2 * kMatCols;
   static constexpr uint32_t kSfBase = 2 * kAccCols;
@@ -335,6 +339,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) &
                                            ~uintptr_t(1023));
   float* fix = reinterpret_cast<float*>(sm + (size_t)kStages * kStageBytes);
+  float* actbuf = reinterpret_cast<float*>(sm + (size_t)kStages * kStageBytes + kFixBytes);
+  // many tokens per tile: each lane splits one token's group (no cross-lane work); one token
+  // per tile: the warp splits the group together
+  constexpr bool kLaneSplit = Y::kActBufBytes > 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;
 
@@ -700,6 +708,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
 #pragma unroll
           for (int jj = 0; jj < TB; ++jj)
             act[jj] = activation(v[jj][0], v[jj][NM - 1], f.act_kind, f.b1, f.b2);
+          if constexpr (kLaneSplit) {
+            float* sb = actbuf + q * (kTokTile * 33);
+#pragma unroll
+            for (int jj = 0; jj < TB; ++jj)
+              if (jj < nj) sb[(j0 + jj) * 33 + lane] = act[jj];
+            continue;
+          }
           uint32_t words[TB][kTerms], sfb[TB][kTerms];
           mx_split_groups<TB>(act, words, sfb);
           if (in_range) {
@@ -731,6 +746,41 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&accempty[b]);
+      if constexpr (kLaneSplit) {
+        // lane j: token j's group of 32 rows (this warp's rows) into kTerms MXFP4 terms, the
+        // same arithmetic as mx_split_group, one 16-byte store per term
+        if (!write_part) {
+          __syncwarp();
+          if (lane < ti.ntok && in_range) {
+            const float* sb = actbuf + q * (kTokTile * 33) + lane * 33;
+            float r[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = sb[i];
+            const size_t p = (size_t)(ti.pos0 + lane);
+#pragma unroll 1
+            for (int t = 0; t < kTerms; ++t) {
+              float amax = 0.f;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(r[i]));
+              const int e = mx_scale_exp(amax);
+              const float down = pow2f(-e), up = pow2f(e);
+              uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                float qv;
+                const uint32_t code = e2m1_rne(r[i] * down, &qv);
+                r[i] -= qv * up;
+                w[i >> 3] |= code << (4 * (i & 7));
+              }
+              const size_t r2 = p * kTerms + t;
+              *reinterpret_cast<uint4*>(f.act_q + r2 * (size_t)(f.I >> 1) + grp * 16) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
+              f.act_sf[r2 * (size_t)(f.I >> 5) + grp] = (uint8_t)(e + 127);
+            }
+          }
+          __syncwarp();
+        }
+      }
       if (write_part) {
         __threadfence();
         named_bar(kEpiBar, 128);

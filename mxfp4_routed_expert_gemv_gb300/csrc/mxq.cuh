@@ -25,19 +25,16 @@ __device__ __forceinline__ int mx_scale_exp(float amax) {
 }
 
 // Round a (|a| <= 6) to the nearest E2M1 value, ties to the even code; returns the 4-bit
-// code (bit 3 = sign) and the value it stands for.
+// code (bit 3 = sign) and the value it stands for.  Branch-free (lanes of a warp hold
+// different magnitudes): the code counts the rounding boundaries at or below |a|, with
+// < or <= at each midpoint so that a tie goes to the even code.
 __device__ __forceinline__ uint32_t e2m1_rne(float a, float* val) {
   const float m = fabsf(a);
-  uint32_t c;
-  float v;
-  if (m <= 0.25f) { c = 0; v = 0.f; }
-  else if (m < 0.75f) { c = 1; v = 0.5f; }
-  else if (m <= 1.25f) { c = 2; v = 1.f; }
-  else if (m < 1.75f) { c = 3; v = 1.5f; }
-  else if (m <= 2.5f) { c = 4; v = 2.f; }
-  else if (m < 3.5f) { c = 5; v = 3.f; }
-  else if (m <= 5.f) { c = 6; v = 4.f; }
-  else { c = 7; v = 6.f; }
+  const uint32_t c = (uint32_t)(m > 0.25f) + (uint32_t)(m >= 0.75f) + (uint32_t)(m > 1.25f) +
+                     (uint32_t)(m >= 1.75f) + (uint32_t)(m > 2.5f) + (uint32_t)(m >= 3.5f) +
+                     (uint32_t)(m > 5.f);
+  // E2M1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 by code
+  const float v = c <= 4u ? 0.5f * (float)c : (c == 7u ? 6.f : (float)c - 2.f);
   const bool neg = __float_as_uint(a) >> 31;
   *val = neg ? -v : v;
   return c | (neg ? 8u : 0u);
@@ -48,33 +45,49 @@ __device__ __forceinline__ float pow2f(int e) {
   return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00200000u);
 }
 
+// Warp-wide max of |r| in one reduction: the bit patterns of non-negative floats are in
+// their numeric order.
+__device__ __forceinline__ float warp_absmax(float r) {
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(r))));
+}
+
+// The 4-bit codes of this lane's group of 8 lanes (lanes 8g .. 8g+7), packed lane 8g first
+// in the low nibble: one ballot per code bit, then each ballot's 8 bits spread to every
+// fourth bit position.
+__device__ __forceinline__ uint32_t pack_codes8(uint32_t code, int lane) {
+  const int sh = lane & 24;
+  uint32_t w = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t x = (__ballot_sync(0xffffffffu, (code >> k) & 1u) >> sh) & 0xFFu;
+    x = (x | (x << 12)) & 0x000F000Fu;
+    x = (x | (x << 6)) & 0x03030303u;
+    x = (x | (x << 3)) & 0x11111111u;
+    w |= x << k;
+  }
+  return w;
+}
+
 // One warp, one group of 32 elements (lane i holds element i): the kTerms terms.  On return
-// lanes 0, 8, 16, 24 hold word (lane/8) of each term's 16 packed bytes (low nibble = even
-// element) in words[t], and every lane holds each term's E8M0 byte in sf[t].
+// every lane holds word (lane/8) of each term's 16 packed bytes (low nibble = even element)
+// in words[t], and each term's E8M0 byte in sf[t].
 __device__ __forceinline__ void mx_split_group(float v, uint32_t (&words)[kTerms],
                                                uint32_t (&sf)[kTerms]) {
   const int lane = threadIdx.x & 31;
   float r = v;
 #pragma unroll
   for (int t = 0; t < kTerms; ++t) {
-    float amax = fabsf(r);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const int e = mx_scale_exp(amax);
+    const int e = mx_scale_exp(warp_absmax(r));
     float q;
     const uint32_t code = e2m1_rne(r * pow2f(-e), &q);
     r -= q * pow2f(e);
-    uint32_t w = code << (4 * (lane & 7));
-    w |= __shfl_xor_sync(0xffffffffu, w, 1);
-    w |= __shfl_xor_sync(0xffffffffu, w, 2);
-    w |= __shfl_xor_sync(0xffffffffu, w, 4);
-    words[t] = w;
+    words[t] = pack_codes8(code, lane);
     sf[t] = (uint32_t)(e + 127);
   }
 }
 
 // The same for TB independent groups at once (one value each per lane): the terms of all
-// groups advance together, so their shuffle chains interleave.
+// groups advance together, so their reductions and ballots interleave.
 template <int TB>
 __device__ __forceinline__ void mx_split_groups(const float (&v)[TB], uint32_t (&words)[TB][kTerms],
                                                 uint32_t (&sf)[TB][kTerms]) {
@@ -86,27 +99,18 @@ __device__ __forceinline__ void mx_split_groups(const float (&v)[TB], uint32_t (
   for (int t = 0; t < kTerms; ++t) {
     float amax[TB];
 #pragma unroll
-    for (int b = 0; b < TB; ++b) amax[b] = fabsf(r[b]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-      for (int b = 0; b < TB; ++b) amax[b] = fmaxf(amax[b], __shfl_xor_sync(0xffffffffu, amax[b], o));
-    uint32_t w[TB];
+    for (int b = 0; b < TB; ++b) amax[b] = warp_absmax(r[b]);
+    uint32_t code[TB];
 #pragma unroll
     for (int b = 0; b < TB; ++b) {
       const int e = mx_scale_exp(amax[b]);
       float q;
-      const uint32_t code = e2m1_rne(r[b] * pow2f(-e), &q);
+      code[b] = e2m1_rne(r[b] * pow2f(-e), &q);
       r[b] -= q * pow2f(e);
-      w[b] = code << (4 * (lane & 7));
       sf[b][t] = (uint32_t)(e + 127);
     }
 #pragma unroll
-    for (int o = 1; o <= 4; o <<= 1)
-#pragma unroll
-      for (int b = 0; b < TB; ++b) w[b] |= __shfl_xor_sync(0xffffffffu, w[b], o);
-#pragma unroll
-    for (int b = 0; b < TB; ++b) words[b][t] = w[b];
+    for (int b = 0; b < TB; ++b) words[b][t] = pack_codes8(code[b], lane);
   }
 }
 
