@@ -376,13 +376,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
   // logits it routes from) was complete before phase 0 passed this point (phase 0 lets this
   // launch start only after its own wait), and only the activation terms come from phase 0,
   // so only the thread that loads them waits.
-  if (PH == 0) pdl_wait();
-  pdl_launch();
+  // (A single routed token has k token groups whatever the routing, so its CTAs lay out
+  // their ranges before the wait and route after it.)
+  if (!ONE) {
+    if (PH == 0) pdl_wait();
+    pdl_launch();
+  }
   const uint32_t t0 = tbase;
   volatile int* abort_v = &abort_flag;
-  const int ngroups = ONE ? route_one_token<PH>(f, sm, own_tiles, own_perm, own_gate,
-                                                        PH == 0 && cta == 0)
-                                  : f.meta[2];
+  const int ngroups = ONE ? f.k : f.meta[2];
 
   const Split sp(ngroups * f.RT * f.KC, G);
   const Range rg = make_range(sp, f.KC, cta);
@@ -402,6 +404,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
   int nfix = 0;
   for (int c = fix_c0; c <= fix_c1; ++c) nfix += idle(c) ? 0 : 1;
   const bool fix_smem = (size_t)nfix * pf * 4 <= kFixBytes;
+  if (ONE) {
+    if (PH == 0) pdl_wait();
+    pdl_launch();
+    if (route_one_token<PH>(f, sm, own_tiles, own_perm, own_gate, PH == 0 && cta == 0) == 0)
+      *abort_v = 1;  // the routing flag never came: every role stops at its first wait
+  }
 
   if (warp == kProdWarp || warp == kBWarp) {
     // ------------------------------------- TMA: weights (warp 8), activations (warp 10)
