@@ -194,36 +194,111 @@ __device__ __forceinline__ OneTokenChoice topk_one_token(const float* lt, const 
       key[j] = ((unsigned long long)ordered_bits(sg + bs[j]) << 32) | (uint32_t)(~(uint32_t)e);
     }
   }
+  // Fast path: the (k+1)-th best of the lists' maxima is a lower bound of the (k+1)-th best
+  // key (k+1 lists each hold a key at least that good), so the keys at or above it contain
+  // the top k+1.  They are few (gathered in shared memory); warp 0 sorts at most 64 of them.
+  // More than 64 (many equal scores), or fewer lists than k+1: the full sort below.
+  const int nl = (E + 31) >> 5;
+  unsigned long long acc = 0ull;
+  bool fast = false;
+  if (k + 1 <= nl && nl <= 32) {
+    unsigned long long* lmax = lists;       // [32] best key of each list
+    unsigned long long* cand = lists + 32;  // [64] candidates
+    unsigned int* ncand = reinterpret_cast<unsigned int*>(lists + 96);
+    unsigned long long m[LPW];
 #pragma unroll
-  for (int size = 2; size <= 32; size <<= 1) {
+    for (int j = 0; j < LPW; ++j) m[j] = key[j];
 #pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const bool desc = (lane & size) == 0, lo = (lane & stride) == 0;
+    for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
       for (int j = 0; j < LPW; ++j) {
-        const unsigned long long o = __shfl_xor_sync(0xffffffffu, key[j], stride);
-        const unsigned long long mx = key[j] > o ? key[j] : o, mn = key[j] > o ? o : key[j];
-        key[j] = (lo == desc) ? mx : mn;
+        const unsigned long long x = __shfl_xor_sync(0xffffffffu, m[j], o);
+        m[j] = x > m[j] ? x : m[j];
+      }
+    if (lane == 0)
+#pragma unroll
+      for (int j = 0; j < LPW; ++j)
+        if (warp * LPW + j < 32) lmax[warp * LPW + j] = m[j];
+    if (threadIdx.x == 0) *ncand = 0u;
+    __syncthreads();
+    if (warp == 0) {
+      const unsigned long long mine = lane < nl ? lmax[lane] : 0ull;
+      int rank = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const unsigned long long x = __shfl_sync(0xffffffffu, mine, i);
+        rank += (i < nl && x > mine) ? 1 : 0;
+      }
+      if (lane < nl && rank == k) lists[97] = mine;
+    }
+    __syncthreads();
+    const unsigned long long th = lists[97];
+#pragma unroll
+    for (int j = 0; j < LPW; ++j) {
+      const bool in = key[j] >= th;
+      const unsigned int bal = __ballot_sync(0xffffffffu, in);
+      unsigned int base = 0u;
+      if (lane == 0 && bal) base = atomicAdd(ncand, (unsigned int)__popc(bal));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      const unsigned int pos = base + __popc(bal & ((1u << lane) - 1u));
+      if (in && pos < 64u) cand[pos] = key[j];
+    }
+    __syncthreads();
+    const unsigned int nc = *ncand;
+    if (nc <= 64u) {
+      fast = true;
+      if (warp == 0) {
+        unsigned long long a0 = lane < (int)nc ? cand[lane] : 0ull;
+        unsigned long long a1 = lane + 32 < (int)nc ? cand[lane + 32] : 0ull;
+#pragma unroll
+        for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+          for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const bool desc = (lane & size) == 0, lo = (lane & stride) == 0;
+            const unsigned long long o0 = __shfl_xor_sync(0xffffffffu, a0, stride);
+            const unsigned long long o1 = __shfl_xor_sync(0xffffffffu, a1, stride);
+            a0 = (lo == desc) ? (a0 > o0 ? a0 : o0) : (a0 > o0 ? o0 : a0);
+            a1 = (lo == desc) ? (a1 > o1 ? a1 : o1) : (a1 > o1 ? o1 : a1);
+          }
+        }
+        const unsigned long long o = __shfl_sync(0xffffffffu, a1, 31 - lane);
+        acc = top32_clean(a0 > o ? a0 : o, lane);
       }
     }
+    __syncthreads();  // the full path below reuses the scratch
   }
-  unsigned long long acc = key[0];
+  if (!fast) {
 #pragma unroll
-  for (int j = 1; j < LPW; ++j) {
-    const unsigned long long o = __shfl_sync(0xffffffffu, key[j], 31 - lane);
-    acc = top32_clean(acc > o ? acc : o, lane);
-  }
-  lists[warp * 32 + lane] = acc;
-  __syncthreads();
-  for (int n = nwarps; n > 1;) {
-    const int h = (n + 1) >> 1;
-    if (warp < n - h) {
-      const unsigned long long o = lists[(warp + h) * 32 + 31 - lane];
-      acc = top32_clean(acc > o ? acc : o, lane);
-      lists[warp * 32 + lane] = acc;
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const bool desc = (lane & size) == 0, lo = (lane & stride) == 0;
+#pragma unroll
+        for (int j = 0; j < LPW; ++j) {
+          const unsigned long long o = __shfl_xor_sync(0xffffffffu, key[j], stride);
+          const unsigned long long mx = key[j] > o ? key[j] : o, mn = key[j] > o ? o : key[j];
+          key[j] = (lo == desc) ? mx : mn;
+        }
+      }
     }
-    n = h;
+    acc = key[0];
+#pragma unroll
+    for (int j = 1; j < LPW; ++j) {
+      const unsigned long long o = __shfl_sync(0xffffffffu, key[j], 31 - lane);
+      acc = top32_clean(acc > o ? acc : o, lane);
+    }
+    lists[warp * 32 + lane] = acc;
     __syncthreads();
+    for (int n = nwarps; n > 1;) {
+      const int h = (n + 1) >> 1;
+      if (warp < n - h) {
+        const unsigned long long o = lists[(warp + h) * 32 + 31 - lane];
+        acc = top32_clean(acc > o ? acc : o, lane);
+        lists[warp * 32 + lane] = acc;
+      }
+      n = h;
+      __syncthreads();
+    }
   }
   OneTokenChoice c = {-1, 0.f, 0};
   if (warp == 0) {

@@ -5,6 +5,7 @@ tails, both bucketing paths, k == E, SiTU, NaN-scale groups, dropped and duplica
 indices and T == 0.  The Kimi-K3 workloads run at full size in the launch configuration
 the benchmark times; the oracle checks every index it computes and y on sampled tokens.
 """
+import dataclasses
 import gc
 
 import numpy as np
@@ -140,6 +141,28 @@ def test_batch_of_one_equals_row():
     for t in (0, 5):
         y1 = dl.run(h=dl.h[t:t + 1].contiguous(), x=dl.x[t:t + 1].contiguous())[0]
         assert np.array_equal(y1[0], y[t])
+
+
+@pytest.mark.parametrize("case", ["all_scores_equal", "boosted_block", "boosted_spread"])
+def test_one_token_routing_ties(case):
+    """One token, 896 experts, top-16, with exact score ties (zero router weight): the tie
+    rule (lower index first) must give the oracle's set and order exactly.  All scores equal
+    leaves the in-kernel top-k more candidates than its fast path takes; a boosted block of
+    40 experts ties within itself; a spread boost of 20 ties across lists."""
+    w = synth.small_workload(T=1, E=896, k=16, latent=512, inter=512, hidden=256, seed=31)
+    li = synth.layer_inputs(w, 0)
+    bias = np.zeros(w.E, dtype=np.float32)
+    if case == "boosted_block":
+        bias[300:340] = 1.0
+    elif case == "boosted_spread":
+        bias[np.arange(20) * 41 + 7] = 0.75
+    li = dataclasses.replace(li, wr=np.zeros_like(li.wr), bias=bias)
+    dl = DeviceLayer(w, li=li)
+    y, idx, gate, gap, status = dl.run()
+    r = oracle.route(oracle_cfg(w), li.h, li.wr, li.bias)
+    assert np.array_equal(idx, r.idx), (idx, r.idx)
+    np.testing.assert_allclose(gate, r.gate, rtol=1e-5)
+    _check_layer(w, dl)
 
 
 # ---- Kimi-K3 workloads at full size ----------------------------------------------------
