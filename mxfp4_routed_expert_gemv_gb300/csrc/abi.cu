@@ -100,7 +100,7 @@ size_t carve(const k3moe_cfg* c, int32_t T, void* base, bool host_stage, Workspa
   t.b.nvalid = cv.take<int32_t>(Tt);
   t.b.inv = cv.take<int32_t>(P);
   t.b.ntile_base = cv.take<int32_t>(E + 1);
-  t.b.flags = cv.take<int32_t>(kTcFlags);
+  t.b.flags = cv.take<int32_t>(kTcFlagWords);
   t.b.tiles = cv.take<int4>((P + kTcTokTile - 1) / kTcTokTile + E + 1);
   t.tc = tc_path_supported((int)L, (int)I);
   if (t.tc) {
@@ -197,7 +197,7 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
                                 T, E, c->hidden, w.logits, s, true,
                                 static_cast<const uint16_t*>(x), L, one ? w.xq : nullptr,
                                 one ? w.xsf : nullptr, one ? w.b.flags : nullptr,
-                                one ? kTcFlags : 0, status));
+                                one ? kTcFlagWords : 0, status));
     if (!fused_topk)
       K3_TRY(launch_topk(w.logits, bias, T, E, K, c->renorm, c->routed_scale, idx, gate, gap, s,
                          true));
@@ -206,7 +206,7 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
   PrepArgs p{fused_topk ? w.logits : nullptr, bias, E, K, c->renorm, c->routed_scale, idx, gate,
              gap, T, L, static_cast<const uint16_t*>(x), w.tc ? nullptr : w.x16, w.xexp, w.b, y,
              status};
-  const RouteOne ro{w.logits, bias, c->renorm, c->routed_scale, idx, gate, gap};
+  const RouteOne ro{w.logits, bias, c->renorm, c->routed_scale, idx, gate, gap, y};
   if (!one) {
     K3_TRY(launch_prep(p, s, route));
     if (w.tc)
@@ -227,7 +227,8 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
     K3_TRY(launch_gemm2(ep, L, I, E, T, K, w.act, gate, w.b, w.ybuf, status, s, true));
     K3_TRY(phase(4, s));
   }
-  K3_TRY(launch_combine(w.ybuf, idx, T, K, E, L, y, s, true));
+  // one routed token: the second GEMM already summed the slots into y
+  if (!one) K3_TRY(launch_combine(w.ybuf, idx, T, K, E, L, y, s, true));
   K3_TRY(phase(5, s));
   return K3MOE_OK;
 }

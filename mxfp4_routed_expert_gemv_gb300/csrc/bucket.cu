@@ -86,7 +86,7 @@ __device__ void publish_counts(int c, int E, const BucketOut& o, int* excl_out) 
     o.ntile_base[nact] = nt_tot;
     o.meta[2] = nt_tot;
   }
-  for (int i = e; i < kTcFlags; i += blockDim.x) o.flags[i] = 0;
+  for (int i = e; i < kTcFlagWords; i += blockDim.x) o.flags[i] = 0;
   *excl_out = excl;
 }
 

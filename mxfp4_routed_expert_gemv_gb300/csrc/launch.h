@@ -59,6 +59,10 @@ constexpr int kTcMaxGrid = 160;
 // [kTcRouteFlag] the single-token routing published by the first GEMM.
 constexpr int kTcRouteFlag = 2 * kTcMaxGrid;
 constexpr int kTcFlags = 2 * kTcMaxGrid + 1;
+// One routed token: after the flags, per 128-row tile of y, the slots written so far (the
+// second GEMM sums the token's slots into y where the count completes; L <= 4096).
+constexpr int kTcYCount = kTcFlags;
+constexpr int kTcFlagWords = kTcFlags + 4096 / 128;
 
 // bucket.cu
 struct BucketOut {
@@ -73,7 +77,7 @@ struct BucketOut {
   int32_t* nvalid;      // [T]    valid assignments per token
   int32_t* inv;         // [T*k]  perm position of each valid assignment id
   int32_t* ntile_base;  // [E+1]  tensor-core tiles (kTcTokTile tokens) before each active expert
-  int32_t* flags;       // [kTcFlags] tensor-core path flags (zeroed before each call)
+  int32_t* flags;       // [kTcFlagWords] tensor-core path flags and counts (zeroed per call)
   int4* tiles;          // [P/16 + E + 1] per token group: expert, first position, tokens, 0
 };
 
@@ -136,6 +140,7 @@ struct RouteOne {
   float routed_scale;
   int32_t* idx;
   float *gate, *gap;
+  float* y;  // [L]: the second GEMM sums the slots here (no combine launch)
 };
 cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k,
                               const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,

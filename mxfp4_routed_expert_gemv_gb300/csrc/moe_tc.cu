@@ -99,6 +99,8 @@ struct FArgs {
   float *gate_out, *gap_out;
   int4* tiles_out;
   int32_t *perm_out, *route_flag;
+  float* y;                // one routed token: y [L], summed by the second GEMM
+  int32_t* ycount;         // [L / 128] slots written per 128-row tile of y (zeroed)
   int k, L, I, act_kind;
   float b1, b2;
   int KC, RT, R;           // reduction chunks, row tiles, rows per expert
@@ -183,6 +185,13 @@ struct TileCursor {
 
 __device__ __forceinline__ void st_release(int32_t* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Release-acquire add at GPU scope: its release covers what a CTA barrier before it
+// ordered, its acquire what a barrier after it orders.
+__device__ __forceinline__ int atom_add_acq_rel(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 __device__ __forceinline__ int ld_acquire(const int32_t* p) {
   int v;
@@ -332,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
   __shared__ __align__(8) uint64_t fullA[kStages], fullB[kStages], sfready[kStages], empty[kStages];
   __shared__ __align__(8) uint64_t accfull[2], accempty[2], drained, fixfull;
   __shared__ uint32_t tbase;
-  __shared__ int abort_flag;
+  __shared__ int abort_flag, y_last;
   __shared__ int4 own_tiles[32];  // route_one: this CTA's table of token groups
   __shared__ int own_perm[32];
   __shared__ float own_gate[32];
@@ -794,6 +803,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
         named_bar(kEpiBar, 128);
         if (threadIdx.x == 0) st_release(f.flags + cta, 1);
       }
+      if constexpr (ONE && PH == 1) {
+        if (!write_part) {
+          // the combine: count this slot for its 128-row tile of y; the CTA that writes the
+          // k-th slot of a tile sums the token's slots there in slot order (as k_combine)
+          named_bar(kEpiBar, 128);  // orders every row's slot write before the release
+          if (threadIdx.x == 0) y_last = atom_add_acq_rel(f.ycount + ti.rt, 1) == f.k - 1;
+          named_bar(kEpiBar, 128);
+          const int r = ti.rt * kRowsTile + row;
+          if (y_last && r < f.R) {
+            float sv[kMaxTopk];
+#pragma unroll
+            for (int sl = 0; sl < kMaxTopk; ++sl)
+              sv[sl] = sl < f.k ? __ldcg(f.ybuf + (size_t)sl * f.L + r) : 0.f;
+            float acc = 0.f;
+#pragma unroll
+            for (int sl = 0; sl < kMaxTopk; ++sl)
+              if (sl < f.k) acc += sv[sl];
+            f.y[r] = acc;
+          }
+        }
+      }
     }
   }
 
@@ -929,6 +959,7 @@ cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, i
     f.renorm = ro->renorm; f.routed_scale = ro->routed_scale;
     f.idx_out = ro->idx; f.gate_out = ro->gate; f.gap_out = ro->gap;
     f.tiles_out = b.tiles; f.perm_out = b.perm; f.route_flag = b.flags + kTcRouteFlag;
+    f.y = ro->y; f.ycount = b.flags + kTcYCount;
   }
   // phase 0 (w1, w3), then phase 1 (w2): the second launch reads what the first wrote, across
   // the kernel boundary (its CTAs wait in griddepcontrol.wait until the first has completed)
