@@ -13,8 +13,8 @@
 namespace k3 {
 namespace {
 
-constexpr int kRowsPerCta = 2;    // router rows per CTA
 constexpr int kQuarters = 4;      // warps per row, each a quarter of the hidden width
+constexpr int kRpcFew = 2;        // router rows per CTA for one or two tokens
 constexpr int kVecPerLane = 8;    // 16-byte pieces a lane keeps in flight per batch
 
 // logits[t][e] = sum_i h[t][i] * wr[e][i].  A CTA holds 2 rows; each row is split into 4
@@ -24,8 +24,8 @@ constexpr int kVecPerLane = 8;    // 16-byte pieces a lane keeps in flight per b
 // With xq set (one token), warps 0 .. L/32-1 of the grid also write the token's x as kTerms
 // MXFP4 terms (rows 0 .. kTerms-1 of xq / xsf), and CTA 0 zeroes `zero` [nzero]: work that
 // does not depend on the routing, done here so that no separate launch is spent on it.
-template <int TT>
-__global__ void __launch_bounds__(256) k_router_logits(const uint16_t* __restrict__ h,
+template <int TT, int RPC>
+__global__ void __launch_bounds__(RPC * kQuarters * 32) k_router_logits(const uint16_t* __restrict__ h,
                                                        const uint16_t* __restrict__ wr, int T,
                                                        int E, int H,
                                                        float* __restrict__ logits,
@@ -37,9 +37,9 @@ __global__ void __launch_bounds__(256) k_router_logits(const uint16_t* __restric
   pdl_launch();
   if (zero && blockIdx.x == 0 && blockIdx.y == 0)  // counters the next launches start from
     for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
-  __shared__ float part[8][TT];
+  __shared__ float part[RPC * kQuarters][TT];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * kRowsPerCta + (warp >> 2);
+  const int e = blockIdx.x * RPC + (warp >> 2);
   const int q = warp & 3;
   const int t0 = blockIdx.y * TT;
   const int nvec = H >> 3;
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(256) k_router_logits(const uint16_t* __restric
     logits[(size_t)(t0 + lane) * E + e] = s;
   }
   if (xq) {
-    const int grp = blockIdx.x * 8 + warp;
+    const int grp = blockIdx.x * (RPC * kQuarters) + warp;
     if (grp < (L >> 5)) {
       const float v = __uint_as_float((uint32_t)x[32 * grp + lane] << 16);
       uint32_t words[kTerms], sf[kTerms];
@@ -248,13 +248,16 @@ cudaError_t launch_router_logits(const uint16_t* h, const uint16_t* wr, int T, i
     return launch_kernel(k_router_tc, dim3((E + 127) / 128, (T + 127) / 128), dim3(128), smem, s,
                          pdl, mw, mh, T, E, H, logits, status);
   }
-  const unsigned gx = (E + kRowsPerCta - 1) / kRowsPerCta;
-  if (xq && (T != 1 || (int)gx * 8 < (L >> 5))) return cudaErrorInvalidValue;
-  if (T <= 2)
-    return launch_kernel(k_router_logits<1>, dim3(gx, T), dim3(256), 0, s, pdl, h, wr, T, E, H,
-                         logits, x, L, xq, xsf, zero, nzero);
-  return launch_kernel(k_router_logits<4>, dim3(gx, (T + 3) / 4), dim3(256), 0, s, pdl, h, wr, T,
-                       E, H, logits, x, L, xq, xsf, zero, nzero);
+  if (T <= 2) {
+    const unsigned gx = (E + kRpcFew - 1) / kRpcFew;
+    if (xq && (T != 1 || (int)gx * kRpcFew * kQuarters < (L >> 5))) return cudaErrorInvalidValue;
+    return launch_kernel(k_router_logits<1, kRpcFew>, dim3(gx, T), dim3(kRpcFew * kQuarters * 32),
+                         0, s, pdl, h, wr, T, E, H, logits, x, L, xq, xsf, zero, nzero);
+  }
+  if (xq) return cudaErrorInvalidValue;
+  const unsigned gx = (E + 1) / 2;
+  return launch_kernel(k_router_logits<4, 2>, dim3(gx, (T + 3) / 4), dim3(2 * kQuarters * 32), 0,
+                       s, pdl, h, wr, T, E, H, logits, x, L, xq, xsf, zero, nzero);
 }
 
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,
