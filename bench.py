@@ -4,9 +4,12 @@ Default workload: the batch-1 decode layer (1 token, 896 experts, top-16, bias N
 the configuration the headline metric "MoE-layer tokens/s and achieved HBM TB/s (MXFP4
 experts, 896 choose 16)" is quoted on.  A step is one full layer: router GEMV, top-k,
 bucketing, GEMM1 (w1, w3, SwiGLU), GEMM2 (w2, gates), combine.  Inputs are seeded and
-synthetic (synth/), resident in HBM when the timed region starts.
+synthetic (synth/), resident in HBM when the timed region starts.  The steps cycle through
+--layers independent layers (default 8, 126 GB of experts), as a decode pass cycles through
+the model's layers, so that no layer's weights are still in L2 when its next step comes.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 1]
+                  [--layers 8]
 
 --gpus N > 1 runs under torchrun, one rank per GPU: every rank holds its own copy of the
 layer and decodes its own token stream (weak scaling, no collective on the data path); the
@@ -274,25 +277,33 @@ def run_ours(args):
         w = dataclasses.replace(w, E=args.experts, name=w.name + f" [profiling variant: {args.experts} experts]")
     if w.layers != 1:
         raise SystemExit("the stacked workload is a parity case, not a bench line")
+    # Steps cycle through NL independent layers (own experts, router weight and bias), as a
+    # decode pass does: between two uses of one layer, NL - 1 others stream their weights, so
+    # nothing of a layer is still in L2 when it comes back.  (With one layer, consecutive
+    # tokens share about half their experts, because the correction bias dominates the
+    # selection, and part of a step would come from L2.)
+    NL = max(1, args.layers)
     free, total = torch.cuda.mem_get_info(dev)
-    need = w.E * w.expert_bytes + (4 << 30)
+    need = NL * w.E * w.expert_bytes + (4 << 30)
     if need > free:
         raise SystemExit(f"needs {need / 1e9:.1f} GB of HBM, {free / 1e9:.1f} GB free")
 
     cfg = k3.Cfg(hidden=w.hidden, n_experts=w.E, topk=w.k, latent=w.latent, inter=w.inter,
                  routed_scale=w.routed_scale)
-    experts = k3.Experts.from_dict(synth.experts_device(w, 0, dev))
+    experts_l = [k3.Experts.from_dict(synth.experts_device(w, l, dev)) for l in range(NL)]
     rotation = args.rotation if w.T == 1 else 4
-    li = synth.layer_inputs(w, 0, T=w.T * rotation * world)
+    rotation = ((rotation + NL - 1) // NL) * NL  # whole layer cycles per graph
     off = rank_token_offset(rank, rotation * w.T)
 
     def bf16(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
-    H = bf16(li.h[off:off + rotation * w.T]).view(rotation, w.T, w.hidden)
-    X = bf16(li.x[off:off + rotation * w.T]).view(rotation, w.T, w.latent)
-    wr = bf16(li.wr)
-    bias = None if li.bias is None else torch.from_numpy(li.bias).to(dev)
+    lis = [synth.layer_inputs(w, l, T=w.T * rotation * world) for l in range(NL)]
+    # step r: layer r % NL, the token inputs of slot r drawn from that layer's stream
+    H = torch.stack([bf16(lis[r % NL].h[off + r * w.T:off + (r + 1) * w.T]) for r in range(rotation)])
+    X = torch.stack([bf16(lis[r % NL].x[off + r * w.T:off + (r + 1) * w.T]) for r in range(rotation)])
+    wr_l = [bf16(li_.wr) for li_ in lis]
+    bias_l = [None if li_.bias is None else torch.from_numpy(li_.bias).to(dev) for li_ in lis]
     T = w.T
     ws = k3.workspace(cfg, T, dev)
     y = torch.empty((T, w.latent), dtype=torch.float32, device=dev)
@@ -302,7 +313,9 @@ def run_ours(args):
 
     def step(i):  # one layer on the current stream
         r = i % rotation
-        k3.k3moe_layer(cfg, H[r], wr, bias, experts, X[r], y, idx[r], gate, None, status, ws)
+        l = r % NL
+        k3.k3moe_layer(cfg, H[r], wr_l[l], bias_l[l], experts_l[l], X[r], y, idx[r], gate, None,
+                       status, ws)
 
     # eager warm-up (also configures the kernels' shared-memory limits before any capture)
     n0 = k3.k3moe_launch_count()
@@ -402,12 +415,14 @@ def run_ours(args):
     xh.copy_(X.cpu())
     yh = torch.empty((T, w.latent), dtype=torch.float32).pin_memory()
     for i in range(min(args.warmup, 50)):
-        k3.k3moe_layer_host(cfg, hh[i % rotation], wr, bias, experts, xh[i % rotation], yh, status, wsh)
+        k3.k3moe_layer_host(cfg, hh[i % rotation], wr_l[i % NL], bias_l[i % NL], experts_l[i % NL],
+                            xh[i % rotation], yh, status, wsh)
     if world > 1:
         dist.barrier()
     t0 = time.perf_counter()
     for i in range(n_e2e):
-        k3.k3moe_layer_host(cfg, hh[i % rotation], wr, bias, experts, xh[i % rotation], yh, status, wsh)
+        k3.k3moe_layer_host(cfg, hh[i % rotation], wr_l[i % NL], bias_l[i % NL], experts_l[i % NL],
+                            xh[i % rotation], yh, status, wsh)
     e2e_dt = max_over_ranks(time.perf_counter() - t0, world, dev)
     e2e_value = sum_over_ranks(T * n_e2e, world, dev) / e2e_dt
 
@@ -425,7 +440,10 @@ def run_ours(args):
                    "achieved_layer_TBps": lb * args.steps / elapsed / 1e12,
                    "layer_frac_of_hbm_peak": lb * args.steps / elapsed / 1e9 / peak,
                    "l2": f"inputs larger than L2: each step streams {lb / 1e6:.0f} MB (> {L2_BYTES / 1e6:.0f} MB L2) "
-                         f"and rotates among {rotation} seeded token inputs, so consecutive steps pick different experts",
+                         f"and the steps cycle through {NL} independent layers (own experts, router, bias; "
+                         f"{NL * w.E * w.expert_bytes / 1e9:.0f} GB resident) with {rotation} seeded token inputs, "
+                         f"so a layer's weights are not in L2 when it comes back",
+                   "layers_rotated": NL,
                    "phase_ms": {n: float(ph[:, j].mean() * 1e3) for j, n in
                                 enumerate(["route", "bucket+prep", "gemm1", "gemm2", "combine"])},
                    "launch": "CUDA graph replay, programmatic dependent launch between kernels",
@@ -463,6 +481,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=1, choices=[0, 1, 2, 3])
     ap.add_argument("--rotation", type=int, default=64)
+    ap.add_argument("--layers", type=int, default=8,
+                    help="independent layers the steps cycle through (L2 stays cold per layer)")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count (small-memory profiling variant, not a bench line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
