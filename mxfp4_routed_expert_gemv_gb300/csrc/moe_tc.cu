@@ -45,8 +45,6 @@ constexpr int kThreads = 352;
 constexpr int kSfWarp0 = 4, kProdWarp = 8, kMmaWarp = 9, kBWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kEpiBar = 1;  // named barrier of the four epilogue warps
-// One routed token: second-GEMM units each first-GEMM CTA prefetches into L2 at its end.
-constexpr int kTcPrefetchUnits = 3;
 
 // Shared-memory and TMEM layout for tiles of at most NMAX activation rows (MMA N: 16 for
 // batches of up to 4 tokens, 64 otherwise), NM weight matrices per unit (2 in the first
@@ -101,7 +99,6 @@ struct FArgs {
   float *gate_out, *gap_out;
   int4* tiles_out;
   int32_t *perm_out, *route_flag;
-  int pf_units;            // one token, first GEMM: second-GEMM units to prefetch into L2
   float* y;                // one routed token: y [L], summed by the second GEMM
   int32_t* ycount;         // [L / 128] slots written per 128-row tile of y (zeroed)
   int k, L, I, act_kind;
@@ -306,7 +303,7 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
 }
 
 struct Maps {
-  CUtensorMap m[8];  // [6], [7]: the second GEMM's w2 and scales (first GEMM: L2 prefetch)
+  CUtensorMap m[6];
 };
 
 // The CTA's range in tiles: the first tile (maybe shared, part at the front), whole tiles,
@@ -481,26 +478,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
                 tc::tma_load_2d(st + kOffSB + ks * kSBBytes + b * 256, &mp.m[5],
                                 (kc * KS + ks) * 16, brow0 + 16 * b, &fullB[s]);
               }
-            }
-          }
-        }
-      }
-      if constexpr (ONE && PH == 0) {
-        if (wts && !stop && f.pf_units > 0) {
-          // this CTA index's first units of the second GEMM (one token: its tiles are known
-          // here): into L2 while this GEMM's last copies land, so that the second GEMM's
-          // first stages come from L2
-          const int KS2 = (f.I / kKStage) % 2 == 0 ? 2 : 1;  // the second GEMM's unit shape
-          const int RT2 = (f.L + kRowsTile - 1) / kRowsTile, KC2 = f.I / (KS2 * kKStage);
-          const Split sp2(f.k * RT2 * KC2, G);
-          const int u0 = sp2.lo(cta), u1 = min(sp2.lo(cta + 1), u0 + f.pf_units);
-          for (int u = u0; u < u1; ++u) {
-            const int tile = u / KC2, kc = u - tile * KC2, ntg = tile / RT2;
-            const int arow = own_tiles[ntg].x * f.L + (tile - ntg * RT2) * kRowsTile;
-            for (int ks = 0; ks < KS2; ++ks) {
-              tc::tma_prefetch_l2_2d(&mp.m[6], (kc * KS2 + ks) * 256, arow);
-              tc::tma_prefetch_l2_2d(&mp.m[6], (kc * KS2 + ks) * 256 + 128, arow);
-              tc::tma_prefetch_l2_2d(&mp.m[7], (kc * KS2 + ks) * 16, arow);
             }
           }
         }
@@ -964,10 +941,6 @@ cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, i
     return cudaErrorInvalidValue;
   m1.m[2] = m1.m[0];
   m1.m[3] = m1.m[1];
-  m0.m[6] = m1.m[0];
-  m0.m[7] = m1.m[1];
-  m1.m[6] = m1.m[0];
-  m1.m[7] = m1.m[1];
   // unit counts stay below 2^31 (32-bit range arithmetic in the kernel)
   const uint64_t groups = (uint64_t)T * k / kTokTile + E + 1;
   if (groups * ((L + kRowsTile - 1) / kRowsTile) * (L / kKStage) >= (1ull << 31) ||
@@ -994,7 +967,6 @@ cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, i
   f.one_token = T == 1;
   f.KC = L / kKStage; f.RT = (I + kRowsTile - 1) / kRowsTile; f.R = I;
   f.flags = b.flags;
-  f.pf_units = kTcPrefetchUnits;
   cudaError_t e = launch_tc(m0, f, T, s, pdl);
   if (e != cudaSuccess) return e;
   if (between) between(s);
@@ -1002,7 +974,6 @@ cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, i
   f.one_token = 0;
   f.KC = I / kKStage; f.RT = (L + kRowsTile - 1) / kRowsTile; f.R = L;
   f.flags = b.flags + kTcMaxGrid;
-  f.pf_units = 0;
   return launch_tc(m1, f, T, s, true);
 }
 
