@@ -60,17 +60,20 @@ constexpr int kEpiBar = 1;  // named barrier of the four epilogue warps
 //          from kSfBase, stage s at + kSfStageCols s: A scales of sb, MMA j at + 32 sb + 4 j
 //          (+ lane quarter), B scales of ks at + 32 (NM KS + ks) + 4 j (+ 1 for B rows 32..63);
 //   fix:   the parts a head tile adds, after the ring (kFixBytes), then the act buffer.
-template <int NMAX, int NM, int KS>
+template <int NMAX, int NM, int KS, int BR>
 struct Lay {
-  static constexpr uint32_t kBKatom = NMAX * 128;
+  // BR activation rows are stored per chunk: NMAX, or 8 for one token (its 4 term rows; the
+  // MMA's rows 8..15 read the same 8 rows again, columns that are never used), which keeps
+  // a third ring stage in reach of the second GEMM
+  static constexpr uint32_t kBKatom = BR * 128;
   static constexpr uint32_t kBBytes = 2 * kBKatom;
-  static constexpr uint32_t kSBBytes = NMAX * (kKStage / 32);
+  static constexpr uint32_t kSBBytes = BR * (kKStage / 32);
   static constexpr uint32_t kOffB = NM * KS * kABytes, kOffSA = kOffB + KS * kBBytes;
   static constexpr uint32_t kOffSB = kOffSA + NM * KS * kSABytes;
   static constexpr uint32_t kStageBytes = ((kOffSB + KS * kSBBytes + 1023) / 1024) * 1024;
   static constexpr int kStages =
-      NM * KS == 2 ? (NMAX <= 16 && NM == 2 ? 3 : 2) : (NMAX <= 16 ? 5 : 4);
-  static constexpr uint32_t kFixBytes = NMAX <= 16 && NM == 2 ? 4096 : 16384;
+      NM * KS == 2 ? ((NMAX <= 16 && NM == 2) || BR == 8 ? 3 : 2) : (NMAX <= 16 ? 5 : 4);
+  static constexpr uint32_t kFixBytes = (NMAX <= 16 && NM == 2) || BR == 8 ? 4096 : 16384;
   // first GEMM with 64-row activation tiles: act of a tile's tokens, [warp][token][33]
   // floats, so that one lane can split one token's group of 32 rows (see the epilogue)
   static constexpr uint32_t kActBufBytes = NMAX == 64 && NM == 2 ? 4 * kTokTile * 33 * 4 : 0;
@@ -330,7 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
                                                         const FArgs f) {
   constexpr int NM = PH == 0 ? 2 : 1;  // weight matrices per unit: w1 and w3, or w2
   constexpr int TB = NMAX / 16;        // tokens per epilogue step
-  using Y = Lay<NMAX, NM, KS>;
+  constexpr int BR = ONE ? 8 : NMAX;   // activation rows stored per chunk
+  using Y = Lay<NMAX, NM, KS, BR>;
   constexpr int kStages = Y::kStages;
   constexpr uint32_t kStageBytes = Y::kStageBytes, kBKatom = Y::kBKatom;
   constexpr uint32_t kOffB = Y::kOffB, kOffSA = Y::kOffSA, kOffSB = Y::kOffSB;
@@ -436,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
         const TileInfo ti = cur.get<ONE>(tile, f, own_tiles);
         const int kb = ti_ == 0 ? rg.u0 - tile * f.KC : 0;
         const int ke = ti_ == ntiles - 1 ? rg.u1 - tile * f.KC : f.KC;
-        const int nbox = ti.N / 16;
+        const int nbox = ONE ? 1 : ti.N / 16;  // boxes of BR (one token) or 16 rows
         const int arow = ti.expert * f.R + ti.rt * kRowsTile;
         for (int kc = kb; kc < ke && !stop; ++kc, ++it) {
           const int s = it % kStages;
@@ -466,16 +470,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
             // one token: its terms are rows 0 .. kTerms-1 whatever the position (the router
             // launch writes only those; the per-position layout repeats them)
             const int brow0 = f.one_token ? 0 : ti.pos0 * kTerms;
-            mbar_arrive_expect_tx(&fullB[s], (uint32_t)(KS * nbox) * (2 * 2048 + 256));
+            constexpr uint32_t kBox = (ONE ? 8 : 16) * 128, kSBox = (ONE ? 8 : 16) * 16;
+            mbar_arrive_expect_tx(&fullB[s], (uint32_t)(KS * nbox) * (2 * kBox + kSBox));
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
               uint8_t* sbk = st + kOffB + ks * kBBytes;
               const int x = (kc * KS + ks) * 256;
               for (int b = 0; b < nbox; ++b) {
-                tc::tma_load_2d(sbk + b * 2048, &mp.m[4], x, brow0 + 16 * b, &fullB[s]);
-                tc::tma_load_2d(sbk + kBKatom + b * 2048, &mp.m[4], x + 128, brow0 + 16 * b,
+                tc::tma_load_2d(sbk + b * kBox, &mp.m[4], x, brow0 + 16 * b, &fullB[s]);
+                tc::tma_load_2d(sbk + kBKatom + b * kBox, &mp.m[4], x + 128, brow0 + 16 * b,
                                 &fullB[s]);
-                tc::tma_load_2d(st + kOffSB + ks * kSBBytes + b * 256, &mp.m[5],
+                tc::tma_load_2d(st + kOffSB + ks * kSBBytes + b * kSBox, &mp.m[5],
                                 (kc * KS + ks) * 16, brow0 + 16 * b, &fullB[s]);
               }
             }
@@ -557,7 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
         for (int ks = 0; ks < KS; ++ks) {
           const uint32_t rb = ring + 32 * (NM * KS + ks);
           const uint8_t* sbs = st + kOffSB + ks * kSBBytes;
-          const uint4 sb0 = *reinterpret_cast<const uint4*>(sbs + 16 * lane);
+          const uint4 sb0 = lane < BR ? *reinterpret_cast<const uint4*>(sbs + 16 * lane)
+                                      : make_uint4(0u, 0u, 0u, 0u);
           const uint32_t wb0[4] = {sb0.x, sb0.y, sb0.z, sb0.w};
 #pragma unroll
           for (int j = 0; j < kMmas; ++j)
@@ -618,7 +624,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
                 const uint32_t kboff =
                     ks * kBBytes + (uint32_t)(j >> 2) * kBKatom + (uint32_t)(j & 3) * 32u;
                 const uint64_t ad = tc::smem_desc(st + koff, 16, 1024, tc::kLayout128B);
-                const uint64_t bd = tc::smem_desc(st + kOffB + kboff, 16, 1024, tc::kLayout128B);
+                // one token: SBO 0, the second 8-row group reads the first again
+                const uint64_t bd =
+                    tc::smem_desc(st + kOffB + kboff, 16, BR == 8 ? 0 : 1024, tc::kLayout128B);
                 tc::mma_mxf4(d, ad, bd, idesc, sfr + 32 * sb + 4 * j,
                              sfr + 32 * (NM * KS + ks) + 4 * j,
                              (kc == kb && ks == 0 && j == 0) ? 0u : 1u);
@@ -873,7 +881,7 @@ __global__ void __launch_bounds__(512) k_split_x(const uint16_t* __restrict__ x,
 template <int NMAX, int PH, int KS, bool ONE>
 cudaError_t launch_tc_n(const Maps& mp, FArgs f, cudaStream_t s, bool pdl) {
   static int configured[64] = {0};
-  constexpr size_t smem = Lay<NMAX, PH == 0 ? 2 : 1, KS>::kSmemBytes;
+  constexpr size_t smem = Lay<NMAX, PH == 0 ? 2 : 1, KS, ONE ? 8 : NMAX>::kSmemBytes;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !configured[dev]) {
@@ -926,18 +934,20 @@ cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, i
                               const float* gate, float* ybuf, float* part, int32_t* status,
                               cudaStream_t s, bool pdl, void (*between)(cudaStream_t),
                               const RouteOne* ro) {
+  // activation boxes: 8 rows for one routed token (its 4 term rows), else 16
+  const uint32_t brows = ro ? 8 : 16;
   const uint64_t P4 = (uint64_t)T * k * kTerms;
   Maps m0, m1;
   if (!make_map_2d(&m0.m[0], w.w1p, L / 2, (uint64_t)E * I, 128, 128, true) ||
       !make_map_2d(&m0.m[1], w.w1s, L / 32, (uint64_t)E * I, 16, 128, false) ||
       !make_map_2d(&m0.m[2], w.w3p, L / 2, (uint64_t)E * I, 128, 128, true) ||
       !make_map_2d(&m0.m[3], w.w3s, L / 32, (uint64_t)E * I, 16, 128, false) ||
-      !make_map_2d(&m0.m[4], xq, L / 2, P4, 128, 16, true) ||
-      !make_map_2d(&m0.m[5], xsf, L / 32, P4, 16, 16, false) ||
+      !make_map_2d(&m0.m[4], xq, L / 2, P4, 128, brows, true) ||
+      !make_map_2d(&m0.m[5], xsf, L / 32, P4, 16, brows, false) ||
       !make_map_2d(&m1.m[0], w.w2p, I / 2, (uint64_t)E * L, 128, 128, true) ||
       !make_map_2d(&m1.m[1], w.w2s, I / 32, (uint64_t)E * L, 16, 128, false) ||
-      !make_map_2d(&m1.m[4], act_q, I / 2, P4, 128, 16, true) ||
-      !make_map_2d(&m1.m[5], act_sf, I / 32, P4, 16, 16, false))
+      !make_map_2d(&m1.m[4], act_q, I / 2, P4, 128, brows, true) ||
+      !make_map_2d(&m1.m[5], act_sf, I / 32, P4, 16, brows, false))
     return cudaErrorInvalidValue;
   m1.m[2] = m1.m[0];
   m1.m[3] = m1.m[1];
