@@ -15,6 +15,7 @@ namespace {
 
 constexpr int kQuarters = 4;      // warps per row, each a quarter of the hidden width
 constexpr int kRpcFew = 2;        // router rows per CTA for one or two tokens
+constexpr int kTopkBlockMaxTokens = 1024;  // block-per-token top-k up to this batch
 constexpr int kVecPerLane = 8;    // 16-byte pieces a lane keeps in flight per batch
 
 // logits[t][e] = sum_i h[t][i] * wr[e][i].  A CTA holds 2 rows; each row is split into 4
@@ -224,6 +225,29 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits,
             gate + (size_t)t * k, gap ? gap + t : nullptr, threadIdx.x & 31);
 }
 
+// Batches up to kTopkBlockMaxTokens: one CTA of 11 warps per token, the block top-k of the
+// single-token path (topk_one_token: the keys at or above the (k+1)-th best list maximum,
+// sorted by one warp; the full sort when ties leave too many).  Same choice, order, tie
+// rule and gates as k_topk; E <= 1056, k <= 31 (or k == E).
+__global__ void __launch_bounds__(352) k_topk_block(const float* __restrict__ logits,
+                                                    const float* __restrict__ bias, int E, int k,
+                                                    int renorm, float routed_scale,
+                                                    int32_t* __restrict__ idx,
+                                                    float* __restrict__ gate,
+                                                    float* __restrict__ gap) {
+  __shared__ unsigned long long lists[11 * 32];
+  __shared__ float sig[1056];
+  pdl_wait();
+  pdl_launch();
+  const int t = blockIdx.x;
+  const OneTokenChoice c = topk_one_token<3>(logits + (size_t)t * E, bias, E, k, renorm,
+                                             routed_scale, gap ? gap + t : nullptr, lists, sig);
+  if (threadIdx.x < k) {
+    idx[(size_t)t * k + threadIdx.x] = c.e;
+    gate[(size_t)t * k + threadIdx.x] = c.g;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_router_logits(const uint16_t* h, const uint16_t* wr, int T, int E, int H,
@@ -263,6 +287,9 @@ cudaError_t launch_router_logits(const uint16_t* h, const uint16_t* wr, int T, i
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,
                         float routed_scale, int32_t* idx, float* gate, float* gap,
                         cudaStream_t s, bool pdl) {
+  if (T <= kTopkBlockMaxTokens && E <= 1056 && (k <= 31 || k == E))
+    return launch_kernel(k_topk_block, dim3(T), dim3(352), 0, s, pdl, logits, bias, E, k, renorm,
+                         routed_scale, idx, gate, gap);
   return launch_kernel(k_topk, dim3((T + 7) / 8), dim3(256), 0, s, pdl, logits, bias, T, E, k,
                        renorm, routed_scale, idx, gate, gap);
 }
