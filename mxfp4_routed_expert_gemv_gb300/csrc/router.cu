@@ -34,10 +34,6 @@ __global__ void __launch_bounds__(RPC * kQuarters * 32) k_router_logits(const ui
                                                        uint8_t* __restrict__ xq,
                                                        uint8_t* __restrict__ xsf,
                                                        int32_t* __restrict__ zero, int nzero) {
-  pdl_wait();
-  pdl_launch();
-  if (zero && blockIdx.x == 0 && blockIdx.y == 0)  // counters the next launches start from
-    for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
   __shared__ float part[RPC * kQuarters][TT];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * RPC + (warp >> 2);
@@ -46,6 +42,15 @@ __global__ void __launch_bounds__(RPC * kQuarters * 32) k_router_logits(const ui
   const int nvec = H >> 3;
   const int qn = (nvec + kQuarters - 1) / kQuarters;
   const int qb = q * qn, qe = min(nvec, qb + qn);
+  // The router weights are constants of the layer, not results of the preceding kernel: while
+  // that kernel drains, bring this warp's quarter row into L2 (a hint; the loads below come
+  // after the wait and read whatever memory holds then).
+  if (blockIdx.y == 0 && lane == 0 && e < E && qe > qb)
+    prefetch_l2_bulk(wr + (size_t)e * H + (size_t)qb * 8, (uint32_t)(qe - qb) * 16u);
+  pdl_wait();
+  pdl_launch();
+  if (zero && blockIdx.x == 0 && blockIdx.y == 0)  // counters the next launches start from
+    for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
   float a0[TT], a1[TT];
 #pragma unroll
   for (int tt = 0; tt < TT; ++tt) a0[tt] = a1[tt] = 0.f;

@@ -151,7 +151,7 @@ __device__ __forceinline__ void topk_block_sort(const float* lt, const float* bi
 //     lists, then the warps' lists merge pairwise in a tree through shared memory;
 //  3. warp 0 ends with the top 32 keys, best first: choice j < k on lane j, key k for the gap.
 // Needs k <= 31 (or k == E), E <= 32 * LPW * (warps); every thread calls it.  lists: shared
-// [warps * 32]; sig: shared [E] (each expert's unbiased score, for the gates).  On warp 0,
+// [max(warps * 32, 129)]; sig: shared [E] (each expert's unbiased score, for the gates).  On warp 0,
 // lane j < k returns choice j's expert e, gate g, and rank (its place among the chosen
 // experts in ascending index order); lane 0 writes the gap when gap is set.
 struct OneTokenChoice {
@@ -196,74 +196,77 @@ __device__ __forceinline__ OneTokenChoice topk_one_token(const float* lt, const 
   }
   // Fast path: the (k+1)-th best of the lists' maxima is a lower bound of the (k+1)-th best
   // key (k+1 lists each hold a key at least that good), so the keys at or above it contain
-  // the top k+1.  They are few (gathered in shared memory); warp 0 sorts at most 64 of them.
-  // More than 64 (many equal scores), or fewer lists than k+1: the full sort below.
+  // the top k+1.  They are few (gathered in shared memory), and each finds its place by
+  // counting the candidates that beat it: a few dependent steps, where a sort in one warp
+  // would chain twenty.  More than 64 (many equal scores), or fewer lists than k+1: the
+  // full sort below.
   const int nl = (E + 31) >> 5;
   unsigned long long acc = 0ull;
   bool fast = false;
   if (k + 1 <= nl && nl <= 32) {
     unsigned long long* lmax = lists;       // [32] best key of each list
     unsigned long long* cand = lists + 32;  // [64] candidates
-    unsigned int* ncand = reinterpret_cast<unsigned int*>(lists + 96);
+    unsigned long long* top = lists + 96;   // [32] the best candidates, best first
+    unsigned int* ncand = reinterpret_cast<unsigned int*>(lists + 128);
+    // each list's best key: the highest score (one max over the warp), then among the lanes
+    // holding it the lowest expert (the highest ~e)
     unsigned long long m[LPW];
 #pragma unroll
-    for (int j = 0; j < LPW; ++j) m[j] = key[j];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-      for (int j = 0; j < LPW; ++j) {
-        const unsigned long long x = __shfl_xor_sync(0xffffffffu, m[j], o);
-        m[j] = x > m[j] ? x : m[j];
-      }
+    for (int j = 0; j < LPW; ++j) {
+      const uint32_t hi = (uint32_t)(key[j] >> 32);
+      const uint32_t mh = __reduce_max_sync(0xffffffffu, hi);
+      const uint32_t ml = __reduce_max_sync(0xffffffffu, hi == mh ? (uint32_t)key[j] : 0u);
+      m[j] = ((unsigned long long)mh << 32) | ml;
+    }
     if (lane == 0)
 #pragma unroll
       for (int j = 0; j < LPW; ++j)
         if (warp * LPW + j < 32) lmax[warp * LPW + j] = m[j];
     if (threadIdx.x == 0) *ncand = 0u;
     __syncthreads();
-    if (warp == 0) {
-      const unsigned long long mine = lane < nl ? lmax[lane] : 0ull;
-      int rank = 0;
+    // every warp finds the threshold itself: the list maximum with exactly k better ones
+    // (keys are distinct, so exactly one lane has that rank)
+    const unsigned long long mine = lane < nl ? lmax[lane] : 0ull;
+    int rank = 0;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const unsigned long long x = __shfl_sync(0xffffffffu, mine, i);
-        rank += (i < nl && x > mine) ? 1 : 0;
-      }
-      if (lane < nl && rank == k) lists[97] = mine;
-    }
-    __syncthreads();
-    const unsigned long long th = lists[97];
+    for (int i = 0; i < 32; ++i) rank += (i < nl && lmax[i] > mine) ? 1 : 0;
+    const unsigned int who = __ballot_sync(0xffffffffu, lane < nl && rank == k);
+    const unsigned long long th = __shfl_sync(0xffffffffu, mine, __ffs(who) - 1);
+    // gather the keys at or above it: one shared-memory atomic per warp
+    unsigned int bal[LPW], cnt = 0u;
 #pragma unroll
     for (int j = 0; j < LPW; ++j) {
-      const bool in = key[j] >= th;
-      const unsigned int bal = __ballot_sync(0xffffffffu, in);
-      unsigned int base = 0u;
-      if (lane == 0 && bal) base = atomicAdd(ncand, (unsigned int)__popc(bal));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      const unsigned int pos = base + __popc(bal & ((1u << lane) - 1u));
-      if (in && pos < 64u) cand[pos] = key[j];
+      bal[j] = __ballot_sync(0xffffffffu, key[j] >= th);
+      cnt += __popc(bal[j]);
+    }
+    unsigned int base = 0u;
+    if (lane == 0 && cnt) base = atomicAdd(ncand, cnt);
+    base = __shfl_sync(0xffffffffu, base, 0);
+#pragma unroll
+    for (int j = 0; j < LPW; ++j) {
+      const unsigned int pos = base + __popc(bal[j] & ((1u << lane) - 1u));
+      if (((bal[j] >> lane) & 1u) && pos < 64u) cand[pos] = key[j];
+      base += __popc(bal[j]);
     }
     __syncthreads();
     const unsigned int nc = *ncand;
     if (nc <= 64u) {
       fast = true;
-      if (warp == 0) {
-        unsigned long long a0 = lane < (int)nc ? cand[lane] : 0ull;
-        unsigned long long a1 = lane + 32 < (int)nc ? cand[lane + 32] : 0ull;
+      // candidate i's place = how many candidates beat it (distinct keys: a permutation);
+      // threads 0..nc-1 count side by side, reading the list by broadcast
+      if (threadIdx.x < nc) {
+        const unsigned long long ci = cand[threadIdx.x];
+        int r = 0;
+#pragma unroll 1
+        for (unsigned int j0 = 0; j0 < nc; j0 += 8) {
 #pragma unroll
-        for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-          for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const bool desc = (lane & size) == 0, lo = (lane & stride) == 0;
-            const unsigned long long o0 = __shfl_xor_sync(0xffffffffu, a0, stride);
-            const unsigned long long o1 = __shfl_xor_sync(0xffffffffu, a1, stride);
-            a0 = (lo == desc) ? (a0 > o0 ? a0 : o0) : (a0 > o0 ? o0 : a0);
-            a1 = (lo == desc) ? (a1 > o1 ? a1 : o1) : (a1 > o1 ? o1 : a1);
-          }
+          for (unsigned int jj = 0; jj < 8; ++jj)
+            r += (j0 + jj < nc && cand[j0 + jj] > ci) ? 1 : 0;
         }
-        const unsigned long long o = __shfl_sync(0xffffffffu, a1, 31 - lane);
-        acc = top32_clean(a0 > o ? a0 : o, lane);
+        if (r < 32) top[r] = ci;
       }
+      __syncthreads();
+      if (warp == 0) acc = lane < (int)nc ? top[lane] : 0ull;
     }
     __syncthreads();  // the full path below reuses the scratch
   }
