@@ -55,14 +55,17 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
 constexpr int kTcTokTile = 16;
 constexpr int kTcMaxGrid = 160;
 // Flags of the tensor-core path, zeroed before each call: [0, kTcMaxGrid) parts of the first
-// GEMM's shared tiles written, [kTcMaxGrid, 2 kTcMaxGrid) the same for the second GEMM,
-// [kTcRouteFlag] the single-token routing published by the first GEMM.
-constexpr int kTcRouteFlag = 2 * kTcMaxGrid;
-constexpr int kTcFlags = 2 * kTcMaxGrid + 1;
+// GEMM's shared tiles written, [kTcMaxGrid, 2 kTcMaxGrid) the same for the second GEMM.
+constexpr int kTcFlags = 2 * kTcMaxGrid;
 // One routed token: after the flags, per 128-row tile of y, the slots written so far (the
 // second GEMM sums the token's slots into y where the count completes; L <= 4096).
 constexpr int kTcYCount = kTcFlags;
-constexpr int kTcFlagWords = kTcFlags + 4096 / 128;
+// Then (8-byte aligned) the single-token routing as one 64-bit word per chosen expert, in
+// ascending expert order: gate bits << 32 | 1 << 31 | choice index << 16 | expert.  A word
+// is its own ready flag (zeroed words have bit 31 clear).
+constexpr int kTcRouteTable = kTcYCount + 4096 / 128;
+static_assert(kTcRouteTable % 2 == 0, "route table alignment");
+constexpr int kTcFlagWords = kTcRouteTable + 2 * 32;
 
 // bucket.cu
 struct BucketOut {

@@ -92,16 +92,15 @@ struct FArgs {
   int ph;                  // 0: w1, w3 -> act terms; 1: w2 -> gate * o
   int one_token;           // T == 1: phase-0 activation rows are 0 .. kTerms-1
   // route_one: one token, no preparation launch.  Phase-0 CTAs each route the token from the
-  // router's logits; CTA 0 publishes idx, gate, gap, the tile table (tiles_out, perm_out)
-  // and then route_flag; phase-1 CTAs read the published table.
+  // router's logits; CTA 0 publishes idx, gate, gap and the route words; phase-1 CTAs read
+  // the route words.
   int route_one;
   const float *logits, *bias;
   int E, renorm;
   float routed_scale;
   int32_t* idx_out;
   float *gate_out, *gap_out;
-  int4* tiles_out;
-  int32_t *perm_out, *route_flag;
+  unsigned long long* route_words;  // [k] the routing, one self-flagged word per expert
   float* y;                // one routed token: y [L], summed by the second GEMM
   int32_t* ycount;         // [L / 128] slots written per 128-row tile of y (zeroed)
   int k, L, I, act_kind;
@@ -204,8 +203,9 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
 
 // One token's routing for an expert-GEMM CTA (every thread calls it).  Phase 0: the CTA
 // routes the token itself from the router's logits (the ring, free until the producers
-// start, is the scratch); CTA 0 also publishes the result and then the route flag.  Phase 1:
-// the table CTA 0 of phase 0 published, after its flag.  Out (shared): tiles[i] =
+// start, is the scratch); CTA 0 also publishes the result, the routing as one self-flagged
+// 64-bit word per expert (no fence: each word carries its own ready bit).  Phase 1: the
+// words CTA 0 of phase 0 published, one load each once written.  Out (shared): tiles[i] =
 // (expert, i, 1) for the chosen experts in ascending order, perm[i] = the choice index of
 // tile i, gate[j] = gate of choice j.  Returns the number of token groups (0 after a timeout).
 template <int PH>
@@ -225,29 +225,33 @@ __device__ __forceinline__ int route_one_token(const FArgs& f, uint8_t* scratch,
         if (publish) {
           f.idx_out[lane] = c.e;
           f.gate_out[lane] = c.g;
-          f.tiles_out[c.rank] = make_int4(c.e, c.rank, 1, 0);
-          f.perm_out[c.rank] = lane;
-        }
-      }
-      if (publish) {
-        __syncwarp();
-        if (lane == 0) {
-          __threadfence();
-          st_release(f.route_flag, 1);
+          const unsigned long long w =
+              ((unsigned long long)__float_as_uint(c.g) << 32) |
+              (0x80000000u | ((uint32_t)lane << 16) | (uint32_t)c.e);
+          asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(f.route_words + c.rank),
+                       "l"(w)
+                       : "memory");
         }
       }
       if (lane == 0) ngroups = k;
     }
   } else if (warp == 0) {
-    int got = 0;
-    for (uint32_t q = 0; q < kWaitPolls && !got; ++q) {
-      got = ld_acquire(f.route_flag) == 1;
-      if (!got) __nanosleep(64);
+    // lane i: the word of the i-th chosen expert (ascending index), polled until written
+    unsigned long long w = 0ull;
+    if (lane < k) {
+      for (uint32_t q = 0; q < kWaitPolls; ++q) {
+        asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(f.route_words + lane)
+                     : "memory");
+        if (w & 0x80000000ull) break;
+        __nanosleep(64);
+      }
     }
+    const bool got = __all_sync(0xffffffffu, lane >= k || (w & 0x80000000ull) != 0ull);
     if (got && lane < k) {
-      tiles[lane] = __ldcg(f.tiles_out + lane);
-      perm[lane] = __ldcg(f.perm_out + lane);
-      gate[lane] = __ldcg(f.gate_out + lane);
+      const int e = (int)(w & 0xFFFFu), j = (int)((w >> 16) & 0x7FFFu);
+      tiles[lane] = make_int4(e, lane, 1, 0);
+      perm[lane] = j;
+      gate[j] = __uint_as_float((uint32_t)(w >> 32));
     }
     if (lane == 0) {
       ngroups = got ? k : 0;
@@ -968,7 +972,7 @@ cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, i
     f.logits = ro->logits; f.bias = ro->bias; f.E = E;
     f.renorm = ro->renorm; f.routed_scale = ro->routed_scale;
     f.idx_out = ro->idx; f.gate_out = ro->gate; f.gap_out = ro->gap;
-    f.tiles_out = b.tiles; f.perm_out = b.perm; f.route_flag = b.flags + kTcRouteFlag;
+    f.route_words = reinterpret_cast<unsigned long long*>(b.flags + kTcRouteTable);
     f.y = ro->y; f.ycount = b.flags + kTcYCount;
   }
   // phase 0 (w1, w3), then phase 1 (w2): the second launch reads what the first wrote, across
