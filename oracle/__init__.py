@@ -100,6 +100,13 @@ def lib() -> ctypes.CDLL:
         L.k3o_experts.argtypes = [ctypes.POINTER(_Cfg), ctypes.POINTER(_Expert), i, vp, vp, vp, i, vp]
         L.k3o_rmsnorm.restype = None
         L.k3o_rmsnorm.argtypes = [vp, vp, i, ctypes.c_double]
+        L.k3o_rmsnorm_w.restype = None
+        L.k3o_rmsnorm_w.argtypes = [vp, vp, vp, i, ctypes.c_double]
+        L.k3o_matvec_bf16.restype = None
+        L.k3o_matvec_bf16.argtypes = [vp, vp, vp, i, i]
+        L.k3o_latent_moe.restype = i
+        L.k3o_latent_moe.argtypes = [ctypes.POINTER(_Cfg), ctypes.POINTER(_Latent), vp, vp, vp,
+                                     ctypes.POINTER(_Expert), i, i, vp, vp, vp]
         L.k3o_threads.restype, L.k3o_threads.argtypes = i, []
         _lib = L
     return _lib
@@ -302,6 +309,81 @@ def stack_link(y: np.ndarray, norm: bool, eps: float = 1e-5):
     xb = bf16_from_f32(v)
     hb = np.concatenate([xb, xb], axis=1)
     return xb, hb
+
+
+def rmsnorm_w(x: np.ndarray, w: Optional[np.ndarray], eps: float) -> np.ndarray:
+    """x / sqrt(mean(x^2) + eps) * w (w fp32, or None for unit weight), fp64."""
+    x = _c(x, np.float64, name="x")
+    wv = None if w is None else _c(w, np.float32, (x.size,), "w")
+    out = np.empty_like(x)
+    lib().k3o_rmsnorm_w(_ptr(out), _ptr(x), _ptr(wv), x.size, float(eps))
+    return out
+
+
+def matvec_bf16(x: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """y[r] = sum_c W[r, c] x[c] in fp64; W: bf16 bits [rows, in]."""
+    W = _c(W, np.uint16, name="W")
+    rows, n = W.shape
+    x = _c(x, np.float64, (n,), "x")
+    y = np.empty(rows, dtype=np.float64)
+    lib().k3o_matvec_bf16(_ptr(y), _ptr(x), _ptr(W), n, rows)
+    return y
+
+
+@dataclasses.dataclass
+class LatentWeights:
+    """The LatentMoE wrapper's dense tensors (bf16 bits unless noted): down [L, H], up [H, L],
+    norm_w fp32 [L] or None, sh1/sh3 [n_shared*I, H], sh2 [H, n_shared*I]."""
+    down: np.ndarray
+    up: np.ndarray
+    norm_w: Optional[np.ndarray] = None
+    latent_norm: bool = True
+    rms_eps: float = 1e-5
+    n_shared: int = 0
+    sh1: Optional[np.ndarray] = None
+    sh3: Optional[np.ndarray] = None
+    sh2: Optional[np.ndarray] = None
+
+
+class _Latent(ctypes.Structure):
+    _fields_ = [("down", ctypes.c_void_p), ("up", ctypes.c_void_p), ("norm_w", ctypes.c_void_p),
+                ("latent_norm", ctypes.c_int), ("rms_eps", ctypes.c_double),
+                ("n_shared", ctypes.c_int), ("sh1", ctypes.c_void_p), ("sh3", ctypes.c_void_p),
+                ("sh2", ctypes.c_void_p)]
+
+
+def latent_moe(cfg: Cfg, lw: LatentWeights, h: np.ndarray, wr: np.ndarray,
+               bias: Optional[np.ndarray], table: Mapping[int, ExpertBytes]):
+    """The LatentMoE layer (README Part II section 9, k3_moe) for T tokens, fp64.
+
+    h: bf16 bits [T, H].  Returns (out fp64 [T, H], idx [T, k], gate [T, k])."""
+    T = h.shape[0]
+    H, L, SI = cfg.hidden, cfg.latent, cfg.inter * lw.n_shared
+    h = _c(h, np.uint16, (T, H), "h")
+    wr = _c(wr, np.uint16, (cfg.n_experts, H), "wr")
+    bias = None if bias is None else _c(bias, np.float32, (cfg.n_experts,), "bias")
+    keep = [_c(lw.down, np.uint16, (L, H), "down"), _c(lw.up, np.uint16, (H, L), "up"),
+            None if lw.norm_w is None else _c(lw.norm_w, np.float32, (L,), "norm_w")]
+    if lw.n_shared > 0:
+        keep += [_c(lw.sh1, np.uint16, (SI, H), "sh1"), _c(lw.sh3, np.uint16, (SI, H), "sh3"),
+                 _c(lw.sh2, np.uint16, (H, SI), "sh2")]
+    else:
+        keep += [None, None, None]
+    st = _Latent(_ptr(keep[0]), _ptr(keep[1]), _ptr(keep[2]), int(bool(lw.latent_norm)),
+                 float(lw.rms_eps), int(lw.n_shared), _ptr(keep[3]), _ptr(keep[4]), _ptr(keep[5]))
+    checked = {int(e): ex.checked(cfg) for e, ex in table.items()}
+    arr = (_Expert * cfg.n_experts)()
+    for e, ex in checked.items():
+        arr[e] = _expert_struct(ex)
+    out = np.empty((T, H), dtype=np.float64)
+    idx = np.empty((T, cfg.topk), dtype=np.int32)
+    gate = np.empty((T, cfg.topk), dtype=np.float64)
+    c = cfg.c()
+    rc = lib().k3o_latent_moe(ctypes.byref(c), ctypes.byref(st), _ptr(h), _ptr(wr), _ptr(bias),
+                              arr, cfg.n_experts, T, _ptr(idx), _ptr(gate), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"k3o_latent_moe failed with code {rc}")
+    return out, idx, gate
 
 
 def threads() -> int:

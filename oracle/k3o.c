@@ -244,10 +244,79 @@ int k3o_experts(const k3o_cfg *c, const k3o_expert *table, int n_table, const ui
 
 void k3o_rmsnorm(double *out, const double *x, int n, double eps)
 {
+    k3o_rmsnorm_w(out, x, NULL, n, eps);
+}
+
+void k3o_rmsnorm_w(double *out, const double *x, const float *w, int n, double eps)
+{
     double ss = 0.0;
     for (int i = 0; i < n; i++) ss += x[i] * x[i];
     const double inv = 1.0 / sqrt(ss / (double)n + eps);
-    for (int i = 0; i < n; i++) out[i] = x[i] * inv;
+    for (int i = 0; i < n; i++) out[i] = x[i] * inv * (w ? (double)w[i] : 1.0);
+}
+
+/* ---- the LatentMoE wrapper (README Part II section 9, k3_moe) ----------------------- */
+
+void k3o_matvec_bf16(double *y, const double *x, const uint16_t *W, int in, int rows)
+{
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (int r = 0; r < rows; r++) {
+        const uint16_t *wr = W + (size_t)r * in;
+        double acc = 0.0;
+        for (int c = 0; c < in; c++) acc += k3o_bf16_value(wr[c]) * x[c];
+        y[r] = acc;
+    }
+}
+
+int k3o_latent_moe(const k3o_cfg *c, const k3o_latent *lw, const uint16_t *h,
+                   const uint16_t *wr, const float *bias, const k3o_expert *table, int n_table,
+                   int T, int32_t *idx, double *gate, double *out)
+{
+    if (!c || !lw || !h || !wr || !table || !idx || !gate || !out || T < 0) return K3O_ERR_ARG;
+    if (!lw->down || !lw->up || lw->n_shared < 0) return K3O_ERR_ARG;
+    if (lw->n_shared > 0 && (!lw->sh1 || !lw->sh3 || !lw->sh2)) return K3O_ERR_ARG;
+    const int H = c->hidden, L = c->latent, SI = c->inter * lw->n_shared;
+    int rc = k3o_route(c, h, wr, bias, T, idx, gate, NULL, NULL, NULL);
+    if (rc != K3O_OK) return rc;
+    const size_t nh = (size_t)H, nl = (size_t)L, ns = (size_t)(SI > 0 ? SI : 1);
+    double *hd = malloc(nh * sizeof *hd), *zd = malloc(nl * sizeof *zd);
+    double *acc = malloc(nl * sizeof *acc), *a = malloc(nl * sizeof *a);
+    double *g = malloc(ns * sizeof *g), *u = malloc(ns * sizeof *u), *act = malloc(ns * sizeof *act);
+    double *o = malloc(nh * sizeof *o);
+    uint16_t *zb = malloc(nl * sizeof *zb);
+    if (!hd || !zd || !acc || !a || !g || !u || !act || !o || !zb) {
+        rc = K3O_ERR_NOMEM;
+        goto done;
+    }
+    for (int t = 0; t < T && rc == K3O_OK; t++) {
+        const uint16_t *ht = h + (size_t)t * H;
+        for (int i = 0; i < H; i++) hd[i] = k3o_bf16_value(ht[i]);
+        /* down-projection into the latent, rounded to the experts' bf16 input */
+        k3o_matvec_bf16(zd, hd, lw->down, H, L);
+        for (int i = 0; i < L; i++) zb[i] = k3o_bf16_from_f32((float)zd[i]);
+        /* the routed experts on z, with this token's choice and gates */
+        rc = k3o_experts(c, table, n_table, zb, idx + (size_t)t * c->topk,
+                         gate + (size_t)t * c->topk, 1, acc);
+        if (rc != K3O_OK) break;
+        /* the aggregate's norm, then back up to full width */
+        if (lw->latent_norm) k3o_rmsnorm_w(a, acc, lw->norm_w, L, lw->rms_eps);
+        else memcpy(a, acc, nl * sizeof *a);
+        double *ot = out + (size_t)t * H;
+        k3o_matvec_bf16(ot, a, lw->up, L, H);
+        /* shared experts on the full-width input, added unweighted */
+        if (SI > 0) {
+            k3o_matvec_bf16(g, hd, lw->sh1, H, SI);
+            k3o_matvec_bf16(u, hd, lw->sh3, H, SI);
+            k3o_activation(c, g, u, act, SI);
+            k3o_matvec_bf16(o, act, lw->sh2, SI, H);
+            for (int i = 0; i < H; i++) ot[i] += o[i];
+        }
+    }
+done:
+    free(hd); free(zd); free(acc); free(a); free(g); free(u); free(act); free(o); free(zb);
+    return rc;
 }
 
 int k3o_threads(void)

@@ -108,6 +108,44 @@ int k3o_experts(const k3o_cfg *c, const k3o_expert *table, int n_table, const ui
  * (README section 5): out = x / sqrt(mean(x^2) + eps). */
 void k3o_rmsnorm(double *out, const double *x, int n, double eps);
 
+/* RMSNorm with a per-element weight (NULL: unit weight), eps inside the square root, fp64
+ * throughout (README section 5): out[i] = x[i] / sqrt(mean(x^2) + eps) * w[i]. */
+void k3o_rmsnorm_w(double *out, const double *x, const float *w, int n, double eps);
+
+/* Dense mat-vec with bf16 weights W[rows][in] (row-major): y[r] = sum_c W[r][c] x[c], fp64.
+ * The README's dense matmul of the LatentMoE wrapper (section 9, k3_moe's k3_mmw). */
+void k3o_matvec_bf16(double *y, const double *x, const uint16_t *W, int in, int rows);
+
+/* The dense tensors of the LatentMoE wrapper around the routed experts (README Part II
+ * section 9, k3_moe), bf16 row-major unless noted:
+ *   down [latent][hidden]     z = down . h          (routed experts run on z)
+ *   up   [hidden][latent]     out = up . norm(acc)  (acc = the routed-expert sum)
+ *   norm_w [latent] fp32 or NULL (unit); latent_norm = 1 applies the RMSNorm to acc
+ *   sh1, sh3 [n_shared*inter][hidden], sh2 [hidden][n_shared*inter]: the shared experts,
+ *   on the full-width h, added unweighted; n_shared = 0 for none. */
+typedef struct k3o_latent {
+    const uint16_t *down, *up;
+    const float *norm_w;
+    int latent_norm;
+    double rms_eps;
+    int n_shared;
+    const uint16_t *sh1, *sh3, *sh2;
+} k3o_latent;
+
+/* The LatentMoE layer for T tokens, per token t (README Part II section 9, k3_moe):
+ *   route on h[t] (k3o_route: idx, gate);
+ *   z = bf16(down . h[t])                  (the latent enters the experts as bf16: the
+ *                                           library's expert input type; fp64 -> fp32 ->
+ *                                           bf16 round to nearest even);
+ *   acc = sum_j gate_j FFN_{idx_j}(z)      (k3o_experts);
+ *   a = latent_norm ? rmsnorm_w(acc) : acc;
+ *   out[t] = up . a  +  sh2 . act(sh1 . h[t], sh3 . h[t])   (act: cfg->act, as the experts).
+ * h is bf16 [T][hidden]; out fp64 [T][hidden]; idx [T][k], gate [T][k] are written.
+ * Returns K3O_OK, K3O_ERR_ARG, K3O_ERR_MISSING_EXPERT or K3O_ERR_NOMEM. */
+int k3o_latent_moe(const k3o_cfg *c, const k3o_latent *lw, const uint16_t *h,
+                   const uint16_t *wr, const float *bias, const k3o_expert *table, int n_table,
+                   int T, int32_t *idx, double *gate, double *out);
+
 /* Number of OpenMP threads the oracle will use (1 when built without OpenMP). */
 int k3o_threads(void);
 

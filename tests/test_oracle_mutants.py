@@ -3,8 +3,10 @@
 Every mutant is a one-line change to a temporary copy of ``oracle/k3o.c``: a swapped
 nibble order, an off-by-one exponent bias, a flipped tie rule, gates taken from the biased
 score, a dropped renormalisation, a dropped group, gate and up swapped in SwiGLU, w1 and w3
-swapped, a transposed activation operand.  ``tests/test_oracle_pins.py`` runs against each
-mutant in a subprocess and must fail.  The oracle itself is never modified.
+swapped, a transposed activation operand, and in the LatentMoE wrapper a dropped norm
+weight, a transposed dense mat-vec, a mis-rounded latent, a skipped aggregate norm, weighted
+or swapped shared experts.  ``tests/test_oracle_pins.py`` and ``tests/test_oracle_latent.py``
+run against each mutant in a subprocess and must fail.  The oracle itself is never modified.
 """
 import os
 import shutil
@@ -30,6 +32,12 @@ MUTANTS = {
     "bias_ignored": ("ch[te] = sc[te] + (bias ? (double)bias[e] : 0.0);", "ch[te] = sc[te];"),
     "situ_capped_sigmoid": ("tanh(g[i] / c->situ_b1) * sigmoid(g[i])", "tanh(g[i] / c->situ_b1) * sigmoid(tanh(g[i]))"),
     "rmsnorm_eps_outside": ("1.0 / sqrt(ss / (double)n + eps)", "1.0 / (sqrt(ss / (double)n) + eps)"),
+    "rmsnorm_weight_dropped": ("x[i] * inv * (w ? (double)w[i] : 1.0)", "x[i] * inv"),
+    "matvec_bf16_transposed": ("k3o_bf16_value(wr[c]) * x[c]", "k3o_bf16_value(W[(size_t)c * rows + r]) * x[c]"),
+    "latent_z_misrounded": ("k3o_bf16_from_f32((float)zd[i])", "k3o_bf16_from_f32((float)(zd[i] * 1.0078125))"),
+    "latent_norm_skipped": ("if (lw->latent_norm) k3o_rmsnorm_w", "if (0) k3o_rmsnorm_w"),
+    "latent_shared_weighted": ("for (int i = 0; i < H; i++) ot[i] += o[i];", "for (int i = 0; i < H; i++) ot[i] += 0.5 * o[i];"),
+    "latent_shared_gate_is_up": ("k3o_matvec_bf16(g, hd, lw->sh1, H, SI);", "k3o_matvec_bf16(g, hd, lw->sh3, H, SI);"),
 }
 
 
@@ -47,6 +55,7 @@ def test_pins_reject_mutant(name, tmp_path):
                     str(d / "k3o.c"), "-o", lib, "-lm"], check=True)
     env = dict(os.environ, K3O_LIB=lib)
     r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_latent.py"),
                         "-x", "-q", "-p", "no:cacheprovider"], cwd=ROOT, env=env,
                        capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
