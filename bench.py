@@ -473,6 +473,126 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def latent_dense_bytes(w: synth.Workload, n_shared: int) -> int:
+    """Bytes the LatentMoE wrapper adds per token at decode: down and up (bf16 L x H each),
+    the shared experts' sh1, sh3 (S x H) and sh2 (H x S) in bf16, the norm weight."""
+    S = n_shared * w.inter
+    return 2 * (2 * w.latent * w.hidden) + 2 * (3 * S * w.hidden) + 4 * w.latent
+
+
+def run_latent(args):
+    """The LatentMoE layer around the routed experts (route on h, routed experts on the
+    bf16 latent z = down . h, RMSNorm of their sum, up-projection, shared experts on h):
+    an extra bench line for that wrapper, timed like the main line (graph replay over
+    rotated expert layers, one set of dense weights: 367 MB per step, far above L2)."""
+    import torch
+    import mxfp4_routed_expert_gemv_gb300 as k3
+
+    rank, world, local = dist_env()
+    if world > 1:
+        raise SystemExit("--latent runs on one GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = synth.WORKLOADS[args.workload]
+    if w.T != 1 or w.layers != 1:
+        raise SystemExit("--latent times the one-token decode workload")
+    NL = max(1, args.layers)
+    cfg = k3.Cfg(hidden=w.hidden, n_experts=w.E, topk=w.k, latent=w.latent, inter=w.inter,
+                 routed_scale=w.routed_scale)
+    experts_l = [k3.Experts.from_dict(synth.experts_device(w, l, dev)) for l in range(NL)]
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    lw = synth.latent_weights(w, 0, n_shared=args.n_shared)
+    S = args.n_shared
+    lat = k3.Latent(down=bf16(lw.down), up=bf16(lw.up), latent_norm_w=torch.from_numpy(lw.norm_w).to(dev),
+                    latent_norm=True, rms_eps=1e-5, n_shared=S,
+                    sh1=bf16(lw.sh1) if S else None, sh3=bf16(lw.sh3) if S else None,
+                    sh2=bf16(lw.sh2) if S else None)
+    rotation = ((args.rotation + NL - 1) // NL) * NL
+    lis = [synth.layer_inputs(w, l, T=rotation) for l in range(NL)]
+    H = torch.stack([bf16(lis[r % NL].h[r:r + 1]) for r in range(rotation)])
+    wr_l = [bf16(li_.wr) for li_ in lis]
+    bias_l = [torch.from_numpy(li_.bias).to(dev) for li_ in lis]
+    ws = k3.latent_workspace(cfg, lat, 1, dev)
+    out = torch.empty((1, w.hidden), dtype=torch.float32, device=dev)
+    idx = torch.empty((rotation, 1, w.k), dtype=torch.int32, device=dev)
+    status = torch.zeros(4, dtype=torch.int32, device=dev)
+
+    def step(i):
+        r = i % rotation
+        l = r % NL
+        k3.k3moe_latent_layer(cfg, lat, H[r], wr_l[l], bias_l[l], experts_l[l], out, idx[r], None,
+                              None, status, ws)
+
+    n0 = k3.k3moe_launch_count()
+    step(0)
+    launches_per_step = k3.k3moe_launch_count() - n0
+    for i in range(1, args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    cap_stream = torch.cuda.Stream(dev)
+
+    def capture(n_steps):
+        g = torch.cuda.CUDAGraph()
+        cap_stream.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.graph(g, stream=cap_stream):
+            for i in range(n_steps):
+                step(i)
+        torch.cuda.current_stream(dev).wait_stream(cap_stream)
+        return g
+
+    full = capture(rotation)
+    rem = args.steps % rotation
+    tail = capture(rem) if rem else None
+    for _ in range(2):
+        full.replay()
+    torch.cuda.synchronize(dev)
+    distinct = float(np.mean([len(set(idx[r].reshape(-1).tolist())) for r in range(rotation)]))
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps // rotation):
+            full.replay()
+        if tail is not None:
+            tail.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    elapsed = e0.elapsed_time(e1) / 1e3
+    st = status.cpu().numpy()
+    if st[0] or st[1]:
+        raise SystemExit(f"device status reports dropped={st[0]} timeouts={st[1]}")
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = json.load(open(peaks_path)) if os.path.exists(peaks_path) else {}
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or 6800.0
+    lb = layer_bytes(w, distinct, 1) + latent_dense_bytes(w, S)
+    achieved = lb * args.steps / elapsed / 1e9
+    line = {
+        "metric": METRIC, "value": args.steps / elapsed, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "routed experts e2m1 x e2m1 (tcgen05 kind::mxf4); dense bf16 x bf16/fp32, fp32 accumulation",
+        "data": "synthetic",
+        "config": {"workload": f"LatentMoE layer (down, routed experts, norm, up, {S} shared experts): "
+                               f"{w.name}",
+                   "tokens_per_step_per_gpu": 1, "hidden": w.hidden, "latent": w.latent,
+                   "inter": w.inter, "n_shared": S, "distinct_experts_per_step": distinct,
+                   "algorithmic_bytes_per_step": lb, "layers_rotated": NL,
+                   "l2": f"inputs larger than L2: {lb / 1e6:.0f} MB per step; expert layers rotated",
+                   "launch": "CUDA graph replay, programmatic dependent launch between kernels"},
+        "roofline": {"bound": "hbm", "kernel": "the whole layer (six launches)", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} hbm_gbs", "traffic": None},
+        "gpu_launches": int(launches_per_step * args.steps),
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -486,11 +606,16 @@ def main():
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count (small-memory profiling variant, not a bench line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--latent", action="store_true",
+                    help="time the LatentMoE wrapper layer instead (an extra line, not the headline)")
+    ap.add_argument("--n-shared", type=int, default=2)
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.latent:
+        run_latent(args)
     else:
         run_ours(args)
 

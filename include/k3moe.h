@@ -161,6 +161,43 @@ int k3moe_matvec_mxfp4(float *y, const void *x, const uint8_t *packed, const uin
 int k3moe_stack_link(const float *y, int32_t T, int32_t L, int32_t norm, float eps,
                      void *x_out, void *h_out, void *stream);
 
+/* The LatentMoE wrapper's dense tensors around the routed experts (README Part II section
+ * 9, k3_moe).  Device pointers, bf16 row-major unless noted, each 16-byte aligned; the
+ * caller owns them:
+ *   down [latent][hidden]      z = down . h, the experts' latent input (rounded to bf16);
+ *   up   [hidden][latent]      out = up . a, a = the routed sum after its RMSNorm;
+ *   latent_norm_w fp32 [latent], or NULL for unit weight; latent_norm 1 applies the RMSNorm
+ *   (fp64 sum of squares, eps = rms_eps inside the square root, README section 5), 0 skips;
+ *   sh1, sh3 [n_shared*inter][hidden] and sh2 [hidden][n_shared*inter]: the shared experts,
+ *   on the full-width h, with the layer's activation, added unweighted; n_shared 0: none
+ *   (the three pointers are then ignored). */
+typedef struct k3moe_latent {
+  const void *down, *up;
+  const float *latent_norm_w;
+  int32_t latent_norm;
+  float rms_eps;
+  int32_t n_shared;
+  const void *sh1, *sh3, *sh2;
+} k3moe_latent;
+
+/* Device workspace bytes of k3moe_latent_layer for T tokens: k3moe_workspace_size's plus
+ * the latent z, the routed sum and its norm, and the shared experts' activations. */
+int k3moe_latent_workspace_size(const k3moe_cfg *cfg, const k3moe_latent *lat, int32_t T,
+                                size_t *bytes);
+
+/* The LatentMoE layer for T tokens (README Part II section 9, k3_moe), per token:
+ *   route on h (idx, gate, gap as k3moe_layer: each may be NULL);
+ *   z = bf16(down . h); acc = sum_j gate_j FFN_{idx_j}(z)  (the routed experts, as
+ *   k3moe_layer with x = z);
+ *   out = up . (latent_norm ? rmsnorm(acc) * latent_norm_w : acc)
+ *         + sh2 . act(sh1 . h, sh3 . h).
+ *   h: bf16 [T][hidden]; out: fp32 [T][hidden] (out, fully written); other arguments and
+ *   errors as k3moe_layer.  T is at most 262140.  Enqueues six launches on the stream. */
+int k3moe_latent_layer(const k3moe_cfg *cfg, const k3moe_latent *lat, const void *h,
+                       const void *wr, const float *bias, const k3moe_experts *experts,
+                       int32_t T, float *out, int32_t *idx, float *gate, float *gap,
+                       int32_t *status, void *ws, size_t ws_bytes, void *stream);
+
 /* k3moe_layer for callers that cannot allocate device memory.  No counterpart on the
  * pages: this is a deployment variant, not part of the method.
  *

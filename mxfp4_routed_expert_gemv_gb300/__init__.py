@@ -25,13 +25,14 @@ __all__ = [
     "k3moe_layer", "k3moe_layer_host", "k3moe_matvec_mxfp4", "k3moe_stack_link",
     "k3moe_launch_count", "k3moe_strerror", "k3moe_abi_version", "k3moe_set_phase_events",
     "k3moe_layer_static_scratch", "STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
+    "Latent", "k3moe_latent_workspace_size", "latent_workspace", "k3moe_latent_layer",
 ]
 
 EXPORTED_SYMBOLS = (
     "k3moe_workspace_size", "k3moe_workspace_size_host", "k3moe_route", "k3moe_experts_mxfp4",
     "k3moe_layer", "k3moe_layer_host", "k3moe_matvec_mxfp4", "k3moe_stack_link",
     "k3moe_launch_count", "k3moe_strerror", "k3moe_abi_version", "k3moe_set_phase_events",
-    "k3moe_layer_static_scratch",
+    "k3moe_layer_static_scratch", "k3moe_latent_workspace_size", "k3moe_latent_layer",
 )
 
 # Capacity of the library's file-scope scratch array (K3MOE_STATIC_SCRATCH_BYTES).
@@ -104,6 +105,34 @@ class Experts:
         return cls(d["w1p"], d["w1s"], d["w3p"], d["w3s"], d["w2p"], d["w2s"])
 
 
+class _CLatent(ctypes.Structure):
+    _fields_ = [("down", ctypes.c_void_p), ("up", ctypes.c_void_p),
+                ("latent_norm_w", ctypes.c_void_p), ("latent_norm", ctypes.c_int32),
+                ("rms_eps", ctypes.c_float), ("n_shared", ctypes.c_int32),
+                ("sh1", ctypes.c_void_p), ("sh3", ctypes.c_void_p), ("sh2", ctypes.c_void_p)]
+
+
+@dataclasses.dataclass
+class Latent:
+    """The LatentMoE wrapper's dense tensors (torch, device; bf16 unless noted):
+    down [L, H], up [H, L], latent_norm_w fp32 [L] or None, sh1/sh3 [n_shared*I, H],
+    sh2 [H, n_shared*I] (None when n_shared == 0)."""
+
+    down: "object"
+    up: "object"
+    latent_norm_w: "object" = None
+    latent_norm: bool = True
+    rms_eps: float = 1e-5
+    n_shared: int = 0
+    sh1: "object" = None
+    sh3: "object" = None
+    sh2: "object" = None
+
+    def c(self) -> _CLatent:
+        return _CLatent(_p(self.down), _p(self.up), _p(self.latent_norm_w), int(bool(self.latent_norm)),
+                        float(self.rms_eps), int(self.n_shared), _p(self.sh1), _p(self.sh3), _p(self.sh2))
+
+
 _lib = None
 
 
@@ -123,6 +152,9 @@ def lib() -> ctypes.CDLL:
         L.k3moe_layer_host.argtypes = [pc, vp, vp, vp, pe, vp, i32, vp, vp, vp, sz, vp]
         L.k3moe_layer_static_scratch.argtypes = [pc, vp, vp, vp, pe, vp, i32, vp, vp, vp, vp, vp, vp]
         L.k3moe_matvec_mxfp4.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
+        pl = ctypes.POINTER(_CLatent)
+        L.k3moe_latent_workspace_size.argtypes = [pc, pl, i32, ctypes.POINTER(sz)]
+        L.k3moe_latent_layer.argtypes = [pc, pl, vp, vp, vp, pe, i32, vp, vp, vp, vp, vp, vp, sz, vp]
         L.k3moe_stack_link.argtypes = [vp, i32, i32, i32, ctypes.c_float, vp, vp, vp]
         L.k3moe_set_phase_events.restype = ctypes.c_int
         L.k3moe_set_phase_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
@@ -134,7 +166,8 @@ def lib() -> ctypes.CDLL:
         L.k3moe_abi_version.argtypes = []
         for n in ("k3moe_workspace_size", "k3moe_workspace_size_host", "k3moe_route",
                   "k3moe_experts_mxfp4", "k3moe_layer", "k3moe_layer_host", "k3moe_matvec_mxfp4",
-                  "k3moe_stack_link", "k3moe_layer_static_scratch"):
+                  "k3moe_stack_link", "k3moe_layer_static_scratch", "k3moe_latent_workspace_size",
+                  "k3moe_latent_layer"):
             getattr(L, n).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -345,3 +378,54 @@ def k3moe_stack_link(y, x_out, h_out=None, norm: bool = True, eps: float = 1e-5,
         _expect(h_out, "h_out", torch.bfloat16, (T, 2 * L))
     _check("k3moe_stack_link", lib().k3moe_stack_link(_p(y), T, L, 1 if norm else 0, float(eps), _p(x_out),
                                                       _p(h_out), _stream(stream)))
+
+
+def k3moe_latent_workspace_size(cfg: Cfg, lat: Latent, T: int) -> int:
+    n = ctypes.c_size_t(0)
+    c, la = cfg.c(), lat.c()
+    _check("k3moe_latent_workspace_size",
+           lib().k3moe_latent_workspace_size(ctypes.byref(c), ctypes.byref(la), int(T), ctypes.byref(n)))
+    return int(n.value)
+
+
+def latent_workspace(cfg: Cfg, lat: Latent, T: int, device="cuda"):
+    """A device workspace (uint8 tensor) of k3moe_latent_layer for T tokens."""
+    import torch
+    return torch.empty(k3moe_latent_workspace_size(cfg, lat, T), dtype=torch.uint8, device=device)
+
+
+def k3moe_latent_layer(cfg: Cfg, lat: Latent, h, wr, bias, experts: Experts, out, idx=None,
+                       gate=None, gap=None, status=None, ws=None, stream=None) -> None:
+    """The LatentMoE layer (README Part II section 9, k3_moe): route on h, the routed experts
+    on z = bf16(down . h), RMSNorm of their sum, up-projection, plus the shared experts on h."""
+    import torch
+    T = h.shape[0]
+    H, L = cfg.hidden, cfg.latent
+    SI = cfg.inter * lat.n_shared
+    _expect(h, "h", torch.bfloat16, (T, H))
+    _expect(wr, "wr", torch.bfloat16, (cfg.n_experts, H))
+    if bias is not None:
+        _expect(bias, "bias", torch.float32, (cfg.n_experts,))
+    _expect(lat.down, "down", torch.bfloat16, (L, H))
+    _expect(lat.up, "up", torch.bfloat16, (H, L))
+    if lat.latent_norm_w is not None:
+        _expect(lat.latent_norm_w, "latent_norm_w", torch.float32, (L,))
+    if lat.n_shared > 0:
+        _expect(lat.sh1, "sh1", torch.bfloat16, (SI, H))
+        _expect(lat.sh3, "sh3", torch.bfloat16, (SI, H))
+        _expect(lat.sh2, "sh2", torch.bfloat16, (H, SI))
+    _expect(out, "out", torch.float32, (T, H))
+    if idx is not None:
+        _expect(idx, "idx", torch.int32, (T, cfg.topk))
+    if gate is not None:
+        _expect(gate, "gate", torch.float32, (T, cfg.topk))
+    if gap is not None:
+        _expect(gap, "gap", torch.float32, (T,))
+    if status is not None:
+        _expect(status, "status", torch.int32, (4,))
+    if ws is None:
+        raise ValueError("ws (workspace) is required")
+    c, la, e = cfg.c(), lat.c(), experts.c()
+    _check("k3moe_latent_layer", lib().k3moe_latent_layer(
+        ctypes.byref(c), ctypes.byref(la), _p(h), _p(wr), _p(bias), ctypes.byref(e), T, _p(out),
+        _p(idx), _p(gate), _p(gap), _p(status), _p(ws), ws.numel(), _stream(stream)))

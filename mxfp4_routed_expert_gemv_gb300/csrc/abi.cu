@@ -132,6 +132,50 @@ int check_ws(const k3moe_cfg* c, int32_t T, void* ws, size_t ws_bytes, bool host
   return K3MOE_OK;
 }
 
+// The LatentMoE wrapper's regions, after the layer's own workspace.
+struct LatentWs {
+  uint16_t* z;  // [T][L] bf16: the experts' latent input
+  float* y;     // [T][L]: the routed sum
+  float* yn;    // [T][L]: after its RMSNorm
+  float* act;   // [T][SI]: the shared experts' activations
+};
+
+constexpr int32_t kMaxLatentTokens = 4 * 65535;  // grid rows of four tokens
+
+int shared_width(const k3moe_cfg* c, const k3moe_latent* lat) {
+  return lat->n_shared > 0 ? lat->n_shared * c->inter : 0;
+}
+
+size_t carve_latent(const k3moe_cfg* c, const k3moe_latent* lat, int32_t T, void* base,
+                    Workspace* w, LatentWs* lw) {
+  Carver cv{static_cast<uint8_t*>(base)};
+  cv.off = carve(c, T, base, false, w);
+  const size_t Tt = (size_t)std::max(T, 1), L = c->latent;
+  LatentWs t{};
+  t.z = cv.take<uint16_t>(Tt * L);
+  t.y = cv.take<float>(Tt * L);
+  t.yn = cv.take<float>(Tt * L);
+  t.act = cv.take<float>(Tt * (size_t)std::max(shared_width(c, lat), 1));
+  if (lw) *lw = t;
+  return (cv.off + 255) & ~size_t(255);
+}
+
+int check_latent(const k3moe_cfg* c, const k3moe_latent* lat) {
+  if (!lat || !lat->down || !lat->up) return K3MOE_ERR_INVALID;
+  if (lat->latent_norm != 0 && lat->latent_norm != 1) return K3MOE_ERR_INVALID;
+  if (!(lat->rms_eps >= 0.f) || lat->n_shared < 0) return K3MOE_ERR_INVALID;
+  if (!aligned(lat->down, 16) || !aligned(lat->up, 16) ||
+      (lat->latent_norm_w && !aligned(lat->latent_norm_w, 4)))
+    return K3MOE_ERR_ALIGN;
+  if (lat->n_shared > 0) {
+    if (!lat->sh1 || !lat->sh3 || !lat->sh2) return K3MOE_ERR_INVALID;
+    if (!aligned(lat->sh1, 16) || !aligned(lat->sh3, 16) || !aligned(lat->sh2, 16))
+      return K3MOE_ERR_ALIGN;
+    if ((int64_t)lat->n_shared * c->inter > (1 << 20)) return K3MOE_ERR_UNSUPPORTED;
+  }
+  return K3MOE_OK;
+}
+
 int check_experts(const k3moe_experts* e) {
   if (!e) return K3MOE_ERR_INVALID;
   const void* p[6] = {e->w1_packed, e->w1_scale, e->w3_packed, e->w3_scale, e->w2_packed,
@@ -387,6 +431,55 @@ int k3moe_layer_host(const k3moe_cfg* cfg, const void* h_host, const void* wr, c
     return rc;
   K3_TRY(cudaMemcpyAsync(y_host, w.y_stage, yb, cudaMemcpyDeviceToHost, s));
   K3_TRY(cudaStreamSynchronize(s));
+  return K3MOE_OK;
+}
+
+int k3moe_latent_workspace_size(const k3moe_cfg* cfg, const k3moe_latent* lat, int32_t T,
+                                size_t* bytes) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if ((rc = check_latent(cfg, lat))) return rc;
+  if (!bytes || T < 0) return K3MOE_ERR_INVALID;
+  if (T > kMaxLatentTokens) return K3MOE_ERR_UNSUPPORTED;
+  *bytes = carve_latent(cfg, lat, T, nullptr, nullptr, nullptr);
+  return K3MOE_OK;
+}
+
+int k3moe_latent_layer(const k3moe_cfg* cfg, const k3moe_latent* lat, const void* h,
+                       const void* wr, const float* bias, const k3moe_experts* experts,
+                       int32_t T, float* out, int32_t* idx, float* gate, float* gap,
+                       int32_t* status, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if ((rc = check_latent(cfg, lat))) return rc;
+  if ((rc = check_experts(experts))) return rc;
+  if (T < 0) return K3MOE_ERR_INVALID;
+  if (T > kMaxLatentTokens) return K3MOE_ERR_UNSUPPORTED;
+  if (T == 0) return K3MOE_OK;
+  if (!h || !wr || !out) return K3MOE_ERR_INVALID;
+  if (!aligned(h, 16) || !aligned(wr, 16) || !aligned(out, 16) || (bias && !aligned(bias, 4)) ||
+      (idx && !aligned(idx, 4)) || (gate && !aligned(gate, 4)) || (gap && !aligned(gap, 4)) ||
+      (status && !aligned(status, 4)))
+    return K3MOE_ERR_ALIGN;
+  if (!ws || !aligned(ws, 256)) return K3MOE_ERR_WORKSPACE;
+  if (ws_bytes < carve_latent(cfg, lat, T, nullptr, nullptr, nullptr)) return K3MOE_ERR_WORKSPACE;
+  Workspace w;
+  LatentWs lw;
+  carve_latent(cfg, lat, T, ws, &w, &lw);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int H = cfg->hidden, L = cfg->latent, SI = shared_width(cfg, lat);
+  const auto* h16 = static_cast<const uint16_t*>(h);
+  K3_TRY(launch_dense_in(h16, T, H, static_cast<const uint16_t*>(lat->down), L, lw.z,
+                         static_cast<const uint16_t*>(lat->sh1),
+                         static_cast<const uint16_t*>(lat->sh3), SI, lw.act, cfg->act,
+                         cfg->situ_b1, cfg->situ_b2, s, true));
+  if ((rc = run_pipeline(cfg, true, h, wr, bias, experts, lw.z, idx ? idx : w.idx,
+                         gate ? gate : w.gate, gap ? gap : w.gap, T, lw.y, status, w, s)))
+    return rc;
+  K3_TRY(launch_latent_norm(lw.y, T, L, lat->latent_norm, lat->latent_norm_w, lat->rms_eps,
+                            lw.yn, s, true));
+  K3_TRY(launch_dense_out(lw.yn, T, L, static_cast<const uint16_t*>(lat->up), H, lw.act,
+                          static_cast<const uint16_t*>(lat->sh2), SI, out, s, true));
   return K3MOE_OK;
 }
 

@@ -152,6 +152,18 @@ cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, i
                               cudaStream_t s, bool pdl, void (*between)(cudaStream_t),
                               const RouteOne* ro = nullptr);
 
+// dense.cu (the LatentMoE wrapper): z = bf16(down . h) and act = activation(sh1 . h,
+// sh3 . h); yn = the RMSNorm of y (or y); out = up . yn + sh2 . act.
+cudaError_t launch_dense_in(const uint16_t* h, int T, int H, const uint16_t* down, int L,
+                            uint16_t* z, const uint16_t* sh1, const uint16_t* sh3, int SI,
+                            float* act, int act_kind, float b1, float b2, cudaStream_t s,
+                            bool pdl);
+cudaError_t launch_latent_norm(const float* y, int T, int L, int norm, const float* w, float eps,
+                               float* yn, cudaStream_t s, bool pdl);
+cudaError_t launch_dense_out(const float* yn, int T, int L, const uint16_t* up, int H,
+                             const float* act, const uint16_t* sh2, int SI, float* out,
+                             cudaStream_t s, bool pdl);
+
 // stack.cu
 cudaError_t launch_stack_link(const float* y, int T, int L, int norm, float eps, uint16_t* x_out,
                               uint16_t* h_out, cudaStream_t s);

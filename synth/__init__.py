@@ -28,6 +28,12 @@ Distributions (the five K3-shaped workloads):
   32 seeded distinct "hot" experts instead.
 * packed bytes uniform over 0..255 (each nibble uniform over the 16 E2M1 codes);
   scale bytes uniform over the 9 integers 118..126.
+
+The LatentMoE wrapper's dense tensors (the pages give them no distribution; these keep
+every stage near unit scale): down ~ N(0, 1/H) bf16 [L, H] (so z has unit variance), up ~
+N(0, 1/L) bf16 [H, L] (the normed aggregate has unit RMS), the aggregate's norm weight
+1 + N(0, 0.01) fp32 [L], shared experts sh1, sh3 ~ N(0, 1/H) bf16 [S, H] and sh2 ~
+N(0, 1/S) bf16 [H, S], S = n_shared * I.
 """
 from __future__ import annotations
 
@@ -48,6 +54,7 @@ _LAYER_MUL = np.uint64(0xD1B54A32D192ED03)
 # tensor ids of the streams
 W1P, W1S, W3P, W3S, W2P, W2S = 0, 1, 2, 3, 4, 5
 T_H, T_WR, T_BIAS, T_X, T_HOT = 10, 11, 12, 13, 14
+T_DOWN, T_UP, T_NORM, T_SH1, T_SH3, T_SH2 = 15, 16, 17, 18, 19, 20
 
 SCALE_LO, SCALE_SPAN = 118, 9
 
@@ -261,3 +268,32 @@ def experts_device(w: Workload, layer: int, device="cuda"):
         fill_expert_tensor_device(t.data_ptr(), w.E, r * c, w, layer, name, stream)
         out[name] = t
     return out
+
+
+@dataclasses.dataclass
+class LatentWeights:
+    down: np.ndarray               # uint16 bf16 bits [L, H]
+    up: np.ndarray                 # uint16 bf16 bits [H, L]
+    norm_w: np.ndarray             # float32 [L]
+    n_shared: int
+    sh1: Optional[np.ndarray]      # uint16 bf16 bits [S, H]
+    sh3: Optional[np.ndarray]
+    sh2: Optional[np.ndarray]      # uint16 bf16 bits [H, S]
+
+
+def latent_weights(w: Workload, layer: int = 0, n_shared: int = 2) -> LatentWeights:
+    """Host dense tensors of one layer's LatentMoE wrapper (distributions in the module
+    docstring)."""
+    s, H, L = w.layer_seed(layer), w.hidden, w.latent
+    S = n_shared * w.inter
+
+    def bf(tid, shape, var):
+        return f32_to_bf16_bits(normal_f32(stream_key(s, layer, tid), shape, var ** 0.5))
+
+    norm_w = (np.float32(1.0) + normal_f32(stream_key(s, layer, T_NORM), (L,), 0.1)).astype(np.float32)
+    return LatentWeights(
+        down=bf(T_DOWN, (L, H), 1.0 / H), up=bf(T_UP, (H, L), 1.0 / L), norm_w=norm_w,
+        n_shared=n_shared,
+        sh1=bf(T_SH1, (S, H), 1.0 / H) if S else None,
+        sh3=bf(T_SH3, (S, H), 1.0 / H) if S else None,
+        sh2=bf(T_SH2, (H, S), 1.0 / S) if S else None)

@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -97,3 +98,40 @@ def test_host_checks_refuse_null_pointers_without_cuda():
                          ctypes.c_void_p(256), 1, ctypes.c_void_p(256), None, None, None, None,
                          ctypes.c_void_p(258), 1 << 40, None)
     assert rc == 4
+
+
+def test_latent_workspace_and_checks_without_cuda():
+    """The LatentMoE entry points' host-side checks (no device memory is touched: the size
+    query only reads the pointers' values)."""
+    import mxfp4_routed_expert_gemv_gb300 as k3
+    cfg = k3.KIMI_K3
+    L, H, I = cfg.latent, cfg.hidden, cfg.inter
+    buf = torch.zeros(64, dtype=torch.uint8)  # any aligned non-null address
+    lat = k3.Latent(down=buf, up=buf, n_shared=2, sh1=buf, sh3=buf, sh2=buf)
+    n1 = k3.k3moe_latent_workspace_size(cfg, lat, 1)
+    n4 = k3.k3moe_latent_workspace_size(cfg, lat, 4)
+    # the layer's workspace plus z (bf16), the routed sum and its norm (fp32), act (fp32)
+    assert n1 >= k3.k3moe_workspace_size(cfg, 1) + L * 2 + 2 * L * 4 + 2 * I * 4
+    assert n4 > n1
+    lat0 = k3.Latent(down=buf, up=buf, n_shared=0)
+    assert k3.k3moe_latent_workspace_size(cfg, lat0, 1) < n1
+    for bad, code in ((dict(down=None), 1), (dict(n_shared=-1), 1), (dict(sh2=None), 1),
+                      (dict(rms_eps=-1.0), 1), (dict(n_shared=1000), 2)):
+        b = k3.Latent(**{**lat.__dict__, **bad})
+        with pytest.raises(k3.K3moeError) as ei:
+            k3.k3moe_latent_workspace_size(cfg, b, 1)
+        assert ei.value.status == code, bad
+    raw = lat.c()
+    raw.latent_norm = 2  # the C check itself (the binding passes a bool)
+    n = ctypes.c_size_t(0)
+    assert k3.lib().k3moe_latent_workspace_size(ctypes.byref(cfg.c()), ctypes.byref(raw), 1, ctypes.byref(n)) == 1
+    # a null output is refused before any CUDA call
+    lib = k3.lib()
+    c, la, e = cfg.c(), lat.c(), k3._CExperts(*([buf.data_ptr()] * 6))
+    rc = lib.k3moe_latent_layer(ctypes.byref(c), ctypes.byref(la), buf.data_ptr(), buf.data_ptr(), None,
+                                ctypes.byref(e), 1, None, None, None, None, None, None, 0, None)
+    assert rc == 1
+    # T = 0: nothing to do
+    rc = lib.k3moe_latent_layer(ctypes.byref(c), ctypes.byref(la), None, None, None, ctypes.byref(e), 0,
+                                None, None, None, None, None, None, 0, None)
+    assert rc == 0
