@@ -1,7 +1,7 @@
 // dense.cu -- the LatentMoE wrapper's dense layers around the routed experts (README
 // "kimi-k3-in-c", Part II section 9, k3_moe): the down-projection of h into the experts'
 // latent, the shared experts' gate and up rows on h, the RMSNorm of the routed aggregate
-// (Part II section 5: sum of squares in fp64, eps inside the square root), and the
+// (Part II section 5: eps inside the square root), and the
 // up-projection together with the shared experts' down rows.  Every weight is bf16 and read
 // once per call for a few tokens, so each launch streams its weights from HBM: a row is
 // split into four quarters, one warp each, and every lane issues all its 16-byte loads of
@@ -85,6 +85,64 @@ __device__ __forceinline__ void quarter_dot(const uint16_t* __restrict__ w,
   for (int tt = 0; tt < TT; ++tt) acc[tt] = warp_sum(a0[tt] + a1[tt]);
 }
 
+// quarter_dot for two rows of the same length against fp32 token vectors, every weight
+// load of both rows issued before the first multiply; V 16-byte pieces per lane and row in
+// a batch (six cover the quarter of a 6144-wide row in one batch, with registers left for
+// three CTAs per SM).
+template <int TT, int V = 6>
+__device__ __forceinline__ void quarter_dot2(const uint16_t* __restrict__ w0,
+                                             const uint16_t* __restrict__ w1,
+                                             const float* __restrict__ x, size_t xs, int nt, int n,
+                                             int q, int lane, float (&acc0)[TT],
+                                             float (&acc1)[TT]) {
+  const Quarter Q = quarter_of(n, q);
+  float a0[TT], a1[TT], b0[TT], b1[TT];
+#pragma unroll
+  for (int tt = 0; tt < TT; ++tt) a0[tt] = a1[tt] = b0[tt] = b1[tt] = 0.f;
+  const uint4 *u4 = reinterpret_cast<const uint4*>(w0), *v4 = reinterpret_cast<const uint4*>(w1);
+  for (int base = Q.qb; base < Q.qe; base += 32 * V) {
+    uint4 wu[V], wv[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int c = base + lane + 32 * i;
+      wu[i] = c < Q.qe ? ldg_stream(u4 + c) : make_uint4(0u, 0u, 0u, 0u);
+      wv[i] = c < Q.qe ? ldg_stream(v4 + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt) {
+      if (tt >= nt) break;
+      const float4* xr = reinterpret_cast<const float4*>(x + (size_t)tt * xs);
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int c = base + lane + 32 * i;
+        if (c >= Q.qe) continue;
+        const float4 p = __ldg(xr + 2 * c), r = __ldg(xr + 2 * c + 1);
+        a0[tt] = fmaf(bf16lo(wu[i].x), p.x, a0[tt]);
+        a1[tt] = fmaf(bf16hi(wu[i].x), p.y, a1[tt]);
+        a0[tt] = fmaf(bf16lo(wu[i].y), p.z, a0[tt]);
+        a1[tt] = fmaf(bf16hi(wu[i].y), p.w, a1[tt]);
+        a0[tt] = fmaf(bf16lo(wu[i].z), r.x, a0[tt]);
+        a1[tt] = fmaf(bf16hi(wu[i].z), r.y, a1[tt]);
+        a0[tt] = fmaf(bf16lo(wu[i].w), r.z, a0[tt]);
+        a1[tt] = fmaf(bf16hi(wu[i].w), r.w, a1[tt]);
+        b0[tt] = fmaf(bf16lo(wv[i].x), p.x, b0[tt]);
+        b1[tt] = fmaf(bf16hi(wv[i].x), p.y, b1[tt]);
+        b0[tt] = fmaf(bf16lo(wv[i].y), p.z, b0[tt]);
+        b1[tt] = fmaf(bf16hi(wv[i].y), p.w, b1[tt]);
+        b0[tt] = fmaf(bf16lo(wv[i].z), r.x, b0[tt]);
+        b1[tt] = fmaf(bf16hi(wv[i].z), r.y, b1[tt]);
+        b0[tt] = fmaf(bf16lo(wv[i].w), r.z, b0[tt]);
+        b1[tt] = fmaf(bf16hi(wv[i].w), r.w, b1[tt]);
+      }
+    }
+  }
+#pragma unroll
+  for (int tt = 0; tt < TT; ++tt) {
+    acc0[tt] = warp_sum(a0[tt] + a1[tt]);
+    acc1[tt] = warp_sum(b0[tt] + b1[tt]);
+  }
+}
+
 // Everything that reads h: CTAs [0, ceil(L/2)) take two rows of `down` each (warps 0-3 and
 // 4-7) and write z = bf16(down . h) (nearest even), the experts' latent input; CTAs
 // [ceil(L/2), ceil(L/2) + SI) take row r of sh1 (warps 0-3) and of sh3 (warps 4-7) and write
@@ -134,67 +192,97 @@ __global__ void __launch_bounds__(256) k_dense_in(const uint16_t* __restrict__ h
   }
 }
 
-// The RMSNorm of the routed aggregate y [T][L] (one CTA per token), as the README's
-// k3_rmsnorm: the sum of squares in fp64, inv = (float)(1 / sqrt(ss / L + eps)), then
-// yn = y * inv * w in fp32 (w NULL: unit weight).  norm 0: yn = y.
+// The RMSNorm of the routed aggregate y [T][L] (one CTA per token): yn = y * inv * w in fp32
+// (w NULL: unit weight), inv = 1 / sqrt(mean(y^2) + eps), eps inside the square root as the
+// README's k3_rmsnorm.  The README sums the squares in fp64; here they are summed in fp32
+// by a fixed tree (each thread's elements pairwise, then the warp, then the warps), whose
+// relative error, a few fp32 ulps times log2(L), stays far below the layer's tolerance: this
+// kernel sits between two HBM-bound launches on the critical path, and an fp64 version
+// measured 19 us on this GPU against a few us for this one.  norm 0: yn = y.
 __global__ void __launch_bounds__(256) k_latent_norm(const float* __restrict__ y, int L, int norm,
                                                      const float* __restrict__ w, float eps,
                                                      float* __restrict__ yn) {
-  __shared__ double wsum[8];
+  __shared__ float wsum[8];
   pdl_wait();
   pdl_launch();
   const int t = blockIdx.x;
   const float* yr = y + (size_t)t * L;
   float inv = 1.f;
   if (norm) {
-    double ss = 0.0;
-    for (int c = threadIdx.x; c < L; c += blockDim.x) ss += (double)yr[c] * (double)yr[c];
+    // this thread's elements c = threadIdx.x + 256 i, added pairwise in a fixed order
+    float sq[16];
+    const int nmine = (L - (int)threadIdx.x + 255) / 256;
+    float ss = 0.f;
+    for (int i0 = 0; i0 < nmine; i0 += 16) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      for (int i = 0; i < 16; ++i) {
+        const int c = threadIdx.x + 256 * (i0 + i);
+        const float v = i0 + i < nmine ? __ldg(yr + c) : 0.f;
+        sq[i] = v * v;
+      }
+#pragma unroll
+      for (int h = 8; h > 0; h >>= 1)
+#pragma unroll
+        for (int i = 0; i < h; ++i) sq[i] += sq[i + h];
+      ss += sq[0];
+    }
+    ss = warp_sum(ss);
     if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = ss;
     __syncthreads();
-    double tot = 0.0;
-    for (int i = 0; i < 8; ++i) tot += wsum[i];
-    inv = (float)(1.0 / sqrt(tot / (double)L + (double)eps));
+    const float tot = ((wsum[0] + wsum[1]) + (wsum[2] + wsum[3])) +
+                      ((wsum[4] + wsum[5]) + (wsum[6] + wsum[7]));
+    inv = 1.0f / sqrtf(tot / (float)L + eps);
   }
   for (int c = threadIdx.x; c < L; c += blockDim.x)
     yn[(size_t)t * L + c] = norm ? yr[c] * inv * (w ? w[c] : 1.0f) : yr[c];
 }
 
-// out[t][r] = up[r] . yn[t] + sh2[r] . act[t]: one output row per CTA, the up row on warps
-// 0-3 and the shared experts' down row on warps 4-7 (idle without shared experts); the two
-// sums are added last, each in a fixed order.  Grid y: groups of TT tokens.
+// out[t][r] = up[r] . yn[t] + sh2[r] . act[t]: two output rows per CTA, the up rows on warps
+// 0-3 and the shared experts' down rows on warps 4-7 (idle without shared experts), each warp
+// a quarter of both rows with all their loads in flight together (the up rows are short:
+// one row's quarter alone left too few bytes in flight); the two sums are added last, each
+// in a fixed order.  Grid y: groups of TT tokens.
 template <int TT>
-__global__ void __launch_bounds__(256) k_dense_out(const float* __restrict__ yn, int T, int L,
+__global__ void __launch_bounds__(256, TT == 1 ? 3 : 1) k_dense_out(const float* __restrict__ yn, int T, int L,
                                                    const uint16_t* __restrict__ up, int H,
                                                    const float* __restrict__ act,
                                                    const uint16_t* __restrict__ sh2, int SI,
                                                    float* __restrict__ out) {
-  __shared__ float part[8][TT];
+  __shared__ float part[2][8][TT];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, half = warp >> 2;
-  const int r = blockIdx.x;
-  const uint16_t* w = half == 0 ? up + (size_t)r * L : (SI > 0 ? sh2 + (size_t)r * SI : nullptr);
+  const int r0 = 2 * blockIdx.x, r1 = min(r0 + 1, H - 1);  // an odd H repeats the last row
   const int n = half == 0 ? L : SI;
-  if (w && blockIdx.y == 0 && lane == 0) prefetch_quarter(w, n, q);
+  const uint16_t* base = half == 0 ? up : (SI > 0 ? sh2 : nullptr);
+  const uint16_t* w0 = base ? base + (size_t)r0 * n : nullptr;
+  const uint16_t* w1 = base ? base + (size_t)r1 * n : nullptr;
+  if (base && blockIdx.y == 0 && lane == 0) {
+    prefetch_quarter(w0, n, q);
+    prefetch_quarter(w1, n, q);
+  }
   pdl_wait();
   pdl_launch();
   const int t0 = blockIdx.y * TT, nt = min(TT, T - t0);
-  float acc[TT];
+  float acc0[TT], acc1[TT];
 #pragma unroll
-  for (int tt = 0; tt < TT; ++tt) acc[tt] = 0.f;
-  if (w)
-    quarter_dot<TT, true>(w, half == 0 ? (const void*)(yn + (size_t)t0 * L)
-                                       : (const void*)(act + (size_t)t0 * SI),
-                          (size_t)n, nt, n, q, lane, acc);
+  for (int tt = 0; tt < TT; ++tt) acc0[tt] = acc1[tt] = 0.f;
+  if (base)
+    quarter_dot2<TT>(w0, w1, half == 0 ? yn + (size_t)t0 * L : act + (size_t)t0 * SI, (size_t)n,
+                     nt, n, q, lane, acc0, acc1);
   if (lane == 0)
 #pragma unroll
-    for (int tt = 0; tt < TT; ++tt) part[warp][tt] = acc[tt];
+    for (int tt = 0; tt < TT; ++tt) {
+      part[0][warp][tt] = acc0[tt];
+      part[1][warp][tt] = acc1[tt];
+    }
   __syncthreads();
   const int i = threadIdx.x;
-  if (i < nt) {
-    const float a = (part[0][i] + part[1][i]) + (part[2][i] + part[3][i]);
-    const float b = (part[4][i] + part[5][i]) + (part[6][i] + part[7][i]);
-    out[(size_t)(t0 + i) * H + r] = a + b;
+  if (i < 2 * TT) {
+    const int k = i / TT, tt = i - k * TT, r = r0 + k;
+    if (r < H && tt < nt) {
+      const float a = (part[k][0][tt] + part[k][1][tt]) + (part[k][2][tt] + part[k][3][tt]);
+      const float b = (part[k][4][tt] + part[k][5][tt]) + (part[k][6][tt] + part[k][7][tt]);
+      out[(size_t)(t0 + tt) * H + r] = a + b;
+    }
   }
 }
 
@@ -220,10 +308,11 @@ cudaError_t launch_latent_norm(const float* y, int T, int L, int norm, const flo
 cudaError_t launch_dense_out(const float* yn, int T, int L, const uint16_t* up, int H,
                              const float* act, const uint16_t* sh2, int SI, float* out,
                              cudaStream_t s, bool pdl) {
+  const unsigned gx = (unsigned)((H + 1) / 2);
   if (T <= 2)
-    return launch_kernel(k_dense_out<1>, dim3(H, T), dim3(256), 0, s, pdl, yn, T, L, up, H, act,
+    return launch_kernel(k_dense_out<1>, dim3(gx, T), dim3(256), 0, s, pdl, yn, T, L, up, H, act,
                          sh2, SI, out);
-  return launch_kernel(k_dense_out<4>, dim3(H, (T + 3) / 4), dim3(256), 0, s, pdl, yn, T, L, up,
+  return launch_kernel(k_dense_out<4>, dim3(gx, (T + 3) / 4), dim3(256), 0, s, pdl, yn, T, L, up,
                        H, act, sh2, SI, out);
 }
 
