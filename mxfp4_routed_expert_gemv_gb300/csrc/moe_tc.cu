@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
     if (PH == 0) pdl_wait();
     pdl_launch();
     if (route_one_token<PH>(f, sm, own_tiles, own_perm, own_gate, PH == 0 && cta == 0) == 0)
-      *abort_v = 1;  // the routing flag never came: every role stops at its first wait
+      *abort_v = 1;  // the routing words never came: every role stops at its first wait
   }
 
   if (warp == kProdWarp || warp == kBWarp) {
