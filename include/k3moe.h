@@ -192,7 +192,8 @@ int k3moe_latent_workspace_size(const k3moe_cfg *cfg, const k3moe_latent *lat, i
  *   out = up . (latent_norm ? rmsnorm(acc) * latent_norm_w : acc)
  *         + sh2 . act(sh1 . h, sh3 . h).
  *   h: bf16 [T][hidden]; out: fp32 [T][hidden] (out, fully written); other arguments and
- *   errors as k3moe_layer.  T is at most 262140.  Enqueues six launches on the stream. */
+ *   errors as k3moe_layer.  T is at most 262140.  One token takes six launches on the
+ *   stream (the three of k3moe_layer plus the two dense launches and the norm). */
 int k3moe_latent_layer(const k3moe_cfg *cfg, const k3moe_latent *lat, const void *h,
                        const void *wr, const float *bias, const k3moe_experts *experts,
                        int32_t T, float *out, int32_t *idx, float *gate, float *gap,
