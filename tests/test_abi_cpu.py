@@ -135,3 +135,18 @@ def test_latent_workspace_and_checks_without_cuda():
     rc = lib.k3moe_latent_layer(ctypes.byref(c), ctypes.byref(la), None, None, None, ctypes.byref(e), 0,
                                 None, None, None, None, None, None, 0, None)
     assert rc == 0
+
+
+def test_header_is_plain_c_and_cxx(tmp_path):
+    """include/k3moe.h compiles as C99 and as C++17 with no CUDA header: the boundary uses
+    plain pointers and sizes only."""
+    import subprocess
+    src = tmp_path / "use.c"
+    src.write_text('#include "k3moe.h"\n'
+                   'int main(void) { k3moe_cfg c; (void)c; k3moe_latent l; (void)l;\n'
+                   '  return (int)(sizeof(k3moe_experts) > 0) - 1; }\n')
+    inc = os.path.join(ROOT, "include")
+    for cmd in (["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-I", inc, str(src)],
+                ["g++", "-std=c++17", "-x", "c++", "-Wall", "-Werror", "-fsyntax-only", "-I", inc, str(src)]):
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
