@@ -63,3 +63,25 @@ def test_host_fill_matches_numpy_statement():
     w1 = synth.WORKLOADS[4]
     assert np.array_equal(synth.expert_tensor(w1, 5, 801, "w1s"), synth.expert_tensor_numpy(w1, 5, 801, "w1s"))
     assert np.array_equal(synth.expert_tensor(w1, 5, 801, "w2p"), synth.expert_tensor_numpy(w1, 5, 801, "w2p"))
+
+
+def test_latent_weights_recipe():
+    """The LatentMoE wrapper's dense tensors: seeded (same call, same bits), the stated shapes
+    and variances (down, sh1, sh3 1/H; up 1/L; sh2 1/S; norm weight 1 + N(0, 0.01))."""
+    w = synth.small_workload(latent=256, inter=192, hidden=512)
+    a = synth.latent_weights(w, 0, n_shared=2)
+    b = synth.latent_weights(w, 0, n_shared=2)
+    for n in ("down", "up", "sh1", "sh3", "sh2"):
+        assert np.array_equal(getattr(a, n), getattr(b, n)), n
+    H, L, S = w.hidden, w.latent, 2 * w.inter
+    assert a.down.shape == (L, H) and a.up.shape == (H, L)
+    assert a.sh1.shape == (S, H) and a.sh3.shape == (S, H) and a.sh2.shape == (H, S)
+    for n, var in (("down", 1 / H), ("up", 1 / L), ("sh1", 1 / H), ("sh3", 1 / H), ("sh2", 1 / S)):
+        v = synth.bf16_bits_to_f32(getattr(a, n)).astype(np.float64)
+        assert abs(v.mean()) < 0.05 * var ** 0.5, n
+        assert abs(v.var() / var - 1) < 0.02, n
+    assert abs(a.norm_w.mean() - 1) < 0.01 and abs(a.norm_w.std() - 0.1) < 0.02
+    # distinct tensors come from distinct streams
+    assert not np.array_equal(a.sh1, a.sh3)
+    c = synth.latent_weights(w, 0, n_shared=0)
+    assert c.sh1 is None and c.sh2 is None and np.array_equal(c.down, a.down)
