@@ -121,7 +121,10 @@ int k3moe_route(const k3moe_cfg *cfg, const void *h, const void *wr, const float
  *   y:    fp32 [T][latent] (out)    fully overwritten (not accumulated into)
  *   status: int32[4] device status block or NULL.  An index outside [0, E) skips that
  *   assignment (its term is zero) and counts it in status[0].
- * Expert weights stay packed in HBM; they are decoded in registers and never expanded. */
+ * Expert weights stay packed in HBM and are never expanded: the tensor-core path feeds the
+ * checkpoint's E2M1 bytes and E8M0 scales straight to the block-scaled MMA (kind::mxf4);
+ * widths that are not multiples of 512 take a CUDA-core path that decodes nibbles in
+ * registers. */
 int k3moe_experts_mxfp4(const k3moe_cfg *cfg, const k3moe_experts *experts, const void *x,
                         const int32_t *idx, const float *gate, int32_t T, float *y,
                         int32_t *status, void *ws, size_t ws_bytes, void *stream);
@@ -167,7 +170,8 @@ int k3moe_stack_link(const float *y, int32_t T, int32_t L, int32_t norm, float e
  *   down [latent][hidden]      z = down . h, the experts' latent input (rounded to bf16);
  *   up   [hidden][latent]      out = up . a, a = the routed sum after its RMSNorm;
  *   latent_norm_w fp32 [latent], or NULL for unit weight; latent_norm 1 applies the RMSNorm
- *   (fp64 sum of squares, eps = rms_eps inside the square root, README section 5), 0 skips;
+ *   (sum of squares in fp32 by a fixed reduction tree, eps = rms_eps inside the square root,
+ *   README section 5), 0 skips;
  *   sh1, sh3 [n_shared*inter][hidden] and sh2 [hidden][n_shared*inter]: the shared experts,
  *   on the full-width h, with the layer's activation, added unweighted; n_shared 0: none
  *   (the three pointers are then ignored). */
@@ -213,8 +217,10 @@ int k3moe_latent_layer(const k3moe_cfg *cfg, const k3moe_latent *lat, const void
  *   - Capacity: a call whose k3moe_workspace_size(cfg, T) exceeds the array returns
  *     K3MOE_ERR_TOO_LARGE and enqueues nothing (Kimi K3 shape: up to 27 tokens).
  *   - Set-up: the first call on a device, with that device current, looks up the array's
- *     device address (cudaGetSymbolAddress) and caches it; make that first call before any
- *     stream capture begins.
+ *     device address (cudaGetSymbolAddress) and caches it with the device's current
+ *     context; make that first call before any stream capture begins.  A call that finds
+ *     another context current (the old one was destroyed, e.g. by cudaDeviceReset) looks
+ *     the address up again, so no stale address is used.
  *   - Sharing: all calls on a device share the one array and it keeps the previous call's
  *     contents.  Every scratch value a call reads is written earlier in the same call, so
  *     no clearing is needed between calls; but calls that overlap on the GPU (different streams, no ordering between
@@ -235,6 +241,18 @@ int k3moe_layer_static_scratch(const k3moe_cfg *cfg, const void *h, const void *
  * recording breaks programmatic launch overlap between phases, so time throughput with
  * the hook off.  Returns K3MOE_ERR_INVALID if n != 6 with non-NULL events. */
 int k3moe_set_phase_events(void *const *events, int32_t n);
+
+/* Limit of the waits that cross CTAs: how many times a kernel polls a flag or routing word
+ * that another CTA writes (the routing words of a one-token layer, the "part written" flags
+ * of a tile that several CTAs share) before it gives up.  A wait that gives up counts one
+ * timeout in status[1], its CTA stops its work and waits for its own copies and MMAs in
+ * flight, and the kernel returns; results of that call are then incomplete, and later calls
+ * are unaffected.  polls < 0 restores the default (4,194,304); 0 makes every such wait give
+ * up at once (a way to exercise the timeout path without a fault).  Waits inside a CTA's
+ * pipeline are not affected.  Process-wide; read when a call enqueues its launches (a
+ * captured graph keeps the value it was captured with).  Returns K3MOE_ERR_INVALID if
+ * polls > 4,294,967,295. */
+int k3moe_set_flag_wait_polls(int64_t polls);
 
 /* Number of kernels the library launched through the entry points above since load
  * (host counter; for launch accounting in benchmarks). */

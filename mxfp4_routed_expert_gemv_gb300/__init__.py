@@ -26,6 +26,7 @@ __all__ = [
     "k3moe_launch_count", "k3moe_strerror", "k3moe_abi_version", "k3moe_set_phase_events",
     "k3moe_layer_static_scratch", "STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
     "Latent", "k3moe_latent_workspace_size", "latent_workspace", "k3moe_latent_layer",
+    "k3moe_set_flag_wait_polls",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -33,6 +34,7 @@ EXPORTED_SYMBOLS = (
     "k3moe_layer", "k3moe_layer_host", "k3moe_matvec_mxfp4", "k3moe_stack_link",
     "k3moe_launch_count", "k3moe_strerror", "k3moe_abi_version", "k3moe_set_phase_events",
     "k3moe_layer_static_scratch", "k3moe_latent_workspace_size", "k3moe_latent_layer",
+    "k3moe_set_flag_wait_polls",
 )
 
 # Capacity of the library's file-scope scratch array (K3MOE_STATIC_SCRATCH_BYTES).
@@ -159,6 +161,8 @@ def lib() -> ctypes.CDLL:
         L.k3moe_set_phase_events.restype = ctypes.c_int
         L.k3moe_set_phase_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
         L.k3moe_launch_count.restype = ctypes.c_int64
+        L.k3moe_set_flag_wait_polls.restype = ctypes.c_int
+        L.k3moe_set_flag_wait_polls.argtypes = [ctypes.c_int64]
         L.k3moe_launch_count.argtypes = []
         L.k3moe_strerror.restype = ctypes.c_char_p
         L.k3moe_strerror.argtypes = [ctypes.c_int]
@@ -216,6 +220,12 @@ def k3moe_abi_version() -> int:
 
 def k3moe_launch_count() -> int:
     return int(lib().k3moe_launch_count())
+
+
+def k3moe_set_flag_wait_polls(polls: int) -> None:
+    """How many polls a wait on another CTA's flag makes before giving up (status[1] counts
+    it); negative restores the default, 0 makes such waits give up at once."""
+    _check("k3moe_set_flag_wait_polls", lib().k3moe_set_flag_wait_polls(int(polls)))
 
 
 def k3moe_set_phase_events(events) -> None:

@@ -3,6 +3,9 @@
 #include <algorithm>
 #include <atomic>
 #include <cstring>
+#include <mutex>
+
+#include <cuda.h>
 
 #include "launch.h"
 #include "mxq.cuh"
@@ -10,6 +13,9 @@
 namespace k3 {
 
 std::atomic<int64_t> g_launches{0};
+std::atomic<uint32_t> g_flag_polls{kWaitPolls};
+
+uint32_t flag_wait_polls() { return g_flag_polls.load(std::memory_order_relaxed); }
 
 int sm_count() {
   static int cached[64] = {0};
@@ -281,17 +287,49 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
 // host code g_static_scratch names a host-side stand-in; its device address comes from
 // cudaGetSymbolAddress, looked up once per device with that device current.
 static __device__ __align__(256) unsigned char g_static_scratch[K3MOE_STATIC_SCRATCH_BYTES];
-std::atomic<void*> g_static_scratch_addr[64];
+
+// The address is cached per device together with the context it was looked up in: a
+// destroyed and re-created primary context (cudaDeviceReset) holds the array at another
+// address, so a change of context triggers a new lookup.
+struct ScratchAddr {
+  std::mutex m;
+  void* ctx = nullptr;
+  void* addr = nullptr;
+};
+ScratchAddr g_static_scratch_addr[64];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<CtxGetCurrentFn>(nullptr);
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  return fn;
+}
 
 int static_scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return K3MOE_ERR_CUDA;
-  void* p = g_static_scratch_addr[dev].load();
-  if (!p) {
+  CtxGetCurrentFn get = ctx_get_current_fn();
+  CUcontext ctx = nullptr;
+  if (!get || get(&ctx) != CUDA_SUCCESS) return K3MOE_ERR_CUDA;
+  ScratchAddr& c = g_static_scratch_addr[dev];
+  std::lock_guard<std::mutex> lk(c.m);
+  if (!ctx || c.ctx != static_cast<void*>(ctx) || !c.addr) {
+    // (no context yet on this thread: the lookup makes the device's primary context current)
+    void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return K3MOE_ERR_CUDA;
-    g_static_scratch_addr[dev].store(p);
+    if (!ctx && (get(&ctx) != CUDA_SUCCESS || !ctx)) return K3MOE_ERR_CUDA;
+    c.ctx = ctx;
+    c.addr = p;
   }
-  *out = p;
+  *out = c.addr;
   return K3MOE_OK;
 }
 
@@ -515,6 +553,12 @@ int k3moe_set_phase_events(void* const* events, int32_t n) {
     g_phase[i] = static_cast<cudaEvent_t>(events[i]);
   }
   g_phase_on = true;
+  return K3MOE_OK;
+}
+
+int k3moe_set_flag_wait_polls(int64_t polls) {
+  if (polls > (int64_t)UINT32_MAX) return K3MOE_ERR_INVALID;
+  g_flag_polls.store(polls < 0 ? kWaitPolls : (uint32_t)polls);
   return K3MOE_OK;
 }
 

@@ -240,6 +240,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase, int32_t
   return false;
 }
 
+// The same wait, which also gives up (without counting a timeout) once the CTA's abort flag
+// is set, so that one role's failure winds the others down at once.  Only for waits on work
+// whose completion the CTA does not need to see before it leaves: the waits that drain
+// copies or MMAs still in flight use mbar_wait.
+__device__ __forceinline__ bool mbar_wait_ab(uint64_t* bar, uint32_t phase, int32_t* status,
+                                             volatile int* abort_v) {
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    if (mbar_try_wait(bar, phase)) return true;
+    if (*abort_v) return false;
+  }
+  if (status) atomicAdd(status + kStatTimeout, 1);
+  return false;
+}
+
+// Add `bytes` to the transaction count of the barrier's current phase without arriving (the
+// phase completes once its arrivals are in and the count is back to zero).
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;"
+               ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
 // Bulk global -> shared copy of `bytes` (multiple of 16, both addresses 16-byte aligned),
 // completing as transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes,

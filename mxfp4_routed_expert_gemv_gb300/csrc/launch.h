@@ -35,6 +35,10 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
 
+// Polls a kernel's wait on a flag or routing word written by another CTA makes before it
+// gives up and counts a timeout (k3moe_set_flag_wait_polls; kWaitPolls unless changed).
+uint32_t flag_wait_polls();
+
 // router.cu
 // With xq set (T == 1 only) the launch also writes x's kTerms MXFP4 terms into rows
 // 0 .. kTerms-1 of xq / xsf.

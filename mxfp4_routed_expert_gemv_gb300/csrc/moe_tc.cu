@@ -116,6 +116,7 @@ struct FArgs {
   int npart;                // tokens per part
   int32_t* flags;           // [kTcMaxGrid] part written (zeroed before the launch)
   int32_t* status;
+  uint32_t flag_polls;      // polls a wait on a flag or routing word makes before it gives up
 };
 
 // Units [lo(c), lo(c+1)) of U go to CTA c of G: lo(c) = floor(U c / G), from U = q G + r as
@@ -239,7 +240,7 @@ __device__ __forceinline__ int route_one_token(const FArgs& f, uint8_t* scratch,
     // lane i: the word of the i-th chosen expert (ascending index), polled until written
     unsigned long long w = 0ull;
     if (lane < k) {
-      for (uint32_t q = 0; q < kWaitPolls; ++q) {
+      for (uint32_t q = 0; q < f.flag_polls; ++q) {
         asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(f.route_words + lane)
                      : "memory");
         if (w & 0x80000000ull) break;
@@ -449,7 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
         for (int kc = kb; kc < ke && !stop; ++kc, ++it) {
           const int s = it % kStages;
           if (*abort_v ||
-              (it >= kStages && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1, f.status))) {
+              (it >= kStages &&
+               !mbar_wait_ab(&empty[s], ((it / kStages) - 1) & 1, f.status, abort_v))) {
             *abort_v = 1;
             stop = true;
             break;
@@ -493,14 +495,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
       }
       if (!wts && !stop && rg.head_last && fix_smem) {
         // parts of the shared last tile: wait for each later CTA's flag, then bulk-copy its
-        // part into `fix` (it lands while this CTA's last MMAs run)
-        mbar_arrive_expect_tx(&fixfull, (uint32_t)(nfix * pf * 4));
+        // part into `fix` (it lands while this CTA's last MMAs run).  Each copy adds its bytes
+        // to the barrier's count before it starts and the one arrival comes after the last
+        // copy (or the wait that gave up), so the phase completes once every copy that was
+        // started has landed, whether or not all of them were.
         bool ok = true;
         int slot = 0;
         for (int c = fix_c0; c <= fix_c1 && ok; ++c) {
           if (idle(c)) continue;
           int got = 0;
-          for (uint32_t q = 0; q < kWaitPolls && !got && !*abort_v; ++q) {
+          for (uint32_t q = 0; q < f.flag_polls && !got && !*abort_v; ++q) {
             got = ld_acquire(f.flags + c) == 1;
             if (!got) __nanosleep(256);
           }
@@ -509,13 +513,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
             break;
           }
           fence_proxy_async_global();
+          mbar_expect_tx(&fixfull, (uint32_t)(pf * 4));
           bulk_g2s(fix + (size_t)slot * pf, parts + (size_t)c * pf, (uint32_t)(pf * 4), &fixfull);
           ++slot;
         }
+        mbar_arrive(&fixfull);
         if (!ok) {
           if (!*abort_v && f.status) atomicAdd(f.status + kStatTimeout, 1);
           *abort_v = 1;
           stop = true;
+          mbar_wait(&fixfull, 0, nullptr);  // the copies already started land first
         }
       }
       if (*abort_v) {
@@ -543,8 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
         const int s = it % kStages;
         const uint32_t par = (it / kStages) & 1;
         const bool ok = !*abort_v &&
-                        mbar_wait(&fullA[s], par, lane == 0 ? f.status : nullptr) &&
-                        mbar_wait(&fullB[s], par, lane == 0 ? f.status : nullptr);
+                        mbar_wait_ab(&fullA[s], par, lane == 0 ? f.status : nullptr, abort_v) &&
+                        mbar_wait_ab(&fullB[s], par, lane == 0 ? f.status : nullptr, abort_v);
         if (!__all_sync(0xffffffffu, ok)) {
           *abort_v = 1;
           stop = true;
@@ -597,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
         const int kb = ti_ == 0 ? rg.u0 - tile * f.KC : 0;
         const int ke = ti_ == ntiles - 1 ? rg.u1 - tile * f.KC : f.KC;
         const int b = ti_ & 1;
-        if (ti_ >= 2 && !mbar_wait(&accempty[b], ((ti_ >> 1) - 1) & 1, f.status)) {
+        if (ti_ >= 2 && !mbar_wait_ab(&accempty[b], ((ti_ >> 1) - 1) & 1, f.status, abort_v)) {
           *abort_v = 1;
           stop = true;
           break;
@@ -606,8 +613,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
         for (int kc = kb; kc < ke && !stop; ++kc, ++it) {
           const int s = it % kStages;
           const uint32_t par = (it / kStages) & 1;
-          if (*abort_v || !mbar_wait(&fullA[s], par, f.status) ||
-              !mbar_wait(&fullB[s], par, f.status) || !mbar_wait(&sfready[s], par, f.status)) {
+          if (*abort_v || !mbar_wait_ab(&fullA[s], par, f.status, abort_v) ||
+              !mbar_wait_ab(&fullB[s], par, f.status, abort_v) ||
+              !mbar_wait_ab(&sfready[s], par, f.status, abort_v)) {
             *abort_v = 1;
             stop = true;
             break;
@@ -659,18 +667,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
       const int b = ti_ & 1;
       const bool write_part = ti_ == 0 && rg.tail_first;          // leave a part for the head
       const bool add_parts = ti_ == ntiles - 1 && rg.head_last;    // add the later CTAs' parts
-      int bad = (*abort_v || !mbar_wait(&accfull[b], (ti_ >> 1) & 1, f.status)) ? 1 : 0;
+      int bad = (*abort_v || !mbar_wait_ab(&accfull[b], (ti_ >> 1) & 1, f.status, abort_v)) ? 1 : 0;
       if (add_parts && !bad) {
         if (fix_smem) {
           // the helper's copies complete this phase; if it gave up it set abort_v, and the
           // bounded wait ends here as well
-          bad = (*abort_v || !mbar_wait(&fixfull, 0, f.status)) ? 1 : 0;
+          bad = (*abort_v || !mbar_wait_ab(&fixfull, 0, f.status, abort_v)) ? 1 : 0;
         } else if (threadIdx.x == 0) {
           // parts too large for `fix`: wait for their flags here, read them from global below
           for (int c = fix_c0; c <= fix_c1 && !bad; ++c) {
             if (idle(c)) continue;
             int got = 0;
-            for (uint32_t qq = 0; qq < kWaitPolls && !got && !*abort_v; ++qq) {
+            for (uint32_t qq = 0; qq < f.flag_polls && !got && !*abort_v; ++qq) {
               got = ld_acquire(f.flags + c) == 1;
               if (!got) __nanosleep(256);
             }
@@ -967,6 +975,7 @@ cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, i
   f.act_q = act_q; f.act_sf = act_sf; f.gate = gate; f.ybuf = ybuf;
   f.part = part; f.npart = tc_npart(T);
   f.status = status;
+  f.flag_polls = flag_wait_polls();
   if (ro) {
     f.route_one = 1;
     f.logits = ro->logits; f.bias = ro->bias; f.E = E;

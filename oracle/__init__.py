@@ -88,6 +88,8 @@ def lib() -> ctypes.CDLL:
         L.k3o_bf16_from_f32.restype, L.k3o_bf16_from_f32.argtypes = ctypes.c_uint16, [ctypes.c_float]
         L.k3o_matvec_mxfp4.restype = None
         L.k3o_matvec_mxfp4.argtypes = [vp, vp, vp, vp, i, i, i]
+        L.k3o_dequant_mxfp4.restype = None
+        L.k3o_dequant_mxfp4.argtypes = [vp, vp, vp, i, i, i]
         L.k3o_route.restype = i
         L.k3o_route.argtypes = [ctypes.POINTER(_Cfg), vp, vp, vp, i, vp, vp, vp, vp, vp]
         L.k3o_gates_for.restype = None
@@ -166,6 +168,17 @@ def matvec_mxfp4(x: np.ndarray, packed: np.ndarray, scales: np.ndarray, group: i
     y = np.empty(rows, dtype=np.float64)
     lib().k3o_matvec_mxfp4(_ptr(y), _ptr(x), _ptr(packed), _ptr(scales), n_in, rows, group)
     return y
+
+
+def dequant_mxfp4(packed: np.ndarray, scales: np.ndarray, n_in: int, group: int = 32) -> np.ndarray:
+    """The dense fp64 matrix W [rows, n_in] of an MXFP4 matrix: W = E2M1[nibble] * 2^(s-127),
+    a scale byte of 255 zeroing its group (README Part II section 4)."""
+    rows = packed.shape[0]
+    packed = _c(packed, np.uint8, (rows, (n_in + 1) // 2), "packed")
+    scales = _c(scales, np.uint8, (rows, (n_in + group - 1) // group), "scales")
+    w = np.empty((rows, n_in), dtype=np.float64)
+    lib().k3o_dequant_mxfp4(_ptr(w), _ptr(packed), _ptr(scales), n_in, rows, group)
+    return w
 
 
 # ---- router ---------------------------------------------------------------------------
@@ -282,6 +295,40 @@ def experts(cfg: Cfg, table: Mapping[int, ExpertBytes], x: np.ndarray, idx: np.n
     rc = lib().k3o_experts(ctypes.byref(c), arr, cfg.n_experts, _ptr(x), _ptr(idx), _ptr(gate), T, _ptr(y))
     if rc != 0:
         raise ValueError(f"k3o_experts failed with code {rc} (missing expert or bad index)")
+    return y
+
+
+def experts_dense(cfg: Cfg, table: Mapping[int, ExpertBytes], x: np.ndarray, idx: np.ndarray,
+                  gate: np.ndarray) -> np.ndarray:
+    """The routed sum of ``experts`` for large batches, fp64, in another arrangement of the
+    same definition: each chosen expert's three matrices are expanded to dense fp64
+    (``dequant_mxfp4``) and all of its tokens go through them at once with a library matmul
+    (g = X W1^T, u = X W3^T, act, o = act W2^T); y[t] then sums gate[t, j] * o in slot order
+    j = 0..k-1.  Only the order of the fp64 additions differs from ``experts`` (rounding
+    order, about 1e-15 relative).  An index outside [0, E) raises, as in ``experts``."""
+    T = x.shape[0]
+    L, I, G = cfg.latent, cfg.inter, cfg.group
+    x = _c(x, np.uint16, (T, L), "x")
+    idx = _c(idx, np.int32, (T, cfg.topk), "idx")
+    gate = _c(gate, np.float64, (T, cfg.topk), "gate")
+    if T and (idx.min() < 0 or idx.max() >= cfg.n_experts):
+        raise ValueError("expert index out of range")
+    xd = bf16_to_f64(x)
+    o = np.zeros((T, cfg.topk, L), dtype=np.float64)
+    for e in np.unique(idx):
+        e = int(e)
+        if e not in table:
+            raise ValueError(f"expert {e} missing from the table")
+        ex = table[e].checked(cfg)
+        tok, slot = np.nonzero(idx == e)
+        xe = xd[tok]
+        g = xe @ dequant_mxfp4(ex.w1p, ex.w1s, L, G).T
+        u = xe @ dequant_mxfp4(ex.w3p, ex.w3s, L, G).T
+        a = activation(cfg, g, u)
+        o[tok, slot] = a @ dequant_mxfp4(ex.w2p, ex.w2s, I, G).T
+    y = np.zeros((T, L), dtype=np.float64)
+    for j in range(cfg.topk):
+        y += gate[:, j:j + 1] * o[:, j]
     return y
 
 

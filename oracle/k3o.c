@@ -90,6 +90,26 @@ void k3o_matvec_mxfp4(double *y, const double *x, const uint8_t *packed,
     }
 }
 
+/* The whole matrix W[r][c] = E2M1[nibble(r, c)] * 2^(scale(r, c / group) - 127) in fp64,
+ * a NaN scale (255) giving a zero group: the same definition as the mat-vec above, written
+ * out element by element so that a library matmul can take the multiply-adds. */
+void k3o_dequant_mxfp4(double *w, const uint8_t *packed, const uint8_t *scales, int in,
+                       int rows, int group)
+{
+    const int ngroup = (in + group - 1) / group;
+    const size_t rowbytes = (size_t)(in + 1) / 2;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (int r = 0; r < rows; r++) {
+        const uint8_t *prow = packed + (size_t)r * rowbytes;
+        const uint8_t *srow = scales + (size_t)r * ngroup;
+        double *wr = w + (size_t)r * in;
+        for (int col = 0; col < in; col++)
+            wr[col] = k3o_e2m1(nibble_at(prow, col)) * k3o_e8m0(srow[col / group]);
+    }
+}
+
 /* ---- router (README Part II section 9) --------------------------------------------- */
 
 static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }

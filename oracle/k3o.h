@@ -70,6 +70,12 @@ uint16_t k3o_bf16_from_f32(float v);
 void k3o_matvec_mxfp4(double *y, const double *x, const uint8_t *packed,
                       const uint8_t *scales, int in, int rows, int group);
 
+/* The dense fp64 matrix W [rows][in] of an MXFP4 matrix (packed [rows][ceil(in/2)],
+ * scales [rows][ceil(in/group)]): W[r][c] = E2M1[nibble] * 2^(s - 127), s = 255 -> 0
+ * (README Part II section 4). */
+void k3o_dequant_mxfp4(double *w, const uint8_t *packed, const uint8_t *scales, int in,
+                       int rows, int group);
+
 /* Router for T tokens (README section 9):
  *   logit[t][e] = sum_i h[t][i]*Wr[e][i]            (bf16 inputs, fp64 sum)
  *   sc = 1/(1+exp(-logit))                           unbiased score

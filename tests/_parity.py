@@ -8,10 +8,12 @@ Rules (the workloads' statement, with the readings listed in the design notes):
     counted.  Tokens with gap <= GAP_TIE may pick a different set: counted, and their y is
     checked against the oracle's expert sum for the GPU's choice, with gates the oracle
     computes for that choice from its own scores.
-  * gates: |gate_gpu - gate_ref| <= GATE_RTOL * |gate_ref| (fp32 sigmoid of an fp32 sum
-    against fp64; from 64 tokens the router's sums run on the tensor cores, whose fp32
-    accumulation of the bf16 products rounds differently from a sequential fp32 sum, hence
-    1e-4 rather than the 1e-5 a CUDA-core dot reaches).
+  * gates: |gate_gpu - gate_ref| <= rtol * |gate_ref| (fp32 sigmoid of an fp32 sum against
+    fp64), with rtol chosen by the router that ran: GATE_RTOL_CUDA_CORE = 1e-5 below 64
+    tokens (the warp-per-row GEMV, a sequential fp32 dot per lane), GATE_RTOL_TENSOR = 1e-4
+    from 64 tokens, where the logits come from the tensor cores (bf16 x bf16 with fp32
+    accumulation in tensor memory, whose rounding order differs from a sequential sum;
+    errors up to 1.1e-5 were measured there).
   * y: ||dy||_2 / ||y_ref||_2 <= REL_L2 and max|dy| / max|y_ref| <= MAX_REL.
 """
 from __future__ import annotations
@@ -25,7 +27,16 @@ import oracle
 import synth
 
 GAP_TIE = 1e-4
-GATE_RTOL = 1e-4
+GATE_RTOL_CUDA_CORE = 1e-5
+GATE_RTOL_TENSOR = 1e-4
+ROUTER_TC_MIN_TOKENS = 64  # from this many tokens the router runs on the tensor cores
+
+
+def gate_rtol(T: int, hidden: int) -> float:
+    """The gate tolerance of the router that a T-token call runs (the tensor-core router
+    needs hidden >= 64 and hidden % 8 == 0)."""
+    tc = T >= ROUTER_TC_MIN_TOKENS and hidden >= 64 and hidden % 8 == 0
+    return GATE_RTOL_TENSOR if tc else GATE_RTOL_CUDA_CORE
 REL_L2 = 2e-3
 MAX_REL = 1e-2
 
@@ -65,8 +76,8 @@ class RoutingReport:
 
 
 def compare_routing(cfg: oracle.Cfg, idx_gpu: np.ndarray, gate_gpu: np.ndarray, r: oracle.Routing,
-                    rows: np.ndarray) -> RoutingReport:
-    """rows[i] is the oracle row (token) of GPU row i."""
+                    rows: np.ndarray, gate_rtol_: float) -> RoutingReport:
+    """rows[i] is the oracle row (token) of GPU row i; gate_rtol_ from gate_rtol()."""
     near = changes = swaps = 0
     max_gate_rel = 0.0
     for i, t in enumerate(rows):
@@ -84,7 +95,7 @@ def compare_routing(cfg: oracle.Cfg, idx_gpu: np.ndarray, gate_gpu: np.ndarray, 
                 swaps += 1
         ref_gate = oracle.gates_for(cfg, r.sc[t], gi)
         rel = np.max(np.abs(gate_gpu[i] - ref_gate) / np.abs(ref_gate))
-        assert rel <= GATE_RTOL, f"token {t}: gate relative error {rel:.3e}"
+        assert rel <= gate_rtol_, f"token {t}: gate relative error {rel:.3e} > {gate_rtol_}"
         max_gate_rel = max(max_gate_rel, float(rel))
     return RoutingReport(len(rows), near, changes, swaps, max_gate_rel)
 

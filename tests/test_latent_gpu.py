@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import synth
-from _parity import (compare_routing, compare_y, gpu_cfg, oracle_cfg, oracle_table, to_dev_bf16)
+from _parity import (compare_routing, compare_y, gate_rtol, gpu_cfg, oracle_cfg, oracle_table, to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -48,7 +48,7 @@ def _run(w: synth.Workload, n_shared: int, T: int, latent_norm=True, act=0, laye
 
     ocfg = oracle_cfg(w, act)
     r = oracle.route(ocfg, li.h, li.wr, li.bias)
-    compare_routing(ocfg, idx, gate, r, np.arange(T))
+    compare_routing(ocfg, idx, gate, r, np.arange(T), gate_rtol(T, w.hidden))
     table = oracle_table(w, layer, r.idx.ravel())
     olw = oracle.LatentWeights(down=lw.down, up=lw.up, norm_w=lw.norm_w, latent_norm=latent_norm,
                                rms_eps=1e-5, n_shared=n_shared, sh1=lw.sh1, sh3=lw.sh3, sh2=lw.sh2)

@@ -2,7 +2,8 @@
 
 Every mutant is a one-line change to a temporary copy of ``oracle/k3o.c``: a swapped
 nibble order, an off-by-one exponent bias, a flipped tie rule, gates taken from the biased
-score, a dropped renormalisation, a dropped group, gate and up swapped in SwiGLU, w1 and w3
+score, a dropped renormalisation, a dropped group, a shifted scale or a neighbour's nibble in the dense expansion, gate and
+up swapped in SwiGLU, w1 and w3
 swapped, a transposed activation operand, and in the LatentMoE wrapper a dropped norm
 weight, a transposed dense mat-vec, a mis-rounded latent, a skipped aggregate norm, weighted
 or swapped shared experts.  ``tests/test_oracle_pins.py`` and ``tests/test_oracle_latent.py``
@@ -37,6 +38,8 @@ MUTANTS = {
     "latent_z_misrounded": ("k3o_bf16_from_f32((float)zd[i])", "k3o_bf16_from_f32((float)(zd[i] * 1.0078125))"),
     "latent_norm_skipped": ("if (lw->latent_norm) k3o_rmsnorm_w", "if (0) k3o_rmsnorm_w"),
     "latent_shared_weighted": ("for (int i = 0; i < H; i++) ot[i] += o[i];", "for (int i = 0; i < H; i++) ot[i] += 0.5 * o[i];"),
+    "dequant_scale_off_by_one": ("* k3o_e8m0(srow[col / group]);", "* k3o_e8m0(srow[col / group] + 1);"),
+    "dequant_neighbour_column": ("wr[col] = k3o_e2m1(nibble_at(prow, col))", "wr[col] = k3o_e2m1(nibble_at(prow, col ^ 1))"),
     "latent_shared_gate_is_up": ("k3o_matvec_bf16(g, hd, lw->sh1, H, SI);", "k3o_matvec_bf16(g, hd, lw->sh3, H, SI);"),
 }
 

@@ -173,6 +173,19 @@ def test_matvec_dense_equivalence_numpy():
         np.testing.assert_allclose(oracle.matvec_mxfp4(x, packed, scales), W @ x, rtol=1e-12, atol=1e-12)
 
 
+def test_dequant_matches_printed_decode():
+    """The dense expansion equals the printed decode rule element by element, NaN-scale
+    groups included (zero)."""
+    rng = np.random.default_rng(10)
+    for cols, rows in ((64, 3), (77, 5), (3584 // 16, 7)):
+        packed, scales = rand_mx(rng, rows, cols)
+        scales[0, 0] = 255
+        W = oracle.dequant_mxfp4(packed, scales, cols)
+        ref = dense_from_mx(packed, scales, cols)
+        assert np.array_equal(W, ref)
+        assert not W[0, :min(32, cols)].any()
+
+
 # ---- expert FFN ---------------------------------------------------------------------
 
 def test_expert_ffn_dense_torch_fp64_and_bf16():
@@ -215,6 +228,24 @@ def test_experts_sum_matches_per_expert_ffn():
         xt = oracle.bf16_to_f64(x[t])
         ref = sum(r.gate[t, j] * oracle.expert_ffn(cfg, table[int(r.idx[t, j])], xt) for j in range(cfg.topk))
         np.testing.assert_allclose(y[t], ref, rtol=1e-12, atol=1e-9)
+
+
+def test_experts_dense_equals_scalar_sum():
+    """The batched dense arrangement of the routed sum (for full-size checks) gives the
+    scalar oracle's y up to fp64 rounding order, with repeated experts in a token's list
+    and a NaN-scale group planted."""
+    cfg, table, h, wr, bias, x = _layer_case(seed=23, T=7)
+    table[2].w1s[5, 1] = 255
+    r = oracle.route(cfg, h, wr, bias)
+    idx = r.idx.copy()
+    idx[3] = [2, 2, 5]
+    y = oracle.experts(cfg, table, x, idx, r.gate)
+    yd = oracle.experts_dense(cfg, table, x, idx, r.gate)
+    np.testing.assert_allclose(yd, y, rtol=1e-12, atol=1e-12 * float(np.abs(y).max()))
+    with pytest.raises(ValueError):
+        bad = idx.copy()
+        bad[0, 0] = cfg.n_experts
+        oracle.experts_dense(cfg, table, x, bad, r.gate)
 
 
 def test_invariant_w2_scale_plus_one_doubles_y():

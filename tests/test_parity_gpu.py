@@ -2,9 +2,13 @@
 
 Small shapes (the oracle finishes in well under a second) cover several tiles and ragged
 tails, both bucketing paths, k == E, SiTU, NaN-scale groups, dropped and duplicate
-indices and T == 0.  The Kimi-K3 workloads run at full size in the launch configuration
-the benchmark times; the oracle checks every index it computes and y on sampled tokens.
+indices, inputs with a large dynamic range inside each group of 32, and T == 0.  The
+Kimi-K3 workloads run at full size in the launch configuration the benchmark times, and
+every token is checked: routing against the oracle's router, y against the oracle's routed
+sum (the scalar form, or for the 4096-token prefill the dense form of the same definition,
+``oracle.experts_dense``).  Each prints one JSON line with its counts.
 """
+import json
 import dataclasses
 import gc
 
@@ -13,8 +17,8 @@ import pytest
 
 import oracle
 import synth
-from _parity import (DeviceLayer, compare_routing, compare_y, gpu_cfg, oracle_cfg, oracle_table,
-                     reference_routing_for_gpu, to_dev_bf16)
+from _parity import (DeviceLayer, compare_routing, compare_y, gate_rtol, gpu_cfg, oracle_cfg,
+                     oracle_table, reference_routing_for_gpu, to_dev_bf16)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -25,22 +29,32 @@ def _k3():
     return k3
 
 
-def _check_layer(w, dl, rows=None, act=0, layer=0):
-    """Run the GPU layer on all tokens; check routing on `rows` (default: all) and y."""
+def _check_layer(w, dl, act=0, layer=0, dense=False):
+    """Run the GPU layer on all tokens and check every token: routing and y."""
     y, idx, gate, gap, status = dl.run(act=act)
     T = dl.h.shape[0]
-    rows = np.arange(T) if rows is None else np.asarray(rows)
     ocfg = oracle_cfg(w, act)
-    r = oracle.route(ocfg, dl.li.h[rows], dl.li.wr, dl.li.bias)
-    local = np.arange(len(rows))
-    rep = compare_routing(ocfg, idx[rows], gate[rows], r, local)
-    ridx, rgate = reference_routing_for_gpu(ocfg, idx[rows], r, local)
+    r = oracle.route(ocfg, dl.li.h, dl.li.wr, dl.li.bias)
+    rows = np.arange(T)
+    rep = compare_routing(ocfg, idx, gate, r, rows, gate_rtol(T, w.hidden))
+    ridx, rgate = reference_routing_for_gpu(ocfg, idx, r, rows)
     table = oracle_table(w, layer, ridx.reshape(-1))
-    y_ref = oracle.experts(ocfg, table, dl.li.x[rows], ridx, rgate)
-    yr = compare_y(y[rows], y_ref)
+    y_ref = (oracle.experts_dense if dense else oracle.experts)(ocfg, table, dl.li.x, ridx, rgate)
+    yr = compare_y(y, y_ref)
     assert status[0] == 0 and status[1] == 0
-    np.testing.assert_allclose(gap[rows], r.gap, rtol=1e-3, atol=1e-5)
-    return rep, yr
+    np.testing.assert_allclose(gap, r.gap, rtol=1e-3, atol=1e-5)
+    return rep, yr, idx
+
+
+def _record(name, w, rep, yr, idx):
+    """One JSON line per full-size workload: the counts the index rule asks to report."""
+    counts = np.bincount(idx.reshape(-1), minlength=w.E)
+    print("\nPARITY " + json.dumps({
+        "workload": name, "tokens": rep.tokens, "near_ties": rep.near_ties,
+        "set_changes": rep.set_changes, "order_swaps": rep.order_swaps,
+        "max_gate_rel": rep.max_gate_rel, "rel_l2": yr.rel_l2, "max_rel": yr.max_rel,
+        "max_abs": yr.max_abs, "distinct_experts": int((counts > 0).sum()),
+        "max_tokens_per_expert": int(counts.max())}))
 
 
 SMALL = [
@@ -79,7 +93,7 @@ def test_nan_scale_and_zero_nibble_groups():
     y, idx, gate, gap, status = dl.run()
     ocfg = oracle_cfg(w)
     r = oracle.route(ocfg, dl.li.h, dl.li.wr, dl.li.bias)
-    compare_routing(ocfg, idx, gate, r, np.arange(w.T))
+    compare_routing(ocfg, idx, gate, r, np.arange(w.T), gate_rtol(w.T, w.hidden))
     table = {e: oracle.ExpertBytes(*(d[n][e].cpu().numpy() for n in synth.TENSOR_SHAPES)) for e in range(w.E)}
     compare_y(y, oracle.experts(ocfg, table, dl.li.x, r.idx, r.gate))
 
@@ -175,43 +189,74 @@ def _free():
 def test_k3_tiny_4_tokens_64_experts():
     w = synth.WORKLOADS[0]
     dl = DeviceLayer(w)
-    rep, yr = _check_layer(w, dl)
-    print(f"\n[tiny] routing {rep}  y {yr}")
+    rep, yr, idx = _check_layer(w, dl)
+    _record("tiny", w, rep, yr, idx)
 
 
 def test_k3_decode_batch1():
     w = synth.WORKLOADS[1]
     dl = DeviceLayer(w)
-    rep, yr = _check_layer(w, dl)
-    print(f"\n[decode T=1] routing {rep}  y {yr}")
+    rep, yr, idx = _check_layer(w, dl)
+    _record("batch-1 decode", w, rep, yr, idx)
     del dl
     _free()
 
 
 def test_k3_batched_decode_64_skewed():
+    """All 64 tokens: routing (the tensor-core router) and y."""
     w = synth.WORKLOADS[2]
     dl = DeviceLayer(w)
-    y, idx, gate, gap, status = dl.run()
-    ocfg = oracle_cfg(w)
-    r_all = oracle.route(ocfg, dl.li.h, dl.li.wr, dl.li.bias)
-    rep = compare_routing(ocfg, idx, gate, r_all, np.arange(w.T))
+    rep, yr, idx = _check_layer(w, dl)
     counts = np.bincount(idx.reshape(-1), minlength=w.E)
     assert counts[dl.li.hot].min() >= 1
-    rows = np.arange(0, w.T, 4)
-    sub = oracle.Routing(r_all.idx[rows], r_all.gate[rows], r_all.gap[rows], r_all.sc[rows], r_all.ch[rows])
-    ridx, rgate = reference_routing_for_gpu(ocfg, idx[rows], sub, np.arange(len(rows)))
-    y_ref = oracle.experts(ocfg, oracle_table(w, 0, ridx.reshape(-1)), dl.li.x[rows], ridx, rgate)
-    yr = compare_y(y[rows], y_ref)
-    print(f"\n[batched decode T=64] routing {rep}  y {yr}  tokens/expert max {counts.max()}")
+    _record("batched decode", w, rep, yr, idx)
     del dl
     _free()
 
 
-def test_k3_prefill_4096_sampled():
+def test_k3_prefill_4096_all_tokens():
+    """All 4096 tokens: routing against the oracle's router, y against the dense form of the
+    oracle's routed sum (the same definition with a library matmul as its multiply step)."""
     w = synth.WORKLOADS[3]
     dl = DeviceLayer(w)
-    rows = np.linspace(0, w.T - 1, 24).astype(np.int64)
-    rep, yr = _check_layer(w, dl, rows=rows)
-    print(f"\n[prefill T=4096, 24 sampled tokens] routing {rep}  y {yr}")
+    rep, yr, idx = _check_layer(w, dl, dense=True)
+    _record("prefill", w, rep, yr, idx)
     del dl
     _free()
+
+
+# ---- large dynamic range inside a group of 32 (the activation split's worst inputs) --------
+
+def _adversarial_x(li, kind, seed):
+    """x with one element per group of 32 at 2^8 .. 2^12 times the rest (kind "spike"), or
+    drawn from a Cauchy distribution clipped to +-2^14 (kind "cauchy"), as bf16 bits; the
+    heavy tails of x carry through g and u into a heavy-tailed act for the second GEMM."""
+    rng = np.random.default_rng(seed)
+    T, L = li.x.shape
+    if kind == "spike":
+        v = rng.standard_normal((T, L // 32, 32)).astype(np.float32)
+        pos = rng.integers(0, 32, size=(T, L // 32))
+        p = rng.integers(8, 13, size=(T, L // 32)).astype(np.float32)
+        sign = np.where(rng.random((T, L // 32)) < 0.5, -1.0, 1.0).astype(np.float32)
+        t_i, g_i = np.meshgrid(np.arange(T), np.arange(L // 32), indexing="ij")
+        v[t_i, g_i, pos] = sign * np.exp2(p) * (1.0 + rng.random((T, L // 32), dtype=np.float32))
+        v = v.reshape(T, L)
+    else:
+        v = np.clip(rng.standard_cauchy((T, L)), -2.0 ** 14, 2.0 ** 14).astype(np.float32)
+    return synth.f32_to_bf16_bits(v)
+
+
+@pytest.mark.parametrize("T", [1, 3, 9])
+@pytest.mark.parametrize("kind", ["spike", "cauchy"])
+def test_tensor_core_path_large_in_group_range(kind, T):
+    """The tensor-core expert path (4-term MXFP4 activations) against the oracle on inputs
+    whose groups of 32 span 2^8 .. 2^12 (or Cauchy tails), at the workload tolerances.  One
+    token takes the single-token kernels, 3 tokens 16-column tiles, 9 tokens 64-column
+    tiles."""
+    import dataclasses
+    w = synth.small_workload(T=T, E=24, k=6, latent=1024, inter=1536, hidden=512, seed=40 + T)
+    li = synth.layer_inputs(w, 0)
+    li = dataclasses.replace(li, x=_adversarial_x(li, kind, seed=T))
+    dl = DeviceLayer(w, li=li)
+    rep, yr, idx = _check_layer(w, dl)
+    print(f"\n[{kind} T={T}] y {yr}")
