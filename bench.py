@@ -261,6 +261,241 @@ def run_reference(args):
 
 # ---- GPU arm --------------------------------------------------------------------------
 
+def load_peaks():
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = json.load(open(peaks_path)) if os.path.exists(peaks_path) else {}
+    hbm = peaks.get("hbm_gbs")
+    bf16 = peaks.get("bf16_tflops")
+    return {"hbm_gbs": hbm or 6800.0, "hbm_src": "measured" if hbm else "fallback",
+            "fp4_tflops": (bf16 or 1900.0) * 6.0,
+            "fp4_src": ("measured bf16_tflops" if bf16 else "fallback 1.9 PFLOP/s bf16")
+                       + " x 6 (the nominal dense fp4 : bf16 ratio, 13.5 : 2.25 PFLOP/s)"}
+
+
+def gemm_kernel_name(T: int) -> str:
+    n = 16 if T * TERMS <= 16 else 64
+    return (f"k_moe_tc<{n},0> (w1+w3 block-scaled tcgen05 GEMM fed by TMA, SwiGLU + "
+            "MXFP4-term epilogue)")
+
+
+class GraphTimer:
+    """Times `steps` calls of step(i) (i = 0 .. steps-1) replayed from CUDA graphs of
+    `rotation` consecutive steps, with CUDA events on the launching stream and nvidia-smi
+    clocks sampled during the timed region; a second pass with event-record nodes between
+    the library's phases gives per-phase means."""
+
+    def __init__(self, torch, k3, dev, local, step, rotation, n_phase_calls):
+        self.torch, self.k3, self.dev, self.local = torch, k3, dev, local
+        self.step, self.rotation, self.n_calls = step, rotation, n_phase_calls
+        self.cap_stream = torch.cuda.Stream(dev)
+
+    def capture(self, n_steps, phase_events=None):
+        torch, k3 = self.torch, self.k3
+        g = torch.cuda.CUDAGraph()
+        self.cap_stream.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.graph(g, stream=self.cap_stream):
+            for i in range(n_steps):
+                self.step(i, phase_events[i] if phase_events is not None else None)
+            if phase_events is not None:
+                k3.k3moe_set_phase_events(None)
+        torch.cuda.current_stream(self.dev).wait_stream(self.cap_stream)
+        return g
+
+    def run(self, steps, warmup, world=1):
+        torch, k3, dev = self.torch, self.k3, self.dev
+        n0 = k3.k3moe_launch_count()
+        self.step(0, None)
+        launches_per_step = k3.k3moe_launch_count() - n0
+        for i in range(1, warmup):
+            self.step(i, None)
+        torch.cuda.synchronize(dev)
+        full = self.capture(self.rotation)
+        rem = steps % self.rotation
+        tail = self.capture(rem) if rem else None
+        for _ in range(2):
+            full.replay()
+        torch.cuda.synchronize(dev)
+        stream = torch.cuda.current_stream(dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(self.local) as clk:
+            e0.record(stream)
+            for _ in range(steps // self.rotation):
+                full.replay()
+            if tail is not None:
+                tail.replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        elapsed = e0.elapsed_time(e1) / 1e3
+        # phase pass: the same steps with event-record nodes between the phases of each call
+        evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(self.n_calls)]
+               for _ in range(self.rotation)]
+        for a in evs:  # torch creates the CUDA event at its first record
+            for row in a:
+                for ev in row:
+                    ev.record(stream)
+        torch.cuda.synchronize(dev)
+        timed = self.capture(self.rotation, evs)
+        samples = []
+        for _ in range(max(1, min(20, steps // self.rotation))):
+            timed.replay()
+            torch.cuda.synchronize(dev)
+            samples.append([[[evs[i][c][j].elapsed_time(evs[i][c][j + 1]) for j in range(5)]
+                             for c in range(self.n_calls)] for i in range(self.rotation)])
+        ph = np.array(samples).reshape(-1, 5) / 1e3  # one row per library call
+        return {"elapsed": elapsed, "launches_per_step": launches_per_step, "phase_s": ph.mean(axis=0),
+                "clocks": clk.summary()}
+
+
+PHASES = ["route", "bucket+prep", "gemm1", "gemm2", "combine"]
+
+
+def bf16_dev(torch, dev, a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def layer_setup(torch, k3, w, dev, NL, rotation, off=0, world=1):
+    """NL independent layers (own experts, router weight, bias) and `rotation` token batches:
+    batch r is drawn from layer r % NL's seeded stream."""
+    cfg = k3.Cfg(hidden=w.hidden, n_experts=w.E, topk=w.k, latent=w.latent, inter=w.inter,
+                 routed_scale=w.routed_scale)
+    experts_l = [k3.Experts.from_dict(synth.experts_device(w, l, dev)) for l in range(NL)]
+    lis = [synth.layer_inputs(w, l, T=w.T * rotation * world) for l in range(NL)]
+    H = torch.stack([bf16_dev(torch, dev, lis[r % NL].h[off + r * w.T:off + (r + 1) * w.T]) for r in range(rotation)])
+    X = torch.stack([bf16_dev(torch, dev, lis[r % NL].x[off + r * w.T:off + (r + 1) * w.T]) for r in range(rotation)])
+    wr_l = [bf16_dev(torch, dev, li_.wr) for li_ in lis]
+    bias_l = [None if li_.bias is None else torch.from_numpy(li_.bias).to(dev) for li_ in lis]
+    return cfg, experts_l, H, X, wr_l, bias_l
+
+
+def measure_layer_workload(torch, k3, w, dev, local, peaks, steps, warmup, NL, rotation):
+    """One sub-record: a single-layer workload (batched decode, prefill) timed like the
+    headline line, with its own routing's distinct-expert count and the layer's bytes."""
+    rotation = ((rotation + NL - 1) // NL) * NL
+    cfg, experts_l, H, X, wr_l, bias_l = layer_setup(torch, k3, w, dev, NL, rotation)
+    T = w.T
+    ws = k3.workspace(cfg, T, dev)
+    y = torch.empty((T, w.latent), dtype=torch.float32, device=dev)
+    idx = torch.empty((rotation, T, w.k), dtype=torch.int32, device=dev)
+    gate = torch.empty((T, w.k), dtype=torch.float32, device=dev)
+    status = torch.zeros(4, dtype=torch.int32, device=dev)
+
+    def step(i, ev):
+        r = i % rotation
+        l = r % NL
+        if ev is not None:
+            k3.k3moe_set_phase_events(ev[0])
+        k3.k3moe_layer(cfg, H[r], wr_l[l], bias_l[l], experts_l[l], X[r], y, idx[r], gate, None, status, ws)
+
+    gt = GraphTimer(torch, k3, dev, local, step, rotation, 1)
+    res = gt.run(steps, warmup)
+    st = status.cpu().numpy()
+    if st[0] or st[1]:
+        raise SystemExit(f"{w.name}: device status reports dropped={st[0]} timeouts={st[1]}")
+    distinct = float(np.mean([len(set(idx[r].reshape(-1).tolist())) for r in range(rotation)]))
+    t_layer = res["elapsed"] / steps
+    lb = layer_bytes(w, distinct, T)
+    ph = res["phase_s"]
+    g1 = float(ph[2])
+    rec = {
+        "workload": w.name, "tokens_per_step": T, "steps": steps, "warmup": warmup,
+        "tokens_per_s": T / t_layer, "us_per_layer": t_layer * 1e6,
+        "distinct_experts_per_layer": distinct, "algorithmic_bytes_per_layer": lb,
+        "achieved_TBps": lb / t_layer / 1e12, "frac_of_hbm_peak": lb / t_layer / 1e9 / peaks["hbm_gbs"],
+        "phase_us": {n: float(ph[j] * 1e6) for j, n in enumerate(PHASES)},
+        "dominant_kernel": {"name": gemm_kernel_name(T), "avg_launch_us": g1 * 1e6,
+                            "algorithmic_bytes_per_launch": gemm1_bytes(w, distinct, T),
+                            "achieved_GBps": gemm1_bytes(w, distinct, T) / g1 / 1e9,
+                            "frac_of_hbm_peak": gemm1_bytes(w, distinct, T) / g1 / 1e9 / peaks["hbm_gbs"]},
+        "layers_rotated": NL, "token_batches_rotated": rotation,
+        "l2": f"{lb / 1e6:.0f} MB per step (> {L2_BYTES / 1e6:.0f} MB L2), {NL} independent layers rotated",
+        "gpu_launches_per_step": res["launches_per_step"], "clocks": res["clocks"],
+    }
+    if T >= 1024:
+        flops = gemm1_flops(w, T) * 1.5  # both expert GEMMs: 3 matrices of I x L per pair
+        gemms = float(ph[2] + ph[3])
+        useful = flops / gemms / 1e12
+        rec["tensor"] = {"expert_gemms_us": gemms * 1e6, "useful_tflops": useful,
+                         "issued_tflops": useful * TERMS, "fp4_peak_tflops": peaks["fp4_tflops"],
+                         "fp4_peak_source": peaks["fp4_src"],
+                         "frac_useful": useful / peaks["fp4_tflops"],
+                         "frac_issued": useful * TERMS / peaks["fp4_tflops"],
+                         "note": "issued work is 4x the useful work: each activation enters the "
+                                 "block-scaled MMA as 4 MXFP4 terms"}
+    del experts_l, ws
+    return rec
+
+
+def measure_stack_workload(torch, k3, w, dev, local, peaks, steps, warmup, rotation=4):
+    """The 8-layer stack: one step = 8 chained layers on 16 tokens, each layer's y RMS-
+    normalised and rounded to bf16 into the next layer's x and h = [x, x]."""
+    cfg = k3.Cfg(hidden=w.hidden, n_experts=w.E, topk=w.k, latent=w.latent, inter=w.inter,
+                 routed_scale=w.routed_scale)
+    NL, T = w.layers, w.T
+    experts_l = [k3.Experts.from_dict(synth.experts_device(w, l, dev)) for l in range(NL)]
+    lis = [synth.layer_inputs(w, l, T=T * rotation) for l in range(NL)]
+    wr_l = [bf16_dev(torch, dev, li_.wr) for li_ in lis]
+    bias_l = [torch.from_numpy(li_.bias).to(dev) for li_ in lis]
+    H0 = torch.stack([bf16_dev(torch, dev, lis[0].h[r * T:(r + 1) * T]) for r in range(rotation)])
+    X0 = torch.stack([bf16_dev(torch, dev, lis[0].x[r * T:(r + 1) * T]) for r in range(rotation)])
+    ws = k3.workspace(cfg, T, dev)
+    y = torch.empty((T, w.latent), dtype=torch.float32, device=dev)
+    xs = torch.empty((T, w.latent), dtype=torch.bfloat16, device=dev)
+    hs = torch.empty((T, 2 * w.latent), dtype=torch.bfloat16, device=dev)
+    idx = torch.empty((rotation, NL, T, w.k), dtype=torch.int32, device=dev)
+    status = torch.zeros(4, dtype=torch.int32, device=dev)
+
+    def step(i, ev):
+        r = i % rotation
+        h, x = H0[r], X0[r]
+        for l in range(NL):
+            if ev is not None:
+                k3.k3moe_set_phase_events(ev[l])
+            k3.k3moe_layer(cfg, h, wr_l[l], bias_l[l], experts_l[l], x, y, idx[r, l], None, None, status, ws)
+            if ev is not None:
+                k3.k3moe_set_phase_events(None)
+            k3.k3moe_stack_link(y, xs, hs, norm=True)
+            h, x = hs, xs
+
+    gt = GraphTimer(torch, k3, dev, local, step, rotation, NL)
+    res = gt.run(steps, warmup)
+    st = status.cpu().numpy()
+    if st[0] or st[1]:
+        raise SystemExit(f"{w.name}: device status reports dropped={st[0]} timeouts={st[1]}")
+    distinct = [float(np.mean([len(set(idx[r, l].reshape(-1).tolist())) for r in range(rotation)]))
+                for l in range(NL)]
+    t_step = res["elapsed"] / steps
+    lb = sum(layer_bytes(w, d, T) for d in distinct)
+    ph = res["phase_s"]
+    g1 = float(ph[2])
+    d_mean = float(np.mean(distinct))
+    rec = {
+        "workload": w.name, "tokens_per_step": T, "layers_per_step": NL, "steps": steps, "warmup": warmup,
+        "tokens_per_s": T / t_step, "us_per_layer": t_step / NL * 1e6, "us_per_step": t_step * 1e6,
+        "distinct_experts_per_layer": d_mean, "algorithmic_bytes_per_step": lb,
+        "achieved_TBps": lb / t_step / 1e12, "frac_of_hbm_peak": lb / t_step / 1e9 / peaks["hbm_gbs"],
+        "phase_us_per_layer": {n: float(ph[j] * 1e6) for j, n in enumerate(PHASES)},
+        "dominant_kernel": {"name": gemm_kernel_name(T), "avg_launch_us": g1 * 1e6,
+                            "algorithmic_bytes_per_launch": gemm1_bytes(w, d_mean, T),
+                            "frac_of_hbm_peak": gemm1_bytes(w, d_mean, T) / g1 / 1e9 / peaks["hbm_gbs"]},
+        "link": "RMSNorm (unit weight, eps 1e-5) and bf16 rounding between layers (the stack reading: "
+                "the literal chain leaves fp32 at layer 4)",
+        "l2": f"{lb / 1e9:.1f} GB per step over {NL} layers with their own experts (126 GB resident)",
+        "gpu_launches_per_step": res["launches_per_step"], "clocks": res["clocks"],
+    }
+    del experts_l, ws
+    return rec
+
+
+def steps_for(budget_s: float, est_s: float, cap: int) -> int:
+    return int(max(3, min(cap, round(budget_s / max(est_s, 1e-6)))))
+
+
 def run_ours(args):
     import torch
     import mxfp4_routed_expert_gemv_gb300 as k3
@@ -276,7 +511,7 @@ def run_ours(args):
     if args.experts:
         w = dataclasses.replace(w, E=args.experts, name=w.name + f" [profiling variant: {args.experts} experts]")
     if w.layers != 1:
-        raise SystemExit("the stacked workload is a parity case, not a bench line")
+        raise SystemExit("the stacked workload is a sub-record of the default run, not a headline")
     # Steps cycle through NL independent layers (own experts, router weight and bias), as a
     # decode pass does: between two uses of one layer, NL - 1 others stream their weights, so
     # nothing of a layer is still in L2 when it comes back.  (With one layer, consecutive
@@ -287,23 +522,12 @@ def run_ours(args):
     need = NL * w.E * w.expert_bytes + (4 << 30)
     if need > free:
         raise SystemExit(f"needs {need / 1e9:.1f} GB of HBM, {free / 1e9:.1f} GB free")
+    peaks = load_peaks()
 
-    cfg = k3.Cfg(hidden=w.hidden, n_experts=w.E, topk=w.k, latent=w.latent, inter=w.inter,
-                 routed_scale=w.routed_scale)
-    experts_l = [k3.Experts.from_dict(synth.experts_device(w, l, dev)) for l in range(NL)]
     rotation = args.rotation if w.T == 1 else 4
     rotation = ((rotation + NL - 1) // NL) * NL  # whole layer cycles per graph
     off = rank_token_offset(rank, rotation * w.T)
-
-    def bf16(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
-
-    lis = [synth.layer_inputs(w, l, T=w.T * rotation * world) for l in range(NL)]
-    # step r: layer r % NL, the token inputs of slot r drawn from that layer's stream
-    H = torch.stack([bf16(lis[r % NL].h[off + r * w.T:off + (r + 1) * w.T]) for r in range(rotation)])
-    X = torch.stack([bf16(lis[r % NL].x[off + r * w.T:off + (r + 1) * w.T]) for r in range(rotation)])
-    wr_l = [bf16(li_.wr) for li_ in lis]
-    bias_l = [None if li_.bias is None else torch.from_numpy(li_.bias).to(dev) for li_ in lis]
+    cfg, experts_l, H, X, wr_l, bias_l = layer_setup(torch, k3, w, dev, NL, rotation, off, world)
     T = w.T
     ws = k3.workspace(cfg, T, dev)
     y = torch.empty((T, w.latent), dtype=torch.float32, device=dev)
@@ -311,118 +535,64 @@ def run_ours(args):
     gate = torch.empty((T, w.k), dtype=torch.float32, device=dev)
     status = torch.zeros(4, dtype=torch.int32, device=dev)
 
-    def step(i):  # one layer on the current stream
+    def step(i, ev):  # one layer on the current stream
         r = i % rotation
         l = r % NL
+        if ev is not None:
+            k3.k3moe_set_phase_events(ev[0])
         k3.k3moe_layer(cfg, H[r], wr_l[l], bias_l[l], experts_l[l], X[r], y, idx[r], gate, None,
                        status, ws)
 
-    # eager warm-up (also configures the kernels' shared-memory limits before any capture)
-    n0 = k3.k3moe_launch_count()
-    step(0)
-    launches_per_step = k3.k3moe_launch_count() - n0
-    for i in range(1, args.warmup):
-        step(i)
-    torch.cuda.synchronize(dev)
-
-    # The decode loop is replayed from CUDA graphs: one graph holds `rotation` consecutive
-    # layers (each on its own token input), a second one the K mod rotation remainder.
-    cap_stream = torch.cuda.Stream(dev)
-
-    def capture(n_steps, phase_events=None):
-        g = torch.cuda.CUDAGraph()
-        cap_stream.wait_stream(torch.cuda.current_stream(dev))
-        with torch.cuda.graph(g, stream=cap_stream):
-            for i in range(n_steps):
-                if phase_events is not None:
-                    k3.k3moe_set_phase_events(phase_events[i])
-                step(i)
-            if phase_events is not None:
-                k3.k3moe_set_phase_events(None)
-        torch.cuda.current_stream(dev).wait_stream(cap_stream)
-        return g
-
-    full = capture(rotation)
-    rem = args.steps % rotation
-    tail = capture(rem) if rem else None
-    for _ in range(2):
-        full.replay()
-    torch.cuda.synchronize(dev)
-    distinct = [len(set(idx[r].reshape(-1).tolist())) for r in range(rotation)]
-    stream = torch.cuda.current_stream(dev)
-
-    # timed region: exactly K layers
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        e0.record(stream)
-        for _ in range(args.steps // rotation):
-            full.replay()
-        if tail is not None:
-            tail.replay()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    launches = launches_per_step * args.steps
-    elapsed = e0.elapsed_time(e1) / 1e3
+    # the timed region (exactly K layers replayed from CUDA graphs), then the phase pass
+    gt = GraphTimer(torch, k3, dev, local, step, rotation, 1)
+    res = gt.run(args.steps, args.warmup, world)
+    elapsed = res["elapsed"]
     elapsed_max = max_over_ranks(elapsed, world, dev)
     tokens = sum_over_ranks(T * args.steps, world, dev)
+    launches = res["launches_per_step"] * args.steps
     st = status.cpu().numpy()
     if st[0] or st[1]:
         raise SystemExit(f"device status reports dropped={st[0]} timeouts={st[1]}")
-
-    # phase pass: the same graph with event-record nodes between the phases; GEMM1 (the
-    # dominant kernel) duration = its events' difference on the launching stream
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(rotation)]
-    for row in evs:  # torch creates the CUDA event at its first record
-        for ev in row:
-            ev.record(stream)
-    torch.cuda.synchronize(dev)
-    timed = capture(rotation, evs)
-    samples = []
-    for _ in range(max(1, min(20, args.steps // rotation))):
-        timed.replay()
-        torch.cuda.synchronize(dev)
-        samples.append([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(rotation)])
-    ph = np.array(samples).reshape(-1, 5) / 1e3
-    gemm1_s = float(ph[:, 2].mean())
+    distinct = [len(set(idx[r].reshape(-1).tolist())) for r in range(rotation)]
+    ph = res["phase_s"]
+    gemm1_s = float(ph[2])
     d_mean = float(np.mean(distinct))
     g1_bytes = gemm1_bytes(w, d_mean, T)
-    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    peaks = json.load(open(peaks_path)) if os.path.exists(peaks_path) else {}
-    peak = peaks.get("hbm_gbs")
-    peak_src = "measured" if peak else "fallback"
-    peak = peak or 6800.0
+    peak = peaks["hbm_gbs"]
     achieved = g1_bytes / gemm1_s / 1e9
     g1_flops = gemm1_flops(w, T)
-    fp4_peak = peaks.get("bf16_tflops", 0.0) * 6.0 or None
     traffic = None
     prof = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(prof):
         with open(prof) as f:
             traffic = json.load(f).get(f"gemm1_workload{args.workload}")
 
-    # end to end through the host-buffer entry point (copies in and out, synchronised)
+    # end to end through the host-buffer entry point (copies in and out, synchronised), as a
+    # serving loop runs it: the step's token inputs are placed in fixed pinned staging
+    # buffers (a host copy, inside the timed region), the call copies them to the device,
+    # runs the layer and copies y back into a fixed pinned buffer
     n_e2e = min(args.steps, 2000)
     wsh = k3.workspace_host(cfg, T, dev)
-    hh = torch.empty((rotation, T, w.hidden), dtype=torch.bfloat16).pin_memory()
-    xh = torch.empty((rotation, T, w.latent), dtype=torch.bfloat16).pin_memory()
-    hh.copy_(H.cpu())
-    xh.copy_(X.cpu())
+    hh = H.cpu()
+    xh = X.cpu()
+    h_stage = torch.empty((T, w.hidden), dtype=torch.bfloat16).pin_memory()
+    x_stage = torch.empty((T, w.latent), dtype=torch.bfloat16).pin_memory()
     yh = torch.empty((T, w.latent), dtype=torch.float32).pin_memory()
-    for i in range(min(args.warmup, 50)):
-        k3.k3moe_layer_host(cfg, hh[i % rotation], wr_l[i % NL], bias_l[i % NL], experts_l[i % NL],
-                            xh[i % rotation], yh, status, wsh)
+
+    def e2e_step(i):
+        r = i % rotation
+        h_stage.copy_(hh[r])
+        x_stage.copy_(xh[r])
+        k3.k3moe_layer_host(cfg, h_stage, wr_l[r % NL], bias_l[r % NL], experts_l[r % NL], x_stage,
+                            yh, status, wsh)
+
+    for i in range(max(min(args.warmup, 50), 2 * NL)):
+        e2e_step(i)
     if world > 1:
         dist.barrier()
     t0 = time.perf_counter()
     for i in range(n_e2e):
-        k3.k3moe_layer_host(cfg, hh[i % rotation], wr_l[i % NL], bias_l[i % NL], experts_l[i % NL],
-                            xh[i % rotation], yh, status, wsh)
+        e2e_step(i)
     e2e_dt = max_over_ranks(time.perf_counter() - t0, world, dev)
     e2e_value = sum_over_ranks(T * n_e2e, world, dev) / e2e_dt
 
@@ -444,28 +614,136 @@ def run_ours(args):
                          f"{NL * w.E * w.expert_bytes / 1e9:.0f} GB resident) with {rotation} seeded token inputs, "
                          f"so a layer's weights are not in L2 when it comes back",
                    "layers_rotated": NL,
-                   "phase_ms": {n: float(ph[:, j].mean() * 1e3) for j, n in
-                                enumerate(["route", "bucket+prep", "gemm1", "gemm2", "combine"])},
+                   "phase_ms": {n: float(ph[j] * 1e3) for j, n in enumerate(PHASES)},
                    "launch": "CUDA graph replay, programmatic dependent launch between kernels",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm",
-                     "kernel": f"k_moe_tc<{16 if T * TERMS <= 16 else 64},0> (w1+w3 block-scaled "
-                               "tcgen05 GEMM fed by TMA, SwiGLU + MXFP4-term epilogue)",
+        "roofline": {"bound": "hbm", "kernel": gemm_kernel_name(T),
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": f"{peak_src} hbm_gbs", "traffic": traffic,
+                     "peak_source": f"{peaks['hbm_src']} hbm_gbs", "traffic": traffic,
                      "algorithmic_bytes_per_launch": g1_bytes, "avg_launch_s": gemm1_s,
                      "tensor": {"useful_tflops": g1_flops / gemm1_s / 1e12,
-                                "fp4_peak_tflops": fp4_peak,
-                                "fp4_peak_source": "measured bf16_tflops x 6 (nominal fp4:bf16 ratio)",
-                                "frac_useful": g1_flops / gemm1_s / 1e12 / fp4_peak if fp4_peak else None,
+                                "fp4_peak_tflops": peaks["fp4_tflops"], "fp4_peak_source": peaks["fp4_src"],
+                                "frac_useful": g1_flops / gemm1_s / 1e12 / peaks["fp4_tflops"],
                                 "issued_per_useful": TERMS}},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * (w.hidden + w.latent) * 2,
                 "d2h_bytes_per_step": T * w.latent * 4},
         "gpu_launches": int(launches),
-        "clocks": clk.summary(),
+        "clocks": res["clocks"],
     }
+    del experts_l, H, X, ws, wsh
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
+
+    # the other workloads, one sub-record each, on rank 0 of a single-GPU run (each is timed
+    # for a bounded number of steps: about args.sub_seconds of timed work)
+    if world == 1 and args.workload == 1 and not args.no_sub and not args.experts:
+        subs = {}
+        est = {2: 450e-6, 3: 18e-3, 4: 3e-3}
+        for wi in (2, 3, 4):
+            ws_ = synth.WORKLOADS[wi]
+            n = steps_for(args.sub_seconds, est[wi], args.steps)
+            if wi == 4:
+                rec = measure_stack_workload(torch, k3, ws_, dev, local, peaks, n, max(3, min(args.warmup, 5)))
+            else:
+                rec = measure_layer_workload(torch, k3, ws_, dev, local, peaks, n, max(3, min(args.warmup, 5)),
+                                             NL=8 if wi == 2 else 1, rotation=8 if wi == 2 else 2)
+            subs[{2: "batched_decode", 3: "prefill", 4: "stack_8_layers"}[wi]] = rec
+            gc.collect()
+            torch.cuda.empty_cache()
+        line["config"]["workloads"] = subs
+
     if rank == 0 and world == 1 and not args.no_cpu_baseline and w.T == 1:
         line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_ep(args):
+    """Expert parallelism (one rank per GPU): every rank holds one contiguous block of each
+    layer's experts (expert_block), routes every token itself, sums the terms of its own
+    experts (k3moe_experts_mxfp4_range) and one NCCL all-reduce per layer adds the partial y
+    (strong scaling: the job's work is fixed, N ranks share the experts).  Steps are eager
+    launches (the all-reduce is not captured into a graph), timed with CUDA events between
+    barriers, the slowest rank's time counted."""
+    import gc
+    import torch
+    import torch.distributed as dist
+    import mxfp4_routed_expert_gemv_gb300 as k3
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w = synth.WORKLOADS[args.workload]
+    if w.layers != 1:
+        raise SystemExit("--ep times a single-layer workload")
+    NL = max(1, args.layers)
+    e0, e1 = k3.expert_block(w.E, world, rank)
+    cfg = k3.Cfg(hidden=w.hidden, n_experts=w.E, topk=w.k, latent=w.latent, inter=w.inter,
+                 routed_scale=w.routed_scale)
+    blocks = []
+    for l in range(NL):  # generate a layer, keep this rank's block
+        full = k3.Experts.from_dict(synth.experts_device(w, l, dev))
+        b = full.block(e0, e1)
+        blocks.append(k3.Experts(*(t.clone() for t in (b.w1p, b.w1s, b.w3p, b.w3s, b.w2p, b.w2s))))
+        del full, b
+        gc.collect()
+        torch.cuda.empty_cache()
+    rotation = ((max(4, NL) + NL - 1) // NL) * NL
+    lis = [synth.layer_inputs(w, l, T=w.T * rotation) for l in range(NL)]
+    H = torch.stack([bf16_dev(torch, dev, lis[r % NL].h[r * w.T:(r + 1) * w.T]) for r in range(rotation)])
+    X = torch.stack([bf16_dev(torch, dev, lis[r % NL].x[r * w.T:(r + 1) * w.T]) for r in range(rotation)])
+    wr_l = [bf16_dev(torch, dev, li_.wr) for li_ in lis]
+    bias_l = [None if li_.bias is None else torch.from_numpy(li_.bias).to(dev) for li_ in lis]
+    T = w.T
+    ws = k3.workspace(cfg, T, dev)
+    y = torch.empty((T, w.latent), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, w.k), dtype=torch.int32, device=dev)
+    gate = torch.empty((T, w.k), dtype=torch.float32, device=dev)
+    status = torch.zeros(4, dtype=torch.int32, device=dev)
+
+    def step(i):
+        r = i % rotation
+        l = r % NL
+        k3.k3moe_route(cfg, H[r], wr_l[l], bias_l[l], idx, gate, None, ws)
+        k3.k3moe_experts_mxfp4_range(cfg, blocks[l], e0, e1, X[r], idx, gate, y, status, ws)
+        if world > 1:
+            dist.all_reduce(y)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    stream = torch.cuda.current_stream(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    elapsed = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
+    st = status.cpu().numpy()
+    if st[0] or st[1]:
+        raise SystemExit(f"device status reports dropped={st[0]} timeouts={st[1]}")
+    line = {
+        "metric": METRIC, "value": T * args.steps / elapsed, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
+        "dtype": "e2m1 x e2m1 (tcgen05 kind::mxf4, fp32 accumulation)", "data": "synthetic",
+        "config": {"workload": w.name, "parallelism": f"expert parallel x{world} (router replicated, "
+                   f"experts [{e0}, {e1}) on rank 0, NCCL all-reduce of y per layer)",
+                   "layers_rotated": NL, "launch": "eager launches (all-reduce not in a graph)"},
+        "clocks": clk.summary(),
+    }
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -606,9 +884,15 @@ def main():
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count (small-memory profiling variant, not a bench line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="skip the sub-records of the other workloads (batched decode, prefill, stack)")
+    ap.add_argument("--sub-seconds", type=float, default=1.0,
+                    help="timed work per sub-record (its step count is this over the step estimate)")
     ap.add_argument("--latent", action="store_true",
                     help="time the LatentMoE wrapper layer instead (an extra line, not the headline)")
     ap.add_argument("--n-shared", type=int, default=2)
+    ap.add_argument("--ep", action="store_true",
+                    help="expert parallelism: each rank holds a block of the experts, y is all-reduced")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
@@ -616,6 +900,8 @@ def main():
         run_reference(args)
     elif args.latent:
         run_latent(args)
+    elif args.ep:
+        run_ep(args)
     else:
         run_ours(args)
 

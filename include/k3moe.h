@@ -129,6 +129,23 @@ int k3moe_experts_mxfp4(const k3moe_cfg *cfg, const k3moe_experts *experts, cons
                         const int32_t *idx, const float *gate, int32_t T, float *y,
                         int32_t *status, void *ws, size_t ws_bytes, void *stream);
 
+/* The routed-expert sum over one block of experts, for expert parallelism: the E experts
+ * are split into contiguous blocks, one per device, and each device sums only the terms of
+ * the experts it holds (README Part II section 9's per-token sum, partitioned by expert);
+ * the devices' partial y then add up (an all-reduce) to the layer's y.
+ *   experts: the block [e0, e1) only, stacked from expert e0 (local expert e - e0), layouts
+ *            as in k3moe_experts; cfg->n_experts is the layer's E (0 <= e0 < e1 <= E)
+ *   idx, gate: the routing over all E experts (as k3moe_route writes it)
+ *   y:    fp32 [T][latent] (out), fully overwritten: sum over the assignments whose expert
+ *         is in [e0, e1); a token with none of them gets a zero row
+ *   An index in [0, E) outside the block is another device's and is skipped silently; an
+ *   index outside [0, E) is skipped and counted in status[0] (on every device).
+ *   ws:   at least k3moe_workspace_size(cfg, T) bytes.  Other arguments as k3moe_experts_mxfp4. */
+int k3moe_experts_mxfp4_range(const k3moe_cfg *cfg, const k3moe_experts *experts, int32_t e0,
+                              int32_t e1, const void *x, const int32_t *idx, const float *gate,
+                              int32_t T, float *y, int32_t *status, void *ws, size_t ws_bytes,
+                              void *stream);
+
 /* Router + routed-expert sum in one call (the layer).  idx, gate and gap are optional
  * outputs (NULL: kept in the workspace); other arguments as in the two calls above. */
 int k3moe_layer(const k3moe_cfg *cfg, const void *h, const void *wr, const float *bias,
@@ -142,9 +159,19 @@ int k3moe_workspace_size_host(const k3moe_cfg *cfg, int32_t T, size_t *bytes);
 
 /* k3moe_layer with HOST input and output buffers: copies h (bf16 [T][hidden]) and x
  * (bf16 [T][latent]) from host memory into the workspace, runs the layer, copies y (fp32
- * [T][latent]) back to host memory, and synchronises the stream before returning.  Host
- * buffers should be page-locked for asynchronous copies.  wr, bias, experts and status
- * stay in device memory.  Returns K3MOE_ERR_CUDA if a copy or the synchronisation fails. */
+ * [T][latent]) back to host memory, and synchronises the stream before returning.  The
+ * routing stays in the workspace.  wr, bias, experts and status stay in device memory.
+ * When h, x and y are all page-locked host memory mapped into the device's address space
+ * (cudaHostAlloc'd or registered pinned buffers), the kernels read h and x and write y in
+ * host memory directly (on a Grace-Blackwell node over NVLink-C2C) instead of staging them
+ * through the workspace.
+ * Host buffers should be page-locked: the library then records the first call with a given
+ * set of arguments (configuration, T, every pointer, ws_bytes, stream) as a CUDA graph and
+ * replays it for later calls with the same set (one launch instead of three copies and the
+ * layer's launches; the buffers' contents are read at each replay).  Up to 16 such graphs are
+ * kept per process, least recently used replaced; calls with pageable buffers, or while
+ * phase events are set, run without a graph.  Returns K3MOE_ERR_CUDA if a copy, a launch or
+ * the synchronisation fails. */
 int k3moe_layer_host(const k3moe_cfg *cfg, const void *h_host, const void *wr,
                      const float *bias, const k3moe_experts *experts, const void *x_host,
                      int32_t T, float *y_host, int32_t *status, void *ws, size_t ws_bytes,
@@ -257,6 +284,11 @@ int k3moe_set_flag_wait_polls(int64_t polls);
 /* Number of kernels the library launched through the entry points above since load
  * (host counter; for launch accounting in benchmarks). */
 int64_t k3moe_launch_count(void);
+
+/* The last CUDA failure seen by an entry point on the calling thread: the call that failed
+ * and CUDA's description of the error (for example a refused launch), or "" if none.  The
+ * string stays valid until the thread's next failing call. */
+const char *k3moe_last_error(void);
 
 /* Static string for a status code. */
 const char *k3moe_strerror(int status);

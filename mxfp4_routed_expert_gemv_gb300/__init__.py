@@ -26,7 +26,7 @@ __all__ = [
     "k3moe_launch_count", "k3moe_strerror", "k3moe_abi_version", "k3moe_set_phase_events",
     "k3moe_layer_static_scratch", "STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
     "Latent", "k3moe_latent_workspace_size", "latent_workspace", "k3moe_latent_layer",
-    "k3moe_set_flag_wait_polls",
+    "k3moe_set_flag_wait_polls", "k3moe_last_error", "k3moe_experts_mxfp4_range", "expert_block",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -34,7 +34,7 @@ EXPORTED_SYMBOLS = (
     "k3moe_layer", "k3moe_layer_host", "k3moe_matvec_mxfp4", "k3moe_stack_link",
     "k3moe_launch_count", "k3moe_strerror", "k3moe_abi_version", "k3moe_set_phase_events",
     "k3moe_layer_static_scratch", "k3moe_latent_workspace_size", "k3moe_latent_layer",
-    "k3moe_set_flag_wait_polls",
+    "k3moe_set_flag_wait_polls", "k3moe_last_error", "k3moe_experts_mxfp4_range",
 )
 
 # Capacity of the library's file-scope scratch array (K3MOE_STATIC_SCRATCH_BYTES).
@@ -46,7 +46,8 @@ ACT_SWIGLU, ACT_SITU = 0, 1
 class K3moeError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        super().__init__(f"{fn} failed: {status} ({k3moe_strerror(status)})")
+        detail = f"; {k3moe_last_error()}" if status == 5 else ""
+        super().__init__(f"{fn} failed: {status} ({k3moe_strerror(status)}{detail})")
 
 
 class _CCfg(ctypes.Structure):
@@ -106,6 +107,19 @@ class Experts:
     def from_dict(cls, d) -> "Experts":
         return cls(d["w1p"], d["w1s"], d["w3p"], d["w3s"], d["w2p"], d["w2s"])
 
+    def block(self, e0: int, e1: int) -> "Experts":
+        """Experts e0 .. e1-1 (views of the stacked tensors, no copy)."""
+        return Experts(*(t[e0:e1] for t in (self.w1p, self.w1s, self.w3p, self.w3s, self.w2p, self.w2s)))
+
+
+def expert_block(n_experts: int, world: int, rank: int):
+    """The contiguous block [e0, e1) of experts that rank `rank` of `world` holds under expert
+    parallelism: rank r takes experts floor(E r / N) .. floor(E (r+1) / N) - 1 (every expert on
+    exactly one rank; block sizes differ by at most one).  Host logic only."""
+    if world <= 0 or not 0 <= rank < world:
+        raise ValueError("rank out of range")
+    return (n_experts * rank) // world, (n_experts * (rank + 1)) // world
+
 
 class _CLatent(ctypes.Structure):
     _fields_ = [("down", ctypes.c_void_p), ("up", ctypes.c_void_p),
@@ -150,6 +164,7 @@ def lib() -> ctypes.CDLL:
         L.k3moe_workspace_size_host.argtypes = [pc, i32, ctypes.POINTER(sz)]
         L.k3moe_route.argtypes = [pc, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
         L.k3moe_experts_mxfp4.argtypes = [pc, pe, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+        L.k3moe_experts_mxfp4_range.argtypes = [pc, pe, i32, i32, vp, vp, vp, i32, vp, vp, vp, sz, vp]
         L.k3moe_layer.argtypes = [pc, vp, vp, vp, pe, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]
         L.k3moe_layer_host.argtypes = [pc, vp, vp, vp, pe, vp, i32, vp, vp, vp, sz, vp]
         L.k3moe_layer_static_scratch.argtypes = [pc, vp, vp, vp, pe, vp, i32, vp, vp, vp, vp, vp, vp]
@@ -164,12 +179,14 @@ def lib() -> ctypes.CDLL:
         L.k3moe_set_flag_wait_polls.restype = ctypes.c_int
         L.k3moe_set_flag_wait_polls.argtypes = [ctypes.c_int64]
         L.k3moe_launch_count.argtypes = []
+        L.k3moe_last_error.restype = ctypes.c_char_p
+        L.k3moe_last_error.argtypes = []
         L.k3moe_strerror.restype = ctypes.c_char_p
         L.k3moe_strerror.argtypes = [ctypes.c_int]
         L.k3moe_abi_version.restype = i32
         L.k3moe_abi_version.argtypes = []
         for n in ("k3moe_workspace_size", "k3moe_workspace_size_host", "k3moe_route",
-                  "k3moe_experts_mxfp4", "k3moe_layer", "k3moe_layer_host", "k3moe_matvec_mxfp4",
+                  "k3moe_experts_mxfp4", "k3moe_experts_mxfp4_range", "k3moe_layer", "k3moe_layer_host", "k3moe_matvec_mxfp4",
                   "k3moe_stack_link", "k3moe_layer_static_scratch", "k3moe_latent_workspace_size",
                   "k3moe_latent_layer"):
             getattr(L, n).restype = ctypes.c_int
@@ -212,6 +229,11 @@ def _expect(t, name, dtype, shape, cuda=True):
 
 def k3moe_strerror(status: int) -> str:
     return lib().k3moe_strerror(int(status)).decode()
+
+
+def k3moe_last_error() -> str:
+    """The last CUDA failure an entry point saw on this thread ("" if none)."""
+    return lib().k3moe_last_error().decode()
 
 
 def k3moe_abi_version() -> int:
@@ -294,6 +316,23 @@ def k3moe_experts_mxfp4(cfg: Cfg, experts: Experts, x, idx, gate, y, status, ws,
     _check("k3moe_experts_mxfp4", lib().k3moe_experts_mxfp4(
         ctypes.byref(c), ctypes.byref(e), _p(x), _p(idx), _p(gate), T, _p(y), _p(status), _p(ws),
         ws.numel(), _stream(stream)))
+
+
+def k3moe_experts_mxfp4_range(cfg: Cfg, experts: Experts, e0: int, e1: int, x, idx, gate, y, status,
+                              ws, stream=None) -> None:
+    """The routed sum over experts [e0, e1) only; `experts` holds that block (Experts.block)."""
+    import torch
+    T = x.shape[0]
+    _expect(x, "x", torch.bfloat16, (T, cfg.latent))
+    _expect(idx, "idx", torch.int32, (T, cfg.topk))
+    _expect(gate, "gate", torch.float32, (T, cfg.topk))
+    _expect(y, "y", torch.float32, (T, cfg.latent))
+    if status is not None:
+        _expect(status, "status", torch.int32, (4,))
+    c, e = cfg.c(), experts.c()
+    _check("k3moe_experts_mxfp4_range", lib().k3moe_experts_mxfp4_range(
+        ctypes.byref(c), ctypes.byref(e), int(e0), int(e1), _p(x), _p(idx), _p(gate), T, _p(y),
+        _p(status), _p(ws), ws.numel(), _stream(stream)))
 
 
 def k3moe_layer(cfg: Cfg, h, wr, bias, experts: Experts, x, y, idx=None, gate=None, gap=None,

@@ -1,6 +1,10 @@
 // bucket.cu -- token -> expert bucketing (a counting sort of the T*k assignments) and the
 // per-call preparation of the expert GEMVs.
 //
+// An assignment whose index is kRemoteExpert belongs to an expert held elsewhere (the
+// expert-range entry point marks them so): it is skipped like an out-of-range index, but not
+// counted as a drop.
+//
 // Output: counts[E], offsets[E+1] (exclusive prefix of counts), perm[] = the valid
 // assignment ids a = t*k + j sorted by expert and, within an expert, by token (stable),
 // the list of active experts (count > 0) in ascending order with each one's perm offset
@@ -86,6 +90,18 @@ __device__ void publish_counts(int c, int E, const BucketOut& o, int* excl_out) 
     o.ntile_base[nact] = nt_tot;
     o.meta[2] = nt_tot;
   }
+  // large-batch tiles: the same for groups of kTcWideTok tokens
+  int nw_tot;
+  const int nw_excl = block_exclusive_scan_1024(flag ? (c + kTcWideTok - 1) / kTcWideTok : 0, &nw_tot);
+  if (flag) {
+    o.nbase_w[pos] = nw_excl;
+    for (int n = 0; n * kTcWideTok < c; ++n)
+      o.tiles_w[nw_excl + n] = make_int4(e, excl + n * kTcWideTok, min(kTcWideTok, c - n * kTcWideTok), 0);
+  }
+  if (e == 0) {
+    o.nbase_w[nact] = nw_tot;
+    o.meta[3] = nw_tot;
+  }
   for (int i = e; i < kTcFlagWords; i += blockDim.x) o.flags[i] = 0;
   *excl_out = excl;
 }
@@ -163,7 +179,7 @@ __global__ void __launch_bounds__(1024) k_prep_small(PrepArgs p) {
   for (int a = tid; a < P; a += blockDim.x) {
     const int e = p.idx[a];
     if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-    else ++dropped;
+    else if (e != kRemoteExpert) ++dropped;
   }
   __syncthreads();
   const int c = (tid < E) ? cnt[tid] : 0;
@@ -210,7 +226,7 @@ __global__ void __launch_bounds__(256) k_bucket_count(PrepArgs p, int nchunks) {
   for (int a = t0 * k + threadIdx.x; a < t1 * k; a += blockDim.x) {
     const int e = p.idx[a];
     if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
-    else ++dropped;
+    else if (e != kRemoteExpert) ++dropped;
   }
   if (dropped && p.status) atomicAdd(p.status + kStatDropped, dropped);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -220,27 +236,38 @@ __global__ void __launch_bounds__(256) k_bucket_count(PrepArgs p, int nchunks) {
   for (int e = threadIdx.x; e < E; e += blockDim.x) p.b.chunk_base[(size_t)e * nchunks + c] = hist[e];
 }
 
-// Pass 2 (one block): per-expert running sums over chunks, the global scan, and the
-// per-chunk base positions.
-__global__ void __launch_bounds__(1024) k_bucket_scan(int E, int nchunks, BucketOut o) {
+// Pass 2a: per expert (one warp each), the exclusive prefix of its chunk histograms in chunk
+// order, in place (positions relative to the expert's first), and its total into counts[e].
+__global__ void __launch_bounds__(1024) k_bucket_chunkscan(int E, int nchunks, BucketOut o) {
+  pdl_wait();
+  pdl_launch();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 32 + warp;
+  if (e >= E) return;
+  int32_t* cb = o.chunk_base + (size_t)e * nchunks;
+  int run = 0;
+  for (int c0 = 0; c0 < nchunks; c0 += 32) {
+    const int c = c0 + lane;
+    const int v = c < nchunks ? cb[c] : 0;
+    int incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += n;
+    }
+    if (c < nchunks) cb[c] = run + incl - v;
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) o.counts[e] = run;
+}
+
+// Pass 2b (one block): the scan over experts (offsets, active list, tile tables).
+__global__ void __launch_bounds__(1024) k_bucket_scan(int E, BucketOut o) {
   pdl_wait();
   pdl_launch();
   const int e = threadIdx.x;
-  int run = 0;
-  if (e < E) {
-    int32_t* cb = o.chunk_base + (size_t)e * nchunks;
-    for (int c = 0; c < nchunks; ++c) {
-      const int v = cb[c];
-      cb[c] = run;
-      run += v;
-    }
-  }
   int excl;
-  publish_counts(e < E ? run : 0, E, o, &excl);
-  if (e < E) {
-    int32_t* cb = o.chunk_base + (size_t)e * nchunks;
-    for (int c = 0; c < nchunks; ++c) cb[c] += excl;
-  }
+  publish_counts(e < E ? o.counts[e] : 0, E, o, &excl);
 }
 
 // Pass 3: stable scatter of one chunk, token by token (one warp per block).
@@ -250,7 +277,7 @@ __global__ void __launch_bounds__(32) k_bucket_scatter(const int32_t* __restrict
   pdl_launch();
   __shared__ int cur[kMaxExperts];
   const int c = blockIdx.x, lane = threadIdx.x;
-  for (int e = lane; e < E; e += 32) cur[e] = o.chunk_base[(size_t)e * nchunks + c];
+  for (int e = lane; e < E; e += 32) cur[e] = o.offsets[e] + o.chunk_base[(size_t)e * nchunks + c];
   __syncwarp();
   const int t1 = min(T, (c + 1) * kChunkTokens);
   for (int t = c * kChunkTokens; t < t1; ++t) {
@@ -267,7 +294,23 @@ __global__ void __launch_bounds__(32) k_bucket_scatter(const int32_t* __restrict
   }
 }
 
+__global__ void __launch_bounds__(256) k_localize_idx(const int32_t* __restrict__ idx, int n, int E,
+                                                      int e0, int e1, int32_t* __restrict__ out) {
+  pdl_wait();
+  pdl_launch();
+  const int a = blockIdx.x * blockDim.x + threadIdx.x;
+  if (a >= n) return;
+  const int e = idx[a];
+  out[a] = (e >= e0 && e < e1) ? e - e0 : ((e >= 0 && e < E) ? kRemoteExpert : -1);
+}
+
 }  // namespace
+
+cudaError_t launch_localize_idx(const int32_t* idx, int n, int E, int e0, int e1,
+                                int32_t* idx_local, cudaStream_t s, bool pdl) {
+  return launch_kernel(k_localize_idx, dim3((n + 255) / 256), dim3(256), 0, s, pdl, idx, n, E, e0,
+                       e1, idx_local);
+}
 
 int bucket_chunks(int T) { return (T + kChunkTokens - 1) / kChunkTokens; }
 
@@ -279,7 +322,9 @@ cudaError_t launch_prep(const PrepArgs& p, cudaStream_t s, bool pdl) {
   const int nch = bucket_chunks(p.T);
   cudaError_t err = launch_kernel(k_bucket_count, dim3(nch), dim3(256), 0, s, pdl, p, nch);
   if (err != cudaSuccess) return err;
-  err = launch_kernel(k_bucket_scan, dim3(1), dim3(1024), 0, s, true, p.E, nch, p.b);
+  err = launch_kernel(k_bucket_chunkscan, dim3((p.E + 31) / 32), dim3(1024), 0, s, true, p.E, nch, p.b);
+  if (err != cudaSuccess) return err;
+  err = launch_kernel(k_bucket_scan, dim3(1), dim3(1024), 0, s, true, p.E, p.b);
   if (err != cudaSuccess) return err;
   err = launch_kernel(k_bucket_scatter, dim3(nch), dim3(32), 0, s, true,
                       static_cast<const int32_t*>(p.idx), p.T, p.k, p.E, nch, p.b);

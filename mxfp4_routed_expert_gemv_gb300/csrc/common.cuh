@@ -319,12 +319,28 @@ __device__ __forceinline__ void halfwarp_reduce_scatter16(float (&v)[16], int la
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
+// 1/x from the hardware's approximate reciprocal (1 ulp; 1/inf = 0).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// SwiGLU with the hardware exponential and reciprocal (a few ulp of fp32, far below the
+// activation terms' rounding); SiTU-GLU as in activation().
+__device__ __forceinline__ float activation_fast(float g, float u, int act, float b1, float b2);
+
 __device__ __forceinline__ float activation(float g, float u, int act, float b1, float b2) {
   if (act == K3MOE_ACT_SITU) {
     const float a = b1 * tanhf(g / b1) / (1.0f + expf(-g));  // sigmoid of the uncapped g
     return a * (b2 * tanhf(u / b2));
   }
   return silu_f32(g) * u;
+}
+
+__device__ __forceinline__ float activation_fast(float g, float u, int act, float b1, float b2) {
+  if (act == K3MOE_ACT_SITU) return activation(g, u, act, b1, b2);
+  return g * rcp_approx(1.0f + __expf(-g)) * u;
 }
 
 }  // namespace k3

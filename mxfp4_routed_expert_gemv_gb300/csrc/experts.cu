@@ -406,7 +406,8 @@ __global__ void __launch_bounds__(kThreadsX, 1) k_experts(const XArgs a) {
   }
 }
 
-// y[t][c] = sum over valid j of ybuf[t*k+j][c], in slot order (deterministic).
+// y[t][c] = sum over valid j of ybuf[t*k+j][c], in slot order (deterministic).  Slots are
+// loaded four at a time (independent loads in flight) and added in order.
 __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ ybuf,
                                                  const int32_t* __restrict__ idx, int k, int E,
                                                  int L, float* __restrict__ y) {
@@ -415,25 +416,28 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ ybuf,
   const int t = blockIdx.y;
   const int c4 = blockIdx.x * blockDim.x + threadIdx.x;
   if (c4 * 4 >= L) return;
-  float4 v[kMaxTopk];
-  bool ok[kMaxTopk];
-#pragma unroll
-  for (int j = 0; j < kMaxTopk; ++j) {
-    ok[j] = false;
-    if (j < k) {
-      const int e = idx[(size_t)t * k + j];
-      ok[j] = (e >= 0 && e < E);
-      if (ok[j]) v[j] = reinterpret_cast<const float4*>(ybuf + ((size_t)t * k + j) * L)[c4];
-    }
-  }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j0 = 0; j0 < k; j0 += 4) {
+    float4 v[4];
+    bool ok[4];
 #pragma unroll
-  for (int j = 0; j < kMaxTopk; ++j) {
-    if (ok[j]) {
-      acc.x += v[j].x;
-      acc.y += v[j].y;
-      acc.z += v[j].z;
-      acc.w += v[j].w;
+    for (int jj = 0; jj < 4; ++jj) {
+      const int j = j0 + jj;
+      ok[jj] = false;
+      if (j < k) {
+        const int e = __ldg(idx + (size_t)t * k + j);
+        ok[jj] = (e >= 0 && e < E);
+        if (ok[jj]) v[jj] = __ldcs(reinterpret_cast<const float4*>(ybuf + ((size_t)t * k + j) * L) + c4);
+      }
+    }
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      if (ok[jj]) {
+        acc.x += v[jj].x;
+        acc.y += v[jj].y;
+        acc.z += v[jj].z;
+        acc.w += v[jj].w;
+      }
     }
   }
   reinterpret_cast<float4*>(y + (size_t)t * L)[c4] = acc;

@@ -42,21 +42,39 @@ uint32_t flag_wait_polls();
 // router.cu
 // With xq set (T == 1 only) the launch also writes x's kTerms MXFP4 terms into rows
 // 0 .. kTerms-1 of xq / xsf.
+// part: [router_splits(T, E, H)][T][E] floats of partial logits when that is > 1 (the
+// top-k launch sums them into logits first).
 cudaError_t launch_router_logits(const uint16_t* h, const uint16_t* wr, int T, int E, int H,
                                  float* logits, cudaStream_t s, bool pdl,
                                  const uint16_t* x = nullptr, int L = 0, uint8_t* xq = nullptr,
                                  uint8_t* xsf = nullptr, int32_t* zero = nullptr,
-                                 int nzero = 0, int32_t* status = nullptr);
+                                 int nzero = 0, int32_t* status = nullptr, float* part = nullptr);
 // From this many tokens the router logits run as a tensor-core GEMM (router.cu), when the
-// hidden width allows (router_tc_supported).
-constexpr int kRouterTcMinTokens = 64;
+// hidden width allows (router_tc_supported); up to kRouterSplitMaxTokens its reduction is
+// split across CTAs (router_splits ranges).
+constexpr int kRouterTcMinTokens = 3;
+constexpr int kRouterSplitMaxTokens = 1024;
 inline bool router_tc_supported(int H) { return H >= 64 && H % 8 == 0; }
-cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,
-                        float routed_scale, int32_t* idx, float* gate, float* gap,
-                        cudaStream_t s, bool pdl);
+int router_splits(int T, int E, int H);
+// logits[t][e] = sum over z of part[z][t][e] in z order, for e = i0, i0 + step, ... < E
+__device__ __forceinline__ void sum_router_parts(const float* part, int ks, int T, int E, int t,
+                                                 float* logits, int i0, int step) {
+  for (int e = i0; e < E; e += step) {
+    float acc = 0.f;
+    for (int z = 0; z < ks; ++z) acc += part[((size_t)z * T + t) * E + e];
+    logits[(size_t)t * E + e] = acc;
+  }
+}
+cudaError_t launch_topk(float* logits, const float* part, int ks, const float* bias, int T, int E,
+                        int k, int renorm, float routed_scale, int32_t* idx, float* gate,
+                        float* gap, cudaStream_t s, bool pdl);
 
 // Tensor-core expert path (moe_tc.cu): tokens per tile, and the largest grid it launches.
 constexpr int kTcTokTile = 16;
+// Large batches (moe_wide.cu): positions of one expert per tile, and the batch size from
+// which the layer takes that path.
+constexpr int kTcWideTok = 128;
+constexpr int kWideMinTokens = 256;
 constexpr int kTcMaxGrid = 160;
 // Flags of the tensor-core path, zeroed before each call: [0, kTcMaxGrid) parts of the first
 // GEMM's shared tiles written, [kTcMaxGrid, 2 kTcMaxGrid) the same for the second GEMM.
@@ -72,6 +90,13 @@ static_assert(kTcRouteTable % 2 == 0, "route table alignment");
 constexpr int kTcFlagWords = kTcRouteTable + 2 * 32;
 
 // bucket.cu
+// An expert index that names an expert held by another device (expert-range calls): skipped
+// without counting a drop.
+constexpr int32_t kRemoteExpert = INT32_MIN;
+// idx_local[a] = idx[a] - e0 for e0 <= idx[a] < e1, kRemoteExpert for another index in
+// [0, E), and -1 (a counted drop) outside [0, E).
+cudaError_t launch_localize_idx(const int32_t* idx, int n, int E, int e0, int e1,
+                                int32_t* idx_local, cudaStream_t s, bool pdl);
 struct BucketOut {
   int32_t* counts;      // [E]
   int32_t* offsets;     // [E+1]
@@ -79,13 +104,16 @@ struct BucketOut {
   int32_t* active;      // [E]    expert ids with at least one token, ascending
   int32_t* seg_off;     // [E]    perm offset of each active expert's tokens
   int32_t* seg_cnt;     // [E]    number of tokens of each active expert
-  int32_t* meta;        // [16]   [0] active experts, [1] valid assignments, [2] token groups
+  int32_t* meta;        // [16]   [0] active experts, [1] valid assignments, [2] token groups,
+                        //        [3] large-batch token groups
   int32_t* chunk_base;  // [E][nchunks] scratch of the multi-block path
   int32_t* nvalid;      // [T]    valid assignments per token
   int32_t* inv;         // [T*k]  perm position of each valid assignment id
   int32_t* ntile_base;  // [E+1]  tensor-core tiles (kTcTokTile tokens) before each active expert
   int32_t* flags;       // [kTcFlagWords] tensor-core path flags and counts (zeroed per call)
   int4* tiles;          // [P/16 + E + 1] per token group: expert, first position, tokens, 0
+  int32_t* nbase_w;     // [E+1]  large-batch groups (kTcWideTok tokens) before each active expert
+  int4* tiles_w;        // [P/kTcWideTok + E + 1] the same table for groups of kTcWideTok tokens
 };
 
 // Everything the per-call preparation touches.  logits == nullptr: idx/gate come from the
@@ -149,6 +177,20 @@ struct RouteOne {
   float *gate, *gap;
   float* y;  // [L]: the second GEMM sums the slots here (no combine launch)
 };
+// moe_wide.cu: the expert GEMMs of a large batch (positions as the MMA's M, 256 weight rows
+// as N); reads the per-position x terms (launch_split_x) and the kTcWideTok group table.
+bool wide_path_supported(int L, int I);
+// x into per-position terms for the large-batch path (scales in its stage-major layout)
+cudaError_t launch_split_x_wide(const uint16_t* x, int T, int L, int k, int E, const int32_t* idx,
+                                const BucketOut& b, uint8_t* xq, uint8_t* xsf, cudaStream_t s,
+                                bool pdl);
+// Tile descriptors of both expert GEMMs of a large batch (workspace int4 entries).
+size_t wide_desc_count(int L, int I, int E, int T, int k);
+cudaError_t launch_wide_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k,
+                                const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,
+                                uint8_t* act_q, uint8_t* act_sf, int act_kind, float b1, float b2,
+                                const float* gate, float* ybuf, int4* desc, int32_t* status,
+                                cudaStream_t s, void (*between)(cudaStream_t));
 cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k,
                               const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,
                               uint8_t* act_q, uint8_t* act_sf, int act_kind, float b1, float b2,

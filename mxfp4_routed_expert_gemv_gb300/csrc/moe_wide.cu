@@ -1,0 +1,647 @@
+// moe_wide.cu -- the routed experts of a large batch on the block-scaled tensor cores.
+//
+// README "kimi-k3-in-c", Part II sections 4 and 9: every selected expert multiplies its
+// packed E2M1 weights (one E8M0 scale per 32) straight from the checkpoint bytes:
+//   g = W1[e] x,  u = W3[e] x,  act = silu(g) u (or SiTU-GLU),  o = W2[e] act,
+//   ybuf[assignment] = gate * o   (the slots are summed by k_combine, in slot order).
+//
+// When many tokens share an expert (a prefill: about 700 per active expert, some experts
+// chosen by every token) the work is a grouped GEMM, and the shape of a tile decides how
+// often each byte is brought into shared memory.  Here a tile is 128 positions of one expert
+// (its tokens, in bucket order) as the MMA's M and 256 weight rows as its N, over the whole
+// reduction:
+//   * the activation's kTerms MXFP4 terms (mxq.cuh) are folded into the reduction: per
+//     K-step of 64 the tile issues one MMA per term, same weights, same accumulator, so a
+//     token costs one TMEM column whatever the number of terms, and the weight tile in
+//     shared memory feeds kTerms MMAs;
+//   * GEMM1's 256 rows are 128 rows of w1 and the same 128 rows of w3, so g and u of a row
+//     meet in one thread of the epilogue (SwiGLU with no exchange), and the thread holds
+//     whole groups of 32 act values of its position: it writes their MXFP4 terms alone.
+// Tiles run expert by expert, and within an expert row block by row block with the token
+// tiles fastest, CTA c taking tiles c, c + G, ...: the CTAs working at one time share a few
+// weight blocks and one expert's activation terms, which stay in L2.
+//
+// Scales travel by TMA as well.  The activation terms' E8M0 bytes are stored stage-major on
+// this path (k_split_x_wide and GEMM1's epilogue write them so): for each 128-wide stage of
+// the reduction, one 16-byte row per position holding its 4 groups' kTerms scale bytes
+// (group-major: one 4-byte word per group), so a stage's scales are one 2 KB box.  The weights' scales stay in the checkpoint layout and
+// come as 16-byte boxes of 512-wide chunks (four stages) into a two-slot ring.
+//
+// Pipeline (448 threads, one CTA per SM): warp 8 issues the TMA copies of a stage (K = 128:
+// the kTerms term tiles of the positions, 64-byte swizzle, their scales, and the 256 weight
+// rows; the weight scales once per four stages), warps 10-13 move the scales from shared
+// memory into TMEM (each warp its lane quarter), warp 9 allocates TMEM and issues the MMAs
+// (tcgen05.mma kind::mxf4, M = 128, N = 256, fp32 accumulators in TMEM), warps 0-7 run the
+// epilogue.  GEMM1's epilogue moves act (fp32) into shared memory and frees the accumulator
+// before it splits act into terms, so the split overlaps the next tile's MMAs.  Every wait
+// is bounded; one that runs out counts a timeout in the status block and the CTA stops.
+#include "launch.h"
+#include "mxq.cuh"
+#include "tc.cuh"
+#include "tmap.h"
+
+namespace k3 {
+namespace {
+
+constexpr int kWK = 128;                                 // reduction elements per stage
+constexpr int kWM = kTcWideTok;                          // positions per tile (MMA M)
+constexpr int kWN = 256;                                 // weight rows per tile (MMA N)
+constexpr uint32_t kAtBytes = kWM * (kWK / 2);           // one term's position tile: 8 KB
+constexpr uint32_t kBwBytes = kWN * (kWK / 2);           // the weight tile: 16 KB
+constexpr uint32_t kAsBytes = kWM * 16;                 // the positions' scales: 2 KB
+constexpr uint32_t kStageW = kTerms * kAtBytes + kBwBytes + kAsBytes;  // 50 KB
+constexpr uint32_t kWsBytes = kWN * 16;                  // one weight-scale ring slot: 4 KB
+constexpr int kThreadsW = 448;
+constexpr int kEpiWarpsW = 8, kProdWarpW = 8, kMmaWarpW = 9, kSfWarpW0 = 10;
+constexpr uint32_t kAccColsW = kWN;                      // one fp32 accumulator, N columns
+// TMEM scale ring, per stage: A (positions) scales of term t, K-step j at 8 t + 4 j (4
+// columns: row m reads lane m of column + m/32); B (weight) scales of K-step j at 32 + 8 j
+// (8 columns: row n reads column + n/32 in every lane quarter).
+constexpr uint32_t kSfColsW = 8 * kTerms + 16;
+constexpr uint32_t kTmemColsW = 512;
+constexpr int kActStride = 132;  // floats per position row of GEMM1's act staging
+constexpr int kEpiBarW = 1;      // named barrier of the 256 epilogue threads
+
+template <int PH>
+struct WLay {
+  static constexpr int kStages = PH == 0 ? 3 : 4;
+  static constexpr uint32_t kActBytes = PH == 0 ? kWM * kActStride * 4 : 0;
+  static constexpr size_t kSmemBytes = (size_t)kStages * kStageW + kActBytes + 2 * kWsBytes + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
+  static_assert(kAccColsW + kStages * kSfColsW <= kTmemColsW, "TMEM budget");
+};
+
+struct WArgs {
+  int K;            // reduction width: L (GEMM1) or I (GEMM2)
+  int R;            // weight rows per expert: I (GEMM1, w1 and w3) or L (GEMM2)
+  int RB;           // row blocks per expert: R / 128 (GEMM1) or R / 256 (GEMM2)
+  int P;            // position rows of the activation terms (T * k)
+  const int32_t *meta, *perm;
+  const int4* desc;         // [tiles] expert, first position, positions, rb | groups << 8
+  uint8_t *act_q, *act_sf;  // GEMM1 output: act terms [P * kTerms][I / 2], scales stage-major
+  int I;
+  int act_kind;
+  float b1, b2;
+  const float* gate;        // GEMM2: [T * k]
+  float* ybuf;              // GEMM2 output [T * k][L]
+  int L;
+  int32_t* status;
+};
+
+struct WMaps {
+  CUtensorMap a;      // activation terms, 3-D: [P][kTerms][K / 2], boxes of 128 positions
+  CUtensorMap as;     // their scales, stage-major: [K / 128 * P][16 B], boxes of 128 rows
+  CUtensorMap w0, w1; // weights: w1 and w3 (boxes of 128 rows) or w2 (twice, 256 rows)
+  CUtensorMap s0, s1; // weight scales [E * R][K / 32 B], boxes of 16 B (512-wide chunks)
+};
+
+struct WTile {
+  int expert, pos0, ntok, rb, groups;
+};
+
+__device__ __forceinline__ WTile unpack_tile(int4 d) {
+  WTile w;
+  w.expert = d.x;
+  w.pos0 = d.y;
+  w.ntok = d.z;
+  w.rb = d.w & 255;
+  w.groups = d.w >> 8;
+  return w;
+}
+
+// The descriptors of a launch's tiles, from the preparation's group table: tile t is the
+// active expert whose block holds t (bisection over the group prefix), its row block and its
+// token group (token groups fastest).  One thread per tile, so that the expert GEMM reads one
+// descriptor per tile instead of walking the prefix.
+__global__ void __launch_bounds__(256) k_wide_tiles(const int32_t* __restrict__ meta,
+                                                    const int32_t* __restrict__ nbase,
+                                                    const int4* __restrict__ groups, int RB,
+                                                    int4* __restrict__ desc) {
+  pdl_wait();
+  pdl_launch();
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  const int nact = meta[0];
+  if (nact <= 0 || t >= nbase[nact] * RB) return;
+  int lo = 0, hi = nact - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (nbase[mid] * RB <= t) lo = mid; else hi = mid - 1;
+  }
+  const int gb = nbase[lo], n = nbase[lo + 1] - gb;
+  const int local = t - gb * RB;
+  const int rb = local / n;
+  const int4 g = groups[gb + (local - rb * n)];
+  desc[t] = make_int4(g.x, g.y, g.z, rb | (n << 8));
+}
+
+__device__ __forceinline__ int bar_or_w(uint32_t id, uint32_t n, int v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v), "r"(id), "r"(n)
+      : "memory");
+  return (int)r;
+}
+
+// Byte offset of the 4-byte word of group `grp` at position `pos` (byte t: term t's E8M0
+// scale) in the stage-major layout of activation-term scales: [K / 128][P][4 groups][kTerms].
+__host__ __device__ __forceinline__ size_t wide_sf_offset(int grp, int pos, int P) {
+  return (((size_t)(grp >> 2) * P + pos) * 4 + (grp & 3)) * kTerms;
+}
+static_assert(kTerms == 4, "one 32-bit word of scales per group");
+
+// bytes 0xFF -> 0x00 (an E8M0 "no value" becomes the smallest scale: the group adds nothing
+// measurable, as the README decoder's zero group)
+__device__ __forceinline__ uint32_t clear_ff(uint32_t w) {
+  const uint32_t t = ~w;
+  const uint32_t y = ((t & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | t;
+  const uint32_t ff = (~y & 0x80808080u) >> 7;
+  return w & ~(ff * 0xFFu);
+}
+
+template <int PH>
+__global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant__ WMaps mp,
+                                                           const WArgs f) {
+  using Y = WLay<PH>;
+  constexpr int S = Y::kStages;
+  extern __shared__ uint8_t dsm[];
+  __shared__ __align__(8) uint64_t full[S], sfready[S], empty[S];
+  __shared__ __align__(8) uint64_t accfull, accempty, drained, wsfull[2], wsempty[2];
+  __shared__ uint32_t tbase;
+  __shared__ int abort_flag;
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) &
+                                           ~uintptr_t(1023));
+  float* actbuf = reinterpret_cast<float*>(sm + (size_t)S * kStageW);
+  uint8_t* wsring = sm + (size_t)S * kStageW + Y::kActBytes;  // two weight-scale slots
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&sfready[s], 4);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&accfull, 1);
+    mbar_init(&accempty, 1);
+    mbar_init(&drained, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&wsfull[i], 1);
+      mbar_init(&wsempty[i], 4);
+    }
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  if (warp == kMmaWarpW) {
+    tc::tmem_alloc(&tbase, kTmemColsW);
+    tc::tmem_relinquish();
+  }
+  if (warp == kProdWarpW && lane == 0) {
+    tc::tma_prefetch_map(&mp.a);
+    tc::tma_prefetch_map(&mp.as);
+    tc::tma_prefetch_map(&mp.w0);
+    tc::tma_prefetch_map(&mp.w1);
+    tc::tma_prefetch_map(&mp.s0);
+    tc::tma_prefetch_map(&mp.s1);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  // the tile table comes from the preparation and the activation terms from the previous
+  // launch: everyone waits for the preceding kernel
+  pdl_wait();
+  pdl_launch();
+  const uint32_t t0 = tbase;
+  volatile int* abort_v = &abort_flag;
+  const int ntiles = f.meta[3] * f.RB;
+  const int KC = f.K / kWK;
+
+  if (warp == kProdWarpW) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t once = tc::make_policy_evict_first(), reused = tc::make_policy_evict_normal();
+      int it = 0, ch = 0;  // stages and weight-scale chunks issued
+      bool stop = false;
+      int4 next = cta < ntiles ? __ldg(f.desc + cta) : make_int4(0, 0, 0, 0);
+      for (int t = cta; t < ntiles && !stop; t += G) {
+        const WTile wt = unpack_tile(next);
+        if (t + G < ntiles) next = __ldg(f.desc + t + G);  // in flight during this tile
+        const uint64_t pol = wt.groups > 1 ? reused : once;
+        const int wrow = wt.expert * f.R + wt.rb * (PH == 0 ? 128 : 256);
+        for (int kc = 0; kc < KC; ++kc, ++it) {
+          const int s = it % S;
+          if (*abort_v ||
+              (it >= S && !mbar_wait_ab(&empty[s], ((it / S) - 1) & 1, f.status, abort_v))) {
+            *abort_v = 1;
+            stop = true;
+            break;
+          }
+          if ((kc & 3) == 0) {
+            // the weight scales of stages kc .. kc + 3 into slot ch % 2, once the scale warps
+            // are done with the chunk that last used it
+            const int slot = ch & 1;
+            if (ch >= 2 && !mbar_wait_ab(&wsempty[slot], ((ch >> 1) - 1) & 1, f.status, abort_v)) {
+              *abort_v = 1;
+              stop = true;
+              break;
+            }
+            uint8_t* ws = wsring + slot * kWsBytes;
+            mbar_arrive_expect_tx(&wsfull[slot], kWsBytes);
+            if (PH == 0) {
+              tc::tma_load_2d(ws, &mp.s0, (kc >> 2) * 16, wrow, &wsfull[slot]);
+              tc::tma_load_2d(ws + kWsBytes / 2, &mp.s1, (kc >> 2) * 16, wrow, &wsfull[slot]);
+            } else {
+              tc::tma_load_2d(ws, &mp.s0, (kc >> 2) * 16, wrow, &wsfull[slot]);
+            }
+            ++ch;
+          }
+          uint8_t* st = sm + (size_t)s * kStageW;
+          mbar_arrive_expect_tx(&full[s], kStageW);
+#pragma unroll
+          for (int tt = 0; tt < kTerms; ++tt)
+            tc::tma_load_3d(st + tt * kAtBytes, &mp.a, kc * (kWK / 2), tt, wt.pos0, &full[s]);
+          tc::tma_load_2d(st + kTerms * kAtBytes + kBwBytes, &mp.as, 0, kc * f.P + wt.pos0, &full[s]);
+          uint8_t* sb = st + kTerms * kAtBytes;
+          if (PH == 0) {
+            tc::tma_load_2d_hint(sb, &mp.w0, kc * (kWK / 2), wrow, &full[s], pol);
+            tc::tma_load_2d_hint(sb + kBwBytes / 2, &mp.w1, kc * (kWK / 2), wrow, &full[s], pol);
+          } else {
+            tc::tma_load_2d_hint(sb, &mp.w0, kc * (kWK / 2), wrow, &full[s], pol);
+          }
+        }
+      }
+      if (*abort_v) {
+        // copies still in flight land before the CTA leaves
+        for (int d = 1; d <= S && d <= it; ++d) {
+          const int i = it - d;
+          mbar_wait(&full[i % S], (i / S) & 1, nullptr);
+        }
+        for (int d = 1; d <= 2 && d <= ch; ++d) {
+          const int c = ch - d;
+          mbar_wait(&wsfull[c & 1], (c >> 1) & 1, nullptr);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp >= kSfWarpW0) {
+    // --------------------------------------------------------- scales -> TMEM (4 warps)
+    const int q = warp & 3;
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    int it = 0, ch = -1;
+    bool stop = false;
+    for (int t = cta; t < ntiles && !stop; t += G) {
+      for (int kc = 0; kc < KC; ++kc, ++it) {
+        const int s = it % S;
+        const uint32_t par = (it / S) & 1;
+        // the stage's data has landed: the MMAs that last read this TMEM scale slot are done
+        bool ok = !*abort_v &&
+                  mbar_wait_ab(&full[s], par, lane == 0 ? f.status : nullptr, abort_v);
+        if ((kc & 3) == 0) {
+          ++ch;
+          ok = ok && mbar_wait_ab(&wsfull[ch & 1], (ch >> 1) & 1, lane == 0 ? f.status : nullptr,
+                                  abort_v);
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+          *abort_v = 1;
+          stop = true;
+          break;
+        }
+        const uint8_t* st = sm + (size_t)s * kStageW;
+        const uint4 as = *reinterpret_cast<const uint4*>(st + kTerms * kAtBytes + kBwBytes +
+                                                         16 * (32 * q + lane));
+        // word g holds group g's term bytes; term t's word gathers byte t of each
+        uint32_t aw[kTerms];
+#pragma unroll
+        for (int tt = 0; tt < kTerms; ++tt) {
+          const uint32_t sel = (uint32_t)tt | ((uint32_t)(tt + 4) << 4);
+          aw[tt] = __byte_perm(__byte_perm(as.x, as.y, sel), __byte_perm(as.z, as.w, sel), 0x5410);
+        }
+        const uint8_t* ws = wsring + (ch & 1) * kWsBytes + 4 * (kc & 3);
+        const uint32_t ring = t0 + lane_off + kAccColsW + (uint32_t)s * kSfColsW;
+#pragma unroll
+        for (int tt = 0; tt < kTerms; ++tt) {
+          const uint32_t a = clear_ff(aw[tt]);
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            tc::tmem_st_x1(ring + 8 * tt + 4 * j + q, (a >> (16 * j)) & 0xFFFFu);
+        }
+        uint32_t wv[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          wv[c] = clear_ff(*reinterpret_cast<const uint32_t*>(ws + 16 * (32 * c + lane)));
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          uint32_t v[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) v[c] = (wv[c] >> (16 * j)) & 0xFFFFu;
+          tc::tmem_st_x8(ring + 8 * kTerms + 8 * j, v);
+        }
+        tc::tmem_st_wait();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sfready[s]);
+          if ((kc & 3) == 3) mbar_arrive(&wsempty[ch & 1]);  // done with this chunk's slot
+        }
+      }
+    }
+  } else if (warp == kMmaWarpW) {
+    // ---------------------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_mxf4(kWM, kWN, 0, 0);
+      int it = 0, tl = 0;
+      bool stop = false;
+      for (int t = cta; t < ntiles && !stop; t += G, ++tl) {
+        if (tl >= 1 && !mbar_wait_ab(&accempty, (tl - 1) & 1, f.status, abort_v)) {
+          *abort_v = 1;
+          break;
+        }
+        tc::fence_after_sync();
+        for (int kc = 0; kc < KC; ++kc, ++it) {
+          const int s = it % S;
+          const uint32_t par = (it / S) & 1;
+          if (*abort_v || !mbar_wait_ab(&full[s], par, f.status, abort_v) ||
+              !mbar_wait_ab(&sfready[s], par, f.status, abort_v)) {
+            *abort_v = 1;
+            stop = true;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t st = tc::smem_addr(sm + (size_t)s * kStageW);
+          const uint32_t sfr = t0 + kAccColsW + (uint32_t)s * kSfColsW;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint64_t bd = tc::smem_desc(st + kTerms * kAtBytes + 32 * j, 16, 512, tc::kLayout64B);
+#pragma unroll
+            for (int tt = 0; tt < kTerms; ++tt) {
+              const uint64_t ad = tc::smem_desc(st + tt * kAtBytes + 32 * j, 16, 512, tc::kLayout64B);
+              tc::mma_mxf4(t0, ad, bd, idesc, sfr + 8 * tt + 4 * j, sfr + 8 * kTerms + 8 * j,
+                           (kc == 0 && j == 0 && tt == 0) ? 0u : 1u);
+            }
+          }
+          tc::mma_commit(&empty[s]);
+        }
+        if (!stop) tc::mma_commit(&accfull);
+      }
+      tc::mma_commit(&drained);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 0-7)
+    const int q = warp & 3, hf = warp >> 2;
+    const int m = 32 * q + lane;                  // position within the tile
+    const uint32_t tacc = t0 + ((uint32_t)(32 * q) << 16);
+    const int et = threadIdx.x;                   // 0 .. 255
+    int tl = 0;
+    for (int t = cta; t < ntiles; t += G, ++tl) {
+      const WTile wt = unpack_tile(__ldg(f.desc + t));
+      const int bad = (*abort_v || !mbar_wait_ab(&accfull, tl & 1, f.status, abort_v)) ? 1 : 0;
+      if (bar_or_w(kEpiBarW, 32 * kEpiWarpsW, bad)) {
+        *abort_v = 1;
+        break;
+      }
+      tc::fence_after_sync();
+      if (PH == 0) {
+        // g in columns 0..127, u in 128..255 (rows 128 rb .. 128 rb + 127 of w1 / w3); this
+        // warp takes rows 64 hf .. 64 hf + 63, 16 at a time
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          const int c16 = 4 * hf + cc;  // 16-row piece
+          uint32_t g[16], u[16];
+          tc::tmem_ld_x16(tacc + 16 * c16, g);
+          tc::tmem_ld_x16(tacc + 128 + 16 * c16, u);
+          tc::tmem_ld_wait();
+          float* row = actbuf + (size_t)m * kActStride + 16 * c16;
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            float4 a;
+            a.x = activation_fast(__uint_as_float(g[i]), __uint_as_float(u[i]), f.act_kind, f.b1, f.b2);
+            a.y = activation_fast(__uint_as_float(g[i + 1]), __uint_as_float(u[i + 1]), f.act_kind, f.b1, f.b2);
+            a.z = activation_fast(__uint_as_float(g[i + 2]), __uint_as_float(u[i + 2]), f.act_kind, f.b1, f.b2);
+            a.w = activation_fast(__uint_as_float(g[i + 3]), __uint_as_float(u[i + 3]), f.act_kind, f.b1, f.b2);
+            *reinterpret_cast<float4*>(row + i) = a;
+          }
+        }
+        tc::fence_before_sync();
+        named_bar(kEpiBarW, 32 * kEpiWarpsW);
+        if (et == 0) mbar_arrive(&accempty);  // the next tile's MMAs may start
+        // each thread: two (position, group) items, split into kTerms MXFP4 terms
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          const int item = et + 256 * h;
+          const int c = item >> 7, mm = item & 127;
+          if (mm < wt.ntok) {
+            const float* src = actbuf + (size_t)mm * kActStride + 32 * c;
+            float r[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 v = *reinterpret_cast<const float4*>(src + i);
+              r[i] = v.x;
+              r[i + 1] = v.y;
+              r[i + 2] = v.z;
+              r[i + 3] = v.w;
+            }
+            uint32_t words[kTerms][4], sfb[kTerms];
+            mx_split_lane32(r, words, sfb);
+            const size_t pos = (size_t)(wt.pos0 + mm);
+            const int grp = wt.rb * 4 + c;
+#pragma unroll
+            for (int tt = 0; tt < kTerms; ++tt) {
+              const size_t r2 = pos * kTerms + tt;
+              *reinterpret_cast<uint4*>(f.act_q + r2 * (size_t)(f.I >> 1) + grp * 16) =
+                  make_uint4(words[tt][0], words[tt][1], words[tt][2], words[tt][3]);
+            }
+            *reinterpret_cast<uint32_t*>(f.act_sf + wide_sf_offset(grp, (int)pos, f.P)) =
+                sfb[0] | (sfb[1] << 8) | (sfb[2] << 16) | (sfb[3] << 24);
+          }
+        }
+        named_bar(kEpiBarW, 32 * kEpiWarpsW);  // the staging buffer is free again
+      } else {
+        // o for the 256 output rows 256 rb .. 256 rb + 255, times the assignment's gate;
+        // this warp takes columns 128 hf .. 128 hf + 127
+        int a = 0;
+        float gt = 0.f;
+        const bool mine = m < wt.ntok;
+        if (mine) {
+          a = __ldg(f.perm + wt.pos0 + m);
+          gt = __ldg(f.gate + a);
+        }
+        float* yrow = f.ybuf + (size_t)a * f.L + (size_t)wt.rb * 256 + 128 * hf;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tc::tmem_ld_x32(tacc + 128 * hf + 32 * c, v);
+          tc::tmem_ld_wait();
+          if (mine) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(yrow + 32 * c + i) =
+                  make_float4(gt * __uint_as_float(v[i]), gt * __uint_as_float(v[i + 1]),
+                              gt * __uint_as_float(v[i + 2]), gt * __uint_as_float(v[i + 3]));
+          }
+        }
+        tc::fence_before_sync();
+        named_bar(kEpiBarW, 32 * kEpiWarpsW);
+        if (et == 0) mbar_arrive(&accempty);
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  __syncthreads();
+  if (warp == kMmaWarpW) {
+    if (lane == 0) mbar_wait(&drained, 0, f.status);
+    __syncwarp();
+    tc::fence_after_sync();
+    tc::tmem_dealloc(t0, kTmemColsW);
+  }
+}
+
+// x (bf16, one row per token) -> kTerms MXFP4 terms per (token, expert) position for the
+// large-batch path: codes in rows p * kTerms + t of xq [P * kTerms][L / 2] (as k_split_x),
+// scales stage-major (wide_sf_offset).  Grid (T, L / 512): the block's 16 warps split the
+// token's 16 groups of this 512-wide slice once, into shared memory; then for each valid slot
+// of the token the block writes the slice's codes (per term one 256-byte run) and its four
+// 16-byte scale rows, all as 16-byte stores.
+__global__ void __launch_bounds__(512) k_split_x_wide(const uint16_t* __restrict__ x, int L, int k,
+                                                      int E, int P, const int32_t* __restrict__ idx,
+                                                      const int32_t* __restrict__ inv,
+                                                      uint8_t* __restrict__ xq,
+                                                      uint8_t* __restrict__ xsf) {
+  __shared__ uint4 codes[kTerms][16];         // [term][group of the slice]
+  __shared__ __align__(16) uint32_t sfw[16];  // [group]: its terms' scale bytes
+  pdl_wait();
+  pdl_launch();
+  const int t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = blockIdx.y * 16 + warp;
+  const float v = __uint_as_float((uint32_t)x[(size_t)t * L + 32 * grp + lane] << 16);
+  uint32_t words[kTerms], sf[kTerms];
+  mx_split_group(v, words, sf);
+#pragma unroll
+  for (int tt = 0; tt < kTerms; ++tt) {
+    const uint32_t w0 = __shfl_sync(0xffffffffu, words[tt], 0);
+    const uint32_t w1 = __shfl_sync(0xffffffffu, words[tt], 8);
+    const uint32_t w2 = __shfl_sync(0xffffffffu, words[tt], 16);
+    const uint32_t w3 = __shfl_sync(0xffffffffu, words[tt], 24);
+    if (lane == tt) codes[tt][warp] = make_uint4(w0, w1, w2, w3);
+  }
+  if (lane == 0) sfw[warp] = sf[0] | (sf[1] << 8) | (sf[2] << 16) | (sf[3] << 24);
+  __syncthreads();
+  constexpr int kPerPos = kTerms * 16 + 4;  // 16-byte stores per position
+  for (int q = threadIdx.x; q < k * kPerPos; q += blockDim.x) {
+    const int j = q / kPerPos, r = q - j * kPerPos;
+    const int a = t * k + j;
+    const int e = idx[a];
+    if (e < 0 || e >= E) continue;
+    const size_t pos = (size_t)inv[a];
+    if (r < kTerms * 16) {
+      const int tt = r >> 4, g = r & 15;
+      *reinterpret_cast<uint4*>(xq + (pos * kTerms + tt) * (size_t)(L >> 1) +
+                                (size_t)(blockIdx.y * 16 + g) * 16) = codes[tt][g];
+    } else {
+      const int c = r - kTerms * 16;  // stage chunk of the slice
+      *reinterpret_cast<uint4*>(xsf + wide_sf_offset(blockIdx.y * 16 + 4 * c, (int)pos, P)) =
+          *reinterpret_cast<const uint4*>(&sfw[4 * c]);
+    }
+  }
+}
+
+template <int PH>
+cudaError_t launch_wide_phase(const WMaps& mp, const WArgs& f, cudaStream_t s, bool pdl) {
+  static int configured[64] = {0};
+  constexpr size_t smem = WLay<PH>::kSmemBytes;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_moe_wide<PH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = 1;
+  }
+  const int grid = sm_count() < kTcMaxGrid ? sm_count() : kTcMaxGrid;
+  return launch_kernel(k_moe_wide<PH>, dim3(grid), dim3(kThreadsW), smem, s, pdl, mp, f);
+}
+
+}  // namespace
+
+bool wide_path_supported(int L, int I) { return L % 512 == 0 && I % 512 == 0; }
+
+cudaError_t launch_split_x_wide(const uint16_t* x, int T, int L, int k, int E, const int32_t* idx,
+                                const BucketOut& b, uint8_t* xq, uint8_t* xsf, cudaStream_t s,
+                                bool pdl) {
+  return launch_kernel(k_split_x_wide, dim3(T, L / 512), dim3(512), 0, s, pdl, x, L, k, E, T * k,
+                       idx, static_cast<const int32_t*>(b.inv), xq, xsf);
+}
+
+size_t wide_desc_count(int L, int I, int E, int T, int k) {
+  const size_t groups = ((size_t)T * k + kTcWideTok - 1) / kTcWideTok + E + 1;
+  return groups * (size_t)(I / 128) + groups * (size_t)(L / 256);
+}
+
+cudaError_t launch_wide_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k,
+                                const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,
+                                uint8_t* act_q, uint8_t* act_sf, int act_kind, float b1, float b2,
+                                const float* gate, float* ybuf, int4* desc, int32_t* status,
+                                cudaStream_t s, void (*between)(cudaStream_t)) {
+  const uint64_t P = (uint64_t)T * k;
+  const size_t groups = (P + kTcWideTok - 1) / kTcWideTok + E + 1;
+  int4* desc0 = desc;
+  int4* desc1 = desc + groups * (size_t)(I / 128);
+  for (int ph = 0; ph < 2; ++ph) {
+    const int RB = ph == 0 ? I / 128 : L / 256;
+    const size_t n = groups * (size_t)RB;
+    cudaError_t e = launch_kernel(k_wide_tiles, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
+                                  true, static_cast<const int32_t*>(b.meta),
+                                  static_cast<const int32_t*>(b.nbase_w),
+                                  static_cast<const int4*>(b.tiles_w), RB, ph == 0 ? desc0 : desc1);
+    if (e != cudaSuccess) return e;
+  }
+  WMaps m0, m1;
+  const auto sw64 = CU_TENSOR_MAP_SWIZZLE_64B, none = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (!make_map_3d(&m0.a, xq, L / 2, kTerms, L / 2, P, (uint64_t)kTerms * (L / 2), kWK / 2, kWM, sw64) ||
+      !make_map_2d_sw(&m0.as, xsf, 16, (uint64_t)(L / kWK) * P, 16, kWM, none) ||
+      !make_map_2d_sw(&m0.w0, w.w1p, L / 2, (uint64_t)E * I, kWK / 2, 128, sw64) ||
+      !make_map_2d_sw(&m0.w1, w.w3p, L / 2, (uint64_t)E * I, kWK / 2, 128, sw64) ||
+      !make_map_2d_sw(&m0.s0, w.w1s, L / 32, (uint64_t)E * I, 16, 128, none) ||
+      !make_map_2d_sw(&m0.s1, w.w3s, L / 32, (uint64_t)E * I, 16, 128, none) ||
+      !make_map_3d(&m1.a, act_q, I / 2, kTerms, I / 2, P, (uint64_t)kTerms * (I / 2), kWK / 2, kWM, sw64) ||
+      !make_map_2d_sw(&m1.as, act_sf, 16, (uint64_t)(I / kWK) * P, 16, kWM, none) ||
+      !make_map_2d_sw(&m1.w0, w.w2p, I / 2, (uint64_t)E * L, kWK / 2, 256, sw64) ||
+      !make_map_2d_sw(&m1.s0, w.w2s, I / 32, (uint64_t)E * L, 16, 256, none))
+    return cudaErrorInvalidValue;
+  m1.w1 = m1.w0;
+  m1.s1 = m1.s0;
+  WArgs f{};
+  f.P = (int)P;
+  f.meta = b.meta;
+  f.perm = b.perm;
+  f.act_q = act_q;
+  f.act_sf = act_sf;
+  f.I = I;
+  f.L = L;
+  f.act_kind = act_kind;
+  f.b1 = b1;
+  f.b2 = b2;
+  f.gate = gate;
+  f.ybuf = ybuf;
+  f.status = status;
+  // GEMM1: w1 and w3 -> act terms
+  f.K = L;
+  f.R = I;
+  f.RB = I / 128;
+  f.desc = desc0;
+  cudaError_t e = launch_wide_phase<0>(m0, f, s, true);
+  if (e != cudaSuccess) return e;
+  if (between) between(s);
+  // GEMM2: w2 -> gate * o per assignment
+  f.K = I;
+  f.R = L;
+  f.RB = L / 256;
+  f.desc = desc1;
+  return launch_wide_phase<1>(m1, f, s, true);
+}
+
+}  // namespace k3

@@ -114,4 +114,30 @@ __device__ __forceinline__ void mx_split_groups(const float (&v)[TB], uint32_t (
   }
 }
 
+// One thread, one group of 32 elements r[0..31] (consumed): the kTerms terms, as 16 packed
+// bytes each (words[t][i] holds elements 8i .. 8i+7, element 8i in the low nibble) and an
+// E8M0 byte.  The same arithmetic as mx_split_group, without cross-lane work.
+__device__ __forceinline__ void mx_split_lane32(float (&r)[32], uint32_t (&words)[kTerms][4],
+                                                uint32_t (&sf)[kTerms]) {
+#pragma unroll
+  for (int t = 0; t < kTerms; ++t) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(r[i]));
+    const int e = mx_scale_exp(amax);
+    const float down = pow2f(-e), up = pow2f(e);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      float qv;
+      const uint32_t code = e2m1_rne(r[i] * down, &qv);
+      r[i] -= qv * up;
+      w[i >> 3] |= code << (4 * (i & 7));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) words[t][i] = w[i];
+    sf[t] = (uint32_t)(e + 127);
+  }
+}
+
 }  // namespace k3

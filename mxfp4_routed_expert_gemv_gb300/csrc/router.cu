@@ -108,19 +108,22 @@ __global__ void __launch_bounds__(RPC * kQuarters * 32) k_router_logits(const ui
   }
 }
 
-// Batches (T >= 64): the router as a tensor-core GEMM, logits[t][e] = sum_i h[t][i] Wr[e][i].
-// One CTA per 128 experts x 128 tokens: TMA brings 64-wide K slices of Wr and h (bf16, 128-byte
-// swizzle) into a 4-stage ring, one thread issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32 in
-// TMEM, K = 16 each), and all four warps read the accumulator back (lane = expert row,
-// column = token).  Products of bf16 values are exact; the sums are fp32.  A K tail past H
-// reads zeros.  Every wait is bounded: one that runs out counts a timeout and the CTA skips
-// its output.
+// Batches (T >= 3): the router as a tensor-core GEMM, logits[t][e] = sum_i h[t][i] Wr[e][i].
+// One CTA per 128 experts x 128 tokens x one of `ks` ranges of the reduction: TMA brings
+// 64-wide K slices of Wr and h (bf16, 128-byte swizzle) into a 4-stage ring, one thread issues
+// tcgen05.mma kind::f16 (bf16 x bf16 -> fp32 in TMEM, K = 16 each), and all four warps read the
+// accumulator back (lane = expert row, column = token).  With ks > 1 (few tokens: one range
+// per CTA would leave most SMs idle) each CTA writes its range's partial sums to part
+// [ks][T][E], and the kernel that takes the top-k adds them in range order (deterministic);
+// with ks == 1 it writes the logits.  Products of bf16 values are exact; the sums are fp32.
+// A K tail past H reads zeros.  Every wait is bounded: one that runs out counts a timeout and
+// the CTA skips its output.
 constexpr int kRtStages = 4;
 constexpr uint32_t kRtTile = 128 * 128;  // one 128-row x 128-byte operand slice
 
 __global__ void __launch_bounds__(128, 1) k_router_tc(const __grid_constant__ CUtensorMap mw,
                                                       const __grid_constant__ CUtensorMap mh,
-                                                      int T, int E, int H,
+                                                      int T, int E, int H, int ks,
                                                       float* __restrict__ logits,
                                                       int32_t* __restrict__ status) {
   extern __shared__ uint8_t dsm[];
@@ -131,7 +134,10 @@ __global__ void __launch_bounds__(128, 1) k_router_tc(const __grid_constant__ CU
                                            ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e0 = blockIdx.x * 128, t0 = blockIdx.y * 128;
-  const int nk = (H + 63) / 64;
+  const int nk_all = (H + 63) / 64;
+  const int k_lo = (int)(((long long)nk_all * blockIdx.z) / ks);
+  const int nk = (int)(((long long)nk_all * (blockIdx.z + 1)) / ks) - k_lo;
+  float* const out = logits + (size_t)blockIdx.z * T * E;  // this range's partials (or logits)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRtStages; ++s) {
       mbar_init(&full[s], 1);
@@ -161,8 +167,8 @@ __global__ void __launch_bounds__(128, 1) k_router_tc(const __grid_constant__ CU
       }
       uint8_t* st = sm + (size_t)s * 2 * kRtTile;
       mbar_arrive_expect_tx(&full[s], 2 * kRtTile);
-      tc::tma_load_2d(st, &mw, i * 128, e0, &full[s]);
-      tc::tma_load_2d(st + kRtTile, &mh, i * 128, t0, &full[s]);
+      tc::tma_load_2d(st, &mw, (k_lo + i) * 128, e0, &full[s]);
+      tc::tma_load_2d(st + kRtTile, &mh, (k_lo + i) * 128, t0, &full[s]);
     }
     if (bad)  // copies in flight land before the CTA leaves
       for (int d = 1; d <= kRtStages && d <= i; ++d)
@@ -203,7 +209,7 @@ __global__ void __launch_bounds__(128, 1) k_router_tc(const __grid_constant__ CU
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const int t = t0 + c0 + c;
-          if (t < T) logits[(size_t)t * E + e] = __uint_as_float(r[c]);
+          if (t < T) out[(size_t)t * E + e] = __uint_as_float(r[c]);
         }
       }
     }
@@ -216,7 +222,8 @@ __global__ void __launch_bounds__(128, 1) k_router_tc(const __grid_constant__ CU
   }
 }
 
-__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits,
+__global__ void __launch_bounds__(256) k_topk(float* __restrict__ logits,
+                                              const float* __restrict__ part, int ks,
                                               const float* __restrict__ bias, int T, int E,
                                               int k, int renorm, float routed_scale,
                                               int32_t* __restrict__ idx,
@@ -226,6 +233,10 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits,
   pdl_launch();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
+  if (ks > 1) {
+    sum_router_parts(part, ks, T, E, t, logits, threadIdx.x & 31, 32);
+    __syncwarp();
+  }
   topk_warp(logits + (size_t)t * E, bias, E, k, renorm, routed_scale, idx + (size_t)t * k,
             gate + (size_t)t * k, gap ? gap + t : nullptr, threadIdx.x & 31);
 }
@@ -234,7 +245,8 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits,
 // single-token path (topk_one_token: the keys at or above the (k+1)-th best list maximum,
 // sorted by one warp; the full sort when ties leave too many).  Same choice, order, tie
 // rule and gates as k_topk; E <= 1056, k <= 31 (or k == E).
-__global__ void __launch_bounds__(352) k_topk_block(const float* __restrict__ logits,
+__global__ void __launch_bounds__(352) k_topk_block(float* __restrict__ logits,
+                                                    const float* __restrict__ part, int ks, int T,
                                                     const float* __restrict__ bias, int E, int k,
                                                     int renorm, float routed_scale,
                                                     int32_t* __restrict__ idx,
@@ -245,6 +257,10 @@ __global__ void __launch_bounds__(352) k_topk_block(const float* __restrict__ lo
   pdl_wait();
   pdl_launch();
   const int t = blockIdx.x;
+  if (ks > 1) {
+    sum_router_parts(part, ks, T, E, t, logits, threadIdx.x, blockDim.x);
+    __syncthreads();
+  }
   const OneTokenChoice c = topk_one_token<3>(logits + (size_t)t * E, bias, E, k, renorm,
                                              routed_scale, gap ? gap + t : nullptr, lists, sig);
   if (threadIdx.x < k) {
@@ -255,11 +271,22 @@ __global__ void __launch_bounds__(352) k_topk_block(const float* __restrict__ lo
 
 }  // namespace
 
+int router_splits(int T, int E, int H) {
+  if (T < kRouterTcMinTokens || !router_tc_supported(H) || T > kRouterSplitMaxTokens) return 1;
+  const int ctas = ((E + 127) / 128) * ((T + 127) / 128);
+  const int nk = (H + 63) / 64;
+  int ks = (sm_count() + ctas - 1) / ctas;  // about one CTA per SM
+  ks = ks < nk / 2 ? ks : nk / 2;           // at least two K slices per range
+  return ks > 1 ? ks : 1;
+}
+
 cudaError_t launch_router_logits(const uint16_t* h, const uint16_t* wr, int T, int E, int H,
                                  float* logits, cudaStream_t s, bool pdl, const uint16_t* x,
                                  int L, uint8_t* xq, uint8_t* xsf, int32_t* zero, int nzero,
-                                 int32_t* status) {
+                                 int32_t* status, float* part) {
   if (T >= kRouterTcMinTokens && !xq && !zero && router_tc_supported(H)) {
+    const int ks = router_splits(T, E, H);
+    if (ks > 1 && !part) return cudaErrorInvalidValue;
     CUtensorMap mw, mh;
     if (!make_map_2d(&mw, wr, (uint64_t)H * 2, E, 128, 128, true) ||
         !make_map_2d(&mh, h, (uint64_t)H * 2, T, 128, 128, true))
@@ -274,8 +301,8 @@ cudaError_t launch_router_logits(const uint16_t* h, const uint16_t* wr, int T, i
       if (e != cudaSuccess) return e;
       if (dev >= 0 && dev < 64) configured[dev] = 1;
     }
-    return launch_kernel(k_router_tc, dim3((E + 127) / 128, (T + 127) / 128), dim3(128), smem, s,
-                         pdl, mw, mh, T, E, H, logits, status);
+    return launch_kernel(k_router_tc, dim3((E + 127) / 128, (T + 127) / 128, ks), dim3(128), smem,
+                         s, pdl, mw, mh, T, E, H, ks, ks > 1 ? part : logits, status);
   }
   if (T <= 2) {
     const unsigned gx = (E + kRpcFew - 1) / kRpcFew;
@@ -289,14 +316,14 @@ cudaError_t launch_router_logits(const uint16_t* h, const uint16_t* wr, int T, i
                        s, pdl, h, wr, T, E, H, logits, x, L, xq, xsf, zero, nzero);
 }
 
-cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,
-                        float routed_scale, int32_t* idx, float* gate, float* gap,
-                        cudaStream_t s, bool pdl) {
+cudaError_t launch_topk(float* logits, const float* part, int ks, const float* bias, int T, int E,
+                        int k, int renorm, float routed_scale, int32_t* idx, float* gate,
+                        float* gap, cudaStream_t s, bool pdl) {
   if (T <= kTopkBlockMaxTokens && E <= 1056 && (k <= 31 || k == E))
-    return launch_kernel(k_topk_block, dim3(T), dim3(352), 0, s, pdl, logits, bias, E, k, renorm,
-                         routed_scale, idx, gate, gap);
-  return launch_kernel(k_topk, dim3((T + 7) / 8), dim3(256), 0, s, pdl, logits, bias, T, E, k,
-                       renorm, routed_scale, idx, gate, gap);
+    return launch_kernel(k_topk_block, dim3(T), dim3(352), 0, s, pdl, logits, part, ks, T, bias, E,
+                         k, renorm, routed_scale, idx, gate, gap);
+  return launch_kernel(k_topk, dim3((T + 7) / 8), dim3(256), 0, s, pdl, logits, part, ks, bias, T,
+                       E, k, renorm, routed_scale, idx, gate, gap);
 }
 
 }  // namespace k3

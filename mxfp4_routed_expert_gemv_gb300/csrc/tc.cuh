@@ -8,7 +8,8 @@
 //   bits 32-45  stride byte offset >> 4  (distance between 8-row groups along M or N)
 //   bits 46-47  descriptor version (1)
 //   bits 49-51  base offset (0: every swizzle atom starts 1024-byte aligned)
-//   bits 61-63  layout: 0 no swizzle (8-row x 16-byte core matrices), 2 128-byte swizzle
+//   bits 61-63  layout: 0 no swizzle (8-row x 16-byte core matrices), 2 128-byte swizzle,
+//               4 64-byte swizzle
 // Instruction descriptor (32 bits) of the block-scaled kinds:
 //   bits 4-5 B scale byte id, 7-9 A format, 10-12 B format (E2M1 = 1 for kind::mxf4),
 //   15/16 A/B major (0 = K-major), 17-22 N >> 3, 23 scale format (1 = UE8M0),
@@ -31,7 +32,7 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-constexpr uint32_t kLayoutNone = 0, kLayout128B = 2;
+constexpr uint32_t kLayoutNone = 0, kLayout128B = 2, kLayout64B = 4;
 
 __host__ __device__ constexpr uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
                                                  uint32_t layout) {
@@ -89,6 +90,13 @@ __device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t v0, uint32_t
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
                :: "r"(taddr), "r"(v0), "r"(v1), "r"(v2), "r"(v3) : "memory");
 }
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+      :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+         "r"(v[7])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -99,6 +107,21 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
         "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+// 32 consecutive columns of this warp's lane quarter (not waited for: tmem_ld_wait)
+__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
       : "r"(taddr)
       : "memory");
 }
@@ -155,6 +178,16 @@ __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const CUtensorM
       ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
       :: "r"(smem_addr(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
          "r"(smem_addr(mbar)), "l"(policy)
+      : "memory");
+}
+// 3-D tile (x in bytes, a multiple of 16; y, z rows of the two outer dimensions).
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int32_t x,
+                                            int32_t y, int32_t z, uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3, %4}], [%5];"
+      :: "r"(smem_addr(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
+         "r"(smem_addr(mbar))
       : "memory");
 }
 __device__ __forceinline__ uint64_t make_policy_evict_first() {

@@ -74,6 +74,59 @@ def test_small_layer_parity(w):
     _check_layer(w, dl)
 
 
+# Batches from 256 tokens take the large-batch kernels (tiles of 128 positions of one
+# expert against 256 weight rows): several tiles per expert, ragged last tiles, an expert
+# with most of the batch, and the stacked-row edge of the activation terms.
+WIDE = [
+    synth.small_workload(T=256, E=24, k=6, latent=1024, inter=512, hidden=256, seed=61),
+    synth.small_workload(T=600, E=8, k=4, latent=512, inter=1536, hidden=512, seed=62),
+    synth.small_workload(T=300, E=64, k=16, latent=2048, inter=512, hidden=256, bias="none", seed=63),
+    synth.small_workload(T=1000, E=40, k=3, latent=512, inter=512, hidden=128, seed=64),
+]
+
+
+@pytest.mark.parametrize("w", WIDE, ids=lambda w: w.name)
+def test_large_batch_layer_parity(w):
+    dl = DeviceLayer(w)
+    rep, yr, idx = _check_layer(w, dl, dense=True)
+    counts = np.bincount(idx.reshape(-1), minlength=w.E)
+    print(f"\n[{w.name}] y {yr} tokens/expert max {counts.max()}")
+
+
+def test_large_batch_situ():
+    w = synth.small_workload(T=320, E=16, k=4, latent=1024, inter=1024, hidden=256, seed=65)
+    dl = DeviceLayer(w)
+    _check_layer(w, dl, act=1, dense=True)
+
+
+def test_large_batch_experts_entry_drops_and_duplicates():
+    """The expert entry point at 288 tokens: out-of-range indices are skipped and counted,
+    repeated experts in a token's list count twice."""
+    k3 = _k3()
+    w = synth.small_workload(T=288, E=10, k=4, latent=512, inter=512, hidden=128, seed=66)
+    ex = k3.Experts.from_dict(synth.experts_device(w, 0))
+    li = synth.layer_inputs(w)
+    rng = np.random.default_rng(3)
+    idx = rng.integers(0, w.E, size=(w.T, w.k)).astype(np.int32)
+    idx[5] = [-1, 4, 4, 9]
+    idx[77] = [10, 0, 0, 0]
+    idx[200, 2] = 1 << 20
+    gate = rng.uniform(0.1, 1.0, size=idx.shape).astype(np.float32)
+    cfg = gpu_cfg(w)
+    ws = k3.workspace(cfg, w.T)
+    y = torch.empty((w.T, w.latent), dtype=torch.float32, device="cuda")
+    st = torch.zeros(4, dtype=torch.int32, device="cuda")
+    k3.k3moe_experts_mxfp4(cfg, ex, to_dev_bf16(li.x), torch.from_numpy(idx).cuda(), torch.from_numpy(gate).cuda(),
+                           y, st, ws)
+    torch.cuda.synchronize()
+    assert st.cpu().numpy()[0] == 3
+    valid = (idx >= 0) & (idx < w.E)
+    ridx = np.where(valid, idx, 0).astype(np.int32)
+    rgate = np.where(valid, gate, 0.0).astype(np.float64)
+    table = oracle_table(w, 0, range(w.E))
+    compare_y(y.cpu().numpy(), oracle.experts_dense(oracle_cfg(w), table, li.x, ridx, rgate))
+
+
 def test_small_layer_situ():
     w = synth.small_workload(T=9, E=16, k=4, latent=320, inter=224, hidden=256, seed=21)
     dl = DeviceLayer(w)
@@ -140,21 +193,39 @@ def test_zero_tokens_and_bad_arguments():
     assert ei.value.status == 2
 
 
-def test_repeat_calls_bit_identical():
-    w = synth.small_workload(T=6, E=24, k=6, latent=512, inter=256, hidden=256, seed=25)
+@pytest.mark.parametrize("T,latent,inter", [(6, 512, 256), (6, 1024, 512), (300, 1024, 512)])
+def test_repeat_calls_bit_identical(T, latent, inter):
+    """Deterministic: the CUDA-core path, the tensor-core path and the large-batch path."""
+    w = synth.small_workload(T=T, E=24, k=6, latent=latent, inter=inter, hidden=256, seed=25)
     dl = DeviceLayer(w)
     a = dl.run()[0]
     b = dl.run()[0]
     assert np.array_equal(a, b)
 
 
-def test_batch_of_one_equals_row():
-    w = synth.small_workload(T=8, E=24, k=6, latent=512, inter=256, hidden=256, seed=26)
+@pytest.mark.parametrize("latent,inter", [(512, 256), (1024, 512)])
+def test_batch_of_one_equals_row(latent, inter):
+    """The expert sum of a token does not depend on the rest of its batch: given the same
+    routing, a batch's row equals the token run alone bit for bit.  The whole layer routes a
+    batch of 3 or more on the tensor-core router and one token on the CUDA-core GEMV, so
+    there the indices must agree and y stays within the workload tolerances."""
+    k3 = _k3()
+    w = synth.small_workload(T=8, E=24, k=6, latent=latent, inter=inter, hidden=256, seed=26)
     dl = DeviceLayer(w)
-    y = dl.run()[0]
+    y, idx, gate, _, _ = dl.run()
+    cfg = gpu_cfg(w)
+    idx_d, gate_d = torch.from_numpy(idx).cuda(), torch.from_numpy(gate).cuda()
+    yb = torch.empty((w.T, w.latent), dtype=torch.float32, device="cuda")
+    k3.k3moe_experts_mxfp4(cfg, dl.experts, dl.x, idx_d, gate_d, yb, None, k3.workspace(cfg, w.T))
     for t in (0, 5):
-        y1 = dl.run(h=dl.h[t:t + 1].contiguous(), x=dl.x[t:t + 1].contiguous())[0]
-        assert np.array_equal(y1[0], y[t])
+        y1 = torch.empty((1, w.latent), dtype=torch.float32, device="cuda")
+        k3.k3moe_experts_mxfp4(cfg, dl.experts, dl.x[t:t + 1].contiguous(), idx_d[t:t + 1].contiguous(),
+                               gate_d[t:t + 1].contiguous(), y1, None, k3.workspace(cfg, 1))
+        torch.cuda.synchronize()
+        assert np.array_equal(y1.cpu().numpy()[0], yb.cpu().numpy()[t])
+        y1l, idx1, _, _, _ = dl.run(h=dl.h[t:t + 1].contiguous(), x=dl.x[t:t + 1].contiguous())
+        assert np.array_equal(idx1[0], idx[t])
+        compare_y(y1l[0:1], y[t:t + 1].astype(np.float64))
 
 
 @pytest.mark.parametrize("case", ["all_scores_equal", "boosted_block", "boosted_spread"])
