@@ -794,25 +794,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = sb[i];
             const size_t p = (size_t)(ti.pos0 + lane);
-#pragma unroll 1
+            uint32_t w[kTerms][4], sfb[kTerms];
+            mx_split_lane32(r, w, sfb);
+#pragma unroll
             for (int t = 0; t < kTerms; ++t) {
-              float amax = 0.f;
-#pragma unroll
-              for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(r[i]));
-              const int e = mx_scale_exp(amax);
-              const float down = pow2f(-e), up = pow2f(e);
-              uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                float qv;
-                const uint32_t code = e2m1_rne(r[i] * down, &qv);
-                r[i] -= qv * up;
-                w[i >> 3] |= code << (4 * (i & 7));
-              }
               const size_t r2 = p * kTerms + t;
               *reinterpret_cast<uint4*>(f.act_q + r2 * (size_t)(f.I >> 1) + grp * 16) =
-                  make_uint4(w[0], w[1], w[2], w[3]);
-              f.act_sf[r2 * (size_t)(f.I >> 5) + grp] = (uint8_t)(e + 127);
+                  make_uint4(w[t][0], w[t][1], w[t][2], w[t][3]);
+              f.act_sf[r2 * (size_t)(f.I >> 5) + grp] = (uint8_t)sfb[t];
             }
           }
           __syncwarp();

@@ -460,7 +460,9 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
         named_bar(kEpiBarW, 32 * kEpiWarpsW);  // the staging buffer is free again
       } else {
         // o for the 256 output rows 256 rb .. 256 rb + 255, times the assignment's gate;
-        // this warp takes columns 128 hf .. 128 hf + 127
+        // this warp takes columns 128 hf .. 128 hf + 127 of its 32 positions, 32 at a time:
+        // the 32 x 32 block is transposed across the warp, so that each store instruction
+        // writes 128 contiguous bytes of one assignment's row
         int a = 0;
         float gt = 0.f;
         const bool mine = m < wt.ntok;
@@ -468,18 +470,31 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
           a = __ldg(f.perm + wt.pos0 + m);
           gt = __ldg(f.gate + a);
         }
-        float* yrow = f.ybuf + (size_t)a * f.L + (size_t)wt.rb * 256 + 128 * hf;
+        float* ycol = f.ybuf + (size_t)wt.rb * 256 + 128 * hf + lane;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tc::tmem_ld_x32(tacc + 128 * hf + 32 * c, v);
+          uint32_t u[32];
+          tc::tmem_ld_x32(tacc + 128 * hf + 32 * c, u);
           tc::tmem_ld_wait();
-          if (mine) {
+          float v[32];
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              *reinterpret_cast<float4*>(yrow + 32 * c + i) =
-                  make_float4(gt * __uint_as_float(v[i]), gt * __uint_as_float(v[i + 1]),
-                              gt * __uint_as_float(v[i + 2]), gt * __uint_as_float(v[i + 3]));
+          for (int i = 0; i < 32; ++i) v[i] = gt * __uint_as_float(u[i]);
+          // butterfly transpose: afterwards v[p] = column 32 c + lane of position 32 q + p
+#pragma unroll
+          for (int sh = 16; sh >= 1; sh >>= 1) {
+            const bool up = (lane & sh) != 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (i & sh) continue;
+              const float send = up ? v[i] : v[i + sh];
+              const float recv = __shfl_xor_sync(0xffffffffu, send, sh);
+              if (up) v[i] = recv; else v[i + sh] = recv;
+            }
+          }
+#pragma unroll
+          for (int p = 0; p < 32; ++p) {
+            const int ap = __shfl_sync(0xffffffffu, a, p);
+            if (p < wt.ntok - 32 * q) ycol[(size_t)ap * f.L + 32 * c] = v[p];
           }
         }
         tc::fence_before_sync();

@@ -9,6 +9,7 @@
 // "kimi-k3-in-c", Part II section 4); only the activations are split.
 #pragma once
 #include <cstdint>
+#include <cuda_fp16.h>
 
 namespace k3 {
 
@@ -114,9 +115,27 @@ __device__ __forceinline__ void mx_split_groups(const float (&v)[TB], uint32_t (
   }
 }
 
+// Two values (|v| <= 6 after scaling) rounded to E2M1 by the hardware conversion (nearest,
+// ties to the even code: the same rounding as e2m1_rne), as one byte: lo in the low nibble.
+__device__ __forceinline__ uint32_t e2m1x2_rn(float hi, float lo) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// The values of an E2M1 byte's two codes (exact), low nibble first.
+__device__ __forceinline__ float2 e2m1x2_values(uint32_t byte) {
+  uint32_t h;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h) : "r"(byte));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
 // One thread, one group of 32 elements r[0..31] (consumed): the kTerms terms, as 16 packed
 // bytes each (words[t][i] holds elements 8i .. 8i+7, element 8i in the low nibble) and an
-// E8M0 byte.  The same arithmetic as mx_split_group, without cross-lane work.
+// E8M0 byte.  The same arithmetic as mx_split_group, without cross-lane work; element pairs
+// are rounded by the hardware conversion.
 __device__ __forceinline__ void mx_split_lane32(float (&r)[32], uint32_t (&words)[kTerms][4],
                                                 uint32_t (&sf)[kTerms]) {
 #pragma unroll
@@ -128,11 +147,12 @@ __device__ __forceinline__ void mx_split_lane32(float (&r)[32], uint32_t (&words
     const float down = pow2f(-e), up = pow2f(e);
     uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float qv;
-      const uint32_t code = e2m1_rne(r[i] * down, &qv);
-      r[i] -= qv * up;
-      w[i >> 3] |= code << (4 * (i & 7));
+    for (int i = 0; i < 32; i += 2) {
+      const uint32_t b = e2m1x2_rn(r[i + 1] * down, r[i] * down);
+      const float2 q = e2m1x2_values(b);
+      r[i] -= q.x * up;
+      r[i + 1] -= q.y * up;
+      w[i >> 3] |= b << (4 * (i & 7));
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) words[t][i] = w[i];
