@@ -117,6 +117,8 @@ size_t carve(const k3moe_cfg* c, int32_t T, void* base, bool host_stage, Workspa
   t.b.tiles = cv.take<int4>((P + kTcTokTile - 1) / kTcTokTile + E + 1);
   t.b.nbase_w = cv.take<int32_t>(E + 1);
   t.b.tiles_w = cv.take<int4>((P + kTcWideTok - 1) / kTcWideTok + E + 1);
+  t.b.nbase_r = cv.take<int32_t>(E + 1);
+  t.b.tiles_r = cv.take<int4>((P + kTcRowTok - 1) / kTcRowTok + E + 1);
   t.tc = tc_path_supported((int)L, (int)I);
   if (t.tc) {
     t.xq = cv.take<uint8_t>(P * kTerms * (L / 2));
@@ -124,8 +126,9 @@ size_t carve(const k3moe_cfg* c, int32_t T, void* base, bool host_stage, Workspa
     t.aq = cv.take<uint8_t>(P * kTerms * (I / 2));
     t.asf = cv.take<uint8_t>(P * kTerms * (I / 32));
     t.part = cv.take<float>(tc_part_floats((int)Tt));
-    if (T >= kWideMinTokens && wide_path_supported((int)L, (int)I))
-      t.wdesc = cv.take<int4>(wide_desc_count((int)L, (int)I, (int)E, (int)Tt, (int)K));
+    if (T >= kRowsMinTokens && wide_path_supported((int)L, (int)I))
+      t.wdesc = cv.take<int4>(
+          wide_desc_count((int)L, (int)I, (int)E, (int)Tt, (int)K, T < kWideMinTokens));
   } else {
     t.x16 = cv.take<__half>(Tt * L);
     t.xexp = cv.take<int32_t>(Tt);
@@ -287,8 +290,10 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
              gap, T, L, static_cast<const uint16_t*>(x), w.tc ? nullptr : w.x16, w.xexp, w.b, y,
              status};
   const RouteOne ro{w.logits, bias, c->renorm, c->routed_scale, idx, gate, gap, y};
-  // large batches: positions of one expert as the MMA's M dimension (moe_wide.cu)
-  const bool wide = w.tc && T >= kWideMinTokens && wide_path_supported(L, I);
+  // batches: positions of one expert as the MMA's M dimension (moe_wide.cu), the activation
+  // terms as MMA rows below kWideMinTokens tokens, folded into the reduction from there
+  const bool wide = w.tc && T >= kRowsMinTokens && wide_path_supported(L, I);
+  const bool rows = T < kWideMinTokens;
   if (!one) {
     K3_TRY(launch_prep(p, s, route));
     if (wide)
@@ -300,7 +305,7 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
   }
   if (wide) {
     K3_TRY(phase(2, s));
-    K3_TRY(launch_wide_experts(ep, L, I, E, T, K, w.xq, w.xsf, w.b, w.aq, w.asf, c->act,
+    K3_TRY(launch_wide_experts(ep, L, I, E, T, K, rows, w.xq, w.xsf, w.b, w.aq, w.asf, c->act,
                                c->situ_b1, c->situ_b2, gate, w.ybuf, w.wdesc, status, s, phase3));
     K3_TRY(phase(4, s));
   } else if (w.tc) {

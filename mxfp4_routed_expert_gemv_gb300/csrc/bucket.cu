@@ -102,6 +102,18 @@ __device__ void publish_counts(int c, int E, const BucketOut& o, int* excl_out) 
     o.nbase_w[nact] = nw_tot;
     o.meta[3] = nw_tot;
   }
+  // and for groups of kTcRowTok tokens
+  int nr_tot;
+  const int nr_excl = block_exclusive_scan_1024(flag ? (c + kTcRowTok - 1) / kTcRowTok : 0, &nr_tot);
+  if (flag) {
+    o.nbase_r[pos] = nr_excl;
+    for (int n = 0; n * kTcRowTok < c; ++n)
+      o.tiles_r[nr_excl + n] = make_int4(e, excl + n * kTcRowTok, min(kTcRowTok, c - n * kTcRowTok), 0);
+  }
+  if (e == 0) {
+    o.nbase_r[nact] = nr_tot;
+    o.meta[4] = nr_tot;
+  }
   for (int i = e; i < kTcFlagWords; i += blockDim.x) o.flags[i] = 0;
   *excl_out = excl;
 }

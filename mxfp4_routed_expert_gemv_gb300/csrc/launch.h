@@ -72,9 +72,12 @@ cudaError_t launch_topk(float* logits, const float* part, int ks, const float* b
 // Tensor-core expert path (moe_tc.cu): tokens per tile, and the largest grid it launches.
 constexpr int kTcTokTile = 16;
 // Large batches (moe_wide.cu): positions of one expert per tile, and the batch size from
-// which the layer takes that path.
+// which the layer takes that path; batches from kRowsMinTokens below that take the same
+// kernels with the activation terms as MMA rows, kTcRowTok positions per tile.
 constexpr int kTcWideTok = 128;
 constexpr int kWideMinTokens = 256;
+constexpr int kTcRowTok = 32;
+constexpr int kRowsMinTokens = 3;
 constexpr int kTcMaxGrid = 160;
 // Flags of the tensor-core path, zeroed before each call: [0, kTcMaxGrid) parts of the first
 // GEMM's shared tiles written, [kTcMaxGrid, 2 kTcMaxGrid) the same for the second GEMM.
@@ -105,7 +108,7 @@ struct BucketOut {
   int32_t* seg_off;     // [E]    perm offset of each active expert's tokens
   int32_t* seg_cnt;     // [E]    number of tokens of each active expert
   int32_t* meta;        // [16]   [0] active experts, [1] valid assignments, [2] token groups,
-                        //        [3] large-batch token groups
+                        //        [3] large-batch token groups, [4] kTcRowTok token groups
   int32_t* chunk_base;  // [E][nchunks] scratch of the multi-block path
   int32_t* nvalid;      // [T]    valid assignments per token
   int32_t* inv;         // [T*k]  perm position of each valid assignment id
@@ -114,6 +117,8 @@ struct BucketOut {
   int4* tiles;          // [P/16 + E + 1] per token group: expert, first position, tokens, 0
   int32_t* nbase_w;     // [E+1]  large-batch groups (kTcWideTok tokens) before each active expert
   int4* tiles_w;        // [P/kTcWideTok + E + 1] the same table for groups of kTcWideTok tokens
+  int32_t* nbase_r;     // [E+1]  the same for groups of kTcRowTok tokens
+  int4* tiles_r;        // [P/kTcRowTok + E + 1]
 };
 
 // Everything the per-call preparation touches.  logits == nullptr: idx/gate come from the
@@ -177,16 +182,18 @@ struct RouteOne {
   float *gate, *gap;
   float* y;  // [L]: the second GEMM sums the slots here (no combine launch)
 };
-// moe_wide.cu: the expert GEMMs of a large batch (positions as the MMA's M, 256 weight rows
-// as N); reads the per-position x terms (launch_split_x) and the kTcWideTok group table.
+// moe_wide.cu: the expert GEMMs of a batch (positions as the MMA's M, 256 weight rows as N);
+// reads the per-position x terms (launch_split_x_wide) and the group table of its tile size:
+// rows == false, 128 positions per tile with the terms folded into the reduction (large
+// batches); rows == true, 32 positions x 4 terms as the 128 MMA rows (small batches).
 bool wide_path_supported(int L, int I);
 // x into per-position terms for the large-batch path (scales in its stage-major layout)
 cudaError_t launch_split_x_wide(const uint16_t* x, int T, int L, int k, int E, const int32_t* idx,
                                 const BucketOut& b, uint8_t* xq, uint8_t* xsf, cudaStream_t s,
                                 bool pdl);
 // Tile descriptors of both expert GEMMs of a large batch (workspace int4 entries).
-size_t wide_desc_count(int L, int I, int E, int T, int k);
-cudaError_t launch_wide_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k,
+size_t wide_desc_count(int L, int I, int E, int T, int k, bool rows);
+cudaError_t launch_wide_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k, bool rows,
                                 const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,
                                 uint8_t* act_q, uint8_t* act_sf, int act_kind, float b1, float b2,
                                 const float* gate, float* ybuf, int4* desc, int32_t* status,

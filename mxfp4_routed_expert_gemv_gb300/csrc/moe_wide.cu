@@ -43,32 +43,58 @@
 namespace k3 {
 namespace {
 
-constexpr int kWK = 128;                                 // reduction elements per stage
-constexpr int kWM = kTcWideTok;                          // positions per tile (MMA M)
+constexpr int kWM = kTcWideTok;                          // MMA M (rows of the A tile)
 constexpr int kWN = 256;                                 // weight rows per tile (MMA N)
-constexpr uint32_t kAtBytes = kWM * (kWK / 2);           // one term's position tile: 8 KB
-constexpr uint32_t kBwBytes = kWN * (kWK / 2);           // the weight tile: 16 KB
-constexpr uint32_t kAsBytes = kWM * 16;                 // the positions' scales: 2 KB
-constexpr uint32_t kStageW = kTerms * kAtBytes + kBwBytes + kAsBytes;  // 50 KB
+constexpr int kWsK = 512;                                // reduction per weight-scale box
 constexpr uint32_t kWsBytes = kWN * 16;                  // one weight-scale ring slot: 4 KB
 constexpr int kThreadsW = 448;
 constexpr int kEpiWarpsW = 8, kProdWarpW = 8, kMmaWarpW = 9, kSfWarpW0 = 10;
 constexpr uint32_t kAccColsW = kWN;                      // one fp32 accumulator, N columns
-// TMEM scale ring, per stage: A (positions) scales of term t, K-step j at 8 t + 4 j (4
-// columns: row m reads lane m of column + m/32); B (weight) scales of K-step j at 32 + 8 j
-// (8 columns: row n reads column + n/32 in every lane quarter).
-constexpr uint32_t kSfColsW = 8 * kTerms + 16;
 constexpr uint32_t kTmemColsW = 512;
+
+// The two tile shapes.  Folded (TR false): 128 positions are the MMA's rows and each
+// activation term is its own MMA into the same accumulator (kTerms A tiles per stage; stages
+// of K = 128, 64-byte swizzle).  Rows (TR true): the 128 MMA rows are 32 positions x kTerms
+// terms (the per-position term rows as stored), one MMA per K-step, and the epilogue adds a
+// position's term rows (stages of K = 256, 128-byte swizzle: a stage of this shape has four
+// times fewer MMAs per byte, so it is made twice as long, with rows of 128 bytes).
+// TMEM scale ring, per stage: A scales of term t, K-step j at 4 (t kKSteps + j): 4 columns,
+// row m reads lane m of column + m/32; B (weight) scales of K-step j at kSfB + 8 j: 8
+// columns, row n reads column + n/32 in every lane quarter.
+template <bool TR>
+struct WMode {
+  static constexpr int kPos = TR ? kTcRowTok : kTcWideTok;        // positions per tile
+  static constexpr int kTermMmas = TR ? 1 : kTerms;               // MMAs per K-step
+  static constexpr int kKS = TR ? 256 : 128;                      // reduction per stage
+  static constexpr int kKSteps = kKS / 64;
+  static constexpr uint32_t kRowB = kKS / 2;                      // bytes of a row per stage
+  static constexpr uint32_t kSbo = 8 * kRowB;                     // 8-row group stride
+  static constexpr uint32_t kLayout = TR ? tc::kLayout128B : tc::kLayout64B;
+  static constexpr uint32_t kATile = kWM * kRowB;                 // one 128-row A tile
+  static constexpr uint32_t kABytes = kATile * kTermMmas;         // A tiles of a stage
+  static constexpr uint32_t kBBytes = kWN * kRowB;                // the weight tile
+  static constexpr int kAsBoxes = kKS / 128;                      // 16-byte scale rows per position
+  static constexpr uint32_t kAsBytes = kPos * 16 * kAsBoxes;      // the positions' scales
+  static constexpr uint32_t kStage =
+      ((kABytes + kBBytes + kAsBytes + 1023) / 1024) * 1024;      // 49 KB or 50 KB
+  static constexpr int kStagesPerWs = kWsK / kKS;                 // stages per weight-scale box
+  static constexpr uint32_t kSfB = 4 * kKSteps * kTermMmas;
+  static constexpr uint32_t kSfCols = kSfB + 8 * kKSteps;
+  static_assert(kPos * (TR ? kTerms : 1) == kWM, "A tile rows");
+};
 constexpr int kActStride = 132;  // floats per position row of GEMM1's act staging
 constexpr int kEpiBarW = 1;      // named barrier of the 256 epilogue threads
 
-template <int PH>
+template <int PH, bool TR>
 struct WLay {
-  static constexpr int kStages = PH == 0 ? 3 : 4;
-  static constexpr uint32_t kActBytes = PH == 0 ? kWM * kActStride * 4 : 0;
-  static constexpr size_t kSmemBytes = (size_t)kStages * kStageW + kActBytes + 2 * kWsBytes + 1024;
+  using M = WMode<TR>;
+  static constexpr int kStages = TR ? 4 : (PH == 0 ? 3 : 4);
+  // folded GEMM1 parks act in shared memory to free the accumulator before its MXFP4 split
+  static constexpr uint32_t kActBytes = (PH == 0 && !TR) ? kWM * kActStride * 4 : 0;
+  static constexpr size_t kSmemBytes =
+      (size_t)kStages * M::kStage + kActBytes + 2 * kWsBytes + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
-  static_assert(kAccColsW + kStages * kSfColsW <= kTmemColsW, "TMEM budget");
+  static_assert(kAccColsW + kStages * M::kSfCols <= kTmemColsW, "TMEM budget");
 };
 
 struct WArgs {
@@ -89,8 +115,9 @@ struct WArgs {
 };
 
 struct WMaps {
-  CUtensorMap a;      // activation terms, 3-D: [P][kTerms][K / 2], boxes of 128 positions
-  CUtensorMap as;     // their scales, stage-major: [K / 128 * P][16 B], boxes of 128 rows
+  CUtensorMap a;      // activation terms: folded, 3-D [P][kTerms][K / 2], boxes of 128
+                      // positions of one term; rows, 2-D [P * kTerms][K / 2], boxes of 128 rows
+  CUtensorMap as;     // their scales, stage-major: [K / 128 * P][16 B], boxes of kPos rows
   CUtensorMap w0, w1; // weights: w1 and w3 (boxes of 128 rows) or w2 (twice, 256 rows)
   CUtensorMap s0, s1; // weight scales [E * R][K / 32 B], boxes of 16 B (512-wide chunks)
 };
@@ -117,6 +144,7 @@ __global__ void __launch_bounds__(256) k_wide_tiles(const int32_t* __restrict__ 
                                                     const int32_t* __restrict__ nbase,
                                                     const int4* __restrict__ groups, int RB,
                                                     int4* __restrict__ desc) {
+  // (nbase[active experts] is the group count of the table)
   pdl_wait();
   pdl_launch();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
@@ -152,6 +180,41 @@ __host__ __device__ __forceinline__ size_t wide_sf_offset(int grp, int pos, int 
 }
 static_assert(kTerms == 4, "one 32-bit word of scales per group");
 
+// Rows mode: a position's kTerms term rows are 4 consecutive lanes (a quad, t4 = lane % 4).
+// On entry each lane holds 32 columns of its term row; on exit v[0 .. 7] holds the sums over
+// the four terms of columns 8 t4 .. 8 t4 + 7, added as (t0 + t2) + (t1 + t3): a reduce-scatter
+// in two exchanges (16 values with the lane 2 apart, then 8 with the neighbour).
+__device__ __forceinline__ void quad_reduce_scatter32(float (&v)[32], int t4) {
+  const bool h2 = (t4 & 2) != 0, h1 = (t4 & 1) != 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float send = h2 ? v[i] : v[i + 16];
+    const float keep = h2 ? v[i + 16] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float send = h1 ? v[i] : v[i + 8];
+    const float keep = h1 ? v[i + 8] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+  }
+}
+
+// The MXFP4 terms of one group of 32 act values (consumed) into the per-position rows and
+// the stage-major scale word.
+__device__ __forceinline__ void store_act_group(const WArgs& f, float (&r)[32], size_t pos, int grp) {
+  uint32_t words[kTerms][4], sfb[kTerms];
+  mx_split_lane32(r, words, sfb);
+#pragma unroll
+  for (int tt = 0; tt < kTerms; ++tt) {
+    const size_t r2 = pos * kTerms + tt;
+    *reinterpret_cast<uint4*>(f.act_q + r2 * (size_t)(f.I >> 1) + grp * 16) =
+        make_uint4(words[tt][0], words[tt][1], words[tt][2], words[tt][3]);
+  }
+  *reinterpret_cast<uint32_t*>(f.act_sf + wide_sf_offset(grp, (int)pos, f.P)) =
+      sfb[0] | (sfb[1] << 8) | (sfb[2] << 16) | (sfb[3] << 24);
+}
+
 // bytes 0xFF -> 0x00 (an E8M0 "no value" becomes the smallest scale: the group adds nothing
 // measurable, as the README decoder's zero group)
 __device__ __forceinline__ uint32_t clear_ff(uint32_t w) {
@@ -161,11 +224,13 @@ __device__ __forceinline__ uint32_t clear_ff(uint32_t w) {
   return w & ~(ff * 0xFFu);
 }
 
-template <int PH>
+template <int PH, bool TR>
 __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant__ WMaps mp,
                                                            const WArgs f) {
-  using Y = WLay<PH>;
+  using Y = WLay<PH, TR>;
+  using M = WMode<TR>;
   constexpr int S = Y::kStages;
+  constexpr uint32_t kStageW = M::kStage;
   extern __shared__ uint8_t dsm[];
   __shared__ __align__(8) uint64_t full[S], sfready[S], empty[S];
   __shared__ __align__(8) uint64_t accfull, accempty, drained, wsfull[2], wsempty[2];
@@ -215,20 +280,22 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
   pdl_launch();
   const uint32_t t0 = tbase;
   volatile int* abort_v = &abort_flag;
-  const int ntiles = f.meta[3] * f.RB;
-  const int KC = f.K / kWK;
+  const int ntiles = f.meta[TR ? 4 : 3] * f.RB;
+  const int KC = f.K / M::kKS;
 
   if (warp == kProdWarpW) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint64_t once = tc::make_policy_evict_first(), reused = tc::make_policy_evict_normal();
+      // a stage reads 64 or 128 bytes of each weight row and the tensor maps fill L2 in
+      // 256-byte pieces, so a row's next bytes are read from L2 by the following stages:
+      // weights keep normal priority (evict-first would drop them before that)
+      const uint64_t pol = tc::make_policy_evict_normal();
       int it = 0, ch = 0;  // stages and weight-scale chunks issued
       bool stop = false;
       int4 next = cta < ntiles ? __ldg(f.desc + cta) : make_int4(0, 0, 0, 0);
       for (int t = cta; t < ntiles && !stop; t += G) {
         const WTile wt = unpack_tile(next);
         if (t + G < ntiles) next = __ldg(f.desc + t + G);  // in flight during this tile
-        const uint64_t pol = wt.groups > 1 ? reused : once;
         const int wrow = wt.expert * f.R + wt.rb * (PH == 0 ? 128 : 256);
         for (int kc = 0; kc < KC; ++kc, ++it) {
           const int s = it % S;
@@ -238,9 +305,9 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
             stop = true;
             break;
           }
-          if ((kc & 3) == 0) {
-            // the weight scales of stages kc .. kc + 3 into slot ch % 2, once the scale warps
-            // are done with the chunk that last used it
+          if (kc % M::kStagesPerWs == 0) {
+            // the weight scales of the next kWsK reduction elements into slot ch % 2, once the
+            // scale warps are done with the chunk that last used it
             const int slot = ch & 1;
             if (ch >= 2 && !mbar_wait_ab(&wsempty[slot], ((ch >> 1) - 1) & 1, f.status, abort_v)) {
               *abort_v = 1;
@@ -250,25 +317,39 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
             uint8_t* ws = wsring + slot * kWsBytes;
             mbar_arrive_expect_tx(&wsfull[slot], kWsBytes);
             if (PH == 0) {
-              tc::tma_load_2d(ws, &mp.s0, (kc >> 2) * 16, wrow, &wsfull[slot]);
-              tc::tma_load_2d(ws + kWsBytes / 2, &mp.s1, (kc >> 2) * 16, wrow, &wsfull[slot]);
+              tc::tma_load_2d(ws, &mp.s0, (kc / M::kStagesPerWs) * 16, wrow, &wsfull[slot]);
+              tc::tma_load_2d(ws + kWsBytes / 2, &mp.s1, (kc / M::kStagesPerWs) * 16, wrow,
+                              &wsfull[slot]);
             } else {
-              tc::tma_load_2d(ws, &mp.s0, (kc >> 2) * 16, wrow, &wsfull[slot]);
+              tc::tma_load_2d(ws, &mp.s0, (kc / M::kStagesPerWs) * 16, wrow, &wsfull[slot]);
             }
             ++ch;
           }
           uint8_t* st = sm + (size_t)s * kStageW;
-          mbar_arrive_expect_tx(&full[s], kStageW);
-#pragma unroll
-          for (int tt = 0; tt < kTerms; ++tt)
-            tc::tma_load_3d(st + tt * kAtBytes, &mp.a, kc * (kWK / 2), tt, wt.pos0, &full[s]);
-          tc::tma_load_2d(st + kTerms * kAtBytes + kBwBytes, &mp.as, 0, kc * f.P + wt.pos0, &full[s]);
-          uint8_t* sb = st + kTerms * kAtBytes;
-          if (PH == 0) {
-            tc::tma_load_2d_hint(sb, &mp.w0, kc * (kWK / 2), wrow, &full[s], pol);
-            tc::tma_load_2d_hint(sb + kBwBytes / 2, &mp.w1, kc * (kWK / 2), wrow, &full[s], pol);
+          // rows: only the boxes of 8 positions (32 term rows) that hold the tile's tokens;
+          // the other A rows keep older bytes, which reach only D rows the epilogue skips
+          const int nbox = TR ? (wt.ntok + 7) / 8 : 1;
+          mbar_arrive_expect_tx(&full[s], (TR ? nbox * (M::kATile / 4) : M::kABytes) + M::kBBytes +
+                                              M::kAsBytes);
+          const int x = kc * (int)M::kRowB;
+          if (TR) {
+            for (int b = 0; b < nbox; ++b)
+              tc::tma_load_2d(st + b * (M::kATile / 4), &mp.a, x, (wt.pos0 + 8 * b) * kTerms, &full[s]);
           } else {
-            tc::tma_load_2d_hint(sb, &mp.w0, kc * (kWK / 2), wrow, &full[s], pol);
+#pragma unroll
+            for (int tt = 0; tt < kTerms; ++tt)
+              tc::tma_load_3d(st + tt * M::kATile, &mp.a, x, tt, wt.pos0, &full[s]);
+          }
+#pragma unroll
+          for (int r = 0; r < M::kAsBoxes; ++r)
+            tc::tma_load_2d(st + M::kABytes + M::kBBytes + r * (M::kPos * 16), &mp.as, 0,
+                            (kc * M::kAsBoxes + r) * f.P + wt.pos0, &full[s]);
+          uint8_t* sb = st + M::kABytes;
+          if (PH == 0) {
+            tc::tma_load_2d_hint(sb, &mp.w0, x, wrow, &full[s], pol);
+            tc::tma_load_2d_hint(sb + M::kBBytes / 2, &mp.w1, x, wrow, &full[s], pol);
+          } else {
+            tc::tma_load_2d_hint(sb, &mp.w0, x, wrow, &full[s], pol);
           }
         }
       }
@@ -298,7 +379,7 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
         // the stage's data has landed: the MMAs that last read this TMEM scale slot are done
         bool ok = !*abort_v &&
                   mbar_wait_ab(&full[s], par, lane == 0 ? f.status : nullptr, abort_v);
-        if ((kc & 3) == 0) {
+        if (kc % M::kStagesPerWs == 0) {
           ++ch;
           ok = ok && mbar_wait_ab(&wsfull[ch & 1], (ch >> 1) & 1, lane == 0 ? f.status : nullptr,
                                   abort_v);
@@ -309,41 +390,47 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
           break;
         }
         const uint8_t* st = sm + (size_t)s * kStageW;
-        const uint4 as = *reinterpret_cast<const uint4*>(st + kTerms * kAtBytes + kBwBytes +
-                                                         16 * (32 * q + lane));
-        // word g holds group g's term bytes; term t's word gathers byte t of each
-        uint32_t aw[kTerms];
+        // this lane's A row: a position (folded), or a position's term row (rows)
+        const int arow = 32 * q + lane;
+        const uint8_t* ws = wsring + (ch & 1) * kWsBytes + (kc % M::kStagesPerWs) * (M::kKS / 32);
+        const uint32_t ring = t0 + lane_off + kAccColsW + (uint32_t)s * M::kSfCols;
 #pragma unroll
-        for (int tt = 0; tt < kTerms; ++tt) {
-          const uint32_t sel = (uint32_t)tt | ((uint32_t)(tt + 4) << 4);
-          aw[tt] = __byte_perm(__byte_perm(as.x, as.y, sel), __byte_perm(as.z, as.w, sel), 0x5410);
+        for (int r = 0; r < M::kAsBoxes; ++r) {  // each 16-byte row: 4 groups = 2 K-steps
+          const uint4 as = *reinterpret_cast<const uint4*>(
+              st + M::kABytes + M::kBBytes + r * (M::kPos * 16) + 16 * (TR ? (arow >> 2) : arow));
+          // word g of the row holds group g's term bytes; term t's word gathers byte t of each
+#pragma unroll
+          for (int tt = 0; tt < M::kTermMmas; ++tt) {
+            const uint32_t term = TR ? (uint32_t)(arow & 3) : (uint32_t)tt;
+            const uint32_t sel = term | ((term + 4) << 4);
+            const uint32_t a = clear_ff(
+                __byte_perm(__byte_perm(as.x, as.y, sel), __byte_perm(as.z, as.w, sel), 0x5410));
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj)
+              tc::tmem_st_x1(ring + 4 * (tt * M::kKSteps + 2 * r + jj) + q, (a >> (16 * jj)) & 0xFFFFu);
+          }
         }
-        const uint8_t* ws = wsring + (ch & 1) * kWsBytes + 4 * (kc & 3);
-        const uint32_t ring = t0 + lane_off + kAccColsW + (uint32_t)s * kSfColsW;
 #pragma unroll
-        for (int tt = 0; tt < kTerms; ++tt) {
-          const uint32_t a = clear_ff(aw[tt]);
+        for (int r = 0; r < M::kKSteps / 2; ++r) {  // a weight-scale word: 2 K-steps
+          uint32_t wv[8];
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
-            tc::tmem_st_x1(ring + 8 * tt + 4 * j + q, (a >> (16 * j)) & 0xFFFFu);
-        }
-        uint32_t wv[8];
+          for (int c = 0; c < 8; ++c)
+            wv[c] = clear_ff(*reinterpret_cast<const uint32_t*>(ws + 16 * (32 * c + lane) + 4 * r));
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          wv[c] = clear_ff(*reinterpret_cast<const uint32_t*>(ws + 16 * (32 * c + lane)));
+          for (int jj = 0; jj < 2; ++jj) {
+            uint32_t v[8];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          uint32_t v[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) v[c] = (wv[c] >> (16 * j)) & 0xFFFFu;
-          tc::tmem_st_x8(ring + 8 * kTerms + 8 * j, v);
+            for (int c = 0; c < 8; ++c) v[c] = (wv[c] >> (16 * jj)) & 0xFFFFu;
+            tc::tmem_st_x8(ring + M::kSfB + 8 * (2 * r + jj), v);
+          }
         }
         tc::tmem_st_wait();
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&sfready[s]);
-          if ((kc & 3) == 3) mbar_arrive(&wsempty[ch & 1]);  // done with this chunk's slot
+          if (kc % M::kStagesPerWs == M::kStagesPerWs - 1)
+            mbar_arrive(&wsempty[ch & 1]);  // done with this chunk's slot
         }
       }
     }
@@ -370,14 +457,14 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
           }
           tc::fence_after_sync();
           const uint32_t st = tc::smem_addr(sm + (size_t)s * kStageW);
-          const uint32_t sfr = t0 + kAccColsW + (uint32_t)s * kSfColsW;
+          const uint32_t sfr = t0 + kAccColsW + (uint32_t)s * M::kSfCols;
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const uint64_t bd = tc::smem_desc(st + kTerms * kAtBytes + 32 * j, 16, 512, tc::kLayout64B);
+          for (int j = 0; j < M::kKSteps; ++j) {
+            const uint64_t bd = tc::smem_desc(st + M::kABytes + 32 * j, 16, M::kSbo, M::kLayout);
 #pragma unroll
-            for (int tt = 0; tt < kTerms; ++tt) {
-              const uint64_t ad = tc::smem_desc(st + tt * kAtBytes + 32 * j, 16, 512, tc::kLayout64B);
-              tc::mma_mxf4(t0, ad, bd, idesc, sfr + 8 * tt + 4 * j, sfr + 8 * kTerms + 8 * j,
+            for (int tt = 0; tt < M::kTermMmas; ++tt) {
+              const uint64_t ad = tc::smem_desc(st + tt * M::kATile + 32 * j, 16, M::kSbo, M::kLayout);
+              tc::mma_mxf4(t0, ad, bd, idesc, sfr + 4 * (tt * M::kKSteps + j), sfr + M::kSfB + 8 * j,
                            (kc == 0 && j == 0 && tt == 0) ? 0u : 1u);
             }
           }
@@ -403,7 +490,86 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
         break;
       }
       tc::fence_after_sync();
-      if (PH == 0) {
+      if (TR) {
+        // rows mode: lane = (position 8 q + lane / 4, term lane % 4)
+        const int t4 = lane & 3;
+        const int mpos = 8 * q + (lane >> 2);  // position within the tile
+        if (PH == 0) {
+          // chunk c = 2 hf + cc: rows 32 c .. 32 c + 31 of w1 (g) and w3 (u); the term rows
+          // added (lane t4 then holds rows 32 c + 8 t4 .. + 7), SwiGLU
+          float act[2][8];
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * hf + cc;
+            uint32_t gr[32], ur[32];
+            tc::tmem_ld_x32(tacc + 32 * c, gr);
+            tc::tmem_ld_x32(tacc + 128 + 32 * c, ur);
+            tc::tmem_ld_wait();
+            float g[32], u[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              g[i] = __uint_as_float(gr[i]);
+              u[i] = __uint_as_float(ur[i]);
+            }
+            quad_reduce_scatter32(g, t4);
+            quad_reduce_scatter32(u, t4);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) act[cc][i] = activation_fast(g[i], u[i], f.act_kind, f.b1, f.b2);
+          }
+          tc::fence_before_sync();
+          named_bar(kEpiBarW, 32 * kEpiWarpsW);
+          if (et == 0) mbar_arrive(&accempty);  // the next tile's MMAs may start
+          // the quad splits each chunk's group of 32 act values (every lane takes part in the
+          // shuffles; only positions of the tile store)
+          const bool mine = mpos < wt.ntok;
+          const size_t pos = (size_t)(wt.pos0 + mpos);
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int grp = wt.rb * 4 + 2 * hf + cc;
+            uint32_t wq[kTerms], sfb[kTerms];
+            mx_split_quad8(act[cc], wq, sfb);
+            if (mine) {
+#pragma unroll
+              for (int tt = 0; tt < kTerms; ++tt)
+                *reinterpret_cast<uint32_t*>(f.act_q + (pos * kTerms + tt) * (size_t)(f.I >> 1) +
+                                             grp * 16 + 4 * t4) = wq[tt];
+              if (t4 == 0)
+                *reinterpret_cast<uint32_t*>(f.act_sf + wide_sf_offset(grp, (int)pos, f.P)) =
+                    sfb[0] | (sfb[1] << 8) | (sfb[2] << 16) | (sfb[3] << 24);
+            }
+          }
+        } else {
+          // o for output rows 256 rb + 128 hf .. + 127 of this warp's 8 positions, 32 at a
+          // time; after the term sum lane t4 holds 8 of the 32, stored times the gate
+          int a = 0;
+          float gt = 0.f;
+          const bool mine = mpos < wt.ntok;
+          if (mine) {
+            a = __ldg(f.perm + wt.pos0 + mpos);
+            gt = __ldg(f.gate + a);
+          }
+          float* yrow = f.ybuf + (size_t)a * f.L + (size_t)wt.rb * 256 + 128 * hf + 8 * t4;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t vr[32];
+            tc::tmem_ld_x32(tacc + 128 * hf + 32 * c, vr);
+            tc::tmem_ld_wait();
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(vr[i]);
+            quad_reduce_scatter32(v, t4);
+            if (mine) {
+              *reinterpret_cast<float4*>(yrow + 32 * c) =
+                  make_float4(gt * v[0], gt * v[1], gt * v[2], gt * v[3]);
+              *reinterpret_cast<float4*>(yrow + 32 * c + 4) =
+                  make_float4(gt * v[4], gt * v[5], gt * v[6], gt * v[7]);
+            }
+          }
+          tc::fence_before_sync();
+          named_bar(kEpiBarW, 32 * kEpiWarpsW);
+          if (et == 0) mbar_arrive(&accempty);
+        }
+      } else if (PH == 0) {
         // g in columns 0..127, u in 128..255 (rows 128 rb .. 128 rb + 127 of w1 / w3); this
         // warp takes rows 64 hf .. 64 hf + 63, 16 at a time
 #pragma unroll 1
@@ -443,18 +609,7 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
               r[i + 2] = v.z;
               r[i + 3] = v.w;
             }
-            uint32_t words[kTerms][4], sfb[kTerms];
-            mx_split_lane32(r, words, sfb);
-            const size_t pos = (size_t)(wt.pos0 + mm);
-            const int grp = wt.rb * 4 + c;
-#pragma unroll
-            for (int tt = 0; tt < kTerms; ++tt) {
-              const size_t r2 = pos * kTerms + tt;
-              *reinterpret_cast<uint4*>(f.act_q + r2 * (size_t)(f.I >> 1) + grp * 16) =
-                  make_uint4(words[tt][0], words[tt][1], words[tt][2], words[tt][3]);
-            }
-            *reinterpret_cast<uint32_t*>(f.act_sf + wide_sf_offset(grp, (int)pos, f.P)) =
-                sfb[0] | (sfb[1] << 8) | (sfb[2] << 16) | (sfb[3] << 24);
+            store_act_group(f, r, (size_t)(wt.pos0 + mm), wt.rb * 4 + c);
           }
         }
         named_bar(kEpiBarW, 32 * kEpiWarpsW);  // the staging buffer is free again
@@ -564,20 +719,20 @@ __global__ void __launch_bounds__(512) k_split_x_wide(const uint16_t* __restrict
   }
 }
 
-template <int PH>
+template <int PH, bool TR>
 cudaError_t launch_wide_phase(const WMaps& mp, const WArgs& f, cudaStream_t s, bool pdl) {
   static int configured[64] = {0};
-  constexpr size_t smem = WLay<PH>::kSmemBytes;
+  constexpr size_t smem = WLay<PH, TR>::kSmemBytes;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_moe_wide<PH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_moe_wide<PH, TR>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
   const int grid = sm_count() < kTcMaxGrid ? sm_count() : kTcMaxGrid;
-  return launch_kernel(k_moe_wide<PH>, dim3(grid), dim3(kThreadsW), smem, s, pdl, mp, f);
+  return launch_kernel(k_moe_wide<PH, TR>, dim3(grid), dim3(kThreadsW), smem, s, pdl, mp, f);
 }
 
 }  // namespace
@@ -591,18 +746,20 @@ cudaError_t launch_split_x_wide(const uint16_t* x, int T, int L, int k, int E, c
                        idx, static_cast<const int32_t*>(b.inv), xq, xsf);
 }
 
-size_t wide_desc_count(int L, int I, int E, int T, int k) {
-  const size_t groups = ((size_t)T * k + kTcWideTok - 1) / kTcWideTok + E + 1;
+size_t wide_desc_count(int L, int I, int E, int T, int k, bool rows) {
+  const int pos = rows ? kTcRowTok : kTcWideTok;
+  const size_t groups = ((size_t)T * k + pos - 1) / pos + E + 1;
   return groups * (size_t)(I / 128) + groups * (size_t)(L / 256);
 }
 
-cudaError_t launch_wide_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k,
+cudaError_t launch_wide_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k, bool rows,
                                 const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,
                                 uint8_t* act_q, uint8_t* act_sf, int act_kind, float b1, float b2,
                                 const float* gate, float* ybuf, int4* desc, int32_t* status,
                                 cudaStream_t s, void (*between)(cudaStream_t)) {
   const uint64_t P = (uint64_t)T * k;
-  const size_t groups = (P + kTcWideTok - 1) / kTcWideTok + E + 1;
+  const int pos_tile = rows ? kTcRowTok : kTcWideTok;
+  const size_t groups = (P + pos_tile - 1) / pos_tile + E + 1;
   int4* desc0 = desc;
   int4* desc1 = desc + groups * (size_t)(I / 128);
   for (int ph = 0; ph < 2; ++ph) {
@@ -610,21 +767,31 @@ cudaError_t launch_wide_experts(const ExpertPtrs& w, int L, int I, int E, int T,
     const size_t n = groups * (size_t)RB;
     cudaError_t e = launch_kernel(k_wide_tiles, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
                                   true, static_cast<const int32_t*>(b.meta),
-                                  static_cast<const int32_t*>(b.nbase_w),
-                                  static_cast<const int4*>(b.tiles_w), RB, ph == 0 ? desc0 : desc1);
+                                  static_cast<const int32_t*>(rows ? b.nbase_r : b.nbase_w),
+                                  static_cast<const int4*>(rows ? b.tiles_r : b.tiles_w), RB,
+                                  ph == 0 ? desc0 : desc1);
     if (e != cudaSuccess) return e;
   }
   WMaps m0, m1;
   const auto sw64 = CU_TENSOR_MAP_SWIZZLE_64B, none = CU_TENSOR_MAP_SWIZZLE_NONE;
-  if (!make_map_3d(&m0.a, xq, L / 2, kTerms, L / 2, P, (uint64_t)kTerms * (L / 2), kWK / 2, kWM, sw64) ||
-      !make_map_2d_sw(&m0.as, xsf, 16, (uint64_t)(L / kWK) * P, 16, kWM, none) ||
-      !make_map_2d_sw(&m0.w0, w.w1p, L / 2, (uint64_t)E * I, kWK / 2, 128, sw64) ||
-      !make_map_2d_sw(&m0.w1, w.w3p, L / 2, (uint64_t)E * I, kWK / 2, 128, sw64) ||
+  // activation terms: boxes of 128 positions of one term (folded, 64-byte rows) or of 128
+  // term rows (rows, 128-byte rows); weights: rows of the same width
+  const auto sw = rows ? CU_TENSOR_MAP_SWIZZLE_128B : sw64;
+  const uint32_t rowb = rows ? 128 : 64;
+  auto amap = [&](CUtensorMap* m, const void* base, int K) {
+    return rows ? make_map_2d_sw(m, base, K / 2, P * kTerms, rowb, kWM / 4, sw)
+                : make_map_3d(m, base, K / 2, kTerms, K / 2, P, (uint64_t)kTerms * (K / 2), rowb,
+                              kWM, sw);
+  };
+  if (!amap(&m0.a, xq, L) ||
+      !make_map_2d_sw(&m0.as, xsf, 16, (uint64_t)(L / 128) * P, 16, pos_tile, none) ||
+      !make_map_2d_sw(&m0.w0, w.w1p, L / 2, (uint64_t)E * I, rowb, 128, sw) ||
+      !make_map_2d_sw(&m0.w1, w.w3p, L / 2, (uint64_t)E * I, rowb, 128, sw) ||
       !make_map_2d_sw(&m0.s0, w.w1s, L / 32, (uint64_t)E * I, 16, 128, none) ||
       !make_map_2d_sw(&m0.s1, w.w3s, L / 32, (uint64_t)E * I, 16, 128, none) ||
-      !make_map_3d(&m1.a, act_q, I / 2, kTerms, I / 2, P, (uint64_t)kTerms * (I / 2), kWK / 2, kWM, sw64) ||
-      !make_map_2d_sw(&m1.as, act_sf, 16, (uint64_t)(I / kWK) * P, 16, kWM, none) ||
-      !make_map_2d_sw(&m1.w0, w.w2p, I / 2, (uint64_t)E * L, kWK / 2, 256, sw64) ||
+      !amap(&m1.a, act_q, I) ||
+      !make_map_2d_sw(&m1.as, act_sf, 16, (uint64_t)(I / 128) * P, 16, pos_tile, none) ||
+      !make_map_2d_sw(&m1.w0, w.w2p, I / 2, (uint64_t)E * L, rowb, 256, sw) ||
       !make_map_2d_sw(&m1.s0, w.w2s, I / 32, (uint64_t)E * L, 16, 256, none))
     return cudaErrorInvalidValue;
   m1.w1 = m1.w0;
@@ -648,7 +815,8 @@ cudaError_t launch_wide_experts(const ExpertPtrs& w, int L, int I, int E, int T,
   f.R = I;
   f.RB = I / 128;
   f.desc = desc0;
-  cudaError_t e = launch_wide_phase<0>(m0, f, s, true);
+  cudaError_t e = rows ? launch_wide_phase<0, true>(m0, f, s, true)
+                       : launch_wide_phase<0, false>(m0, f, s, true);
   if (e != cudaSuccess) return e;
   if (between) between(s);
   // GEMM2: w2 -> gate * o per assignment
@@ -656,7 +824,7 @@ cudaError_t launch_wide_experts(const ExpertPtrs& w, int L, int I, int E, int T,
   f.R = L;
   f.RB = L / 256;
   f.desc = desc1;
-  return launch_wide_phase<1>(m1, f, s, true);
+  return rows ? launch_wide_phase<1, true>(m1, f, s, true) : launch_wide_phase<1, false>(m1, f, s, true);
 }
 
 }  // namespace k3

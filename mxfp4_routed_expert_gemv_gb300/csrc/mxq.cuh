@@ -160,4 +160,34 @@ __device__ __forceinline__ void mx_split_lane32(float (&r)[32], uint32_t (&words
   }
 }
 
+// Four lanes (a quad, t4 = lane % 4), one group of 32 elements: lane t4 holds elements
+// 8 t4 .. 8 t4 + 7 in r (consumed).  The kTerms terms, with the arithmetic of mx_split_lane32
+// (the group maximum over all 32, each element rounded alone): on return w[t] is lane t4's
+// 4 bytes of term t's 16 code bytes (bytes 4 t4 .. 4 t4 + 3, element 8 t4 in the low nibble)
+// and sf[t] the term's E8M0 byte (the same in the four lanes).  Every lane of the warp calls it.
+__device__ __forceinline__ void mx_split_quad8(float (&r)[8], uint32_t (&w)[kTerms],
+                                               uint32_t (&sf)[kTerms]) {
+#pragma unroll
+  for (int t = 0; t < kTerms; ++t) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(r[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int e = mx_scale_exp(amax);
+    const float down = pow2f(-e), up = pow2f(e);
+    uint32_t word = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      const uint32_t b = e2m1x2_rn(r[i + 1] * down, r[i] * down);
+      const float2 q = e2m1x2_values(b);
+      r[i] -= q.x * up;
+      r[i + 1] -= q.y * up;
+      word |= b << (4 * i);
+    }
+    w[t] = word;
+    sf[t] = (uint32_t)(e + 127);
+  }
+}
+
 }  // namespace k3

@@ -28,10 +28,11 @@ CASES = [
     # one token: the second GEMM's CTAs wait for the routing words; 4 reduction units per
     # tile, so the first GEMM also has tiles shared by two CTAs
     synth.small_workload(T=1, E=16, k=4, latent=2048, inter=512, hidden=256, seed=51),
-    # three tokens: tiles of 4 units spread over more CTAs than there are tiles
-    synth.small_workload(T=3, E=12, k=4, latent=2048, inter=512, hidden=256, seed=52),
-    # nine tokens, 8 units per tile: a tile's head collects two or more parts
-    synth.small_workload(T=9, E=12, k=2, latent=4096, inter=512, hidden=256, seed=53),
+    # two tokens: tiles of 4 units spread over more CTAs than there are tiles, so a tile's
+    # head collects several parts (more than its shared-memory buffer holds)
+    synth.small_workload(T=2, E=12, k=4, latent=2048, inter=512, hidden=256, seed=52),
+    # two tokens, 8 units per tile
+    synth.small_workload(T=2, E=12, k=2, latent=4096, inter=512, hidden=256, seed=53),
 ]
 
 
