@@ -127,8 +127,7 @@ size_t carve(const k3moe_cfg* c, int32_t T, void* base, bool host_stage, Workspa
     t.asf = cv.take<uint8_t>(P * kTerms * (I / 32));
     t.part = cv.take<float>(tc_part_floats((int)Tt));
     if (T >= kRowsMinTokens && wide_path_supported((int)L, (int)I))
-      t.wdesc = cv.take<int4>(
-          wide_desc_count((int)L, (int)I, (int)E, (int)Tt, (int)K, T < kWideMinTokens));
+      t.wdesc = cv.take<int4>(wide_desc_count((int)L, (int)I, (int)E, (int)Tt, (int)K));
   } else {
     t.x16 = cv.take<__half>(Tt * L);
     t.xexp = cv.take<int32_t>(Tt);
@@ -286,40 +285,44 @@ int run_pipeline(const k3moe_cfg* c, bool route, const void* h, const void* wr,
                          gate, gap, s, true));
   }
   K3_TRY(phase(1, s));
-  PrepArgs p{fused_topk ? w.logits : nullptr, bias, E, K, c->renorm, c->routed_scale, idx, gate,
-             gap, T, L, static_cast<const uint16_t*>(x), w.tc ? nullptr : w.x16, w.xexp, w.b, y,
-             status};
-  const RouteOne ro{w.logits, bias, c->renorm, c->routed_scale, idx, gate, gap, y};
   // batches: positions of one expert as the MMA's M dimension (moe_wide.cu), the activation
-  // terms as MMA rows below kWideMinTokens tokens, folded into the reduction from there
+  // terms as MMA rows below kWideMinTokens tokens, folded into the reduction from there; the
+  // preparation writes those GEMMs' tile descriptors
   const bool wide = w.tc && T >= kRowsMinTokens && wide_path_supported(L, I);
   const bool rows = T < kWideMinTokens;
+  BucketOut b = w.b;
+  b.wdesc = nullptr;
+  if (wide) wide_desc_setup(b, w.wdesc, L, I, E, T, K, rows);
+  PrepArgs p{fused_topk ? w.logits : nullptr, bias, E, K, c->renorm, c->routed_scale, idx, gate,
+             gap, T, L, static_cast<const uint16_t*>(x), w.tc ? nullptr : w.x16, w.xexp, b, y,
+             status};
+  const RouteOne ro{w.logits, bias, c->renorm, c->routed_scale, idx, gate, gap, y};
   if (!one) {
     K3_TRY(launch_prep(p, s, route));
     if (wide)
-      K3_TRY(launch_split_x_wide(static_cast<const uint16_t*>(x), T, L, K, E, idx, w.b, w.xq,
+      K3_TRY(launch_split_x_wide(static_cast<const uint16_t*>(x), T, L, K, E, idx, b, w.xq,
                                  w.xsf, s, true));
     else if (w.tc)
-      K3_TRY(launch_split_x(static_cast<const uint16_t*>(x), T, L, K, E, idx, w.b, w.xq, w.xsf,
+      K3_TRY(launch_split_x(static_cast<const uint16_t*>(x), T, L, K, E, idx, b, w.xq, w.xsf,
                             s, true));
   }
   if (wide) {
     K3_TRY(phase(2, s));
-    K3_TRY(launch_wide_experts(ep, L, I, E, T, K, rows, w.xq, w.xsf, w.b, w.aq, w.asf, c->act,
-                               c->situ_b1, c->situ_b2, gate, w.ybuf, w.wdesc, status, s, phase3));
+    K3_TRY(launch_wide_experts(ep, L, I, E, T, K, rows, w.xq, w.xsf, b, w.aq, w.asf, c->act,
+                               c->situ_b1, c->situ_b2, gate, w.ybuf, status, s, phase3));
     K3_TRY(phase(4, s));
   } else if (w.tc) {
     K3_TRY(phase(2, s));
-    K3_TRY(launch_tc_experts(ep, L, I, E, T, K, w.xq, w.xsf, w.b, w.aq, w.asf, c->act,
+    K3_TRY(launch_tc_experts(ep, L, I, E, T, K, w.xq, w.xsf, b, w.aq, w.asf, c->act,
                              c->situ_b1, c->situ_b2, gate, w.ybuf, w.part, status, s, true,
                              phase3, one ? &ro : nullptr));
     K3_TRY(phase(4, s));
   } else {
     K3_TRY(phase(2, s));
-    K3_TRY(launch_gemm1(ep, L, I, E, T, K, w.x16, w.xexp, w.b, w.act, c->act, c->situ_b1,
+    K3_TRY(launch_gemm1(ep, L, I, E, T, K, w.x16, w.xexp, b, w.act, c->act, c->situ_b1,
                         c->situ_b2, status, s, true));
     K3_TRY(phase(3, s));
-    K3_TRY(launch_gemm2(ep, L, I, E, T, K, w.act, gate, w.b, w.ybuf, status, s, true));
+    K3_TRY(launch_gemm2(ep, L, I, E, T, K, w.act, gate, b, w.ybuf, status, s, true));
     K3_TRY(phase(4, s));
   }
   // one routed token: the second GEMM already summed the slots into y

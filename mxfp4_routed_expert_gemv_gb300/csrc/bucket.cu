@@ -12,8 +12,8 @@
 // expert index outside [0, E) is skipped and counted in status[0] (the README's "counted,
 // never silent" expert-drop rule, Part II section 9).
 //
-// Decode-sized batches (T <= 32) take one CTA for everything, optionally including the
-// router's top-k, so the whole preparation is one launch.
+// Batches of up to 4096 assignments take one CTA for everything (up to 32 tokens optionally
+// including the router's top-k), so the whole preparation is one launch.
 #include "launch.h"
 #include "mxq.cuh"
 #include "topk.cuh"
@@ -22,7 +22,9 @@ namespace k3 {
 namespace {
 
 constexpr int kChunkTokens = 16;  // tokens per block in the multi-block path
-constexpr int kSmallTokens = 32;
+constexpr int kSmallTokens = 32;     // the one-CTA preparation also takes the top-k up to here
+constexpr int kSortAssign = 4096;    // assignments (T k) the one-CTA preparation takes
+static_assert(kMaxExperts <= (1 << 20) && kSortAssign <= (1 << 12), "sort key fields");
 
 // Exclusive scan of one int per thread over a block of exactly 1024 threads; *total gets
 // the block sum.
@@ -116,6 +118,35 @@ __device__ void publish_counts(int c, int E, const BucketOut& o, int* excl_out) 
   }
   for (int i = e; i < kTcFlagWords; i += blockDim.x) o.flags[i] = 0;
   *excl_out = excl;
+  if (!o.wdesc) return;
+  // The large-batch GEMMs' tile descriptors, from the group table of their tile size: for
+  // each GEMM, tile t is the active expert whose block of (groups x row blocks) holds t
+  // (bisection over the group prefix, kept in shared memory), its row block and its group
+  // (groups fastest): expert, first position, tokens, row block | the expert's groups << 8.
+  __shared__ int gbase[kMaxExperts + 1];
+  const bool rows = o.wmode == 2;
+  if (flag) gbase[pos] = rows ? nr_excl : nw_excl;
+  if (e == 0) gbase[nact] = rows ? nr_tot : nw_tot;
+  __syncthreads();  // gbase, and the group table this block wrote above
+  const int4* groups = rows ? o.tiles_r : o.tiles_w;
+  for (int ph = 0; ph < 2; ++ph) {
+    const int RB = ph == 0 ? o.wrb0 : o.wrb1;
+    int4* desc = o.wdesc + (ph == 0 ? 0 : o.wdesc1);
+    const int n = gbase[nact] * RB;
+    for (int t = threadIdx.x; t < n; t += blockDim.x) {
+      int lo = 0, hi = nact - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (gbase[mid] * RB <= t) lo = mid; else hi = mid - 1;
+      }
+      const int gb = gbase[lo], ng = gbase[lo + 1] - gb;
+      const int local = t - gb * RB;
+      const int rb = local / ng;
+      const int4 g = groups[gb + (local - rb * ng)];
+      desc[t] = make_int4(g.x, g.y, g.z, rb | (ng << 8));
+    }
+  }
+  __syncthreads();  // gbase is reused by the next call
 }
 
 // One warp: x row (bf16) -> f16 scaled by 2^-e with the largest magnitude in [2^14, 2^15).
@@ -166,14 +197,18 @@ __device__ void token_valid_warp(const int32_t* idx_t, int k, int E, int L, int3
     for (int c = lane; c < L; c += 32) y_t[c] = 0.f;
 }
 
-// Single block of 1024 threads, T <= kSmallTokens: [top-k], count, scan, stable scatter
-// token by token (one warp, lane j handles slot j), x prep.
+// Single block of 1024 threads, up to kSortAssign assignments: [top-k, T <= kSmallTokens],
+// count, scan, the stable scatter as a sort, per-token counts, x prep.  The scatter sorts the
+// keys (expert << 12 | assignment id) with a bitonic network in shared memory: sorted
+// position i is then perm position i (experts ascending, assignment ids ascending within an
+// expert, which is the token order), the order of the multi-block path's token-by-token
+// scatter.  Invalid assignments take the largest key and sort past the valid ones.
 __global__ void __launch_bounds__(1024) k_prep_small(PrepArgs p) {
   pdl_wait();
   pdl_launch();
   __shared__ int cnt[kMaxExperts];
-  __shared__ int cur[kMaxExperts];
   __shared__ uint64_t keys[1024];
+  __shared__ uint32_t skey[kSortAssign];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = p.T, k = p.k, E = p.E;
   if (p.logits) {
@@ -187,39 +222,55 @@ __global__ void __launch_bounds__(1024) k_prep_small(PrepArgs p) {
   cnt[tid] = 0;
   __syncthreads();  // top-k results (global, this block) are visible from here on
   const int P = T * k;
+  int NP = 32;  // sort width: a power of two >= P
+  while (NP < P) NP <<= 1;
   int dropped = 0;
-  for (int a = tid; a < P; a += blockDim.x) {
-    const int e = p.idx[a];
-    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-    else if (e != kRemoteExpert) ++dropped;
+  for (int a = tid; a < NP; a += blockDim.x) {
+    uint32_t key = 0xffffffffu;
+    if (a < P) {
+      const int e = p.idx[a];
+      if (e >= 0 && e < E) {
+        atomicAdd(&cnt[e], 1);
+        key = ((uint32_t)e << 12) | (uint32_t)a;
+      } else if (e != kRemoteExpert) {
+        ++dropped;
+      }
+    }
+    skey[a] = key;
   }
   __syncthreads();
   const int c = (tid < E) ? cnt[tid] : 0;
   int excl;
   publish_counts(c, E, p.b, &excl);
-  if (tid < E) cur[tid] = excl;
   int dtot;
   block_exclusive_scan_1024(dropped, &dtot);
   if (tid == 0 && dtot > 0 && p.status) atomicAdd(p.status + kStatDropped, dtot);
-  __syncthreads();
-  if (warp == 0) {
-    for (int t = 0; t < T; ++t) {
-      if (lane < k) {
-        const int a = t * k + lane;
-        const int e = p.idx[a];
-        if (e >= 0 && e < E) {
-          const int pos = atomicAdd(&cur[e], 1);
-          p.b.perm[pos] = a;
-          p.b.inv[a] = pos;
+  for (int size = 2; size <= NP; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < NP; i += blockDim.x) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const uint32_t a = skey[i], b = skey[j];
+          if ((a > b) == ((i & size) == 0)) {
+            skey[i] = b;
+            skey[j] = a;
+          }
         }
       }
-      __syncwarp();
+      __syncthreads();
     }
-  } else {
-    for (int t = warp - 1; t < T; t += 31) {
-      if (p.x16) prep_x_warp(p.x + (size_t)t * p.L, p.L, p.x16 + (size_t)t * p.L, p.xexp + t, lane);
-      token_valid_warp(p.idx + (size_t)t * k, k, E, p.L, p.b.nvalid + t, p.y + (size_t)t * p.L, lane);
+  }
+  for (int i = tid; i < P; i += blockDim.x) {
+    const uint32_t key = skey[i];
+    if (key != 0xffffffffu) {
+      const int a = (int)(key & 0xfffu);
+      p.b.perm[i] = a;
+      p.b.inv[a] = i;
     }
+  }
+  for (int t = warp; t < T; t += 32) {
+    if (p.x16) prep_x_warp(p.x + (size_t)t * p.L, p.L, p.x16 + (size_t)t * p.L, p.xexp + t, lane);
+    token_valid_warp(p.idx + (size_t)t * k, k, E, p.L, p.b.nvalid + t, p.y + (size_t)t * p.L, lane);
   }
 }
 
@@ -282,25 +333,31 @@ __global__ void __launch_bounds__(1024) k_bucket_scan(int E, BucketOut o) {
   publish_counts(e < E ? o.counts[e] : 0, E, o, &excl);
 }
 
-// Pass 3: stable scatter of one chunk, token by token (one warp per block).
-__global__ void __launch_bounds__(32) k_bucket_scatter(const int32_t* __restrict__ idx, int T,
-                                                       int k, int E, int nchunks, BucketOut o) {
+// Pass 3: stable scatter of one chunk, token by token by one warp (the block's other warps
+// help fill the cursors); the chunk's expert indices are loaded before the first token.
+__global__ void __launch_bounds__(256) k_bucket_scatter(const int32_t* __restrict__ idx, int T,
+                                                        int k, int E, int nchunks, BucketOut o) {
   pdl_wait();
   pdl_launch();
   __shared__ int cur[kMaxExperts];
-  const int c = blockIdx.x, lane = threadIdx.x;
-  for (int e = lane; e < E; e += 32) cur[e] = o.offsets[e] + o.chunk_base[(size_t)e * nchunks + c];
-  __syncwarp();
-  const int t1 = min(T, (c + 1) * kChunkTokens);
-  for (int t = c * kChunkTokens; t < t1; ++t) {
-    if (lane < k) {
-      const int a = t * k + lane;
-      const int e = idx[a];
-      if (e >= 0 && e < E) {
-        const int pos = atomicAdd(&cur[e], 1);
-        o.perm[pos] = a;
-        o.inv[a] = pos;
-      }
+  const int c = blockIdx.x, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    cur[e] = o.offsets[e] + o.chunk_base[(size_t)e * nchunks + c];
+  const int t0 = c * kChunkTokens;
+  int ev[kChunkTokens];
+#pragma unroll
+  for (int i = 0; i < kChunkTokens; ++i)
+    ev[i] = (threadIdx.x < 32 && lane < k && t0 + i < T) ? idx[(size_t)(t0 + i) * k + lane] : -1;
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+#pragma unroll
+  for (int i = 0; i < kChunkTokens; ++i) {
+    const int e = ev[i];
+    if (e >= 0 && e < E) {
+      const int a = (t0 + i) * k + lane;
+      const int pos = atomicAdd(&cur[e], 1);
+      o.perm[pos] = a;
+      o.inv[a] = pos;
     }
     __syncwarp();
   }
@@ -329,8 +386,10 @@ int bucket_chunks(int T) { return (T + kChunkTokens - 1) / kChunkTokens; }
 bool prep_is_fused(int T) { return T <= kSmallTokens; }
 
 cudaError_t launch_prep(const PrepArgs& p, cudaStream_t s, bool pdl) {
-  if (prep_is_fused(p.T)) return launch_kernel(k_prep_small, dim3(1), dim3(1024), 0, s, pdl, p);
-  // large batches: the top-k (if requested) runs as its own grid before this point
+  if (p.logits && !prep_is_fused(p.T)) return cudaErrorInvalidValue;
+  if ((size_t)p.T * p.k <= (size_t)kSortAssign)
+    return launch_kernel(k_prep_small, dim3(1), dim3(1024), 0, s, pdl, p);
+  // large batches: the top-k runs as its own grid before this point
   const int nch = bucket_chunks(p.T);
   cudaError_t err = launch_kernel(k_bucket_count, dim3(nch), dim3(256), 0, s, pdl, p, nch);
   if (err != cudaSuccess) return err;
@@ -338,7 +397,7 @@ cudaError_t launch_prep(const PrepArgs& p, cudaStream_t s, bool pdl) {
   if (err != cudaSuccess) return err;
   err = launch_kernel(k_bucket_scan, dim3(1), dim3(1024), 0, s, true, p.E, p.b);
   if (err != cudaSuccess) return err;
-  err = launch_kernel(k_bucket_scatter, dim3(nch), dim3(32), 0, s, true,
+  err = launch_kernel(k_bucket_scatter, dim3(nch), dim3(256), 0, s, true,
                       static_cast<const int32_t*>(p.idx), p.T, p.k, p.E, nch, p.b);
   if (err != cudaSuccess) return err;
   if (!p.x16) return cudaSuccess;

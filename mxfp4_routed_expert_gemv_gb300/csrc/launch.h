@@ -57,11 +57,23 @@ constexpr int kRouterSplitMaxTokens = 1024;
 inline bool router_tc_supported(int H) { return H >= 64 && H % 8 == 0; }
 int router_splits(int T, int E, int H);
 // logits[t][e] = sum over z of part[z][t][e] in z order, for e = i0, i0 + step, ... < E
+// (The loads of eight ranges are issued before their sums, which stay in range order: the
+// partials come from L2, and one dependent load per range would chain ks latencies.)
 __device__ __forceinline__ void sum_router_parts(const float* part, int ks, int T, int E, int t,
                                                  float* logits, int i0, int step) {
+  const size_t zs = (size_t)T * E;
   for (int e = i0; e < E; e += step) {
+    const float* pe = part + (size_t)t * E + e;
     float acc = 0.f;
-    for (int z = 0; z < ks; ++z) acc += part[((size_t)z * T + t) * E + e];
+    int z = 0;
+    for (; z + 8 <= ks; z += 8) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = __ldcg(pe + (size_t)(z + j) * zs);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc += v[j];
+    }
+    for (; z < ks; ++z) acc += __ldcg(pe + (size_t)z * zs);
     logits[(size_t)t * E + e] = acc;
   }
 }
@@ -119,6 +131,12 @@ struct BucketOut {
   int4* tiles_w;        // [P/kTcWideTok + E + 1] the same table for groups of kTcWideTok tokens
   int32_t* nbase_r;     // [E+1]  the same for groups of kTcRowTok tokens
   int4* tiles_r;        // [P/kTcRowTok + E + 1]
+  // Large-batch expert GEMMs (moe_wide.cu): when wdesc is set, the preparation also writes
+  // their tile descriptors, one per (token group, row block) of each GEMM: wrb0 / wrb1 row
+  // blocks, the second GEMM's at wdesc + wdesc1; groups of kTcRowTok (wmode 2) or
+  // kTcWideTok (wmode 1) tokens.
+  int4* wdesc;
+  int32_t wdesc1, wrb0, wrb1, wmode;
 };
 
 // Everything the per-call preparation touches.  logits == nullptr: idx/gate come from the
@@ -191,13 +209,15 @@ bool wide_path_supported(int L, int I);
 cudaError_t launch_split_x_wide(const uint16_t* x, int T, int L, int k, int E, const int32_t* idx,
                                 const BucketOut& b, uint8_t* xq, uint8_t* xsf, cudaStream_t s,
                                 bool pdl);
-// Tile descriptors of both expert GEMMs of a large batch (workspace int4 entries).
-size_t wide_desc_count(int L, int I, int E, int T, int k, bool rows);
+// Tile descriptors of both expert GEMMs (workspace int4 entries) for any call of up to T
+// tokens; wide_desc_setup points b at them for a call of T tokens (the preparation writes them).
+size_t wide_desc_count(int L, int I, int E, int T, int k);
+void wide_desc_setup(BucketOut& b, int4* desc, int L, int I, int E, int T, int k, bool rows);
 cudaError_t launch_wide_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k, bool rows,
                                 const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,
                                 uint8_t* act_q, uint8_t* act_sf, int act_kind, float b1, float b2,
-                                const float* gate, float* ybuf, int4* desc, int32_t* status,
-                                cudaStream_t s, void (*between)(cudaStream_t));
+                                const float* gate, float* ybuf, int32_t* status, cudaStream_t s,
+                                void (*between)(cudaStream_t));
 cudaError_t launch_tc_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k,
                               const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,
                               uint8_t* act_q, uint8_t* act_sf, int act_kind, float b1, float b2,

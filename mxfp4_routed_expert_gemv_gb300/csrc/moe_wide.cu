@@ -136,32 +136,6 @@ __device__ __forceinline__ WTile unpack_tile(int4 d) {
   return w;
 }
 
-// The descriptors of a launch's tiles, from the preparation's group table: tile t is the
-// active expert whose block holds t (bisection over the group prefix), its row block and its
-// token group (token groups fastest).  One thread per tile, so that the expert GEMM reads one
-// descriptor per tile instead of walking the prefix.
-__global__ void __launch_bounds__(256) k_wide_tiles(const int32_t* __restrict__ meta,
-                                                    const int32_t* __restrict__ nbase,
-                                                    const int4* __restrict__ groups, int RB,
-                                                    int4* __restrict__ desc) {
-  // (nbase[active experts] is the group count of the table)
-  pdl_wait();
-  pdl_launch();
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  const int nact = meta[0];
-  if (nact <= 0 || t >= nbase[nact] * RB) return;
-  int lo = 0, hi = nact - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (nbase[mid] * RB <= t) lo = mid; else hi = mid - 1;
-  }
-  const int gb = nbase[lo], n = nbase[lo + 1] - gb;
-  const int local = t - gb * RB;
-  const int rb = local / n;
-  const int4 g = groups[gb + (local - rb * n)];
-  desc[t] = make_int4(g.x, g.y, g.z, rb | (n << 8));
-}
-
 __device__ __forceinline__ int bar_or_w(uint32_t id, uint32_t n, int v) {
   uint32_t r;
   asm volatile(
@@ -274,9 +248,9 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  // the tile table comes from the preparation and the activation terms from the previous
-  // launch: everyone waits for the preceding kernel
-  pdl_wait();
+  // Only the producer's activation-term copies read the preceding launch's output (the tile
+  // table comes from the preparation, which had completed before that launch passed its own
+  // wait), and nothing this kernel writes is read by it: only the producer waits.
   pdl_launch();
   const uint32_t t0 = tbase;
   volatile int* abort_v = &abort_flag;
@@ -292,11 +266,15 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
       const uint64_t pol = tc::make_policy_evict_normal();
       int it = 0, ch = 0;  // stages and weight-scale chunks issued
       bool stop = false;
+      pdl_wait();
       int4 next = cta < ntiles ? __ldg(f.desc + cta) : make_int4(0, 0, 0, 0);
       for (int t = cta; t < ntiles && !stop; t += G) {
         const WTile wt = unpack_tile(next);
         if (t + G < ntiles) next = __ldg(f.desc + t + G);  // in flight during this tile
         const int wrow = wt.expert * f.R + wt.rb * (PH == 0 ? 128 : 256);
+        // rows: only the boxes of 8 positions (32 term rows) that hold the tile's tokens;
+        // the other A rows keep older bytes, which reach only D rows the epilogue skips
+        const int nbox = TR ? (wt.ntok + 7) / 8 : 1;
         for (int kc = 0; kc < KC; ++kc, ++it) {
           const int s = it % S;
           if (*abort_v ||
@@ -325,10 +303,9 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
             }
             ++ch;
           }
+          // one barrier for the whole stage: activation terms, their scales and the weights
+          // (separate barriers for the activation and the weight copies measured slower)
           uint8_t* st = sm + (size_t)s * kStageW;
-          // rows: only the boxes of 8 positions (32 term rows) that hold the tile's tokens;
-          // the other A rows keep older bytes, which reach only D rows the epilogue skips
-          const int nbox = TR ? (wt.ntok + 7) / 8 : 1;
           mbar_arrive_expect_tx(&full[s], (TR ? nbox * (M::kATile / 4) : M::kABytes) + M::kBBytes +
                                               M::kAsBytes);
           const int x = kc * (int)M::kRowB;
@@ -497,7 +474,7 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
         if (PH == 0) {
           // chunk c = 2 hf + cc: rows 32 c .. 32 c + 31 of w1 (g) and w3 (u); the term rows
           // added (lane t4 then holds rows 32 c + 8 t4 .. + 7), SwiGLU
-          float act[2][8];
+          float act[2][8], us[2][8];
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             const int c = 2 * hf + cc;
@@ -514,11 +491,20 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
             quad_reduce_scatter32(g, t4);
             quad_reduce_scatter32(u, t4);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) act[cc][i] = activation_fast(g[i], u[i], f.act_kind, f.b1, f.b2);
+            for (int i = 0; i < 8; ++i) {
+              act[cc][i] = g[i];
+              us[cc][i] = u[i];
+            }
           }
+          // the accumulator is read: the next tile's MMAs may start while this one finishes
           tc::fence_before_sync();
           named_bar(kEpiBarW, 32 * kEpiWarpsW);
-          if (et == 0) mbar_arrive(&accempty);  // the next tile's MMAs may start
+          if (et == 0) mbar_arrive(&accempty);
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              act[cc][i] = activation_fast(act[cc][i], us[cc][i], f.act_kind, f.b1, f.b2);
           // the quad splits each chunk's group of 32 act values (every lane takes part in the
           // shuffles; only positions of the tile store)
           const bool mine = mpos < wt.ntok;
@@ -549,7 +535,8 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
             gt = __ldg(f.gate + a);
           }
           float* yrow = f.ybuf + (size_t)a * f.L + (size_t)wt.rb * 256 + 128 * hf + 8 * t4;
-#pragma unroll 1
+          float o[4][8];
+#pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t vr[32];
             tc::tmem_ld_x32(tacc + 128 * hf + 32 * c, vr);
@@ -558,16 +545,22 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(vr[i]);
             quad_reduce_scatter32(v, t4);
-            if (mine) {
-              *reinterpret_cast<float4*>(yrow + 32 * c) =
-                  make_float4(gt * v[0], gt * v[1], gt * v[2], gt * v[3]);
-              *reinterpret_cast<float4*>(yrow + 32 * c + 4) =
-                  make_float4(gt * v[4], gt * v[5], gt * v[6], gt * v[7]);
-            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[c][i] = v[i];
           }
+          // the accumulator is read: the next tile's MMAs may start during the stores
           tc::fence_before_sync();
           named_bar(kEpiBarW, 32 * kEpiWarpsW);
           if (et == 0) mbar_arrive(&accempty);
+          if (mine) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              *reinterpret_cast<float4*>(yrow + 32 * c) =
+                  make_float4(gt * o[c][0], gt * o[c][1], gt * o[c][2], gt * o[c][3]);
+              *reinterpret_cast<float4*>(yrow + 32 * c + 4) =
+                  make_float4(gt * o[c][4], gt * o[c][5], gt * o[c][6], gt * o[c][7]);
+            }
+          }
         }
       } else if (PH == 0) {
         // g in columns 0..127, u in 128..255 (rows 128 rb .. 128 rb + 127 of w1 / w3); this
@@ -746,32 +739,41 @@ cudaError_t launch_split_x_wide(const uint16_t* x, int T, int L, int k, int E, c
                        idx, static_cast<const int32_t*>(b.inv), xq, xsf);
 }
 
-size_t wide_desc_count(int L, int I, int E, int T, int k, bool rows) {
+// Token groups of the table a call of T tokens reads (rows: kTcRowTok positions per group).
+static size_t wide_groups(int E, int T, int k, bool rows) {
   const int pos = rows ? kTcRowTok : kTcWideTok;
-  const size_t groups = ((size_t)T * k + pos - 1) / pos + E + 1;
-  return groups * (size_t)(I / 128) + groups * (size_t)(L / 256);
+  return ((size_t)T * k + pos - 1) / pos + E + 1;
+}
+
+size_t wide_desc_count(int L, int I, int E, int T, int k) {
+  // a workspace for T tokens serves every call of up to T tokens: the larger of the two tables
+  const int Tr = T < kWideMinTokens ? T : kWideMinTokens - 1;
+  size_t g = wide_groups(E, Tr, k, true);
+  const size_t gw = wide_groups(E, T, k, false);
+  g = g > gw ? g : gw;
+  return g * (size_t)(I / 128) + g * (size_t)(L / 256);
+}
+
+void wide_desc_setup(BucketOut& b, int4* desc, int L, int I, int E, int T, int k, bool rows) {
+  b.wdesc = desc;
+  b.wrb0 = I / 128;
+  b.wrb1 = L / 256;
+  b.wdesc1 = (int32_t)(wide_groups(E, T, k, rows) * (size_t)b.wrb0);
+  b.wmode = rows ? 2 : 1;
 }
 
 cudaError_t launch_wide_experts(const ExpertPtrs& w, int L, int I, int E, int T, int k, bool rows,
                                 const uint8_t* xq, const uint8_t* xsf, const BucketOut& b,
                                 uint8_t* act_q, uint8_t* act_sf, int act_kind, float b1, float b2,
-                                const float* gate, float* ybuf, int4* desc, int32_t* status,
-                                cudaStream_t s, void (*between)(cudaStream_t)) {
+                                const float* gate, float* ybuf, int32_t* status, cudaStream_t s,
+                                void (*between)(cudaStream_t)) {
   const uint64_t P = (uint64_t)T * k;
   const int pos_tile = rows ? kTcRowTok : kTcWideTok;
-  const size_t groups = (P + pos_tile - 1) / pos_tile + E + 1;
-  int4* desc0 = desc;
-  int4* desc1 = desc + groups * (size_t)(I / 128);
-  for (int ph = 0; ph < 2; ++ph) {
-    const int RB = ph == 0 ? I / 128 : L / 256;
-    const size_t n = groups * (size_t)RB;
-    cudaError_t e = launch_kernel(k_wide_tiles, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
-                                  true, static_cast<const int32_t*>(b.meta),
-                                  static_cast<const int32_t*>(rows ? b.nbase_r : b.nbase_w),
-                                  static_cast<const int4*>(rows ? b.tiles_r : b.tiles_w), RB,
-                                  ph == 0 ? desc0 : desc1);
-    if (e != cudaSuccess) return e;
-  }
+  // the preparation wrote the tile descriptors (wide_desc_setup)
+  if (!b.wdesc || b.wmode != (rows ? 2 : 1) || b.wrb0 != I / 128 || b.wrb1 != L / 256)
+    return cudaErrorInvalidValue;
+  int4* desc0 = b.wdesc;
+  int4* desc1 = b.wdesc + b.wdesc1;
   WMaps m0, m1;
   const auto sw64 = CU_TENSOR_MAP_SWIZZLE_64B, none = CU_TENSOR_MAP_SWIZZLE_NONE;
   // activation terms: boxes of 128 positions of one term (folded, 64-byte rows) or of 128

@@ -154,14 +154,24 @@ __global__ void __launch_bounds__(128, 1) k_router_tc(const __grid_constant__ CU
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  pdl_wait();
+  // Only h comes from the preceding launch (the router weights are constants of the layer, and
+  // nothing before reads what this kernel writes): the first stages' weight slices are
+  // requested before the wait, and only the thread that loads h waits.
   pdl_launch();
   const uint32_t tacc = tbase;
   if (warp == 0 && lane == 0) {
-    int i = 0;
+    const int pre = nk < kRtStages ? nk : kRtStages;
+    for (int i = 0; i < pre; ++i) {
+      mbar_arrive_expect_tx(&full[i], 2 * kRtTile);
+      tc::tma_load_2d(sm + (size_t)i * 2 * kRtTile, &mw, (k_lo + i) * 128, e0, &full[i]);
+    }
+    pdl_wait();
+    for (int i = 0; i < pre; ++i)
+      tc::tma_load_2d(sm + (size_t)i * 2 * kRtTile + kRtTile, &mh, (k_lo + i) * 128, t0, &full[i]);
+    int i = pre;
     for (; i < nk; ++i) {
       const int s = i % kRtStages;
-      if (i >= kRtStages && !mbar_wait(&empty[s], ((i / kRtStages) - 1) & 1, status)) {
+      if (!mbar_wait(&empty[s], ((i / kRtStages) - 1) & 1, status)) {
         bad = 1;
         break;
       }
