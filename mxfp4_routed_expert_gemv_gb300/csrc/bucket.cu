@@ -26,127 +26,142 @@ constexpr int kSmallTokens = 32;     // the one-CTA preparation also takes the t
 constexpr int kSortAssign = 4096;    // assignments (T k) the one-CTA preparation takes
 static_assert(kMaxExperts <= (1 << 20) && kSortAssign <= (1 << 12), "sort key fields");
 
-// Exclusive scan of one int per thread over a block of exactly 1024 threads; *total gets
-// the block sum.
-__device__ int block_exclusive_scan_1024(int v, int* total) {
-  __shared__ int warp_tot[32];
-  __shared__ int tot;
+// Exclusive scans of N ints per thread at once over a block of exactly 1024 threads (one
+// round of barriers for all N); tot[i] gets the block sum of component i.
+template <int N>
+__device__ void block_exclusive_scan_1024_n(const int (&v)[N], int (&excl)[N], int (&tot)[N]) {
+  __shared__ int warp_tot[32][N];
+  __shared__ int btot[N];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
+  int incl[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) incl[i] = v[i];
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += n;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const int n = __shfl_up_sync(0xffffffffu, incl[i], o);
+      if (lane >= o) incl[i] += n;
+    }
   }
-  if (lane == 31) warp_tot[warp] = incl;
+  if (lane == 31)
+#pragma unroll
+    for (int i = 0; i < N; ++i) warp_tot[warp][i] = incl[i];
   __syncthreads();
   if (warp == 0) {
-    const int w = warp_tot[lane];
-    int wi = w;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += n;
+    for (int i = 0; i < N; ++i) {
+      const int w = warp_tot[lane][i];
+      int wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += n;
+      }
+      warp_tot[lane][i] = wi - w;  // exclusive prefix of the warp totals
+      if (lane == 31) btot[i] = wi;
     }
-    warp_tot[lane] = wi - w;  // exclusive prefix of the warp totals
-    if (lane == 31) tot = wi;
   }
   __syncthreads();
-  const int excl = warp_tot[warp] + incl - v;
-  *total = tot;
-  __syncthreads();  // warp_tot and tot are reused by the next call
-  return excl;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    excl[i] = warp_tot[warp][i] + incl[i] - v[i];
+    tot[i] = btot[i];
+  }
+  __syncthreads();  // warp_tot and btot are reused by the next call
 }
 
-// Writes offsets/counts/active lists from per-expert counts c (thread e holds c).
-__device__ void publish_counts(int c, int E, const BucketOut& o, int* excl_out) {
-  int total;
-  const int excl = block_exclusive_scan_1024(c, &total);
+// Shared-memory copies of the active experts' segments, for the descriptors below.
+struct SegSmem {
+  int gbase[kMaxExperts + 1];  // groups of the descriptors' table before each active expert
+  int act[kMaxExperts];        // expert id
+  int soff[kMaxExperts];       // perm offset
+  int scnt[kMaxExperts];       // tokens
+};
+
+// Writes offsets/counts/active lists and the group tables from per-expert counts c (thread e
+// holds c; every thread also brings `dropped`, the invalid assignments it saw, whose sum is
+// counted in the status block), and the large-batch tile descriptors when o.wdesc is set.
+// Returns expert e's perm offset on thread e.
+__device__ int publish_counts(int c, int dropped, int E, const BucketOut& o, int32_t* status,
+                              SegSmem& sg) {
   const int e = threadIdx.x;
+  const int flag = (e < E && c > 0) ? 1 : 0;
+  // one scan for everything: tokens, active experts, groups of 16 / kTcWideTok / kTcRowTok
+  // tokens, invalid assignments
+  const int v[6] = {c, flag, flag ? (c + kTcTokTile - 1) / kTcTokTile : 0,
+                    flag ? (c + kTcWideTok - 1) / kTcWideTok : 0,
+                    flag ? (c + kTcRowTok - 1) / kTcRowTok : 0, dropped};
+  int ex[6], tot[6];
+  block_exclusive_scan_1024_n<6>(v, ex, tot);
+  const int excl = ex[0], total = tot[0], pos = ex[1], nact = tot[1];
   if (e < E) {
     o.offsets[e] = excl;
     o.counts[e] = c;
   }
-  if (e == 0) o.offsets[E] = total;
-  const int flag = (e < E && c > 0) ? 1 : 0;
-  int nact;
-  const int pos = block_exclusive_scan_1024(flag, &nact);
+  if (e == 0) {
+    o.offsets[E] = total;
+    o.meta[0] = nact;
+    o.meta[1] = total;
+    o.meta[2] = tot[2];
+    o.meta[3] = tot[3];
+    o.meta[4] = tot[4];
+    o.ntile_base[nact] = tot[2];
+    o.nbase_w[nact] = tot[3];
+    o.nbase_r[nact] = tot[4];
+    if (tot[5] > 0 && status) atomicAdd(status + kStatDropped, tot[5]);
+  }
+  const bool rows = o.wmode == 2;
   if (flag) {
     o.active[pos] = e;
     o.seg_off[pos] = excl;
     o.seg_cnt[pos] = c;
-  }
-  if (e == 0) {
-    o.meta[0] = nact;
-    o.meta[1] = total;
-  }
-  // tensor-core tiles: ceil(count / kTcTokTile) per active expert, prefix over active experts
-  int nt_tot;
-  const int nt_excl = block_exclusive_scan_1024(flag ? (c + kTcTokTile - 1) / kTcTokTile : 0, &nt_tot);
-  if (flag) {
-    o.ntile_base[pos] = nt_excl;
+    // tensor-core tiles and the large-batch group tables: per active expert its groups'
+    // expert, first position and tokens
+    o.ntile_base[pos] = ex[2];
     for (int n = 0; n * kTcTokTile < c; ++n)
-      o.tiles[nt_excl + n] = make_int4(e, excl + n * kTcTokTile, min(kTcTokTile, c - n * kTcTokTile), 0);
-  }
-  if (e == 0) {
-    o.ntile_base[nact] = nt_tot;
-    o.meta[2] = nt_tot;
-  }
-  // large-batch tiles: the same for groups of kTcWideTok tokens
-  int nw_tot;
-  const int nw_excl = block_exclusive_scan_1024(flag ? (c + kTcWideTok - 1) / kTcWideTok : 0, &nw_tot);
-  if (flag) {
-    o.nbase_w[pos] = nw_excl;
+      o.tiles[ex[2] + n] = make_int4(e, excl + n * kTcTokTile, min(kTcTokTile, c - n * kTcTokTile), 0);
+    o.nbase_w[pos] = ex[3];
     for (int n = 0; n * kTcWideTok < c; ++n)
-      o.tiles_w[nw_excl + n] = make_int4(e, excl + n * kTcWideTok, min(kTcWideTok, c - n * kTcWideTok), 0);
-  }
-  if (e == 0) {
-    o.nbase_w[nact] = nw_tot;
-    o.meta[3] = nw_tot;
-  }
-  // and for groups of kTcRowTok tokens
-  int nr_tot;
-  const int nr_excl = block_exclusive_scan_1024(flag ? (c + kTcRowTok - 1) / kTcRowTok : 0, &nr_tot);
-  if (flag) {
-    o.nbase_r[pos] = nr_excl;
+      o.tiles_w[ex[3] + n] = make_int4(e, excl + n * kTcWideTok, min(kTcWideTok, c - n * kTcWideTok), 0);
+    o.nbase_r[pos] = ex[4];
     for (int n = 0; n * kTcRowTok < c; ++n)
-      o.tiles_r[nr_excl + n] = make_int4(e, excl + n * kTcRowTok, min(kTcRowTok, c - n * kTcRowTok), 0);
+      o.tiles_r[ex[4] + n] = make_int4(e, excl + n * kTcRowTok, min(kTcRowTok, c - n * kTcRowTok), 0);
+    sg.gbase[pos] = rows ? ex[4] : ex[3];
+    sg.act[pos] = e;
+    sg.soff[pos] = excl;
+    sg.scnt[pos] = c;
   }
-  if (e == 0) {
-    o.nbase_r[nact] = nr_tot;
-    o.meta[4] = nr_tot;
-  }
+  if (e == 0) sg.gbase[nact] = rows ? tot[4] : tot[3];
   for (int i = e; i < kTcFlagWords; i += blockDim.x) o.flags[i] = 0;
-  *excl_out = excl;
-  if (!o.wdesc) return;
-  // The large-batch GEMMs' tile descriptors, from the group table of their tile size: for
-  // each GEMM, tile t is the active expert whose block of (groups x row blocks) holds t
-  // (bisection over the group prefix, kept in shared memory), its row block and its group
-  // (groups fastest): expert, first position, tokens, row block | the expert's groups << 8.
-  __shared__ int gbase[kMaxExperts + 1];
-  const bool rows = o.wmode == 2;
-  if (flag) gbase[pos] = rows ? nr_excl : nw_excl;
-  if (e == 0) gbase[nact] = rows ? nr_tot : nw_tot;
-  __syncthreads();  // gbase, and the group table this block wrote above
-  const int4* groups = rows ? o.tiles_r : o.tiles_w;
-  for (int ph = 0; ph < 2; ++ph) {
-    const int RB = ph == 0 ? o.wrb0 : o.wrb1;
-    int4* desc = o.wdesc + (ph == 0 ? 0 : o.wdesc1);
-    const int n = gbase[nact] * RB;
-    for (int t = threadIdx.x; t < n; t += blockDim.x) {
-      int lo = 0, hi = nact - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (gbase[mid] * RB <= t) lo = mid; else hi = mid - 1;
+  if (o.wdesc) {
+    // The large-batch GEMMs' tile descriptors: for each GEMM, tile t is the active expert
+    // whose block of (groups x row blocks) holds t (bisection over the group prefix), its row
+    // block and its group (groups fastest): expert, first position, tokens, row block | the
+    // expert's groups << 8.
+    __syncthreads();  // sg
+    const int tok = rows ? kTcRowTok : kTcWideTok;
+    for (int ph = 0; ph < 2; ++ph) {
+      const int RB = ph == 0 ? o.wrb0 : o.wrb1;
+      int4* desc = o.wdesc + (ph == 0 ? 0 : o.wdesc1);
+      const int n = sg.gbase[nact] * RB;
+      for (int t = threadIdx.x; t < n; t += blockDim.x) {
+        int lo = 0, hi = nact - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (sg.gbase[mid] * RB <= t) lo = mid; else hi = mid - 1;
+        }
+        const int gb = sg.gbase[lo], ng = sg.gbase[lo + 1] - gb;
+        const int local = t - gb * RB;
+        const int rb = local / ng;
+        const int g = local - rb * ng;
+        const int n0 = g * tok;
+        desc[t] = make_int4(sg.act[lo], sg.soff[lo] + n0, min(tok, sg.scnt[lo] - n0), rb | (ng << 8));
       }
-      const int gb = gbase[lo], ng = gbase[lo + 1] - gb;
-      const int local = t - gb * RB;
-      const int rb = local / ng;
-      const int4 g = groups[gb + (local - rb * ng)];
-      desc[t] = make_int4(g.x, g.y, g.z, rb | (ng << 8));
     }
   }
-  __syncthreads();  // gbase is reused by the next call
+  __syncthreads();  // sg is reused by the next call
+  return excl;
 }
 
 // One warp: x row (bf16) -> f16 scaled by 2^-e with the largest magnitude in [2^14, 2^15).
@@ -198,17 +213,23 @@ __device__ void token_valid_warp(const int32_t* idx_t, int k, int E, int L, int3
 }
 
 // Single block of 1024 threads, up to kSortAssign assignments: [top-k, T <= kSmallTokens],
-// count, scan, the stable scatter as a sort, per-token counts, x prep.  The scatter sorts the
-// keys (expert << 12 | assignment id) with a bitonic network in shared memory: sorted
-// position i is then perm position i (experts ascending, assignment ids ascending within an
-// expert, which is the token order), the order of the multi-block path's token-by-token
-// scatter.  Invalid assignments take the largest key and sort past the valid ones.
+// count, scan, the stable scatter, per-token counts, x prep.  The scatter ranks each
+// assignment among the earlier ones of its expert: up to kMaskTokens tokens, from a bit mask
+// per expert over the tokens (its rank is the number of lower tokens set, as no token names
+// an expert twice; a token that does takes the other way); otherwise a bitonic sort of the
+// keys (expert << 12 | assignment id) in shared memory, whose position i is perm position i.
+// Either gives the order of the multi-block path (experts ascending, tokens ascending).
+constexpr int kMaskTokens = 128;
+constexpr int kMaskWords = kMaskTokens / 32;
 __global__ void __launch_bounds__(1024) k_prep_small(PrepArgs p) {
   pdl_wait();
   pdl_launch();
   __shared__ int cnt[kMaxExperts];
-  __shared__ uint64_t keys[1024];
-  __shared__ uint32_t skey[kSortAssign];
+  // the one-token top-k's sort keys, then the token masks [E][kMaskWords] or the sort keys
+  __shared__ __align__(16) uint32_t sbuf[kSortAssign];
+  static_assert(kMaxExperts * kMaskWords <= kSortAssign && kSortAssign * 4 >= 1024 * 8, "sbuf");
+  __shared__ SegSmem sg;
+  uint64_t* keys = reinterpret_cast<uint64_t*>(sbuf);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = p.T, k = p.k, E = p.E;
   if (p.logits) {
@@ -219,53 +240,86 @@ __global__ void __launch_bounds__(1024) k_prep_small(PrepArgs p) {
                 p.idx + (size_t)warp * k, p.gate + (size_t)warp * k,
                 p.gap ? p.gap + warp : nullptr, lane);
   }
-  cnt[tid] = 0;
-  __syncthreads();  // top-k results (global, this block) are visible from here on
   const int P = T * k;
+  const bool masks = T <= kMaskTokens;
+  cnt[tid] = 0;
+  if (masks)
+    for (int i = tid; i < E * kMaskWords; i += blockDim.x) sbuf[i] = 0u;
+  __syncthreads();  // top-k results (global, this block) are visible from here on
   int NP = 32;  // sort width: a power of two >= P
   while (NP < P) NP <<= 1;
-  int dropped = 0;
-  for (int a = tid; a < NP; a += blockDim.x) {
+  int dropped = 0, dup = 0;
+  for (int a = tid; a < (masks ? P : NP); a += blockDim.x) {
     uint32_t key = 0xffffffffu;
     if (a < P) {
       const int e = p.idx[a];
       if (e >= 0 && e < E) {
         atomicAdd(&cnt[e], 1);
         key = ((uint32_t)e << 12) | (uint32_t)a;
+        if (masks) {
+          const int t = a / k;
+          const uint32_t bit = 1u << (t & 31);
+          dup |= (atomicOr(&sbuf[e * kMaskWords + (t >> 5)], bit) & bit) ? 1 : 0;
+        }
       } else if (e != kRemoteExpert) {
         ++dropped;
       }
     }
-    skey[a] = key;
+    if (!masks) sbuf[a] = key;
   }
-  __syncthreads();
+  const bool sort = __syncthreads_or(dup) != 0 || !masks;
   const int c = (tid < E) ? cnt[tid] : 0;
-  int excl;
-  publish_counts(c, E, p.b, &excl);
-  int dtot;
-  block_exclusive_scan_1024(dropped, &dtot);
-  if (tid == 0 && dtot > 0 && p.status) atomicAdd(p.status + kStatDropped, dtot);
-  for (int size = 2; size <= NP; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < NP; i += blockDim.x) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const uint32_t a = skey[i], b = skey[j];
-          if ((a > b) == ((i & size) == 0)) {
-            skey[i] = b;
-            skey[j] = a;
-          }
+  const int excl = publish_counts(c, dropped, E, p.b, p.status, sg);
+  if (!sort) {
+    // rank = tokens of this expert below t
+    if (tid < E) cnt[tid] = excl;
+    __syncthreads();
+    for (int a = tid; a < P; a += blockDim.x) {
+      const int e = p.idx[a];
+      if (e >= 0 && e < E) {
+        const int t = a / k;
+        const uint32_t* m = sbuf + e * kMaskWords;
+        int r = __popc(m[t >> 5] & ((1u << (t & 31)) - 1u));
+        for (int w = 0; w < (t >> 5); ++w) r += __popc(m[w]);
+        const int pos = cnt[e] + r;
+        p.b.perm[pos] = a;
+        p.b.inv[a] = pos;
+      }
+    }
+  } else {
+    if (masks) {  // the keys were not kept: a second pass
+      for (int a = tid; a < NP; a += blockDim.x) {
+        uint32_t key = 0xffffffffu;
+        if (a < P) {
+          const int e = p.idx[a];
+          if (e >= 0 && e < E) key = ((uint32_t)e << 12) | (uint32_t)a;
         }
+        sbuf[a] = key;
       }
       __syncthreads();
     }
-  }
-  for (int i = tid; i < P; i += blockDim.x) {
-    const uint32_t key = skey[i];
-    if (key != 0xffffffffu) {
-      const int a = (int)(key & 0xfffu);
-      p.b.perm[i] = a;
-      p.b.inv[a] = i;
+    for (int size = 2; size <= NP; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < NP; i += blockDim.x) {
+          const int j = i ^ stride;
+          if (j > i) {
+            const uint32_t a = sbuf[i], b = sbuf[j];
+            if ((a > b) == ((i & size) == 0)) {
+              sbuf[i] = b;
+              sbuf[j] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = tid; i < P; i += blockDim.x) {
+      const uint32_t key = sbuf[i];
+      if (key != 0xffffffffu) {
+        const int a = (int)(key & 0xfffu);
+        p.b.perm[i] = a;
+        p.b.inv[a] = i;
+      }
     }
   }
   for (int t = warp; t < T; t += 32) {
@@ -328,9 +382,9 @@ __global__ void __launch_bounds__(1024) k_bucket_chunkscan(int E, int nchunks, B
 __global__ void __launch_bounds__(1024) k_bucket_scan(int E, BucketOut o) {
   pdl_wait();
   pdl_launch();
+  __shared__ SegSmem sg;
   const int e = threadIdx.x;
-  int excl;
-  publish_counts(e < E ? o.counts[e] : 0, E, o, &excl);
+  publish_counts(e < E ? o.counts[e] : 0, 0, E, o, nullptr, sg);
 }
 
 // Pass 3: stable scatter of one chunk, token by token by one warp (the block's other warps

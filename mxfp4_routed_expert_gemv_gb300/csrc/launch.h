@@ -77,6 +77,37 @@ __device__ __forceinline__ void sum_router_parts(const float* part, int ks, int 
     logits[(size_t)t * E + e] = acc;
   }
 }
+// The same for one token with a whole block, EPT experts per thread (E <= EPT blockDim.x):
+// the loads of all the thread's experts for eight ranges are in flight together.
+template <int EPT>
+__device__ __forceinline__ void sum_router_parts_block(const float* part, int ks, int T, int E,
+                                                       int t, float* logits) {
+  const size_t zs = (size_t)T * E;
+  const float* pt = part + (size_t)t * E;
+  float acc[EPT];
+  bool on[EPT];
+#pragma unroll
+  for (int j = 0; j < EPT; ++j) {
+    acc[j] = 0.f;
+    on[j] = threadIdx.x + j * blockDim.x < (unsigned)E;
+  }
+  for (int z = 0; z < ks; z += 8) {
+    float v[EPT][8];
+#pragma unroll
+    for (int j = 0; j < EPT; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        v[j][i] = (on[j] && z + i < ks) ? __ldcg(pt + (size_t)(z + i) * zs + threadIdx.x + j * blockDim.x) : 0.f;
+#pragma unroll
+    for (int j = 0; j < EPT; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (z + i < ks) acc[j] += v[j][i];
+  }
+#pragma unroll
+  for (int j = 0; j < EPT; ++j)
+    if (on[j]) logits[(size_t)t * E + threadIdx.x + j * blockDim.x] = acc[j];
+}
 cudaError_t launch_topk(float* logits, const float* part, int ks, const float* bias, int T, int E,
                         int k, int renorm, float routed_scale, int32_t* idx, float* gate,
                         float* gap, cudaStream_t s, bool pdl);

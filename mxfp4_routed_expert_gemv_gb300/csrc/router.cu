@@ -210,8 +210,9 @@ __global__ void __launch_bounds__(128, 1) k_router_tc(const __grid_constant__ CU
   if (__syncthreads_or(!ok || bad) == 0) {
     const int e = e0 + 32 * warp + lane;
     const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    const int ncol = T - t0 < 128 ? T - t0 : 128;  // the tile's tokens
 #pragma unroll 1
-    for (int c0 = 0; c0 < 128; c0 += 16) {
+    for (int c0 = 0; c0 < ncol; c0 += 16) {
       uint32_t r[16];
       tc::tmem_ld_x16(tacc + lane_off + c0, r);
       tc::tmem_ld_wait();
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__(352) k_topk_block(float* __restrict__ logits,
   pdl_launch();
   const int t = blockIdx.x;
   if (ks > 1) {
-    sum_router_parts(part, ks, T, E, t, logits, threadIdx.x, blockDim.x);
+    sum_router_parts_block<3>(part, ks, T, E, t, logits);
     __syncthreads();
   }
   const OneTokenChoice c = topk_one_token<3>(logits + (size_t)t * E, bias, E, k, renorm,
@@ -285,7 +286,7 @@ int router_splits(int T, int E, int H) {
   if (T < kRouterTcMinTokens || !router_tc_supported(H) || T > kRouterSplitMaxTokens) return 1;
   const int ctas = ((E + 127) / 128) * ((T + 127) / 128);
   const int nk = (H + 63) / 64;
-  int ks = (sm_count() + ctas - 1) / ctas;  // about one CTA per SM
+  int ks = sm_count() / ctas;  // at most one CTA per SM (one wave: a CTA fills an SM's smem)
   ks = ks < nk / 2 ? ks : nk / 2;           // at least two K slices per range
   return ks > 1 ? ks : 1;
 }

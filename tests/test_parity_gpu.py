@@ -99,18 +99,21 @@ def test_large_batch_situ():
     _check_layer(w, dl, act=1, dense=True)
 
 
-def test_large_batch_experts_entry_drops_and_duplicates():
-    """The expert entry point at 288 tokens: out-of-range indices are skipped and counted,
-    repeated experts in a token's list count twice."""
+@pytest.mark.parametrize("T,seed", [(288, 66), (100, 67), (40, 68)])
+def test_large_batch_experts_entry_drops_and_duplicates(T, seed):
+    """The expert entry point at 288, 100 and 40 tokens (the one-CTA preparation's sort, and
+    its token-mask ranking falling back to the sort when a token repeats an expert):
+    out-of-range indices are skipped and counted, repeated experts in a token's list count
+    twice."""
     k3 = _k3()
-    w = synth.small_workload(T=288, E=10, k=4, latent=512, inter=512, hidden=128, seed=66)
+    w = synth.small_workload(T=T, E=10, k=4, latent=512, inter=512, hidden=128, seed=seed)
     ex = k3.Experts.from_dict(synth.experts_device(w, 0))
     li = synth.layer_inputs(w)
     rng = np.random.default_rng(3)
     idx = rng.integers(0, w.E, size=(w.T, w.k)).astype(np.int32)
     idx[5] = [-1, 4, 4, 9]
-    idx[77] = [10, 0, 0, 0]
-    idx[200, 2] = 1 << 20
+    idx[min(77, T - 2)] = [10, 0, 0, 0]
+    idx[min(200, T - 1), 2] = 1 << 20
     gate = rng.uniform(0.1, 1.0, size=idx.shape).astype(np.float32)
     cfg = gpu_cfg(w)
     ws = k3.workspace(cfg, w.T)
