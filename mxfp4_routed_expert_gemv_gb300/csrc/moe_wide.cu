@@ -266,8 +266,18 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
       const uint64_t pol = tc::make_policy_evict_normal();
       int it = 0, ch = 0;  // stages and weight-scale chunks issued
       bool stop = false;
-      pdl_wait();
       int4 next = cta < ntiles ? __ldg(f.desc + cta) : make_int4(0, 0, 0, 0);
+      if (cta < ntiles) {
+        // while the preceding launch finishes, the first stages' weights into L2 (they are
+        // constants, and the tile table was complete before that launch started)
+        const WTile w0 = unpack_tile(next);
+        const int wrow0 = w0.expert * f.R + w0.rb * (PH == 0 ? 128 : 256);
+        for (int kc = 0; kc < S && kc < KC; ++kc) {
+          tc::tma_prefetch_l2_2d(&mp.w0, kc * (int)M::kRowB, wrow0);
+          if (PH == 0) tc::tma_prefetch_l2_2d(&mp.w1, kc * (int)M::kRowB, wrow0);
+        }
+      }
+      pdl_wait();
       for (int t = cta; t < ntiles && !stop; t += G) {
         const WTile wt = unpack_tile(next);
         if (t + G < ntiles) next = __ldg(f.desc + t + G);  // in flight during this tile
