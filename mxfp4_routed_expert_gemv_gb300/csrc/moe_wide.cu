@@ -674,51 +674,42 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
 
 // x (bf16, one row per token) -> kTerms MXFP4 terms per (token, expert) position for the
 // large-batch path: codes in rows p * kTerms + t of xq [P * kTerms][L / 2] (as k_split_x),
-// scales stage-major (wide_sf_offset).  Grid (T, L / 512): the block's 16 warps split the
-// token's 16 groups of this 512-wide slice once, into shared memory; then for each valid slot
-// of the token the block writes the slice's codes (per term one 256-byte run) and its four
-// 16-byte scale rows, all as 16-byte stores.
-__global__ void __launch_bounds__(512) k_split_x_wide(const uint16_t* __restrict__ x, int L, int k,
-                                                      int E, int P, const int32_t* __restrict__ idx,
-                                                      const int32_t* __restrict__ inv,
-                                                      uint8_t* __restrict__ xq,
-                                                      uint8_t* __restrict__ xsf) {
-  __shared__ uint4 codes[kTerms][16];         // [term][group of the slice]
-  __shared__ __align__(16) uint32_t sfw[16];  // [group]: its terms' scale bytes
+// scales stage-major (wide_sf_offset).  One block per token, four threads per group of 32
+// (eight elements each, split together by mx_split_quad8 with the hardware E2M1 rounding):
+// each thread then writes its 4 code bytes of every term, and the group's first thread its
+// scale word, to each valid slot's position (a warp's stores of a term row are 128
+// contiguous bytes).
+__global__ void __launch_bounds__(1024) k_split_x_wide(const uint16_t* __restrict__ x, int L, int k,
+                                                       int E, int P, const int32_t* __restrict__ idx,
+                                                       const int32_t* __restrict__ inv,
+                                                       uint8_t* __restrict__ xq,
+                                                       uint8_t* __restrict__ xsf) {
+  __shared__ int spos[kMaxTopk];  // each slot's position, or -1
   pdl_wait();
   pdl_launch();
   const int t = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = blockIdx.y * 16 + warp;
-  const float v = __uint_as_float((uint32_t)x[(size_t)t * L + 32 * grp + lane] << 16);
-  uint32_t words[kTerms], sf[kTerms];
-  mx_split_group(v, words, sf);
-#pragma unroll
-  for (int tt = 0; tt < kTerms; ++tt) {
-    const uint32_t w0 = __shfl_sync(0xffffffffu, words[tt], 0);
-    const uint32_t w1 = __shfl_sync(0xffffffffu, words[tt], 8);
-    const uint32_t w2 = __shfl_sync(0xffffffffu, words[tt], 16);
-    const uint32_t w3 = __shfl_sync(0xffffffffu, words[tt], 24);
-    if (lane == tt) codes[tt][warp] = make_uint4(w0, w1, w2, w3);
-  }
-  if (lane == 0) sfw[warp] = sf[0] | (sf[1] << 8) | (sf[2] << 16) | (sf[3] << 24);
-  __syncthreads();
-  constexpr int kPerPos = kTerms * 16 + 4;  // 16-byte stores per position
-  for (int q = threadIdx.x; q < k * kPerPos; q += blockDim.x) {
-    const int j = q / kPerPos, r = q - j * kPerPos;
-    const int a = t * k + j;
+  if (threadIdx.x < k) {
+    const int a = t * k + threadIdx.x;
     const int e = idx[a];
-    if (e < 0 || e >= E) continue;
-    const size_t pos = (size_t)inv[a];
-    if (r < kTerms * 16) {
-      const int tt = r >> 4, g = r & 15;
-      *reinterpret_cast<uint4*>(xq + (pos * kTerms + tt) * (size_t)(L >> 1) +
-                                (size_t)(blockIdx.y * 16 + g) * 16) = codes[tt][g];
-    } else {
-      const int c = r - kTerms * 16;  // stage chunk of the slice
-      *reinterpret_cast<uint4*>(xsf + wide_sf_offset(blockIdx.y * 16 + 4 * c, (int)pos, P)) =
-          *reinterpret_cast<const uint4*>(&sfw[4 * c]);
-    }
+    spos[threadIdx.x] = (e >= 0 && e < E) ? inv[a] : -1;
+  }
+  const int grp = threadIdx.x >> 2, t4 = threadIdx.x & 3;  // blockDim.x == 4 (L / 32)
+  const uint4 raw =
+      __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * L + 32 * grp + 8 * t4));
+  float r[8] = {bf16lo(raw.x), bf16hi(raw.x), bf16lo(raw.y), bf16hi(raw.y),
+                bf16lo(raw.z), bf16hi(raw.z), bf16lo(raw.w), bf16hi(raw.w)};
+  uint32_t w[kTerms], sf[kTerms];
+  mx_split_quad8(r, w, sf);
+  const uint32_t sfword = sf[0] | (sf[1] << 8) | (sf[2] << 16) | (sf[3] << 24);
+  __syncthreads();  // spos
+  const size_t row = (size_t)(L >> 1);
+  for (int j = 0; j < k; ++j) {
+    const int pos = spos[j];
+    if (pos < 0) continue;
+    uint8_t* dst = xq + (size_t)pos * kTerms * row + grp * 16 + 4 * t4;
+#pragma unroll
+    for (int tt = 0; tt < kTerms; ++tt) *reinterpret_cast<uint32_t*>(dst + tt * row) = w[tt];
+    if (t4 == 0) *reinterpret_cast<uint32_t*>(xsf + wide_sf_offset(grp, pos, P)) = sfword;
   }
 }
 
@@ -745,7 +736,8 @@ bool wide_path_supported(int L, int I) { return L % 512 == 0 && I % 512 == 0; }
 cudaError_t launch_split_x_wide(const uint16_t* x, int T, int L, int k, int E, const int32_t* idx,
                                 const BucketOut& b, uint8_t* xq, uint8_t* xsf, cudaStream_t s,
                                 bool pdl) {
-  return launch_kernel(k_split_x_wide, dim3(T, L / 512), dim3(512), 0, s, pdl, x, L, k, E, T * k,
+  if (k > kMaxTopk || L / 8 > 1024) return cudaErrorInvalidValue;
+  return launch_kernel(k_split_x_wide, dim3(T), dim3(L / 8), 0, s, pdl, x, L, k, E, T * k,
                        idx, static_cast<const int32_t*>(b.inv), xq, xsf);
 }
 

@@ -15,7 +15,7 @@ namespace {
 
 constexpr int kQuarters = 4;      // warps per row, each a quarter of the hidden width
 constexpr int kRpcFew = 2;        // router rows per CTA for one or two tokens
-constexpr int kTopkBlockMaxTokens = 1024;  // block-per-token top-k up to this batch
+constexpr int kTopkBlockMaxTokens = 1 << 20;  // block-per-token top-k up to this batch
 constexpr int kVecPerLane = 8;    // 16-byte pieces a lane keeps in flight per batch
 
 // logits[t][e] = sum_i h[t][i] * wr[e][i].  A CTA holds 2 rows; each row is split into 4
