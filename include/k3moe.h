@@ -21,7 +21,8 @@
  *     `ws` of at least k3moe_workspace_size() bytes (device memory, 256-byte aligned).
  *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy default
  *     stream) and the call returns after enqueueing; results are ready when the stream
- *     reaches that point.  k3moe_layer_host is the exception: it synchronises the stream.
+ *     reaches that point.  k3moe_layer_host is the exception: it synchronises the stream
+ *     (k3moe_layer_host_async does so only when it cannot replay a recorded graph).
  *   - T == 0 is a no-op that returns K3MOE_OK once the configuration is valid (empty
  *     tensors may carry NULL pointers).
  *   - Host-side argument checks run first.  On any failure the call returns a non-zero
@@ -176,6 +177,19 @@ int k3moe_layer_host(const k3moe_cfg *cfg, const void *h_host, const void *wr,
                      const float *bias, const k3moe_experts *experts, const void *x_host,
                      int32_t T, float *y_host, int32_t *status, void *ws, size_t ws_bytes,
                      void *stream);
+
+/* k3moe_layer_host without the final synchronisation, for a serving loop that keeps two calls
+ * in flight (double-buffered host buffers): the call enqueues the layer on `stream` and
+ * returns; y_host holds the result once the stream reaches that point (synchronise the stream
+ * or an event recorded after the call).  The caller must not write h_host or x_host, nor read
+ * y_host, until then.  It returns without waiting only when it can replay a recorded graph
+ * (page-locked mapped buffers, a repeated argument set); otherwise (the first call with an
+ * argument set, pageable buffers, phase events set) it synchronises like k3moe_layer_host.
+ * Arguments and errors as k3moe_layer_host. */
+int k3moe_layer_host_async(const k3moe_cfg *cfg, const void *h_host, const void *wr,
+                           const float *bias, const k3moe_experts *experts, const void *x_host,
+                           int32_t T, float *y_host, int32_t *status, void *ws, size_t ws_bytes,
+                           void *stream);
 
 /* One MXFP4 mat-vec on the GPU (README Part II section 4, the k3_matmul_mxfp4 statement):
  *   y[r] = sum_c W[r][c] x[c],  W = packed [rows][in/2] + scales [rows][in/32]

@@ -27,6 +27,7 @@ __all__ = [
     "k3moe_layer_static_scratch", "STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
     "Latent", "k3moe_latent_workspace_size", "latent_workspace", "k3moe_latent_layer",
     "k3moe_set_flag_wait_polls", "k3moe_last_error", "k3moe_experts_mxfp4_range", "expert_block",
+    "k3moe_layer_host_async",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -35,6 +36,7 @@ EXPORTED_SYMBOLS = (
     "k3moe_launch_count", "k3moe_strerror", "k3moe_abi_version", "k3moe_set_phase_events",
     "k3moe_layer_static_scratch", "k3moe_latent_workspace_size", "k3moe_latent_layer",
     "k3moe_set_flag_wait_polls", "k3moe_last_error", "k3moe_experts_mxfp4_range",
+    "k3moe_layer_host_async",
 )
 
 # Capacity of the library's file-scope scratch array (K3MOE_STATIC_SCRATCH_BYTES).
@@ -167,6 +169,7 @@ def lib() -> ctypes.CDLL:
         L.k3moe_experts_mxfp4_range.argtypes = [pc, pe, i32, i32, vp, vp, vp, i32, vp, vp, vp, sz, vp]
         L.k3moe_layer.argtypes = [pc, vp, vp, vp, pe, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]
         L.k3moe_layer_host.argtypes = [pc, vp, vp, vp, pe, vp, i32, vp, vp, vp, sz, vp]
+        L.k3moe_layer_host_async.argtypes = [pc, vp, vp, vp, pe, vp, i32, vp, vp, vp, sz, vp]
         L.k3moe_layer_static_scratch.argtypes = [pc, vp, vp, vp, pe, vp, i32, vp, vp, vp, vp, vp, vp]
         L.k3moe_matvec_mxfp4.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
         pl = ctypes.POINTER(_CLatent)
@@ -390,9 +393,7 @@ def k3moe_layer_static_scratch(cfg: Cfg, h, wr, bias, experts: Experts, x, y, id
         _p(gap), _p(status), _stream(stream)))
 
 
-def k3moe_layer_host(cfg: Cfg, h_host, wr, bias, experts: Experts, x_host, y_host, status, ws,
-                     stream=None) -> None:
-    """The layer with host (ideally pinned) h, x and y; synchronises the stream."""
+def _layer_host(fn, cfg: Cfg, h_host, wr, bias, experts: Experts, x_host, y_host, status, ws, stream):
     import torch
     T = h_host.shape[0]
     _expect(h_host, "h_host", torch.bfloat16, (T, cfg.hidden), cuda=False)
@@ -400,9 +401,23 @@ def k3moe_layer_host(cfg: Cfg, h_host, wr, bias, experts: Experts, x_host, y_hos
     _expect(y_host, "y_host", torch.float32, (T, cfg.latent), cuda=False)
     _expect(wr, "wr", torch.bfloat16, (cfg.n_experts, cfg.hidden))
     c, e = cfg.c(), experts.c()
-    _check("k3moe_layer_host", lib().k3moe_layer_host(
+    _check(fn, getattr(lib(), fn)(
         ctypes.byref(c), _p(h_host), _p(wr), _p(bias), ctypes.byref(e), _p(x_host), T, _p(y_host),
         _p(status), _p(ws), ws.numel(), _stream(stream)))
+
+
+def k3moe_layer_host(cfg: Cfg, h_host, wr, bias, experts: Experts, x_host, y_host, status, ws,
+                     stream=None) -> None:
+    """The layer with host (ideally pinned) h, x and y; synchronises the stream."""
+    _layer_host("k3moe_layer_host", cfg, h_host, wr, bias, experts, x_host, y_host, status, ws, stream)
+
+
+def k3moe_layer_host_async(cfg: Cfg, h_host, wr, bias, experts: Experts, x_host, y_host, status,
+                           ws, stream=None) -> None:
+    """k3moe_layer_host that returns once the layer is enqueued (when it replays a recorded
+    graph); y_host is ready when the stream reaches this point."""
+    _layer_host("k3moe_layer_host_async", cfg, h_host, wr, bias, experts, x_host, y_host, status, ws,
+                stream)
 
 
 def k3moe_matvec_mxfp4(y, x, packed, scales, stream=None) -> None:

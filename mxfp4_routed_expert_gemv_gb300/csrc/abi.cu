@@ -233,7 +233,8 @@ void phase3(cudaStream_t s) { phase(3, s); }
 thread_local char g_last_error[256] = "";
 
 int cuda_fail(const char* what, cudaError_t e) {
-  std::snprintf(g_last_error, sizeof g_last_error, "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+  std::snprintf(g_last_error, sizeof g_last_error, "%.120s: %.120s (%d)", what, cudaGetErrorString(e),
+                (int)e);
   return K3MOE_ERR_CUDA;
 }
 
@@ -480,6 +481,79 @@ cudaGraphExec_t record_layer_host(const k3moe_cfg* cfg, const void* h_host, cons
   return exec;
 }
 
+// The host-buffer layer: replays a recorded graph when it can, with or without the final
+// synchronisation.
+int layer_host(const k3moe_cfg* cfg, const void* h_host, const void* wr, const float* bias,
+               const k3moe_experts* experts, const void* x_host, int32_t T, float* y_host,
+               int32_t* status, void* ws, size_t ws_bytes, void* stream, bool sync) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if ((rc = check_experts(experts))) return rc;
+  if (T < 0) return K3MOE_ERR_INVALID;
+  if (T > kMaxTokens) return K3MOE_ERR_UNSUPPORTED;
+  if (T == 0) return K3MOE_OK;
+  if (!h_host || !wr || !x_host || !y_host) return K3MOE_ERR_INVALID;
+  if (!aligned(wr, 16) || (bias && !aligned(bias, 4)) || (status && !aligned(status, 4)))
+    return K3MOE_ERR_ALIGN;
+  Workspace w;
+  if ((rc = check_ws(cfg, T, ws, ws_bytes, true, &w))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  K3_TRY(cudaGetDevice(&dev));
+  if (!g_phase_on) {  // (phase events are recorded per call: no graphs while they are on)
+    HostGraphKey key;
+    std::memset(&key, 0, sizeof key);
+    key.cfg = *cfg;
+    key.T = T;
+    key.h = h_host;
+    key.x = x_host;
+    key.wr = wr;
+    key.bias = bias;
+    key.y = y_host;
+    key.ex = *experts;
+    key.status = status;
+    key.ws = ws;
+    key.ws_bytes = ws_bytes;
+    key.stream = s;
+    key.polls = flag_wait_polls();
+    key.dev = dev;
+    std::unique_lock<std::mutex> lk(g_hg_mutex);
+    for (int i = 0; i < g_hg_n; ++i) {
+      if (g_hg[i].key == key) {
+        g_hg[i].used = ++g_hg_clock;
+        if (g_hg[i].exec) {
+          K3_TRY(cudaGraphLaunch(g_hg[i].exec, s));
+          lk.unlock();
+          if (sync) K3_TRY(cudaStreamSynchronize(s));
+          return K3MOE_OK;
+        }
+        lk.unlock();
+        goto plain;  // known not to capture
+      }
+    }
+    lk.unlock();
+    // first call with these arguments: run it directly, then record it for the next ones
+    if ((rc = enqueue_layer_host(cfg, h_host, wr, bias, experts, x_host, T, y_host, status, w, s)))
+      return rc;
+    K3_TRY(cudaStreamSynchronize(s));
+    cudaGraphExec_t exec =
+        record_layer_host(cfg, h_host, wr, bias, experts, x_host, T, y_host, status, w, dev);
+    lk.lock();
+    int slot = g_hg_n < kHostGraphs ? g_hg_n++ : 0;
+    if (slot == 0 && g_hg_n == kHostGraphs) {
+      for (int i = 1; i < kHostGraphs; ++i)
+        if (g_hg[i].used < g_hg[slot].used) slot = i;
+      if (g_hg[slot].exec) cudaGraphExecDestroy(g_hg[slot].exec);
+    }
+    g_hg[slot] = HostGraph{key, exec, ++g_hg_clock};
+    return K3MOE_OK;
+  }
+plain:
+  if ((rc = enqueue_layer_host(cfg, h_host, wr, bias, experts, x_host, T, y_host, status, w, s)))
+    return rc;
+  K3_TRY(cudaStreamSynchronize(s));
+  return K3MOE_OK;
+}
 }  // namespace
 }  // namespace k3
 
@@ -623,73 +697,16 @@ int k3moe_layer_static_scratch(const k3moe_cfg* cfg, const void* h, const void* 
 int k3moe_layer_host(const k3moe_cfg* cfg, const void* h_host, const void* wr, const float* bias,
                      const k3moe_experts* experts, const void* x_host, int32_t T, float* y_host,
                      int32_t* status, void* ws, size_t ws_bytes, void* stream) {
-  int rc = check_cfg(cfg);
-  if (rc) return rc;
-  if ((rc = check_experts(experts))) return rc;
-  if (T < 0) return K3MOE_ERR_INVALID;
-  if (T > kMaxTokens) return K3MOE_ERR_UNSUPPORTED;
-  if (T == 0) return K3MOE_OK;
-  if (!h_host || !wr || !x_host || !y_host) return K3MOE_ERR_INVALID;
-  if (!aligned(wr, 16) || (bias && !aligned(bias, 4)) || (status && !aligned(status, 4)))
-    return K3MOE_ERR_ALIGN;
-  Workspace w;
-  if ((rc = check_ws(cfg, T, ws, ws_bytes, true, &w))) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int dev = 0;
-  K3_TRY(cudaGetDevice(&dev));
-  if (!g_phase_on) {  // (phase events are recorded per call: no graphs while they are on)
-    HostGraphKey key;
-    std::memset(&key, 0, sizeof key);
-    key.cfg = *cfg;
-    key.T = T;
-    key.h = h_host;
-    key.x = x_host;
-    key.wr = wr;
-    key.bias = bias;
-    key.y = y_host;
-    key.ex = *experts;
-    key.status = status;
-    key.ws = ws;
-    key.ws_bytes = ws_bytes;
-    key.stream = s;
-    key.polls = flag_wait_polls();
-    key.dev = dev;
-    std::unique_lock<std::mutex> lk(g_hg_mutex);
-    for (int i = 0; i < g_hg_n; ++i) {
-      if (g_hg[i].key == key) {
-        g_hg[i].used = ++g_hg_clock;
-        if (g_hg[i].exec) {
-          K3_TRY(cudaGraphLaunch(g_hg[i].exec, s));
-          lk.unlock();
-          K3_TRY(cudaStreamSynchronize(s));
-          return K3MOE_OK;
-        }
-        lk.unlock();
-        goto plain;  // known not to capture
-      }
-    }
-    lk.unlock();
-    // first call with these arguments: run it directly, then record it for the next ones
-    if ((rc = enqueue_layer_host(cfg, h_host, wr, bias, experts, x_host, T, y_host, status, w, s)))
-      return rc;
-    K3_TRY(cudaStreamSynchronize(s));
-    cudaGraphExec_t exec =
-        record_layer_host(cfg, h_host, wr, bias, experts, x_host, T, y_host, status, w, dev);
-    lk.lock();
-    int slot = g_hg_n < kHostGraphs ? g_hg_n++ : 0;
-    if (slot == 0 && g_hg_n == kHostGraphs) {
-      for (int i = 1; i < kHostGraphs; ++i)
-        if (g_hg[i].used < g_hg[slot].used) slot = i;
-      if (g_hg[slot].exec) cudaGraphExecDestroy(g_hg[slot].exec);
-    }
-    g_hg[slot] = HostGraph{key, exec, ++g_hg_clock};
-    return K3MOE_OK;
-  }
-plain:
-  if ((rc = enqueue_layer_host(cfg, h_host, wr, bias, experts, x_host, T, y_host, status, w, s)))
-    return rc;
-  K3_TRY(cudaStreamSynchronize(s));
-  return K3MOE_OK;
+  return k3::layer_host(cfg, h_host, wr, bias, experts, x_host, T, y_host, status, ws, ws_bytes,
+                        stream, true);
+}
+
+int k3moe_layer_host_async(const k3moe_cfg* cfg, const void* h_host, const void* wr,
+                           const float* bias, const k3moe_experts* experts, const void* x_host,
+                           int32_t T, float* y_host, int32_t* status, void* ws, size_t ws_bytes,
+                           void* stream) {
+  return k3::layer_host(cfg, h_host, wr, bias, experts, x_host, T, y_host, status, ws, ws_bytes,
+                        stream, false);
 }
 
 int k3moe_latent_workspace_size(const k3moe_cfg* cfg, const k3moe_latent* lat, int32_t T,
