@@ -295,6 +295,83 @@ int k3moe_set_phase_events(void *const *events, int32_t n);
  * polls > 4,294,967,295. */
 int k3moe_set_flag_wait_polls(int64_t polls);
 
+/* ---- Experts beyond HBM: a device cache over an expert store in host memory ------------
+ *
+ * README Part II section 12 "An LRU cache for the experts": the experts live in a large,
+ * slower tier and a fixed number of slots in fast memory hold the recently used ones.  Here
+ * the tier is page-locked host memory (on a Grace-Blackwell node the Grace memory, reached
+ * over NVLink-C2C) and the slots are device memory laid out as a k3moe_experts of n_slots
+ * experts, so that the expert kernels run on the slots unchanged.  A slot holds an expert,
+ * is empty, or is in flight (reserved for an expert whose copy has been issued but not yet
+ * published).  For one call the cache
+ *   1. reserves: experts already resident are marked used; for each missing expert, in
+ *      ascending expert order, an empty slot if there is one, else the least recently used
+ *      slot that this call does not use and that is not in flight (its expert is evicted);
+ *   2. reads: copies each reserved expert host -> device, in ascending expert order (the
+ *      store's offset order);
+ *   3. publishes: a slot whose copy was issued holds its expert from then on (stream order
+ *      makes the data visible to the kernels that follow); a slot whose copy could not be
+ *      issued goes back to empty.
+ * One cache serves one layer's experts; calls on a cache must not overlap (the state is
+ * host memory without locks).  The caller owns every array. */
+#define K3MOE_SLOT_EMPTY (-1)
+#define K3MOE_SLOT_INFLIGHT (-2)
+typedef struct k3moe_expert_cache {
+    int32_t n_experts;      /* E: experts in the host store                                 */
+    int32_t n_slots;        /* C: device slots, 1 <= C <= E                                 */
+    k3moe_experts host;     /* the E experts, page-locked host memory, checkpoint layout    */
+    k3moe_experts slots;    /* room for C experts in device memory, the same layout: slot s
+                               is expert s of these arrays                                  */
+    int32_t *expert_of;     /* host [C]: expert in slot s, K3MOE_SLOT_EMPTY or _INFLIGHT    */
+    int32_t *slot_of;       /* host [E]: slot holding expert e, or -1                       */
+    uint64_t *used_at;      /* host [C]: the clock at the slot's last use                   */
+    uint64_t clock;         /* advanced once per planned call                               */
+} k3moe_expert_cache;
+
+/* Empties every slot and resets the clock (host only, no CUDA call). */
+int k3moe_cache_reset(k3moe_expert_cache *cache);
+
+/* Step 1 for n expert indices (host memory, any order, repeats allowed): marks the resident
+ * ones used, reserves slots for the missing ones (their slots become K3MOE_SLOT_INFLIGHT),
+ * and writes slot_idx[i] = the slot of idx[i] (-1 for an index outside [0, E)) and the
+ * copies to make, fetch_expert[j] -> fetch_slot[j] for j < *n_fetch, in ascending expert
+ * order (both arrays: room for n_slots entries).  Host only, no CUDA call.  Returns
+ * K3MOE_ERR_UNSUPPORTED, with the state unchanged, if the indices name more distinct
+ * experts than there are slots. */
+int k3moe_cache_plan(k3moe_expert_cache *cache, const int32_t *idx, int32_t n, int32_t *slot_idx,
+                     int32_t *fetch_expert, int32_t *fetch_slot, int32_t *n_fetch);
+
+/* Step 3: the first n_ok of the planned copies were issued (their slots now hold their
+ * experts); the rest were not (their slots become empty). */
+int k3moe_cache_publish(k3moe_expert_cache *cache, const int32_t *fetch_expert,
+                        const int32_t *fetch_slot, int32_t n_fetch, int32_t n_ok);
+
+/* Device workspace and host scratch of k3moe_layer_cached for T tokens. */
+int k3moe_cache_workspace_size(const k3moe_cfg *cfg, int32_t T, size_t *bytes);
+int k3moe_cache_host_scratch_size(const k3moe_cfg *cfg, int32_t T, int32_t n_slots, size_t *bytes);
+
+/* The layer with its experts in the cache: routes the T tokens on the device (as
+ * k3moe_route), reads the routing back to the host, plans, copies the missing experts from
+ * the host store into their slots (one cudaMemcpyAsync per tensor), publishes, and runs the
+ * routed-expert sum on the slots (as k3moe_experts_mxfp4 with the routing mapped to slots);
+ * synchronises the stream before returning.  y equals k3moe_layer's for the same inputs
+ * bit for bit when the batch takes the large-batch expert kernels (T >= 3 with latent and
+ * inter multiples of 512: each assignment's result there does not depend on which others
+ * share its tile); otherwise the two agree within rounding (the split of a tile's reduction
+ * across CTAs follows the expert numbering, which the slots change).  Needs topk <= n_slots.
+ *   cache: cache->n_experts == cfg->n_experts; the store and the slots as described above
+ *   h, wr, bias, x, y, status: as in k3moe_layer (device memory)
+ *   ws: device, at least k3moe_cache_workspace_size bytes; host_scratch: host memory (page-
+ *       locked for the read-back to be asynchronous), at least k3moe_cache_host_scratch_size
+ *   n_fetched: optional (out), the experts copied by this call
+ * Returns K3MOE_ERR_UNSUPPORTED if the call's routing names more distinct experts than there
+ * are slots (nothing is computed; y is left as it was), K3MOE_ERR_CUDA if a copy or launch
+ * fails (slots whose copies were not issued are left empty). */
+int k3moe_layer_cached(const k3moe_cfg *cfg, k3moe_expert_cache *cache, const void *h,
+                       const void *wr, const float *bias, const void *x, int32_t T, float *y,
+                       int32_t *status, void *ws, size_t ws_bytes, void *host_scratch,
+                       size_t host_scratch_bytes, int32_t *n_fetched, void *stream);
+
 /* Number of kernels the library launched through the entry points above since load
  * (host counter; for launch accounting in benchmarks). */
 int64_t k3moe_launch_count(void);

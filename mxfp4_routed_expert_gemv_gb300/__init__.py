@@ -27,7 +27,9 @@ __all__ = [
     "k3moe_layer_static_scratch", "STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
     "Latent", "k3moe_latent_workspace_size", "latent_workspace", "k3moe_latent_layer",
     "k3moe_set_flag_wait_polls", "k3moe_last_error", "k3moe_experts_mxfp4_range", "expert_block",
-    "k3moe_layer_host_async",
+    "k3moe_layer_host_async", "ExpertCache", "k3moe_layer_cached", "SLOT_EMPTY", "SLOT_INFLIGHT",
+    "k3moe_cache_reset", "k3moe_cache_plan", "k3moe_cache_publish", "k3moe_cache_workspace_size",
+    "k3moe_cache_host_scratch_size",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -36,7 +38,8 @@ EXPORTED_SYMBOLS = (
     "k3moe_launch_count", "k3moe_strerror", "k3moe_abi_version", "k3moe_set_phase_events",
     "k3moe_layer_static_scratch", "k3moe_latent_workspace_size", "k3moe_latent_layer",
     "k3moe_set_flag_wait_polls", "k3moe_last_error", "k3moe_experts_mxfp4_range",
-    "k3moe_layer_host_async",
+    "k3moe_layer_host_async", "k3moe_cache_reset", "k3moe_cache_plan", "k3moe_cache_publish",
+    "k3moe_cache_workspace_size", "k3moe_cache_host_scratch_size", "k3moe_layer_cached",
 )
 
 # Capacity of the library's file-scope scratch array (K3MOE_STATIC_SCRATCH_BYTES).
@@ -64,6 +67,15 @@ class _CCfg(ctypes.Structure):
 class _CExperts(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("w1_packed", "w1_scale", "w3_packed", "w3_scale", "w2_packed", "w2_scale")]
+
+
+class _CExpertCache(ctypes.Structure):
+    _fields_ = [("n_experts", ctypes.c_int32), ("n_slots", ctypes.c_int32), ("host", _CExperts),
+                ("slots", _CExperts), ("expert_of", ctypes.c_void_p), ("slot_of", ctypes.c_void_p),
+                ("used_at", ctypes.c_void_p), ("clock", ctypes.c_uint64)]
+
+
+SLOT_EMPTY, SLOT_INFLIGHT = -1, -2
 
 
 @dataclasses.dataclass(frozen=True)
@@ -184,6 +196,14 @@ def lib() -> ctypes.CDLL:
         L.k3moe_launch_count.argtypes = []
         L.k3moe_last_error.restype = ctypes.c_char_p
         L.k3moe_last_error.argtypes = []
+        pcc = ctypes.POINTER(_CExpertCache)
+        L.k3moe_cache_reset.argtypes = [pcc]
+        L.k3moe_cache_plan.argtypes = [pcc, vp, i32, vp, vp, vp, ctypes.POINTER(i32)]
+        L.k3moe_cache_publish.argtypes = [pcc, vp, vp, i32, i32]
+        L.k3moe_cache_workspace_size.argtypes = [pc, i32, ctypes.POINTER(sz)]
+        L.k3moe_cache_host_scratch_size.argtypes = [pc, i32, i32, ctypes.POINTER(sz)]
+        L.k3moe_layer_cached.argtypes = [pc, pcc, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp, sz,
+                                         ctypes.POINTER(i32), vp]
         L.k3moe_strerror.restype = ctypes.c_char_p
         L.k3moe_strerror.argtypes = [ctypes.c_int]
         L.k3moe_abi_version.restype = i32
@@ -283,6 +303,118 @@ def workspace(cfg: Cfg, T: int, device="cuda"):
     """A device workspace (uint8 tensor) for T tokens."""
     import torch
     return torch.empty(k3moe_workspace_size(cfg, T), dtype=torch.uint8, device=device)
+
+
+class ExpertCache:
+    """A device cache of `n_slots` experts over a store of all E experts in host memory
+    (k3moe_expert_cache): the state arrays live here (numpy), the store and the slots are
+    Experts (host: page-locked CPU tensors [E, ...]; slots: device tensors [n_slots, ...]).
+    Without store and slots only the host planning (plan, publish) can be used."""
+
+    def __init__(self, n_experts: int, n_slots: int, host: Optional[Experts] = None,
+                 slots: Optional[Experts] = None):
+        import numpy as np
+        self.n_experts, self.n_slots = int(n_experts), int(n_slots)
+        self.host, self.slots = host, slots
+        self.expert_of = np.full(self.n_slots, SLOT_EMPTY, np.int32)
+        self.slot_of = np.full(self.n_experts, -1, np.int32)
+        self.used_at = np.zeros(self.n_slots, np.uint64)
+        self._c = _CExpertCache(self.n_experts, self.n_slots,
+                                host.c() if host is not None else _CExperts(),
+                                slots.c() if slots is not None else _CExperts(),
+                                self.expert_of.ctypes.data, self.slot_of.ctypes.data,
+                                self.used_at.ctypes.data, 0)
+        self.reset()
+
+    @classmethod
+    def with_slots(cls, host: Experts, n_slots: int, device="cuda") -> "ExpertCache":
+        """Device slots shaped like the store's experts, n_slots of them."""
+        import torch
+        slots = Experts(*(torch.empty((n_slots, *t.shape[1:]), dtype=t.dtype, device=device)
+                          for t in (host.w1p, host.w1s, host.w3p, host.w3s, host.w2p, host.w2s)))
+        return cls(host.w1p.shape[0], n_slots, host, slots)
+
+    @property
+    def clock(self) -> int:
+        return int(self._c.clock)
+
+    def reset(self) -> None:
+        k3moe_cache_reset(self)
+
+    def plan(self, idx):
+        return k3moe_cache_plan(self, idx)
+
+    def publish(self, fetch_expert, fetch_slot, n_ok: Optional[int] = None) -> None:
+        k3moe_cache_publish(self, fetch_expert, fetch_slot, n_ok)
+
+    def workspace(self, cfg: Cfg, T: int, device="cuda"):
+        import torch
+        return torch.empty(k3moe_cache_workspace_size(cfg, T), dtype=torch.uint8, device=device)
+
+    def host_scratch(self, cfg: Cfg, T: int):
+        import torch
+        n = k3moe_cache_host_scratch_size(cfg, T, self.n_slots)
+        return torch.empty((n + 3) // 4, dtype=torch.int32).pin_memory()
+
+
+def k3moe_cache_reset(cache: ExpertCache) -> None:
+    _check("k3moe_cache_reset", lib().k3moe_cache_reset(ctypes.byref(cache._c)))
+
+
+def k3moe_cache_plan(cache: ExpertCache, idx):
+    """Host planning of one call (int32 indices): (slot_idx, fetch_expert, fetch_slot); the
+    fetched slots stay in flight until k3moe_cache_publish."""
+    import numpy as np
+    idx = np.ascontiguousarray(idx, dtype=np.int32).reshape(-1)
+    slot_idx = np.empty_like(idx)
+    fe = np.empty(cache.n_slots, np.int32)
+    fs = np.empty(cache.n_slots, np.int32)
+    nf = ctypes.c_int32(0)
+    _check("k3moe_cache_plan", lib().k3moe_cache_plan(
+        ctypes.byref(cache._c), idx.ctypes.data, idx.size, slot_idx.ctypes.data, fe.ctypes.data,
+        fs.ctypes.data, ctypes.byref(nf)))
+    return slot_idx, fe[:nf.value].copy(), fs[:nf.value].copy()
+
+
+def k3moe_cache_publish(cache: ExpertCache, fetch_expert, fetch_slot, n_ok: Optional[int] = None) -> None:
+    import numpy as np
+    fe = np.ascontiguousarray(fetch_expert, dtype=np.int32)
+    fs = np.ascontiguousarray(fetch_slot, dtype=np.int32)
+    n_ok = fe.size if n_ok is None else n_ok
+    _check("k3moe_cache_publish", lib().k3moe_cache_publish(
+        ctypes.byref(cache._c), fe.ctypes.data, fs.ctypes.data, fe.size, int(n_ok)))
+
+
+def k3moe_cache_workspace_size(cfg: Cfg, T: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("k3moe_cache_workspace_size",
+           lib().k3moe_cache_workspace_size(ctypes.byref(cfg.c()), T, ctypes.byref(n)))
+    return n.value
+
+
+def k3moe_cache_host_scratch_size(cfg: Cfg, T: int, n_slots: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("k3moe_cache_host_scratch_size", lib().k3moe_cache_host_scratch_size(
+        ctypes.byref(cfg.c()), T, n_slots, ctypes.byref(n)))
+    return n.value
+
+
+def k3moe_layer_cached(cfg: Cfg, cache: ExpertCache, h, wr, bias, x, y, status, ws, host_scratch,
+                       stream=None) -> int:
+    """The layer with its experts in the cache (synchronises); returns the experts copied."""
+    import torch
+    T = h.shape[0]
+    _expect(h, "h", torch.bfloat16, (T, cfg.hidden))
+    _expect(wr, "wr", torch.bfloat16, (cfg.n_experts, cfg.hidden))
+    _expect(x, "x", torch.bfloat16, (T, cfg.latent))
+    _expect(y, "y", torch.float32, (T, cfg.latent))
+    n = ctypes.c_int32(0)
+    c = cfg.c()
+    _check("k3moe_layer_cached", lib().k3moe_layer_cached(
+        ctypes.byref(c), ctypes.byref(cache._c), _p(h), _p(wr), _p(bias), _p(x), T, _p(y), _p(status),
+        _p(ws), ws.numel(), _p(host_scratch), host_scratch.numel() * 4, ctypes.byref(n),
+        _stream(stream)))
+    return n.value
 
 
 def workspace_host(cfg: Cfg, T: int, device="cuda"):
