@@ -192,7 +192,25 @@ class OracleRunner:
                 "w1/8": (w.inter // 8) * w.latent}[kind]
 
 
-def cpu_baseline(w: synth.Workload, min_seconds: float = 10.0, max_tokens: int = 200):
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def cpu_baseline(w: synth.Workload, min_seconds: float = 10.0, max_tokens: int = 200, one_thread: bool = True):
     import oracle
     run = OracleRunner(w)
     run.token()  # warm caches
@@ -203,9 +221,21 @@ def cpu_baseline(w: synth.Workload, min_seconds: float = 10.0, max_tokens: int =
         if time.perf_counter() - t0 >= min_seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": n / dt, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"the batch-1 decode token's full layer (router over 896 experts + 16 expert FFNs, fp64), "
-                      f"repeated {n} times ({dt:.1f} s); expert bytes generated outside the timed region"}
+    rec = {"value": n / dt, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+           "cpu_model": cpu_model(),
+           "sample": f"the batch-1 decode token's full layer (router over 896 experts + 16 expert FFNs, fp64), "
+                     f"repeated {n} times ({dt:.1f} s); expert bytes generated outside the timed region"}
+    if one_thread:
+        # the same sample on one thread (a child process: the thread count is fixed at start)
+        env = dict(os.environ, OMP_NUM_THREADS="1")
+        try:
+            out = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-only",
+                                  "--workload", "1"], capture_output=True, text=True, env=env,
+                                 timeout=120).stdout
+            rec["one_thread"] = json.loads(out.strip().splitlines()[-1])
+        except (OSError, subprocess.SubprocessError, ValueError, IndexError) as e:
+            rec["one_thread"] = {"unavailable": str(e)[:200]}
+    return rec
 
 
 def run_reference(args):
@@ -273,9 +303,15 @@ def load_peaks():
 
 
 def gemm_kernel_name(T: int) -> str:
-    n = 16 if T * TERMS <= 16 else 64
-    return (f"k_moe_tc<{n},0> (w1+w3 block-scaled tcgen05 GEMM fed by TMA, SwiGLU + "
-            "MXFP4-term epilogue)")
+    """The first expert GEMM the layer launches for T tokens (Kimi-K3 widths)."""
+    if T <= 2:
+        return ("k_moe_tc<16,0,..> (w1+w3 block-scaled tcgen05 GEMM fed by TMA, SwiGLU + "
+                "MXFP4-term epilogue)")
+    if T < 256:
+        return ("k_moe_wide<0,rows> (w1+w3 block-scaled tcgen05 GEMM, 32 positions x 4 terms as the "
+                "MMA rows, 256 weight rows per tile, SwiGLU + MXFP4-term epilogue)")
+    return ("k_moe_wide<0,folded> (w1+w3 block-scaled tcgen05 GEMM, 128 positions per tile with "
+            "the 4 terms folded into the reduction, SwiGLU + MXFP4-term epilogue)")
 
 
 class GraphTimer:
@@ -428,6 +464,60 @@ def measure_layer_workload(torch, k3, w, dev, local, peaks, steps, warmup, NL, r
                          "note": "issued work is 4x the useful work: each activation enters the "
                                  "block-scaled MMA as 4 MXFP4 terms"}
     del experts_l, ws
+    return rec
+
+
+def measure_expert_tier(torch, k3, w, dev, peaks, calls, n_slots, rotation=64):
+    """Sub-record of the expert tier beyond HBM: one layer's experts in page-locked host
+    memory, n_slots of them cached in device slots (k3moe_layer_cached), decode calls cycling
+    through `rotation` token batches of the workload's routing.  Each call routes, reads the
+    routing back, copies its missing experts host -> device and runs the experts on the slots
+    (synchronised per call); timed on the host over `calls` calls after a warm-up pass over
+    the rotation."""
+    import time
+    cfg, experts_l, H, X, wr_l, bias_l = layer_setup(torch, k3, w, dev, 1, rotation)
+    host = k3.Experts(*(t.cpu().pin_memory() for t in (experts_l[0].w1p, experts_l[0].w1s, experts_l[0].w3p,
+                                                      experts_l[0].w3s, experts_l[0].w2p, experts_l[0].w2s)))
+    del experts_l
+    torch.cuda.empty_cache()
+    cache = k3.ExpertCache.with_slots(host, n_slots, dev)
+    T = w.T
+    ws = cache.workspace(cfg, T, dev)
+    scratch = cache.host_scratch(cfg, T)
+    y = torch.empty((T, w.latent), dtype=torch.float32, device=dev)
+    status = torch.zeros(4, dtype=torch.int32, device=dev)
+    idx = torch.empty((T, w.k), dtype=torch.int32, device=dev)
+    gate = torch.empty((T, w.k), dtype=torch.float32, device=dev)
+    ws_r = k3.workspace(cfg, T, dev)
+    distinct = []
+    for r in range(rotation):
+        k3.k3moe_route(cfg, H[r], wr_l[0], bias_l[0], idx, gate, None, ws_r)
+        distinct.append(len(set(idx.cpu().reshape(-1).tolist())))
+    for r in range(rotation):  # warm-up: the cache reaches its steady contents
+        k3.k3moe_layer_cached(cfg, cache, H[r], wr_l[0], bias_l[0], X[r], y, status, ws, scratch)
+    torch.cuda.synchronize(dev)
+    fetched = 0
+    needed = 0
+    t0 = time.perf_counter()
+    for i in range(calls):
+        r = i % rotation
+        fetched += k3.k3moe_layer_cached(cfg, cache, H[r], wr_l[0], bias_l[0], X[r], y, status, ws, scratch)
+        needed += distinct[r]
+    dt = time.perf_counter() - t0
+    st = status.cpu().numpy()
+    if st[0] or st[1]:
+        raise SystemExit(f"expert tier: device status reports dropped={st[0]} timeouts={st[1]}")
+    per_expert = w.inter * w.latent * 3 * (1 / 2 + 1 / 32)
+    rec = {
+        "workload": f"{w.name}, experts in host memory, {n_slots} of {w.E} cached in device slots",
+        "tokens_per_step": T, "calls": calls, "tokens_per_s": T * calls / dt,
+        "us_per_call": dt / calls * 1e6, "slots": n_slots, "hit_rate": 1.0 - fetched / max(1, needed),
+        "experts_copied_per_call": fetched / calls,
+        "h2d_GBps": fetched * per_expert / dt / 1e9,
+        "api": "k3moe_layer_cached (route, read the routing back, copy the misses, experts on the slots; "
+               "synchronised per call)",
+    }
+    del cache, host, ws, ws_r
     return rec
 
 
@@ -675,6 +765,11 @@ def run_ours(args):
             subs[{2: "batched_decode", 3: "prefill", 4: "stack_8_layers"}[wi]] = rec
             gc.collect()
             torch.cuda.empty_cache()
+        for slots in (128, 32):
+            subs[f"expert_tier_{slots}_slots"] = measure_expert_tier(torch, k3, w, dev, peaks, calls=256,
+                                                                     n_slots=slots)
+            gc.collect()
+            torch.cuda.empty_cache()
         line["config"]["workloads"] = subs
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline and w.T == 1:
@@ -908,6 +1003,7 @@ def main():
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count (small-memory profiling variant, not a bench line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-only", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--no-sub", action="store_true",
                     help="skip the sub-records of the other workloads (batched decode, prefill, stack)")
     ap.add_argument("--sub-seconds", type=float, default=1.0,
@@ -920,6 +1016,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
+    if args.cpu_baseline_only:  # (the one-thread child of cpu_baseline)
+        print(json.dumps(cpu_baseline(synth.WORKLOADS[1], min_seconds=8.0, max_tokens=20, one_thread=False)))
+        return
     if args.impl == "reference":
         run_reference(args)
     elif args.latent:
