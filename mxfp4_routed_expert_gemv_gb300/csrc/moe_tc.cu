@@ -661,24 +661,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     const int row = 32 * q + lane;  // row within the tile
     TileCursor cur;
-    // Pass -1 is a dry run of this code on the first tile before its accumulator is ready: it
-    // reads TMEM but uses nothing it reads, writes nothing and signals nothing.  It brings the
-    // epilogue's instructions into the instruction cache while the first weights stream in;
-    // fetched cold at the first tile's end instead (from memory busy with the weight stream)
-    // they held that accumulator for about 12 us, and the MMAs of the tile after next with it.
-    for (int ti_ = -1; ti_ < ntiles; ++ti_) {
-      const bool dry = ti_ < 0;
-      if (dry && ntiles == 0) continue;
-      const int tl = dry ? 0 : ti_;
-      const int tile = rg.t_first + tl;
+    for (int ti_ = 0; ti_ < ntiles; ++ti_) {
+      const int tile = rg.t_first + ti_;
       const TileInfo ti = cur.get<ONE>(tile, f, own_tiles);
-      const int b = tl & 1;
-      const bool write_part = !dry && ti_ == 0 && rg.tail_first;  // leave a part for the head
-      const bool add_parts = !dry && ti_ == ntiles - 1 && rg.head_last;  // add the later parts
-      int bad = (!dry && (*abort_v || !mbar_wait_ab(&accfull[b], (ti_ >> 1) & 1, f.status,
-                                                    abort_v)))
-                    ? 1
-                    : 0;
+      const int b = ti_ & 1;
+      const bool write_part = ti_ == 0 && rg.tail_first;          // leave a part for the head
+      const bool add_parts = ti_ == ntiles - 1 && rg.head_last;    // add the later CTAs' parts
+      int bad = (*abort_v || !mbar_wait_ab(&accfull[b], (ti_ >> 1) & 1, f.status, abort_v)) ? 1 : 0;
       if (add_parts && !bad) {
         if (fix_smem) {
           // the helper's copies complete this phase; if it gave up it set abort_v, and the
@@ -707,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
       tc::fence_after_sync();
       const uint32_t tacc = t0 + lane_off + (uint32_t)b * kAccCols;
       const int grp = (ti.rt * kRowsTile + 32 * q) >> 5;            // phase 0: act group
-      const bool in_range = !dry && ti.rt * kRowsTile + 32 * q < f.R;
+      const bool in_range = ti.rt * kRowsTile + 32 * q < f.R;
       float* mine = parts + (size_t)cta * pf;
       // TB tokens at a time (4 with 64-row activation tiles, 1 otherwise): one TMEM load of
       // their 4 TB columns per matrix, then their epilogues side by side
@@ -787,13 +776,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
             if (jj >= nj) break;
             const int asg = ONE ? own_perm[ti.pos0 + j0 + jj] : f.perm[ti.pos0 + j0 + jj];
             const float gj = ONE ? own_gate[asg] : f.gate[asg];
-            if (!dry && r_exp < f.R) f.ybuf[(size_t)asg * f.L + r_exp] = gj * v[jj][0];
+            if (r_exp < f.R) f.ybuf[(size_t)asg * f.L + r_exp] = gj * v[jj][0];
           }
         }
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0 && !dry) mbar_arrive(&accempty[b]);
+      if (lane == 0) mbar_arrive(&accempty[b]);
       if constexpr (kLaneSplit) {
         // lane j: token j's group of 32 rows (this warp's rows) into kTerms MXFP4 terms, the
         // same arithmetic as mx_split_group, one 16-byte store per term
@@ -824,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
         if (threadIdx.x == 0) st_release(f.flags + cta, 1);
       }
       if constexpr (ONE && PH == 1) {
-        if (!write_part && !dry) {
+        if (!write_part) {
           // the combine: count this slot for its 128-row tile of y; the CTA that writes the
           // k-th slot of a tile sums the token's slots there in slot order (as k_combine)
           named_bar(kEpiBar, 128);  // orders every row's slot write before the release
