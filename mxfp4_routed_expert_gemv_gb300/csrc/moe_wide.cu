@@ -32,9 +32,10 @@
 // rows; the weight scales once per four stages), warps 10-13 move the scales from shared
 // memory into TMEM (each warp its lane quarter), warp 9 allocates TMEM and issues the MMAs
 // (tcgen05.mma kind::mxf4, M = 128, N = 256, fp32 accumulators in TMEM), warps 0-7 run the
-// epilogue.  GEMM1's epilogue moves act (fp32) into shared memory and frees the accumulator
-// before it splits act into terms, so the split overlaps the next tile's MMAs.  Every wait
-// is bounded; one that runs out counts a timeout in the status block and the CTA stops.
+// epilogue.  GEMM1's epilogue keeps act (fp32) in registers and frees the accumulator
+// before it splits act into terms, so the split overlaps the next tile's MMAs; four stages
+// in both GEMMs.  Every wait is bounded; one that runs out counts a timeout in the status
+// block and the CTA stops.
 #include "launch.h"
 #include "mxq.cuh"
 #include "tc.cuh"
@@ -82,17 +83,13 @@ struct WMode {
   static constexpr uint32_t kSfCols = kSfB + 8 * kKSteps;
   static_assert(kPos * (TR ? kTerms : 1) == kWM, "A tile rows");
 };
-constexpr int kActStride = 132;  // floats per position row of GEMM1's act staging
 constexpr int kEpiBarW = 1;      // named barrier of the 256 epilogue threads
 
 template <int PH, bool TR>
 struct WLay {
   using M = WMode<TR>;
-  static constexpr int kStages = TR ? 4 : (PH == 0 ? 3 : 4);
-  // folded GEMM1 parks act in shared memory to free the accumulator before its MXFP4 split
-  static constexpr uint32_t kActBytes = (PH == 0 && !TR) ? kWM * kActStride * 4 : 0;
-  static constexpr size_t kSmemBytes =
-      (size_t)kStages * M::kStage + kActBytes + 2 * kWsBytes + 1024;
+  static constexpr int kStages = 4;
+  static constexpr size_t kSmemBytes = (size_t)kStages * M::kStage + 2 * kWsBytes + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
   static_assert(kAccColsW + kStages * M::kSfCols <= kTmemColsW, "TMEM budget");
 };
@@ -212,8 +209,7 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
   __shared__ int abort_flag;
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) &
                                            ~uintptr_t(1023));
-  float* actbuf = reinterpret_cast<float*>(sm + (size_t)S * kStageW);
-  uint8_t* wsring = sm + (size_t)S * kStageW + Y::kActBytes;  // two weight-scale slots
+  uint8_t* wsring = sm + (size_t)S * kStageW;  // two weight-scale slots
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;
 
@@ -574,48 +570,30 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
         }
       } else if (PH == 0) {
         // g in columns 0..127, u in 128..255 (rows 128 rb .. 128 rb + 127 of w1 / w3); this
-        // warp takes rows 64 hf .. 64 hf + 63, 16 at a time
-#pragma unroll 1
+        // thread: position m, rows 64 hf .. 64 hf + 63 (two groups of 32), 16 at a time, act
+        // kept in registers; the accumulator is released before the groups' MXFP4 split
+        float act[64];
+#pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           const int c16 = 4 * hf + cc;  // 16-row piece
           uint32_t g[16], u[16];
           tc::tmem_ld_x16(tacc + 16 * c16, g);
           tc::tmem_ld_x16(tacc + 128 + 16 * c16, u);
           tc::tmem_ld_wait();
-          float* row = actbuf + (size_t)m * kActStride + 16 * c16;
 #pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            float4 a;
-            a.x = activation_fast(__uint_as_float(g[i]), __uint_as_float(u[i]), f.act_kind, f.b1, f.b2);
-            a.y = activation_fast(__uint_as_float(g[i + 1]), __uint_as_float(u[i + 1]), f.act_kind, f.b1, f.b2);
-            a.z = activation_fast(__uint_as_float(g[i + 2]), __uint_as_float(u[i + 2]), f.act_kind, f.b1, f.b2);
-            a.w = activation_fast(__uint_as_float(g[i + 3]), __uint_as_float(u[i + 3]), f.act_kind, f.b1, f.b2);
-            *reinterpret_cast<float4*>(row + i) = a;
-          }
+          for (int i = 0; i < 16; ++i)
+            act[16 * cc + i] =
+                activation_fast(__uint_as_float(g[i]), __uint_as_float(u[i]), f.act_kind, f.b1, f.b2);
         }
         tc::fence_before_sync();
         named_bar(kEpiBarW, 32 * kEpiWarpsW);
         if (et == 0) mbar_arrive(&accempty);  // the next tile's MMAs may start
-        // each thread: two (position, group) items, split into kTerms MXFP4 terms
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          const int item = et + 256 * h;
-          const int c = item >> 7, mm = item & 127;
-          if (mm < wt.ntok) {
-            const float* src = actbuf + (size_t)mm * kActStride + 32 * c;
-            float r[32];
+        if (m < wt.ntok) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              const float4 v = *reinterpret_cast<const float4*>(src + i);
-              r[i] = v.x;
-              r[i + 1] = v.y;
-              r[i + 2] = v.z;
-              r[i + 3] = v.w;
-            }
-            store_act_group(f, r, (size_t)(wt.pos0 + mm), wt.rb * 4 + c);
-          }
+          for (int jg = 0; jg < 2; ++jg)
+            store_act_group(f, *reinterpret_cast<float(*)[32]>(act + 32 * jg),
+                            (size_t)(wt.pos0 + m), wt.rb * 4 + 2 * hf + jg);
         }
-        named_bar(kEpiBarW, 32 * kEpiWarpsW);  // the staging buffer is free again
       } else {
         // o for the 256 output rows 256 rb .. 256 rb + 255, times the assignment's gate;
         // this warp takes columns 128 hf .. 128 hf + 127 of its 32 positions, 32 at a time:
