@@ -352,7 +352,9 @@ int k3moe_cache_host_scratch_size(const k3moe_cfg *cfg, int32_t T, int32_t n_slo
 
 /* The layer with its experts in the cache: routes the T tokens on the device (as
  * k3moe_route), reads the routing back to the host, plans, copies the missing experts from
- * the host store into their slots (one cudaMemcpyAsync per tensor), publishes, and runs the
+ * the host store into their slots (by a kernel that reads the store where it is mapped page-
+ * locked memory, over NVLink-C2C on a Grace-Blackwell node; otherwise one cudaMemcpyAsync per
+ * tensor), publishes, and runs the
  * routed-expert sum on the slots (as k3moe_experts_mxfp4 with the routing mapped to slots);
  * synchronises the stream before returning.  y equals k3moe_layer's for the same inputs
  * bit for bit when the batch takes the large-batch expert kernels (T >= 3 with latent and

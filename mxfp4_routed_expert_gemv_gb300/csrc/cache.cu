@@ -31,6 +31,46 @@ int check_cache(const k3moe_expert_cache* c) {
 
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
+// The device's address of page-locked host memory it can reach directly (over NVLink-C2C on
+// a Grace-Blackwell node), or nullptr.
+const uint8_t* mapped(const uint8_t* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? static_cast<const uint8_t*>(a.devicePointer) : nullptr;
+}
+
+struct CopyArgs {
+  const uint8_t* src[6];  // the store's tensors (device addresses of the host memory)
+  uint8_t* dst[6];        // the slots' tensors
+  size_t per[6];          // bytes of one expert in each tensor (multiples of 16)
+  const int32_t* fetch;   // [2][n]: experts, then their slots
+  int n;
+};
+
+// The planned experts host -> device by the SMs themselves (loads from the mapped host store,
+// stores to the slots): block (x, j * 6 + m) copies its stretch of tensor m of fetch j, 16 bytes
+// a thread at a time with four loads in flight.
+__global__ void __launch_bounds__(256) k_copy_experts(const CopyArgs a) {
+  const int j = blockIdx.y / 6, m = blockIdx.y - 6 * (blockIdx.y / 6);
+  if (j >= a.n) return;
+  const size_t units = a.per[m] >> 4;
+  const uint4* src = reinterpret_cast<const uint4*>(a.src[m] + (size_t)a.fetch[j] * a.per[m]);
+  uint4* dst = reinterpret_cast<uint4*>(a.dst[m] + (size_t)a.fetch[a.n + j] * a.per[m]);
+  const size_t step = (size_t)gridDim.x * blockDim.x;
+  size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; u + 3 * step < units; u += 4 * step) {
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __ldcs(src + u + i * step);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[u + i * step] = v[i];
+  }
+  for (; u < units; u += step) dst[u] = __ldcs(src + u);
+}
+
 }  // namespace
 }  // namespace k3
 
@@ -155,7 +195,8 @@ int k3moe_cache_workspace_size(const k3moe_cfg* cfg, int32_t T, size_t* bytes) {
   int rc = k3moe_workspace_size(cfg, T, &b);
   if (rc) return rc;
   const size_t P = (size_t)T * cfg->topk;
-  *bytes = align256(b) + 3 * align256(P * 4);
+  // idx, gate, then the slot ids followed by room for a fetch list of up to E experts
+  *bytes = align256(b) + 2 * align256(P * 4) + align256((P + 2 * (size_t)cfg->n_experts) * 4);
   return K3MOE_OK;
 }
 
@@ -209,7 +250,9 @@ int k3moe_layer_cached(const k3moe_cfg* cfg, k3moe_expert_cache* c, const void* 
   int32_t nf = 0;
   if ((rc = k3moe_cache_plan(c, h_idx, (int32_t)P, h_slot, f_exp, f_slot, &nf))) return rc;
 
-  // the reserved experts, host -> device, in ascending expert order
+  // the reserved experts, host -> device, in ascending expert order: by the SMs from the
+  // mapped store when the store is mapped page-locked memory (the slot ids go to the device
+  // with the fetch list), else one copy per tensor
   const size_t L = (size_t)cfg->latent, I = (size_t)cfg->inter;
   const size_t b13 = I * L / 2, s13 = I * L / 32, b2 = L * I / 2, s2 = L * I / 32;
   const uint8_t* src[6] = {hs->w1_packed, hs->w1_scale, hs->w3_packed, hs->w3_scale,
@@ -217,14 +260,38 @@ int k3moe_layer_cached(const k3moe_cfg* cfg, k3moe_expert_cache* c, const void* 
   const uint8_t* dst[6] = {c->slots.w1_packed, c->slots.w1_scale, c->slots.w3_packed,
                            c->slots.w3_scale, c->slots.w2_packed, c->slots.w2_scale};
   const size_t per[6] = {b13, s13, b13, s13, b2, s2};
+  CopyArgs ca{};
+  bool direct = nf > 0;
+  for (int m = 0; m < 6 && direct; ++m) {
+    ca.src[m] = mapped(src[m]);
+    ca.dst[m] = const_cast<uint8_t*>(dst[m]);
+    ca.per[m] = per[m];
+    direct = ca.src[m] != nullptr && per[m] % 16 == 0 && (reinterpret_cast<uintptr_t>(ca.src[m]) % 16) == 0;
+  }
   int32_t ok = 0;
-  for (; ok < nf; ++ok) {
-    bool issued = true;
-    for (int m = 0; m < 6 && issued; ++m)
-      issued = cudaMemcpyAsync(const_cast<uint8_t*>(dst[m]) + (size_t)f_slot[ok] * per[m],
-                               src[m] + (size_t)f_exp[ok] * per[m], per[m],
-                               cudaMemcpyHostToDevice, s) == cudaSuccess;
-    if (!issued) break;
+  if (direct) {
+    // the slot ids and the fetch list in one copy: h_slot [P], then f_exp [C], f_slot [C]
+    int32_t* fs2 = f_exp + nf;  // [experts nf][slots nf], contiguous after h_slot
+    std::memmove(fs2, f_slot, (size_t)nf * 4);
+    f_slot = fs2;
+    if (cudaMemcpyAsync(d_slot, h_slot, (P + 2 * (size_t)nf) * 4, cudaMemcpyHostToDevice, s) !=
+        cudaSuccess) {
+      k3moe_cache_publish(c, f_exp, f_slot, nf, 0);
+      return K3MOE_ERR_CUDA;
+    }
+    ca.fetch = d_slot + P;
+    ca.n = nf;
+    const cudaError_t e = launch_kernel(k_copy_experts, dim3(64, 6 * nf), dim3(256), 0, s, false, ca);
+    ok = e == cudaSuccess ? nf : 0;
+  } else {
+    for (; ok < nf; ++ok) {
+      bool issued = true;
+      for (int m = 0; m < 6 && issued; ++m)
+        issued = cudaMemcpyAsync(const_cast<uint8_t*>(dst[m]) + (size_t)f_slot[ok] * per[m],
+                                 src[m] + (size_t)f_exp[ok] * per[m], per[m],
+                                 cudaMemcpyHostToDevice, s) == cudaSuccess;
+      if (!issued) break;
+    }
   }
   k3moe_cache_publish(c, f_exp, f_slot, nf, ok);
   if (ok < nf) {
@@ -234,7 +301,7 @@ int k3moe_layer_cached(const k3moe_cfg* cfg, k3moe_expert_cache* c, const void* 
   if (n_fetched) *n_fetched = nf;
 
   // the routed-expert sum on the slots
-  if (cudaMemcpyAsync(d_slot, h_slot, P * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+  if (!direct && cudaMemcpyAsync(d_slot, h_slot, P * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return K3MOE_ERR_CUDA;
   k3moe_cfg cs = *cfg;
   cs.n_experts = C;
