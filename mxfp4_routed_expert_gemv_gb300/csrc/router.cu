@@ -93,16 +93,26 @@ __global__ void __launch_bounds__(RPC * kQuarters * 32) k_router_logits(const ui
     logits[(size_t)(t0 + lane) * E + e] = s;
   }
   if (xq) {
-    const int grp = blockIdx.x * (RPC * kQuarters) + warp;
-    if (grp < (L >> 5)) {
-      const float v = __uint_as_float((uint32_t)x[32 * grp + lane] << 16);
-      uint32_t words[kTerms], sf[kTerms];
-      mx_split_group(v, words, sf);
+    // four lanes per group of 32 (eight elements each, the hardware E2M1 rounding), eight
+    // groups per warp: the split is on the critical path of the layer (the expert GEMM waits
+    // for this whole launch), so it is kept to one short chain per warp
+    const int grp = (blockIdx.x * (RPC * kQuarters) + warp) * 8 + (lane >> 2);
+    const int t4 = lane & 3;
+    if (blockIdx.x * (RPC * kQuarters) * 8 < (L >> 5)) {  // whole warps take part
+      float r[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (grp < (L >> 5)) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(x + 32 * grp + 8 * t4));
+        r[0] = bf16lo(raw.x); r[1] = bf16hi(raw.x); r[2] = bf16lo(raw.y); r[3] = bf16hi(raw.y);
+        r[4] = bf16lo(raw.z); r[5] = bf16hi(raw.z); r[6] = bf16lo(raw.w); r[7] = bf16hi(raw.w);
+      }
+      uint32_t w[kTerms], sf[kTerms];
+      mx_split_quad8(r, w, sf);
+      if (grp < (L >> 5)) {
 #pragma unroll
-      for (int t = 0; t < kTerms; ++t) {
-        if ((lane & 7) == 0)
-          *reinterpret_cast<uint32_t*>(xq + (size_t)t * (L >> 1) + grp * 16 + 4 * (lane >> 3)) = words[t];
-        if (lane == 0) xsf[(size_t)t * (L >> 5) + grp] = (uint8_t)sf[t];
+        for (int t = 0; t < kTerms; ++t) {
+          *reinterpret_cast<uint32_t*>(xq + (size_t)t * (L >> 1) + grp * 16 + 4 * t4) = w[t];
+          if (t4 == 0) xsf[(size_t)t * (L >> 5) + grp] = (uint8_t)sf[t];
+        }
       }
     }
   }
@@ -317,7 +327,8 @@ cudaError_t launch_router_logits(const uint16_t* h, const uint16_t* wr, int T, i
   }
   if (T <= 2) {
     const unsigned gx = (E + kRpcFew - 1) / kRpcFew;
-    if (xq && (T != 1 || (int)gx * kRpcFew * kQuarters < (L >> 5))) return cudaErrorInvalidValue;
+    if (xq && (T != 1 || (int)gx * kRpcFew * kQuarters * 8 < (L >> 5) || (L & 7) != 0))
+      return cudaErrorInvalidValue;
     return launch_kernel(k_router_logits<1, kRpcFew>, dim3(gx, T), dim3(kRpcFew * kQuarters * 32),
                          0, s, pdl, h, wr, T, E, H, logits, x, L, xq, xsf, zero, nzero);
   }
