@@ -22,7 +22,7 @@
  *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy default
  *     stream) and the call returns after enqueueing; results are ready when the stream
  *     reaches that point.  k3moe_layer_host is the exception: it synchronises the stream
- *     (k3moe_layer_host_async does so only when it cannot replay a recorded graph).
+ *     (k3moe_layer_host_async does so only when its host buffers are not all mapped).
  *   - T == 0 is a no-op that returns K3MOE_OK once the configuration is valid (empty
  *     tensors may carry NULL pointers).
  *   - Host-side argument checks run first.  On any failure the call returns a non-zero
@@ -182,9 +182,11 @@ int k3moe_layer_host(const k3moe_cfg *cfg, const void *h_host, const void *wr,
  * in flight (double-buffered host buffers): the call enqueues the layer on `stream` and
  * returns; y_host holds the result once the stream reaches that point (synchronise the stream
  * or an event recorded after the call).  The caller must not write h_host or x_host, nor read
- * y_host, until then.  It returns without waiting only when it can replay a recorded graph
- * (page-locked mapped buffers, a repeated argument set); otherwise (the first call with an
- * argument set, pageable buffers, phase events set) it synchronises like k3moe_layer_host.
+ * y_host, until then.  It returns without waiting when h_host, x_host and y_host are all
+ * page-locked host memory mapped into the device's address space: the layer's launches are
+ * then enqueued as they are (no graph: programmatic dependent launch lets consecutive calls
+ * on one stream overlap their first and last kernels), the kernels reading h and x and
+ * writing y in host memory.  Otherwise it behaves like k3moe_layer_host (and synchronises).
  * Arguments and errors as k3moe_layer_host. */
 int k3moe_layer_host_async(const k3moe_cfg *cfg, const void *h_host, const void *wr,
                            const float *bias, const k3moe_experts *experts, const void *x_host,

@@ -546,8 +546,8 @@ def k3moe_layer_host(cfg: Cfg, h_host, wr, bias, experts: Experts, x_host, y_hos
 
 def k3moe_layer_host_async(cfg: Cfg, h_host, wr, bias, experts: Experts, x_host, y_host, status,
                            ws, stream=None) -> None:
-    """k3moe_layer_host that returns once the layer is enqueued (when it replays a recorded
-    graph); y_host is ready when the stream reaches this point."""
+    """k3moe_layer_host that returns once the layer is enqueued (when h, x and y are mapped
+    page-locked host buffers); y_host is ready when the stream reaches this point."""
     _layer_host("k3moe_layer_host_async", cfg, h_host, wr, bias, experts, x_host, y_host, status, ws,
                 stream)
 

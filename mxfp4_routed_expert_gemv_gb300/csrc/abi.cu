@@ -500,6 +500,11 @@ int layer_host(const k3moe_cfg* cfg, const void* h_host, const void* wr, const f
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int dev = 0;
   K3_TRY(cudaGetDevice(&dev));
+  if (!sync && mapped_host(h_host) && mapped_host(x_host) && mapped_host(y_host)) {
+    // kernels read h and x and write y in host memory: the launches are enqueued as they are
+    // (no graph), so that programmatic dependent launch overlaps consecutive calls' edges
+    return enqueue_layer_host(cfg, h_host, wr, bias, experts, x_host, T, y_host, status, w, s);
+  }
   if (!g_phase_on) {  // (phase events are recorded per call: no graphs while they are on)
     HostGraphKey key;
     std::memset(&key, 0, sizeof key);
