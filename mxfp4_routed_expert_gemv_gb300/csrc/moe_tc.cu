@@ -74,11 +74,7 @@ struct Lay {
   static constexpr int kStages =
       NM * KS == 2 ? ((NMAX <= 16 && NM == 2) || BR == 8 ? 3 : 2) : (NMAX <= 16 ? 5 : 4);
   static constexpr uint32_t kFixBytes = (NMAX <= 16 && NM == 2) || BR == 8 ? 4096 : 16384;
-  // first GEMM with 64-row activation tiles: act of a tile's tokens, [warp][token][33]
-  // floats, so that one lane can split one token's group of 32 rows (see the epilogue)
-  static constexpr uint32_t kActBufBytes = NMAX == 64 && NM == 2 ? 4 * kTokTile * 33 * 4 : 0;
-  static constexpr size_t kSmemBytes =
-      (size_t)kStages * kStageBytes + kFixBytes + kActBufBytes + 1024;
+  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kFixBytes + 1024;
   static constexpr uint32_t kMatCols = NMAX <= 16 ? 32 : 64;
   static constexpr uint32_t kAccCols = 2 * kMatCols;
   static constexpr uint32_t kSfBase = 2 * kAccCols;
@@ -357,10 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) &
                                            ~uintptr_t(1023));
   float* fix = reinterpret_cast<float*>(sm + (size_t)kStages * kStageBytes);
-  float* actbuf = reinterpret_cast<float*>(sm + (size_t)kStages * kStageBytes + kFixBytes);
   // many tokens per tile: each lane splits one token's group (no cross-lane work); one token
   // per tile: the warp splits the group together
-  constexpr bool kLaneSplit = Y::kActBufBytes > 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;
 
@@ -579,13 +573,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
 #pragma unroll
           for (int j = 0; j < kMmas; ++j)
             tc::tmem_st_x1(rb + 4 * j, (wb0[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-          if (NMAX > 32 && N > 32) {
-            const uint4 sb1 = *reinterpret_cast<const uint4*>(sbs + 16 * (32 + lane));
-            const uint32_t wb1[4] = {sb1.x, sb1.y, sb1.z, sb1.w};
-#pragma unroll
-            for (int j = 0; j < kMmas; ++j)
-              tc::tmem_st_x1(rb + 1 + 4 * j, (wb1[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-          }
         }
         tc::tmem_st_wait();
         tc::fence_before_sync();
@@ -698,8 +685,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
       const int grp = (ti.rt * kRowsTile + 32 * q) >> 5;            // phase 0: act group
       const bool in_range = ti.rt * kRowsTile + 32 * q < f.R;
       float* mine = parts + (size_t)cta * pf;
-      // TB tokens at a time (4 with 64-row activation tiles, 1 otherwise): one TMEM load of
-      // their 4 TB columns per matrix, then their epilogues side by side
+      // TB tokens at a time: one TMEM load of their 4 TB columns per matrix, then their
+      // epilogues side by side
 #pragma unroll 1
       for (int j0 = 0; j0 < ti.ntok; j0 += TB) {
         float v[TB][2];
@@ -745,13 +732,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
 #pragma unroll
           for (int jj = 0; jj < TB; ++jj)
             act[jj] = activation(v[jj][0], v[jj][NM - 1], f.act_kind, f.b1, f.b2);
-          if constexpr (kLaneSplit) {
-            float* sb = actbuf + q * (kTokTile * 33);
-#pragma unroll
-            for (int jj = 0; jj < TB; ++jj)
-              if (jj < nj) sb[(j0 + jj) * 33 + lane] = act[jj];
-            continue;
-          }
           uint32_t words[TB][kTerms], sfb[TB][kTerms];
           mx_split_groups<TB>(act, words, sfb);
           if (in_range) {
@@ -783,30 +763,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&accempty[b]);
-      if constexpr (kLaneSplit) {
-        // lane j: token j's group of 32 rows (this warp's rows) into kTerms MXFP4 terms, the
-        // same arithmetic as mx_split_group, one 16-byte store per term
-        if (!write_part) {
-          __syncwarp();
-          if (lane < ti.ntok && in_range) {
-            const float* sb = actbuf + q * (kTokTile * 33) + lane * 33;
-            float r[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = sb[i];
-            const size_t p = (size_t)(ti.pos0 + lane);
-            uint32_t w[kTerms][4], sfb[kTerms];
-            mx_split_lane32(r, w, sfb);
-#pragma unroll
-            for (int t = 0; t < kTerms; ++t) {
-              const size_t r2 = p * kTerms + t;
-              *reinterpret_cast<uint4*>(f.act_q + r2 * (size_t)(f.I >> 1) + grp * 16) =
-                  make_uint4(w[t][0], w[t][1], w[t][2], w[t][3]);
-              f.act_sf[r2 * (size_t)(f.I >> 5) + grp] = (uint8_t)sfb[t];
-            }
-          }
-          __syncwarp();
-        }
-      }
       if (write_part) {
         __threadfence();
         named_bar(kEpiBar, 128);
@@ -908,8 +864,10 @@ cudaError_t launch_tc_phase(const Maps& mp, const FArgs& f, cudaStream_t s, bool
 // Batches of up to 4 tokens have at most 4 tokens per expert: 16-row activation tiles.
 cudaError_t launch_tc(const Maps& mp, const FArgs& f, int T, cudaStream_t s, bool pdl) {
   if (f.route_one) return launch_tc_phase<16, true>(mp, f, s, pdl);  // one token
-  if (T * kTerms <= 16) return launch_tc_phase<16, false>(mp, f, s, pdl);
-  return launch_tc_phase<64, false>(mp, f, s, pdl);
+  // one or two tokens (their terms fill at most 16 MMA columns); batches of 3 tokens or more
+  // take the large-batch kernels (moe_wide.cu), which run on every shape this path takes
+  if (T * kTerms > 16) return cudaErrorInvalidValue;
+  return launch_tc_phase<16, false>(mp, f, s, pdl);
 }
 
 }  // namespace
