@@ -600,9 +600,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_tc(const __grid_constant__ 
         for (int kc = kb; kc < ke && !stop; ++kc, ++it) {
           const int s = it % kStages;
           const uint32_t par = (it / kStages) & 1;
-          if (*abort_v || !mbar_wait_ab(&fullA[s], par, f.status, abort_v) ||
-              !mbar_wait_ab(&fullB[s], par, f.status, abort_v) ||
-              !mbar_wait_ab(&sfready[s], par, f.status, abort_v)) {
+          // the scale warps arrive on sfready only after they have seen both of the stage's
+          // copies land, so this one wait covers all three barriers
+          if (*abort_v || !mbar_wait_ab(&sfready[s], par, f.status, abort_v)) {
             *abort_v = 1;
             stop = true;
             break;

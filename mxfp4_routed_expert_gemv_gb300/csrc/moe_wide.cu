@@ -432,8 +432,9 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
         for (int kc = 0; kc < KC; ++kc, ++it) {
           const int s = it % S;
           const uint32_t par = (it / S) & 1;
-          if (*abort_v || !mbar_wait_ab(&full[s], par, f.status, abort_v) ||
-              !mbar_wait_ab(&sfready[s], par, f.status, abort_v)) {
+          // the scale warps arrive on sfready only after they have seen the stage's copies
+          // land (full), so this one wait covers both
+          if (*abort_v || !mbar_wait_ab(&sfready[s], par, f.status, abort_v)) {
             *abort_v = 1;
             stop = true;
             break;

@@ -104,25 +104,28 @@ def test_large_batch_experts_entry_drops_and_duplicates(T, seed):
     """The expert entry point at 288, 100 and 40 tokens (the one-CTA preparation's sort, and
     its token-mask ranking falling back to the sort when a token repeats an expert):
     out-of-range indices are skipped and counted, repeated experts in a token's list count
-    twice."""
+    twice, and a token with no valid slot gets y = 0 (y starts as NaN: every row is
+    written)."""
     k3 = _k3()
     w = synth.small_workload(T=T, E=10, k=4, latent=512, inter=512, hidden=128, seed=seed)
     ex = k3.Experts.from_dict(synth.experts_device(w, 0))
     li = synth.layer_inputs(w)
     rng = np.random.default_rng(3)
     idx = rng.integers(0, w.E, size=(w.T, w.k)).astype(np.int32)
+    idx[3] = [-1, -1, 10, 1 << 20]
     idx[5] = [-1, 4, 4, 9]
     idx[min(77, T - 2)] = [10, 0, 0, 0]
     idx[min(200, T - 1), 2] = 1 << 20
     gate = rng.uniform(0.1, 1.0, size=idx.shape).astype(np.float32)
     cfg = gpu_cfg(w)
     ws = k3.workspace(cfg, w.T)
-    y = torch.empty((w.T, w.latent), dtype=torch.float32, device="cuda")
+    y = torch.full((w.T, w.latent), float("nan"), dtype=torch.float32, device="cuda")
     st = torch.zeros(4, dtype=torch.int32, device="cuda")
     k3.k3moe_experts_mxfp4(cfg, ex, to_dev_bf16(li.x), torch.from_numpy(idx).cuda(), torch.from_numpy(gate).cuda(),
                            y, st, ws)
     torch.cuda.synchronize()
-    assert st.cpu().numpy()[0] == 3
+    assert st.cpu().numpy()[0] == 7
+    assert (y[3] == 0).all()
     valid = (idx >= 0) & (idx < w.E)
     ridx = np.where(valid, idx, 0).astype(np.int32)
     rgate = np.where(valid, gate, 0.0).astype(np.float64)
