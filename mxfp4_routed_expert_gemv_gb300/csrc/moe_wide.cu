@@ -597,46 +597,53 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
         }
       } else {
         // o for the 256 output rows 256 rb .. 256 rb + 255, times the assignment's gate;
-        // this warp takes columns 128 hf .. 128 hf + 127 of its 32 positions, 32 at a time:
-        // the 32 x 32 block is transposed across the warp, so that each store instruction
-        // writes 128 contiguous bytes of one assignment's row
-        int a = 0;
-        float gt = 0.f;
-        const bool mine = m < wt.ntok;
-        if (mine) {
-          a = __ldg(f.perm + wt.pos0 + m);
-          gt = __ldg(f.gate + a);
+        // this warp takes columns 128 hf .. 128 hf + 127 of its 32 positions, read as 16
+        // positions x 32 columns at a time (16x256b: four lanes hold 8 consecutive columns of
+        // one position), so that each 8-byte store of four lanes fills a 32-byte sector of
+        // one assignment's row with no exchange across the warp.  The next piece is read
+        // while this one is stored; the accumulator is released once the last is read.
+        const int t4 = lane & 3, r8 = lane >> 2;
+        int ar[4];
+        float gr[4];
+        bool ok[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // rows 16 (i / 2) + 8 (i % 2) + lane / 4 of the warp's 32
+          const int mm = 32 * q + 16 * (i >> 1) + 8 * (i & 1) + r8;
+          ok[i] = mm < wt.ntok;
+          ar[i] = ok[i] ? __ldg(f.perm + wt.pos0 + mm) : 0;
+          gr[i] = ok[i] ? __ldg(f.gate + ar[i]) : 0.f;
         }
-        float* ycol = f.ybuf + (size_t)wt.rb * 256 + 128 * hf + lane;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t u[32];
-          tc::tmem_ld_x32(tacc + 128 * hf + 32 * c, u);
-          tc::tmem_ld_wait();
-          float v[32];
+        const size_t col0 = (size_t)wt.rb * 256 + 128 * hf + 2 * t4;
+        uint32_t u[2][16];
+        tc::tmem_ld_16x256b_x4(tacc + 128 * hf, u[0]);
+        tc::tmem_ld_wait_regs(u[0]);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = gt * __uint_as_float(u[i]);
-          // butterfly transpose: afterwards v[p] = column 32 c + lane of position 32 q + p
+        for (int pc = 0; pc < 8; ++pc) {  // piece: lanes 16 (pc / 4) .., columns 32 (pc % 4) ..
+          if (pc < 7) {
+            const int nx = pc + 1;
+            tc::tmem_ld_16x256b_x4(tacc + ((uint32_t)(16 * (nx >> 2)) << 16) + 128 * hf + 32 * (nx & 3),
+                                   u[nx & 1]);
+          }
+          const int h = pc >> 2, c = pc & 3;
 #pragma unroll
-          for (int sh = 16; sh >= 1; sh >>= 1) {
-            const bool up = (lane & sh) != 0;
+          for (int e = 0; e < 2; ++e) {  // row lane / 4 (e = 0) or lane / 4 + 8 (e = 1)
+            const int i = 2 * h + e;
+            if (ok[i]) {
+              float* yr = f.ybuf + (size_t)ar[i] * f.L + col0 + 32 * c;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (i & sh) continue;
-              const float send = up ? v[i] : v[i + sh];
-              const float recv = __shfl_xor_sync(0xffffffffu, send, sh);
-              if (up) v[i] = recv; else v[i + sh] = recv;
+              for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<float2*>(yr + 8 * j) =
+                    make_float2(gr[i] * __uint_as_float(u[pc & 1][4 * j + 2 * e]),
+                                gr[i] * __uint_as_float(u[pc & 1][4 * j + 2 * e + 1]));
             }
           }
-#pragma unroll
-          for (int p = 0; p < 32; ++p) {
-            const int ap = __shfl_sync(0xffffffffu, a, p);
-            if (p < wt.ntok - 32 * q) ycol[(size_t)ap * f.L + 32 * c] = v[p];
+          if (pc < 7) tc::tmem_ld_wait_regs(u[(pc + 1) & 1]);
+          if (pc == 6) {
+            tc::fence_before_sync();
+            named_bar(kEpiBarW, 32 * kEpiWarpsW);
+            if (et == 0) mbar_arrive(&accempty);
           }
         }
-        tc::fence_before_sync();
-        named_bar(kEpiBarW, 32 * kEpiWarpsW);
-        if (et == 0) mbar_arrive(&accempty);
       }
     }
   }
