@@ -573,9 +573,12 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
         // g in columns 0..127, u in 128..255 (rows 128 rb .. 128 rb + 127 of w1 / w3); this
         // thread: position m, rows 64 hf .. 64 hf + 63 (two groups of 32), 16 at a time, act
         // kept in registers; the accumulator is released before the groups' MXFP4 split
+        // (the activation of the first two pieces is taken while the accumulator is held,
+        // the last two are read raw and activated after it is released: the activation's
+        // special-function work, not the reads, sets how long the MMAs wait)
         float act[64];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           const int c16 = 4 * hf + cc;  // 16-row piece
           uint32_t g[16], u[16];
           tc::tmem_ld_x16(tacc + 16 * c16, g);
@@ -586,9 +589,22 @@ __global__ void __launch_bounds__(kThreadsW, 1) k_moe_wide(const __grid_constant
             act[16 * cc + i] =
                 activation_fast(__uint_as_float(g[i]), __uint_as_float(u[i]), f.act_kind, f.b1, f.b2);
         }
+        uint32_t g2[2][16], u2[2][16];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          tc::tmem_ld_x16(tacc + 16 * (4 * hf + 2 + cc), g2[cc]);
+          tc::tmem_ld_x16(tacc + 128 + 16 * (4 * hf + 2 + cc), u2[cc]);
+        }
+        tc::tmem_ld_wait();
         tc::fence_before_sync();
         named_bar(kEpiBarW, 32 * kEpiWarpsW);
         if (et == 0) mbar_arrive(&accempty);  // the next tile's MMAs may start
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            act[32 + 16 * cc + i] = activation_fast(__uint_as_float(g2[cc][i]),
+                                                    __uint_as_float(u2[cc][i]), f.act_kind, f.b1, f.b2);
         if (m < wt.ntok) {
 #pragma unroll
           for (int jg = 0; jg < 2; ++jg)
