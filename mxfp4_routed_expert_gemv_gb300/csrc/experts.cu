@@ -407,7 +407,11 @@ __global__ void __launch_bounds__(kThreadsX, 1) k_experts(const XArgs a) {
 }
 
 // y[t][c] = sum over valid j of ybuf[t*k+j][c], in slot order (deterministic).  Slots are
-// loaded four at a time (independent loads in flight) and added in order.
+// taken kBatch at a time: their experts first, then their rows (independent loads in
+// flight), then added in order.  Small batches take 16 (the rows were just written and sit
+// in L2: the time is the loads' latency); large ones 4 (HBM-bound: 16 costs registers and
+// with them resident blocks, 143 -> 208 us at 4096 tokens).
+template <int kBatch>
 __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ ybuf,
                                                  const int32_t* __restrict__ idx, int k, int E,
                                                  int L, float* __restrict__ y) {
@@ -417,21 +421,21 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ ybuf,
   const int c4 = blockIdx.x * blockDim.x + threadIdx.x;
   if (c4 * 4 >= L) return;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j0 = 0; j0 < k; j0 += 4) {
-    float4 v[4];
-    bool ok[4];
+  for (int j0 = 0; j0 < k; j0 += kBatch) {
+    int e[kBatch];
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const int j = j0 + jj;
-      ok[jj] = false;
-      if (j < k) {
-        const int e = __ldg(idx + (size_t)t * k + j);
-        ok[jj] = (e >= 0 && e < E);
-        if (ok[jj]) v[jj] = __ldcs(reinterpret_cast<const float4*>(ybuf + ((size_t)t * k + j) * L) + c4);
-      }
+    for (int jj = 0; jj < kBatch; ++jj)
+      e[jj] = j0 + jj < k ? __ldg(idx + (size_t)t * k + j0 + jj) : -1;
+    float4 v[kBatch];
+    bool ok[kBatch];
+#pragma unroll
+    for (int jj = 0; jj < kBatch; ++jj) {
+      ok[jj] = e[jj] >= 0 && e[jj] < E;
+      if (ok[jj])
+        v[jj] = __ldcs(reinterpret_cast<const float4*>(ybuf + ((size_t)t * k + j0 + jj) * L) + c4);
     }
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
+    for (int jj = 0; jj < kBatch; ++jj) {
       if (ok[jj]) {
         acc.x += v[jj].x;
         acc.y += v[jj].y;
@@ -531,7 +535,8 @@ cudaError_t launch_gemm2(const ExpertPtrs& w, int L, int I, int E, int T, int k,
 cudaError_t launch_combine(const float* ybuf, const int32_t* idx, int T, int k, int E, int L,
                            float* y, cudaStream_t s, bool pdl) {
   dim3 grid(((L >> 2) + 255) / 256, T);
-  return launch_kernel(k_combine, grid, dim3(256), 0, s, pdl, ybuf, idx, k, E, L, y);
+  if (T <= 256) return launch_kernel(k_combine<16>, grid, dim3(256), 0, s, pdl, ybuf, idx, k, E, L, y);
+  return launch_kernel(k_combine<4>, grid, dim3(256), 0, s, pdl, ybuf, idx, k, E, L, y);
 }
 
 }  // namespace k3
